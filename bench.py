@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""PSA self-attention backward throughput on GB300.
+
+One step = one psa_attn_bwd call (every backward kernel: D preprocess, the
+dK/dV/dQ contractions, the dQ write-out) over one batch of synthetic inputs
+already resident in HBM, for the bf16 B=8, heads=2, N=6400 (80x80 map),
+head_dim=32 workload.  The forward (psa_attn_fwd) produces O and LSE once,
+before timing.  L2 (129 MB) is flushed by writing a 256 MB buffer before every
+timed step; each step is timed with CUDA events on the launching stream.
+
+Metric: TFLOP/s counting 12*N^2*d per (batch, head) -- 4*N^2*d for the shared
+S recompute plus 2 * 4*N^2*d for the per-V-half dP/dV and dQ/dK terms.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs the whole workload on its own GPU
+(independent batches, weak scaling, no collective on the data path); the
+slowest rank's time sets the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "PSA attn-bwd TFLOP/s (1 GB300, N=400/1600/6400) and % of roofline"
+UNIT = "TFLOP/s"
+HEADLINE = "psa_bf16_b8_h2_n6400_d32"
+SECONDARY = ["psa_bf16_b32_h8_n400_d64", "psa_bf16_b16_h4_n1600_d64"]
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ accounting
+def metric_flops(w) -> float:
+    """Counted FLOPs of one backward over the whole workload."""
+    return 12.0 * w.N * w.N * w.d * w.BH
+
+
+def alg_bytes(w) -> float:
+    """Algorithmic HBM bytes of one backward: read Q, K, V_lo, V_hi, O_lo, O_hi,
+    dO_lo, dO_hi and LSE (fp32); write dQ, dK, dV_lo, dV_hi."""
+    s = 2 if w.dtype == "bf16" else 4
+    return float(w.BH) * (12.0 * w.N * w.d * s + 4.0 * w.N)
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def tensor_peak(peaks, dtype: str, sustained=False) -> float:
+    bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    # fp32 storage runs on CUDA cores / tf32-class rates: nominal tf32 : bf16 = 1 : 2
+    return bf16 if dtype == "bf16" else bf16 / 2.0
+
+
+def roofline_time_s(w, peaks) -> tuple[float, str]:
+    t_t = metric_flops(w) / (tensor_peak(peaks, w.dtype) * 1e12)
+    t_m = alg_bytes(w) / (peaks["hbm_gbs"] * 1e9)
+    return (t_t, "tensor") if t_t >= t_m else (t_m, "hbm")
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "self_attention_backward_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_slot: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    e = rec.get(workload, {}).get(kernel_slot)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ cpu oracle
+def oracle_sample(w, budget_s: float, max_slices: int | None = None):
+    """Time the fp64 oracle on whole (batch, head) slices of workload w until
+    `budget_s` has elapsed (at least one slice).  Returns (TFLOP/s, slices, s)."""
+    import numpy as np
+    import oracle
+    from self_attention_backward_gb300.inputs import make_inputs
+    inp = make_inputs(w, BH=max_slices or w.BH)
+    done, t_total = 0, 0.0
+    while done < inp.packed.shape[0]:
+        p = inp.packed[done:done + 1].astype(np.float64)
+        vs = np.ascontiguousarray(p[:, 2:4].transpose(1, 0, 2, 3))
+        dos = np.stack([inp.do_lo[done:done + 1], inp.do_hi[done:done + 1]]).astype(np.float64)
+        t0 = time.perf_counter()
+        oracle.attn_bwd(p[:, 0], p[:, 1], vs, dos, inp.scale)
+        t_total += time.perf_counter() - t0
+        done += 1
+        if t_total >= budget_s:
+            break
+    flops = 12.0 * w.N * w.N * w.d * done
+    return flops / t_total / 1e12, done, t_total
+
+
+# ------------------------------------------------------------------ arms
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    if args.warmup > 0:                       # one untimed slice warms caches and threads
+        oracle_sample(w, 0.0, max_slices=1)
+    vals, t_all, slices = [], 0.0, 0
+    for _ in range(args.steps):
+        v, n, t = oracle_sample(w, 0.0, max_slices=1)
+        vals.append(v)
+        t_all += t
+        slices += n
+    value = 12.0 * w.N * w.N * w.d * slices / t_all / 1e12
+    sample = f"{slices} of {w.BH} (batch, head) slices of {w.name}, one per step, fp64"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_all / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": w.name, "B": w.B, "heads": w.heads, "N": w.N, "feature_map": w.fmap,
+            "head_dim": w.d, "storage": w.dtype, "scale": w.scale, "seed": w.seed,
+            "l2": f"flushed ({FLUSH_BYTES >> 20} MB write) before every timed step"}
+
+
+def device_inputs(w, device):
+    import torch
+    from self_attention_backward_gb300 import binding as B
+    from self_attention_backward_gb300.inputs import make_inputs
+    inp = make_inputs(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    dev = lambda a: torch.from_numpy(a).to(device).to(tdt).contiguous()  # noqa: E731
+    packed, do_lo, do_hi = dev(inp.packed), dev(inp.do_lo), dev(inp.do_hi)
+    o_lo, o_hi, lse = B.attn_fwd(packed, w.scale)
+    torch.cuda.synchronize()
+    return packed, o_lo, o_hi, lse, do_lo, do_hi
+
+
+def time_steps(w, bufs, steps, flush, device, algo):
+    """Per-step CUDA-event times (ms) of psa_attn_bwd on the current stream."""
+    import torch
+    from self_attention_backward_gb300 import binding as B
+    packed, o_lo, o_hi, lse, do_lo, do_hi = bufs
+    d_packed = torch.empty_like(packed)
+    ws = B.BwdWorkspace(device)
+    st = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(st)
+        B.attn_bwd(packed, o_lo, o_hi, lse, do_lo, do_hi, w.scale, d_packed=d_packed, workspace=ws, algo=algo)
+        b.record(st)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def run_ours(args, w):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from self_attention_backward_gb300.build import build
+    build()
+    from self_attention_backward_gb300 import binding as B
+    algo = {"auto": B.PSA_ALGO_AUTO, "simt": B.PSA_ALGO_SIMT, "tc": B.PSA_ALGO_TC}[args.algo]
+    peaks, peaks_src = read_peaks()
+
+    bufs = device_inputs(w, device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    time_steps(w, bufs, max(args.warmup, 3), flush, device, algo)       # warm-up
+    B.psa_attn_sync_status()
+
+    B.psa_attn_profile_read()
+    B.psa_attn_profile_enable(True)
+    with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local) as cs:
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        step_ms = time_steps(w, bufs, args.steps, flush, device, algo)
+        torch.cuda.synchronize()
+        barrier(world)
+        wall = time.perf_counter() - t0
+    B.psa_attn_profile_enable(False)
+    prof = B.psa_attn_profile_read()
+    B.psa_attn_sync_status()
+
+    ms_local = sum(step_ms) / len(step_ms)
+    ms = max_over_ranks(ms_local, world, device)
+    value = metric_flops(w) * world / (ms * 1e-3) / 1e12
+    launches = sum(n for _, n in prof.values())
+    # dominant kernel: largest total time in the timed region
+    dom = max((k for k in prof if prof[k][1] > 0), key=lambda k: prof[k][0])
+    dom_ms = prof[dom][0] / prof[dom][1]
+    t_roof, bound = roofline_time_s(w, peaks)
+    # algorithmic work of the dominant kernel per launch
+    used_algo = "tc" if (algo == B.PSA_ALGO_TC or (algo == B.PSA_ALGO_AUTO and B.psa_attn_bwd_workspace_bytes(
+        1, 1, 16, w.d, 1 if w.dtype == "bf16" else 0, B.PSA_ALGO_TC) > 0)) else "simt"
+    if bound == "tensor":
+        share = {"bwd_main": 12.0 if used_algo == "tc" else 10.0, "bwd_dq": 2.0}.get(dom, 0.0)
+        achieved = share / 12.0 * metric_flops(w) / (dom_ms * 1e-3) / 1e12
+        peak, unit = tensor_peak(peaks, w.dtype), "TFLOP/s"
+        peak_note = f"bf16_tflops (burst) of {peaks_src}"
+    else:
+        achieved = alg_bytes(w) / (dom_ms * 1e-3) / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+        peak_note = f"hbm_gbs of {peaks_src}"
+    traffic = recorded_traffic(dom, w.name)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": dict(workload_config(w), parallelism=f"replicas x{world}" if world > 1 else "single GPU",
+                       algo=used_algo),
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": traffic, "kernel": dom, "peak_source": peak_note},
+        "step_roofline_frac": t_roof / (ms * 1e-3),
+        "executed_tflops": value * 14.0 / 12.0 if used_algo == "tc" else value * 20.0 / 12.0,
+        "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]},
+        "gpu_launches": launches,
+        "wall_s_timed_region": wall,
+    }
+    clocks = cs.summary()
+    line["clocks"] = clocks
+
+    if rank == 0 and not args.no_secondary:
+        sec = {}
+        for name in SECONDARY:
+            from self_attention_backward_gb300.inputs import WORKLOADS
+            w2 = WORKLOADS[name]
+            b2 = device_inputs(w2, device)
+            time_steps(w2, b2, 3, flush, device, algo)
+            t2 = statistics.mean(time_steps(w2, b2, max(5, args.steps // 2), flush, device, algo))
+            tr, bd = roofline_time_s(w2, peaks)
+            sec[name] = {"tflops": metric_flops(w2) / (t2 * 1e-3) / 1e12, "ms": t2, "bound": bd,
+                         "roofline_frac": tr / (t2 * 1e-3)}
+            del b2
+        line["other_workloads"] = sec
+
+    if rank == 0:
+        line["e2e"] = run_e2e(w, args, device, algo)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v, n, t = oracle_sample(w, args.cpu_budget)
+        import oracle
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                                "sample": f"{n} of {w.BH} (batch, head) slices of {w.name}, fp64, {t:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(w, args, device, algo):
+    """Same metric through the public API on HOST buffers: per step the inputs
+    are copied host->device from pinned memory and d_packed device->host."""
+    import torch
+    from self_attention_backward_gb300 import binding as B
+    from self_attention_backward_gb300.inputs import make_inputs
+    inp = make_inputs(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    pin = lambda a: torch.from_numpy(a).to(tdt).pin_memory()  # noqa: E731
+    packed, do_lo, do_hi = pin(inp.packed), pin(inp.do_lo), pin(inp.do_hi)
+    o_lo_d, o_hi_d, lse_d = B.attn_fwd(packed.to(device), w.scale)
+    o_lo, o_hi, lse = o_lo_d.cpu().pin_memory(), o_hi_d.cpu().pin_memory(), lse_d.cpu().pin_memory()
+    out = torch.empty(packed.shape, dtype=tdt).pin_memory()
+    dt = B.PSA_BF16 if w.dtype == "bf16" else B.PSA_F32
+    runner = B.HostBwd(w.BH, w.N, w.d, dt, device=device, algo=algo)
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        runner(packed, o_lo, o_hi, lse, do_lo, do_hi, w.scale, out)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(args.steps):
+        runner(packed, o_lo, o_hi, lse, do_lo, do_hi, w.scale, out)
+    b.record(st)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    return {"value": metric_flops(w) / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": runner.h2d_bytes(), "d2h_bytes_per_step": runner.d2h_bytes()}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--algo", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    args = ap.parse_args(argv)
+    from self_attention_backward_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

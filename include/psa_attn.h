@@ -1,0 +1,149 @@
+/*
+ * psa_attn.h -- C ABI of the GB300 (sm_103a) PSA self-attention library.
+ *
+ * PSA attention runs two softmax-attention calls, "lo" and "hi", over one
+ * packed per-(batch, head) buffer.  The calls share the Q and K sections, and
+ * each owns one V section ("Struct PsaFa2Backward", vision_rs yolo attention
+ * psa page: description and "Atomicity" paragraphs).  It is self-attention:
+ * the query and key counts are both N (same page, description).  Because the
+ * two calls share Q, K and therefore one softmax P, this library runs them as
+ * ONE attention with a 2d-wide value [V_lo | V_hi]; the gradients it returns are
+ * exactly those of the two calls, with dQ and dK summed over both.
+ *
+ * Notation, per (b, h) slice, all matrices [N, d] row-major:
+ *   S = scale * Q K^T, LSE_i = ln sum_j exp(S_ij), P = exp(S - LSE 1^T),
+ *   O_lo = P V_lo, O_hi = P V_hi.
+ *
+ * Common conventions
+ *   - BH = B * heads slices; the slice index is the outermost index of every
+ *     tensor.  packed / d_packed are [BH, 4, N, d]: sections 0..3 are
+ *     Q, K, V_lo, V_hi (resp. dQ, dK, dV_lo, dV_hi).  o_lo, o_hi, do_lo, do_hi
+ *     are [BH, N, d]; lse is [BH, N] fp32 (natural log, always fp32, whatever
+ *     the storage type).  All contiguous, no padding.
+ *   - Storage dtype: PSA_F32 or PSA_BF16 for every non-lse tensor; arithmetic
+ *     accumulates in fp32.
+ *   - head_dim (d) is one of 16, 32, 64.
+ *   - All pointers are DEVICE pointers, 16-byte aligned.  The caller allocates
+ *     and owns every buffer, including the backward workspace; the library
+ *     allocates no device memory per call.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on it and do not synchronise the host.
+ *   - Return: 0 on success, a negative psa_status on error.  Arguments are
+ *     checked before anything is launched; on an argument error nothing is
+ *     launched and no buffer is touched.  psa_attn_last_error() returns a
+ *     message for the calling thread's last error.
+ *   - B*heads == 0 or N == 0 is a valid empty call (returns 0, launches nothing).
+ */
+#ifndef PSA_ATTN_H
+#define PSA_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PSA_F32 = 0, PSA_BF16 = 1 } psa_dtype;
+
+typedef enum {
+    PSA_OK = 0,
+    PSA_ERR_ARG = -1,          /* null pointer, negative size, non-finite scale, bad dtype */
+    PSA_ERR_ALIGN = -2,        /* a pointer is not 16-byte aligned */
+    PSA_ERR_UNSUPPORTED = -3,  /* head_dim not in {16, 32, 64}, or a size over the limits */
+    PSA_ERR_WORKSPACE = -4,    /* workspace missing or smaller than psa_attn_bwd_workspace_bytes */
+    PSA_ERR_CUDA = -5,         /* a CUDA launch / driver call failed (message has the CUDA error) */
+    PSA_ERR_TIMEOUT = -6       /* a device-side bounded wait gave up (see psa_attn_sync_status) */
+} psa_status;
+
+/* Backward kernel choice.  AUTO picks the tensor-core (tcgen05) path where it
+ * exists for the (dtype, head_dim) and the CUDA-core (SIMT) path elsewhere. */
+typedef enum { PSA_ALGO_AUTO = 0, PSA_ALGO_SIMT = 1, PSA_ALGO_TC = 2 } psa_algo;
+
+/*
+ * psa_attn_fwd -- PSA forward: O_lo = P V_lo, O_hi = P V_hi and LSE.
+ * Produces the forward outputs that the backward consumes; "Struct
+ * PsaFa2Backward", "Grid" paragraph (the backward shares the forward pass's
+ * decomposition).
+ *   packed  [BH,4,N,d] dtype, read
+ *   o_lo, o_hi [BH,N,d] dtype, written
+ *   lse     [BH,N] fp32, written (natural log of the softmax denominator of scale*q.k)
+ *   scale   softmax scale applied to q.k (finite)
+ */
+int psa_attn_fwd(const void* packed, void* o_lo, void* o_hi, float* lse,
+                 int B, int heads, int N, int head_dim, float scale,
+                 int dtype, void* stream);
+
+/*
+ * Bytes of device workspace psa_attn_bwd needs for these sizes and the kernel
+ * AUTO would pick (fp32 row statistics D and, on the tensor-core path, an fp32
+ * dQ accumulator).  Returns 0 for an empty or invalid problem.
+ */
+size_t psa_attn_bwd_workspace_bytes(int B, int heads, int N, int head_dim, int dtype);
+
+/*
+ * psa_attn_bwd -- PSA backward (the lo/hi pair of FA2 backward calls).
+ * "Struct PsaFa2Backward": description (recompute P from Q, K and the row
+ * statistics; dQ by iterating over keys, dK/dV by iterating over queries),
+ * "Atomicity" (dQ, dK summed over lo and hi; each call owns its dV section).
+ *   packed       [BH,4,N,d] dtype, read (Q, K, V_lo, V_hi)
+ *   o_lo, o_hi   [BH,N,d] dtype, read (forward outputs)
+ *   lse          [BH,N] fp32, read (from psa_attn_fwd)
+ *   do_lo, do_hi [BH,N,d] dtype, read (upstream gradients)
+ *   d_packed     [BH,4,N,d] dtype, OVERWRITTEN with dQ, dK, dV_lo, dV_hi
+ *                (the page's kernel adds into a zeroed buffer; this call writes
+ *                the gradients, so d_packed need not be zeroed first)
+ *   workspace    device scratch of at least workspace_bytes; contents on entry
+ *                are ignored, contents on exit are unspecified
+ * Calls that share a workspace must not overlap on the GPU.
+ */
+int psa_attn_bwd(const void* packed, const void* o_lo, const void* o_hi, const float* lse,
+                 const void* do_lo, const void* do_hi, void* d_packed,
+                 void* workspace, size_t workspace_bytes,
+                 int B, int heads, int N, int head_dim, float scale,
+                 int dtype, void* stream);
+
+/* Like psa_attn_bwd, with an explicit kernel choice (psa_algo).  PSA_ALGO_TC
+ * returns PSA_ERR_UNSUPPORTED where no tensor-core kernel exists for the
+ * (dtype, head_dim). */
+int psa_attn_bwd_algo(const void* packed, const void* o_lo, const void* o_hi, const float* lse,
+                      const void* do_lo, const void* do_hi, void* d_packed,
+                      void* workspace, size_t workspace_bytes,
+                      int B, int heads, int N, int head_dim, float scale,
+                      int dtype, int algo, void* stream);
+
+/* Workspace bytes for an explicit kernel choice (0 if unsupported). */
+size_t psa_attn_bwd_workspace_bytes_algo(int B, int heads, int N, int head_dim, int dtype, int algo);
+
+/*
+ * Synchronises `stream`, then reports whether any kernel of this library gave
+ * up on a bounded device-side wait since the last check (PSA_ERR_TIMEOUT, and
+ * the flag is cleared), or whether the stream has a CUDA error (PSA_ERR_CUDA).
+ * Returns 0 otherwise.
+ */
+int psa_attn_sync_status(void* stream);
+
+/*
+ * Kernel timing (instrumentation; it changes no result and skips no work).
+ * While enabled, every launch this library makes records a pair of CUDA events
+ * around itself on the call's stream, tagged with a slot: 0 = forward,
+ * 1 = backward preprocess (D), 2 = backward main (dK/dV, and dQ on the
+ * tensor-core path), 3 = backward dQ (CUDA-core path) / dQ finalize.
+ * psa_attn_profile_read() synchronises those events, writes per-slot total
+ * milliseconds and launch counts into the caller's arrays (length >= 4) and
+ * clears the records.  Returns the number of slots, or a negative psa_status.
+ */
+int psa_attn_profile_enable(int on);
+int psa_attn_profile_read(float* total_ms, int* launches, int n_slots);
+const char* psa_attn_profile_slot_name(int slot);
+
+/* Message for the calling thread's most recent error ("" if none). */
+const char* psa_attn_last_error(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int psa_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PSA_ATTN_H */

@@ -1,0 +1,249 @@
+"""ctypes binding of the C ABI in ``include/psa_attn.h`` (argument marshalling only).
+
+Every function here turns torch tensors into device pointers and sizes and
+calls the C entry point of the same name; all arithmetic runs in the CUDA
+library.  There is no fallback: if ``_psa_attn.so`` is missing, the first call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_psa_attn.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "psa_attn.h")
+
+PSA_F32, PSA_BF16 = 0, 1
+PSA_OK, PSA_ERR_ARG, PSA_ERR_ALIGN, PSA_ERR_UNSUPPORTED = 0, -1, -2, -3
+PSA_ERR_WORKSPACE, PSA_ERR_CUDA, PSA_ERR_TIMEOUT = -4, -5, -6
+PSA_ALGO_AUTO, PSA_ALGO_SIMT, PSA_ALGO_TC = 0, 1, 2
+
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_SIGS = {
+    "psa_attn_fwd": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp], _i),
+    "psa_attn_bwd_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
+    "psa_attn_bwd_workspace_bytes_algo": ([_i, _i, _i, _i, _i, _i], _sz),
+    "psa_attn_bwd": ([_vp] * 8 + [_sz, _i, _i, _i, _i, _f, _i, _vp], _i),
+    "psa_attn_bwd_algo": ([_vp] * 8 + [_sz, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
+    "psa_attn_sync_status": ([_vp], _i),
+    "psa_attn_profile_enable": ([_i], _i),
+    "psa_attn_profile_read": ([ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), _i], _i),
+    "psa_attn_profile_slot_name": ([_i], ctypes.c_char_p),
+    "psa_attn_last_error": ([], ctypes.c_char_p),
+    "psa_attn_version": ([], _i),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PsaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"psa status {code}: {msg}")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"CUDA library {LIB_PATH} is not built; run "
+                                   "`python -m self_attention_backward_gb300.build` (nvcc, sm_103a)")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (args, res) in _SIGS.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/psa_attn.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(psa_attn_\w+)\s*\(", text)))
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return PSA_F32
+    if t.dtype == torch.bfloat16:
+        return PSA_BF16
+    raise TypeError(f"unsupported storage dtype {t.dtype}")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int) -> int:
+    if rc != PSA_OK:
+        raise PsaError(rc, psa_attn_last_error())
+    return rc
+
+
+def psa_attn_last_error() -> str:
+    return lib().psa_attn_last_error().decode()
+
+
+def psa_attn_version() -> int:
+    return int(lib().psa_attn_version())
+
+
+def psa_attn_fwd(packed, o_lo, o_hi, lse, B, heads, N, head_dim, scale, dtype=None, stream=None,
+                 check=True) -> int:
+    dtype = _dtype_code(packed) if dtype is None else dtype
+    rc = lib().psa_attn_fwd(_ptr(packed), _ptr(o_lo), _ptr(o_hi), _ptr(lse), B, heads, N, head_dim,
+                            float(scale), dtype, _stream(stream))
+    return _check(rc) if check else rc
+
+
+def psa_attn_bwd_workspace_bytes(B, heads, N, head_dim, dtype, algo=PSA_ALGO_AUTO) -> int:
+    return int(lib().psa_attn_bwd_workspace_bytes_algo(B, heads, N, head_dim, dtype, algo))
+
+
+def psa_attn_bwd(packed, o_lo, o_hi, lse, do_lo, do_hi, d_packed, workspace, workspace_bytes,
+                 B, heads, N, head_dim, scale, dtype=None, stream=None, algo=PSA_ALGO_AUTO,
+                 check=True) -> int:
+    dtype = _dtype_code(packed) if dtype is None else dtype
+    rc = lib().psa_attn_bwd_algo(_ptr(packed), _ptr(o_lo), _ptr(o_hi), _ptr(lse), _ptr(do_lo), _ptr(do_hi),
+                                 _ptr(d_packed), _ptr(workspace), int(workspace_bytes), B, heads, N,
+                                 head_dim, float(scale), dtype, algo, _stream(stream))
+    return _check(rc) if check else rc
+
+
+def psa_attn_sync_status(stream=None, check=True) -> int:
+    rc = lib().psa_attn_sync_status(_stream(stream))
+    return _check(rc) if check else rc
+
+
+def psa_attn_profile_enable(on: bool = True) -> int:
+    return _check(lib().psa_attn_profile_enable(1 if on else 0))
+
+
+def psa_attn_profile_slot_name(slot: int) -> str:
+    return lib().psa_attn_profile_slot_name(slot).decode()
+
+
+def psa_attn_profile_read() -> dict:
+    """{slot name: (total ms, launches)} since the last read; clears the records."""
+    n = 4
+    ms = (ctypes.c_float * n)()
+    cnt = (ctypes.c_int * n)()
+    rc = lib().psa_attn_profile_read(ms, cnt, n)
+    if rc < 0:
+        raise PsaError(rc, psa_attn_last_error())
+    return {psa_attn_profile_slot_name(i): (float(ms[i]), int(cnt[i])) for i in range(rc)}
+
+
+# ----------------------------------------------------------------- helpers
+def _torch_dtype(dtype):
+    import torch
+    return {PSA_F32: torch.float32, PSA_BF16: torch.bfloat16}[dtype]
+
+
+def attn_fwd(packed, scale: float, stream=None):
+    """Allocates O_lo, O_hi, LSE on packed's device and runs psa_attn_fwd.
+
+    packed: [BH, 4, N, d] CUDA tensor (fp32 or bf16).  B is taken as BH, heads 1.
+    """
+    import torch
+    BH, four, N, d = packed.shape
+    assert four == 4 and packed.is_contiguous()
+    o_lo = torch.empty((BH, N, d), dtype=packed.dtype, device=packed.device)
+    o_hi = torch.empty_like(o_lo)
+    lse = torch.empty((BH, N), dtype=torch.float32, device=packed.device)
+    psa_attn_fwd(packed, o_lo, o_hi, lse, BH, 1, N, d, scale, stream=stream)
+    return o_lo, o_hi, lse
+
+
+class BwdWorkspace:
+    """A device workspace sized for psa_attn_bwd, grown on demand."""
+
+    def __init__(self, device="cuda"):
+        self.device = device
+        self.buf = None
+
+    def get(self, nbytes: int):
+        import torch
+        if nbytes == 0:
+            return None
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+def attn_bwd(packed, o_lo, o_hi, lse, do_lo, do_hi, scale: float, d_packed=None, workspace=None,
+             algo=PSA_ALGO_AUTO, stream=None):
+    """Runs psa_attn_bwd; returns d_packed [BH, 4, N, d] (dQ, dK, dV_lo, dV_hi)."""
+    import torch
+    BH, _, N, d = packed.shape
+    dt = _dtype_code(packed)
+    if d_packed is None:
+        d_packed = torch.empty_like(packed)
+    nbytes = psa_attn_bwd_workspace_bytes(BH, 1, N, d, dt, algo)
+    ws = (workspace or BwdWorkspace(packed.device)).get(nbytes)
+    psa_attn_bwd(packed, o_lo, o_hi, lse, do_lo, do_hi, d_packed, ws, nbytes, BH, 1, N, d, scale,
+                 dtype=dt, stream=stream, algo=algo)
+    return d_packed
+
+
+class HostBwd:
+    """psa_attn_bwd on HOST tensors: copies the inputs host->device, runs the
+    backward, copies d_packed device->host, all on one stream.  Host tensors
+    should be pinned for asynchronous copies.  Device staging buffers and the
+    workspace are allocated once, for one shape."""
+
+    def __init__(self, BH: int, N: int, d: int, dtype: int, device="cuda", algo=PSA_ALGO_AUTO):
+        import torch
+        tdt = _torch_dtype(dtype)
+        self.shape = (BH, N, d)
+        self.dtype, self.algo = dtype, algo
+        self.packed = torch.empty((BH, 4, N, d), dtype=tdt, device=device)
+        self.o_lo = torch.empty((BH, N, d), dtype=tdt, device=device)
+        self.o_hi = torch.empty_like(self.o_lo)
+        self.do_lo = torch.empty_like(self.o_lo)
+        self.do_hi = torch.empty_like(self.o_lo)
+        self.lse = torch.empty((BH, N), dtype=torch.float32, device=device)
+        self.d_packed = torch.empty_like(self.packed)
+        self.ws_bytes = psa_attn_bwd_workspace_bytes(BH, 1, N, d, dtype, algo)
+        self.ws = BwdWorkspace(device).get(self.ws_bytes)
+
+    def h2d_bytes(self) -> int:
+        ts = (self.packed, self.o_lo, self.o_hi, self.lse, self.do_lo, self.do_hi)
+        return sum(t.numel() * t.element_size() for t in ts)
+
+    def d2h_bytes(self) -> int:
+        return self.d_packed.numel() * self.d_packed.element_size()
+
+    def __call__(self, packed, o_lo, o_hi, lse, do_lo, do_hi, scale: float, out, stream=None):
+        BH, N, d = self.shape
+        for dst, src in ((self.packed, packed), (self.o_lo, o_lo), (self.o_hi, o_hi), (self.lse, lse),
+                         (self.do_lo, do_lo), (self.do_hi, do_hi)):
+            dst.copy_(src, non_blocking=True)
+        psa_attn_bwd(self.packed, self.o_lo, self.o_hi, self.lse, self.do_lo, self.do_hi, self.d_packed,
+                     self.ws, self.ws_bytes, BH, 1, N, d, scale, dtype=self.dtype, stream=stream,
+                     algo=self.algo)
+        out.copy_(self.d_packed, non_blocking=True)
+        return out

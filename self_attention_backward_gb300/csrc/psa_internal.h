@@ -1,0 +1,54 @@
+// psa_internal.h -- host-side interface between the C-ABI front end
+// (psa_attn.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <string>
+
+namespace psa {
+
+struct BwdArgs {
+    const void* packed;
+    const void* o_lo;
+    const void* o_hi;
+    const float* lse;
+    const void* do_lo;
+    const void* do_hi;
+    void* d_packed;
+    void* workspace;
+    size_t workspace_bytes;
+    long long BH;
+    int N;
+    int d;
+    float scale;
+    int dtype;
+    cudaStream_t stream;
+};
+
+// Kernel timing scope (psa_attn_profile_enable): records a CUDA event pair
+// around the launches made while it is alive, when profiling is on.
+enum ProfSlot { kSlotFwd = 0, kSlotPre = 1, kSlotMain = 2, kSlotDq = 3, kNumSlots = 4 };
+class ProfScope {
+  public:
+    ProfScope(int slot, cudaStream_t st);
+    ~ProfScope();
+    ProfScope(const ProfScope&) = delete;
+    ProfScope& operator=(const ProfScope&) = delete;
+
+  private:
+    int slot_;
+    cudaStream_t st_;
+    cudaEvent_t a_ = nullptr, b_ = nullptr;
+};
+
+// Tensor-core (tcgen05) backward: tc_bwd.cu.
+bool tc_supported(int dtype, int d);
+size_t tc_workspace_bytes(long long BH, int N, int d);
+// Returns 0 or a psa_status; `err` receives a message on failure.
+int tc_bwd_launch(const BwdArgs& a, std::string* err);
+// Reads and clears the device-side timeout flag of the tensor-core kernels
+// (call after the stream is synchronised).  Returns 1 if a wait gave up.
+int tc_take_device_error(std::string* err);
+
+}  // namespace psa

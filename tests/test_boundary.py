@@ -1,0 +1,111 @@
+"""The C-ABI library: it loads, exports every function include/psa_attn.h
+declares, and rejects bad arguments before launching anything (no GPU needed:
+every call below fails argument checks, so no CUDA call is made)."""
+import ctypes
+
+import pytest
+
+from self_attention_backward_gb300 import binding as B
+
+
+@pytest.fixture(scope="module")
+def lib():
+    try:
+        from self_attention_backward_gb300.build import build
+        build()
+    except Exception as e:  # nvcc missing is a hard failure for this repo
+        pytest.fail(f"CUDA library failed to build: {e}")
+    return B.lib()
+
+
+def test_exports_every_header_function(lib):
+    names = B.header_functions()
+    assert {"psa_attn_fwd", "psa_attn_bwd", "psa_attn_bwd_workspace_bytes", "psa_attn_last_error"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in B._SIGS, f"binding lacks a signature for {n}"
+
+
+def test_version(lib):
+    assert B.psa_attn_version() >= 100
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: the calls fail checks first
+
+
+def _fwd(**kw):
+    a = dict(packed=FAKE, o_lo=FAKE, o_hi=FAKE, lse=FAKE, B=1, heads=2, N=16, head_dim=16, scale=0.25,
+             dtype=B.PSA_F32, stream=0, check=False)
+    a.update(kw)
+    return B.psa_attn_fwd(**a)
+
+
+def _bwd(**kw):
+    a = dict(packed=FAKE, o_lo=FAKE, o_hi=FAKE, lse=FAKE, do_lo=FAKE, do_hi=FAKE, d_packed=FAKE,
+             workspace=FAKE, workspace_bytes=0, B=1, heads=2, N=16, head_dim=16, scale=0.25,
+             dtype=B.PSA_F32, stream=0, check=False)
+    a.update(kw)
+    return B.psa_attn_bwd(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=48), B.PSA_ERR_UNSUPPORTED),
+    (dict(head_dim=128), B.PSA_ERR_UNSUPPORTED),
+    (dict(N=-1), B.PSA_ERR_ARG),
+    (dict(B=-2), B.PSA_ERR_ARG),
+    (dict(dtype=7), B.PSA_ERR_ARG),
+    (dict(scale=float("nan")), B.PSA_ERR_ARG),
+    (dict(scale=float("inf")), B.PSA_ERR_ARG),
+    (dict(packed=None), B.PSA_ERR_ARG),
+    (dict(lse=None), B.PSA_ERR_ARG),
+    (dict(o_hi=FAKE + 4), B.PSA_ERR_ALIGN),
+    (dict(B=1 << 20, heads=1 << 10, N=1 << 12), B.PSA_ERR_UNSUPPORTED),
+])
+def test_fwd_rejects(lib, kw, code):
+    assert _fwd(**kw) == code
+    assert B.psa_attn_last_error() != ""
+
+
+def test_fwd_empty_is_ok(lib):
+    assert _fwd(N=0, packed=None, o_lo=None, o_hi=None, lse=None) == B.PSA_OK
+    assert _fwd(B=0) == B.PSA_OK
+    assert B.psa_attn_last_error() == ""
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d_packed=None), B.PSA_ERR_ARG),
+    (dict(do_hi=FAKE + 8), B.PSA_ERR_ALIGN),
+    (dict(workspace_bytes=0), B.PSA_ERR_WORKSPACE),
+    (dict(workspace=None, workspace_bytes=1 << 20), B.PSA_ERR_WORKSPACE),
+    (dict(workspace=FAKE + 2, workspace_bytes=1 << 20), B.PSA_ERR_ALIGN),
+    (dict(head_dim=8), B.PSA_ERR_UNSUPPORTED),
+])
+def test_bwd_rejects(lib, kw, code):
+    assert _bwd(**kw) == code
+
+
+def test_bwd_bad_algo(lib):
+    assert _bwd(algo=9, workspace_bytes=1 << 20) == B.PSA_ERR_ARG
+
+
+def test_bwd_tc_unsupported_for_fp32(lib):
+    assert _bwd(algo=B.PSA_ALGO_TC, dtype=B.PSA_F32, workspace_bytes=1 << 20) == B.PSA_ERR_UNSUPPORTED
+
+
+def test_workspace_bytes(lib):
+    assert B.psa_attn_bwd_workspace_bytes(1, 2, 16, 16, B.PSA_F32) >= 2 * 16 * 4
+    assert B.psa_attn_bwd_workspace_bytes(0, 2, 16, 16, B.PSA_F32) == 0
+    assert B.psa_attn_bwd_workspace_bytes(1, 2, 16, 48, B.PSA_F32) == 0
+    assert B.psa_attn_bwd_workspace_bytes(1, 2, 16, 16, B.PSA_F32, B.PSA_ALGO_SIMT) == 2 * 16 * 4
+    # the check does not clobber the thread's last error
+    _fwd(head_dim=48)
+    msg = B.psa_attn_last_error()
+    B.psa_attn_bwd_workspace_bytes(1, 2, 16, 48, B.PSA_F32)
+    assert B.psa_attn_last_error() == msg
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(B, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        B.lib()
