@@ -111,6 +111,40 @@ int psa_attn_bwd_algo(const void* packed, const void* o_lo, const void* o_hi, co
                       int B, int heads, int N, int head_dim, float scale,
                       int dtype, int algo, void* stream);
 
+/*
+ * psa_attn_bwd_noalloc -- the backward for callers that cannot allocate device
+ * memory.  (The pages have no counterpart of this entry point; it is a
+ * convenience of this library.)
+ *
+ * Some callers cannot call cudaMalloc or any allocating routine: a plugin that
+ * is handed only its input and output buffers by a host runtime that owns all
+ * device memory, or an application whose memory budget is fixed after start-up
+ * and forbids libraries from allocating later.  psa_attn_bwd needs a workspace
+ * from its caller; this variant needs none.  It runs the CUDA-core backward
+ * (PSA_ALGO_SIMT) and keeps its only scratch -- the fp32 row statistics D, one
+ * value per query row -- in a static array inside this library's device
+ * memory, 2 MiB per GPU, which every GPU that loads the library holds until the
+ * process exits.  The call itself allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine).
+ *   Arguments and results are those of psa_attn_bwd without the workspace.
+ *   Limit: B*heads*N <= psa_attn_bwd_noalloc_max_rows() (524288); larger
+ *   problems return PSA_ERR_UNSUPPORTED before anything is launched.
+ *   Set-up: the first call on each device looks up the device address of the
+ *   static array (with that device current) and caches it; make that first
+ *   call before any stream capture.
+ *   Sharing: every call on a device uses the same array.  D is rewritten in
+ *   full by each call before it is read, so a call never sees an earlier
+ *   call's values, but calls that overlap on the GPU (different streams, or
+ *   different host threads, without ordering between them) race on it.
+ */
+int psa_attn_bwd_noalloc(const void* packed, const void* o_lo, const void* o_hi, const float* lse,
+                         const void* do_lo, const void* do_hi, void* d_packed,
+                         int B, int heads, int N, int head_dim, float scale,
+                         int dtype, void* stream);
+
+/* Largest B*heads*N psa_attn_bwd_noalloc accepts. */
+long long psa_attn_bwd_noalloc_max_rows(void);
+
 /* Workspace bytes for an explicit kernel choice (0 if unsupported). */
 size_t psa_attn_bwd_workspace_bytes_algo(int B, int heads, int N, int head_dim, int dtype, int algo);
 

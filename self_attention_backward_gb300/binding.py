@@ -28,6 +28,8 @@ _SIGS = {
     "psa_attn_bwd_workspace_bytes_algo": ([_i, _i, _i, _i, _i, _i], _sz),
     "psa_attn_bwd": ([_vp] * 8 + [_sz, _i, _i, _i, _i, _f, _i, _vp], _i),
     "psa_attn_bwd_algo": ([_vp] * 8 + [_sz, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
+    "psa_attn_bwd_noalloc": ([_vp] * 7 + [_i, _i, _i, _i, _f, _i, _vp], _i),
+    "psa_attn_bwd_noalloc_max_rows": ([], ctypes.c_longlong),
     "psa_attn_sync_status": ([_vp], _i),
     "psa_attn_profile_enable": ([_i], _i),
     "psa_attn_profile_read": ([ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), _i], _i),
@@ -131,6 +133,20 @@ def psa_attn_bwd(packed, o_lo, o_hi, lse, do_lo, do_hi, d_packed, workspace, wor
                                  _ptr(d_packed), _ptr(workspace), int(workspace_bytes), B, heads, N,
                                  head_dim, float(scale), dtype, algo, _stream(stream))
     return _check(rc) if check else rc
+
+
+def psa_attn_bwd_noalloc(packed, o_lo, o_hi, lse, do_lo, do_hi, d_packed, B, heads, N, head_dim, scale,
+                         dtype=None, stream=None, check=True) -> int:
+    """Backward without a workspace argument: its scratch is a static array in
+    the library (see include/psa_attn.h).  For callers that cannot allocate."""
+    dtype = _dtype_code(packed) if dtype is None else dtype
+    rc = lib().psa_attn_bwd_noalloc(_ptr(packed), _ptr(o_lo), _ptr(o_hi), _ptr(lse), _ptr(do_lo), _ptr(do_hi),
+                                    _ptr(d_packed), B, heads, N, head_dim, float(scale), dtype, _stream(stream))
+    return _check(rc) if check else rc
+
+
+def psa_attn_bwd_noalloc_max_rows() -> int:
+    return int(lib().psa_attn_bwd_noalloc_max_rows())
 
 
 def psa_attn_sync_status(stream=None, check=True) -> int:

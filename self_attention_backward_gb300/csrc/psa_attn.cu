@@ -167,6 +167,11 @@ size_t workspace_for(const Shape& s, int dtype, int algo) {
 
 }  // namespace
 
+int psa::set_last_error(int code, const std::string& msg) {
+    g_last_error = msg;
+    return code;
+}
+
 extern "C" {
 
 int psa_attn_version(void) { return 100; }

@@ -51,4 +51,8 @@ int tc_bwd_launch(const BwdArgs& a, std::string* err);
 // (call after the stream is synchronised).  Returns 1 if a wait gave up.
 int tc_take_device_error(std::string* err);
 
+// Sets the calling thread's psa_attn_last_error() message ("" clears it) and
+// returns `code`; for entry points defined outside psa_attn.cu.
+int set_last_error(int code, const std::string& msg);
+
 }  // namespace psa
