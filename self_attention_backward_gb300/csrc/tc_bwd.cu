@@ -8,24 +8,40 @@
 // summed (the page's atomic_add into the shared dQ/dK sections is not needed
 // for that).
 //
-// Decomposition: one CTA per (batch*head, 128-key tile).  The CTA keeps K_j,
-// V_lo,j, V_hi,j in shared memory and its dV_lo, dV_hi, dK accumulators in
-// TMEM, and walks over all 128-query tiles i (the page's "dK_n / dV_n by
-// iterating over all Q rows"):
-//   S^T  = K_j Q_i^T                 (M = 128 keys, N = 128 queries, K = d)
-//   dP^T = V_lo,j dO_lo,i^T + V_hi,j dO_hi,i^T          (K = 2d)
-//   P^T  = exp2(S^T * scale*log2e - LSE_i*log2e),  dS^T = P^T o (dP^T - D_i)
-//   dV_h += P^T dO_h,i ;  dK += dS^T Q_i ;  dQ_i(partial) = dS_i K_j
-// The dQ partial of each (key tile, query tile) is added into an fp32
-// accumulator in the workspace; a last kernel scales and casts it into d_packed.
+// Decomposition: one CTA per (batch*head, 128-key tile j).  The CTA keeps K_j,
+// V_lo,j, V_hi,j in shared memory and its dV_lo|dV_hi and dK accumulators in
+// TMEM, and walks over all queries (the page's "dK_n / dV_n by iterating over
+// all Q rows") in 64-query sub-tiles u:
+//   S^T  = K_j Q_u^T                 (M = 128 keys, N = 64 queries, K = d)
+//   dP^T = V_lo,j dO_lo,u^T + V_hi,j dO_hi,u^T          (K = 2d)
+//   P^T  = exp2(S^T * scale*log2e - LSE*log2e),  dS^T = P^T o (dP^T - D)
+//   [dV_lo | dV_hi] += P^T [dO_lo,u | dO_hi,u]          (one N = 2d MMA)
+//   dK += dS^T Q_u
+// and per pair of sub-tiles (128 queries g), dQ_g(partial) = dS_g K_j, added
+// into an fp32 accumulator in the workspace; a last kernel scales and casts it
+// into d_packed.
 //
-// Warp roles (320 threads): warp 0 TMA producer, warp 1 MMA issuer (one
-// thread) and TMEM owner, warps 2-5 softmax-gradient (one key row per
-// thread), warps 6-9 dQ drain (one query row per thread).
+// Pipelining.  S^T/dP^T are double-buffered in TMEM (buffer u & 1) and two
+// softmax-gradient warpgroups take alternate sub-tiles, so the tensor core
+// works on one sub-tile while a warpgroup turns the previous S/dP into P and
+// dS.  dS^T lives in a 4-block shared ring (u & 3), so a pair's dS stays intact
+// until its dQ MMA has read it.  For d <= 32, P^T goes to a 4-slot TMEM ring
+// (bf16 pairs, the A operand of the dV MMA) and S/dP of sub-tile u+2 is issued
+// before dV/dK of u; for d = 64 the accumulators fill TMEM, so P^T goes to a
+// 2-block shared ring and S/dP(u+2) is issued after dV/dK/dQ(u).
+//
+// Cost model that shaped it (measured on GB300): a tcgen05.mma with M = 128,
+// K = 16 costs about max(46, N/2) cycles, so the MMA count, not the flop
+// count, bounds small head dims; the single issuing thread precomputes every
+// descriptor so that issuing an MMA is one add per operand.
+//
+// Warp roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer (one
+// thread) and TMEM owner, warps 2-5 / 6-9 softmax-gradient warpgroups 0 / 1
+// (one key row per thread), warps 10-13 dQ drain (one query row per thread).
 //
 // Every mbarrier wait is bounded (kTimeoutNs); on timeout the CTA sets a device
 // error word (read by psa_attn_sync_status), skips the rest of its work, waits
-// (bounded) for its own TMA copies in flight, frees its TMEM and exits.
+// (bounded) for its own TMA copies and MMAs in flight, frees its TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -40,6 +56,8 @@
 #include "psa_internal.h"
 #include "tc_ptx.cuh"
 
+#pragma nv_diag_suppress 177  // per-variant tile constants not all used by every head_dim
+
 namespace psa {
 namespace {
 
@@ -49,37 +67,45 @@ using bf16 = __nv_bfloat16;
 __device__ int g_tc_error = 0;  // 0 = fine; else (1 + role) << 24 | tile
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 
 template <int D>
 struct Cfg {
-    static constexpr int BM = 128;            // keys per CTA (MMA M)
-    static constexpr int BQ = 128;            // queries per tile
-    static constexpr int ROWB = D * 2;        // bytes per [*, D] bf16 row
-    static constexpr int TILE = 128 * ROWB;   // bytes per [128, D] tile
+    static constexpr bool kPT = D <= 32;           // P^T in TMEM (else shared memory)
+    static constexpr int BM = 128;                 // keys per CTA (MMA M)
+    static constexpr int BS = 64;                  // queries per sub-tile
+    static constexpr int ROWB = D * 2;             // bytes per [*, D] bf16 row
+    static constexpr int KTILE = BM * ROWB;        // [128, D] tile
+    static constexpr int QTILE = BS * ROWB;        // [64, D] tile
+    static constexpr int NST = kPT ? 4 : 3;        // Q/dO stages
     static constexpr uint32_t SW = D == 64 ? 2u : D == 32 ? 4u : 6u;  // swizzle code of [*, D] tiles
     static constexpr int OFF_K = 0;
-    static constexpr int OFF_VL = TILE;
-    static constexpr int OFF_VH = 2 * TILE;
-    static constexpr int OFF_STAGE = 3 * TILE;     // stage s: Q, dO_lo, dO_hi at +s*3*TILE
-    static constexpr int STAGE = 3 * TILE;
-    static constexpr int OFF_PT = 9 * TILE;        // P^T  [128 keys][128 queries] bf16, 2 x 16 KB blocks
-    static constexpr int OFF_DST = OFF_PT + 32768; // dS^T same layout
-    static constexpr int OFF_L2 = OFF_DST + 32768; // 2 stages x 128 fp32: LSE * log2(e)
-    static constexpr int OFF_DD = OFF_L2 + 1024;   // 2 stages x 128 fp32: D
-    static constexpr int OFF_BAR = OFF_DD + 1024;  // 16 mbarriers
-    static constexpr int OFF_MISC = OFF_BAR + 128;
+    static constexpr int OFF_VL = KTILE;
+    static constexpr int OFF_VH = 2 * KTILE;
+    static constexpr int OFF_STAGE = 3 * KTILE;    // stage s: Q, dO_lo, dO_hi at +s*STAGE
+    static constexpr int STAGE = 3 * QTILE;
+    static constexpr int OFF_DS = OFF_STAGE + NST * STAGE;  // dS^T ring: 4 x [128 keys][64 queries] bf16
+    static constexpr int OFF_P = OFF_DS + 4 * 16384;        // P^T ring (shared-memory variant): 2 blocks
+    static constexpr int OFF_L2 = OFF_P + (kPT ? 0 : 2 * 16384);  // NST x 64 fp32: LSE * log2(e)
+    static constexpr int OFF_DD = OFF_L2 + NST * 256;      // NST x 64 fp32: D
+    static constexpr int OFF_BAR = OFF_DD + NST * 256;     // mbarriers
+    static constexpr int OFF_MISC = OFF_BAR + 256;
     static constexpr int USED = OFF_MISC + 64;
-    // + 1 KB for aligning the dynamic smem base to 1024; at least 116 KB so
-    // that one CTA owns an SM (its TMEM allocation is all 512 columns)
+    // + 1 KB to align the base to 1024; at least 116 KB so that one CTA owns
+    // an SM (its TMEM allocation is all 512 columns)
     static constexpr int SMEM = (USED + 1024) > 118784 ? (USED + 1024) : 118784;
-    // TMEM columns (fp32): S^T, dP^T, dV_lo, dV_hi, dK, dQ
-    static constexpr uint32_t C_S = 0, C_DP = 128, C_DVL = 256, C_DVH = 256 + D, C_DK = 256 + 2 * D,
-                              C_DQ = 256 + 3 * D;
+    // TMEM columns (fp32): buffer b = [128b, 128b+128): S^T (64), dP^T (64);
+    // then P^T ring (4 x 32 columns of bf16 pairs, d <= 32 only), dV_lo|dV_hi, dK, dQ
+    static constexpr uint32_t C_P = 256;
+    static constexpr uint32_t C_DV = kPT ? 384 : 256;
+    static constexpr uint32_t C_DK = C_DV + 2 * D, C_DQ = C_DV + 3 * D;
     static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(C_DQ + D <= TMEM_COLS, "TMEM budget");
+    static_assert(USED + 1024 <= 232448, "shared memory budget");
 };
 
-enum Bar { B_KV = 0, B_QF0 = 1, B_QE0 = 3, B_SF = 5, B_PF = 6, B_DQF = 7, B_DQE = 8, B_ACC = 9 };
+// barrier indices
+enum { B_KV = 0, B_SF = 1, B_PF = 3, B_DQF = 5, B_DQE = 6, B_ACC = 7, B_QF = 8, B_QE = 12 };
 
 struct Sync {
     uint32_t bar0;
@@ -89,7 +115,7 @@ struct Sync {
 
 // Bounded wait on a barrier phase, by one thread.  Returns false on timeout or
 // when another thread of the CTA has already aborted.
-__device__ __noinline__ bool wait_bounded(const Sync& s, uint32_t bar, uint32_t parity, int role, int tile) {
+__device__ __noinline__ bool wait_slow(const Sync& s, uint32_t bar, uint32_t parity, int role, int tile) {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -106,6 +132,11 @@ __device__ __noinline__ bool wait_bounded(const Sync& s, uint32_t bar, uint32_t 
         }
     }
 }
+// Fast path first (the phase is often already complete), then the bounded loop.
+__device__ __forceinline__ bool wait_bounded(const Sync& s, uint32_t bar, uint32_t parity, int role, int tile) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(s, bar, parity, role, tile);
+}
 
 // Whole-warp wait: every lane waits, the warp agrees on the outcome.
 __device__ __forceinline__ bool warp_wait(const Sync& s, uint32_t bar, uint32_t parity, int role, int tile) {
@@ -113,12 +144,18 @@ __device__ __forceinline__ bool warp_wait(const Sync& s, uint32_t bar, uint32_t 
     return __all_sync(0xffffffffu, ok);
 }
 
-// Wait without the abort short-cut (used only to drain copies after an abort).
+// Wait without the abort short-cut (used only to drain work after an abort).
 __device__ bool wait_drain(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity))
         if (globaltimer_ns() - t0 > kTimeoutNs) return false;
     return true;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 template <int D>
@@ -136,13 +173,36 @@ __device__ __forceinline__ void tmem_ld_row(uint32_t taddr, uint32_t* v) {
     }
 }
 
+// P and dS of one 32-query chunk of this thread's key row, packed to bf16
+// pairs: P = exp2(S * scale*log2e - L), dS = P (dP - D).
+template <bool MASK>
+__device__ __forceinline__ void softmax_vals(const uint32_t (&sr)[32], const uint32_t (&pr)[32], const float* L2s,
+                                             const float* Ds, float scale_log2, bool kvalid, uint32_t (&pk)[16],
+                                             uint32_t (&dk)[16]) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(L2s + e);
+        const float4 d4 = *reinterpret_cast<const float4*>(Ds + e);
+        float p0 = ex2_approx(fmaf(__uint_as_float(sr[e + 0]), scale_log2, -l4.x));
+        float p1 = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), scale_log2, -l4.y));
+        float p2 = ex2_approx(fmaf(__uint_as_float(sr[e + 2]), scale_log2, -l4.z));
+        float p3 = ex2_approx(fmaf(__uint_as_float(sr[e + 3]), scale_log2, -l4.w));
+        if (MASK && !kvalid) p0 = p1 = p2 = p3 = 0.f;
+        pk[e / 2] = pack_bf16x2(p0, p1);
+        pk[e / 2 + 1] = pack_bf16x2(p2, p3);
+        dk[e / 2] = pack_bf16x2(p0 * (__uint_as_float(pr[e + 0]) - d4.x), p1 * (__uint_as_float(pr[e + 1]) - d4.y));
+        dk[e / 2 + 1] =
+            pack_bf16x2(p2 * (__uint_as_float(pr[e + 2]) - d4.z), p3 * (__uint_as_float(pr[e + 3]) - d4.w));
+    }
+}
+
 // ---------------------------------------------------------------- main kernel
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-bwd_main_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_constant__ CUtensorMap tm_do_lo,
-                const __grid_constant__ CUtensorMap tm_do_hi, const float* __restrict__ lse,
-                const float* __restrict__ Drow, float* __restrict__ dq_acc, bf16* __restrict__ d_packed, int N,
-                int nkt, int nqt, float scale, float scale_log2) {
+bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
+                const __grid_constant__ CUtensorMap tm_do_lo, const __grid_constant__ CUtensorMap tm_do_hi,
+                const float* __restrict__ lse, const float* __restrict__ Drow, float* __restrict__ dq_acc,
+                bf16* __restrict__ d_packed, int N, int nkt, float scale, float scale_log2) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -153,24 +213,34 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_cons
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x / nkt, kt = blockIdx.x % nkt;
     const int k0 = kt * C::BM;
+    const int nsub = (N + C::BS - 1) / C::BS;     // 64-query sub-tiles
+    const int ngrp = (nsub + 1) / 2;              // 128-query groups (dQ granularity)
 
     if (threadIdx.x == 0) {
         mbar_init(sy.bar(B_KV), 1);
-        mbar_init(sy.bar(B_QF0), 32);
-        mbar_init(sy.bar(B_QF0 + 1), 32);
-        mbar_init(sy.bar(B_QE0), 1);
-        mbar_init(sy.bar(B_QE0 + 1), 1);
         mbar_init(sy.bar(B_SF), 1);
+        mbar_init(sy.bar(B_SF + 1), 1);
         mbar_init(sy.bar(B_PF), 128);
+        mbar_init(sy.bar(B_PF + 1), 128);
         mbar_init(sy.bar(B_DQF), 1);
         mbar_init(sy.bar(B_DQE), 128);
         mbar_init(sy.bar(B_ACC), 1);
+        for (int s = 0; s < C::NST; ++s) {
+            mbar_init(sy.bar(B_QF + s), 32);
+            mbar_init(sy.bar(B_QE + s), 1);
+        }
         *sy.abort = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tm_packed);
+        tma_prefetch_desc(&tm_kv);
+        tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_do_lo);
         tma_prefetch_desc(&tm_do_hi);
     }
+    // the dS ring starts zeroed: a last, half-filled 128-query group reads a
+    // block no sub-tile wrote (rows of queries >= N, discarded, but finite)
+    for (int x = threadIdx.x; x < 4 * 16384 / 16; x += kThreads)
+        st_shared_v4(sb + C::OFF_DS + 16 * x, 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
@@ -180,198 +250,225 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_cons
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // issued-copy bookkeeping for the abort drain (producer lane 0 only)
-    int last_issued[2] = {-1, -1};
-
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        int last_issued[C::NST];
+#pragma unroll
+        for (int s = 0; s < C::NST; ++s) last_issued[s] = -1;
         if (lane == 0) {
-            mbar_arrive_expect_tx(sy.bar(B_KV), 3 * C::TILE);
-            tma_load_3d(sb + C::OFF_K, &tm_packed, 0, k0, bh * 4 + 1, sy.bar(B_KV));
-            tma_load_3d(sb + C::OFF_VL, &tm_packed, 0, k0, bh * 4 + 2, sy.bar(B_KV));
-            tma_load_3d(sb + C::OFF_VH, &tm_packed, 0, k0, bh * 4 + 3, sy.bar(B_KV));
+            mbar_arrive_expect_tx(sy.bar(B_KV), 3 * C::KTILE);
+            tma_load_3d(sb + C::OFF_K, &tm_kv, 0, k0, bh * 4 + 1, sy.bar(B_KV));
+            tma_load_3d(sb + C::OFF_VL, &tm_kv, 0, k0, bh * 4 + 2, sy.bar(B_KV));
+            tma_load_3d(sb + C::OFF_VH, &tm_kv, 0, k0, bh * 4 + 3, sy.bar(B_KV));
         }
         float* L2s = reinterpret_cast<float*>(smem + C::OFF_L2);
         float* Ds = reinterpret_cast<float*>(smem + C::OFF_DD);
-        for (int t = 0; t < nqt; ++t) {
-            const int s = t & 1;
-            if (!warp_wait(sy, sy.bar(B_QE0 + s), ((t >> 1) & 1) ^ 1, 0, t)) break;
+        int s = 0, ph = 0;
+        for (int u = 0; u < nsub; ++u) {
+            if (!warp_wait(sy, sy.bar(B_QE + s), ph ^ 1, 0, u)) break;
             if (lane == 0) {
                 const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE;
-                mbar_expect_tx(sy.bar(B_QF0 + s), 3 * C::TILE);
-                tma_load_3d(st, &tm_packed, 0, t * C::BQ, bh * 4 + 0, sy.bar(B_QF0 + s));
-                tma_load_3d(st + C::TILE, &tm_do_lo, 0, t * C::BQ, bh, sy.bar(B_QF0 + s));
-                tma_load_3d(st + 2 * C::TILE, &tm_do_hi, 0, t * C::BQ, bh, sy.bar(B_QF0 + s));
-                last_issued[s] = t;
+                mbar_expect_tx(sy.bar(B_QF + s), 3 * C::QTILE);
+                tma_load_3d(st, &tm_q, 0, u * C::BS, bh * 4 + 0, sy.bar(B_QF + s));
+                tma_load_3d(st + C::QTILE, &tm_do_lo, 0, u * C::BS, bh, sy.bar(B_QF + s));
+                tma_load_3d(st + 2 * C::QTILE, &tm_do_hi, 0, u * C::BS, bh, sy.bar(B_QF + s));
             }
-            // row statistics of the 128 queries: 4 per lane; padded rows get
+#pragma unroll
+            for (int x = 0; x < C::NST; ++x)
+                if (x == s) last_issued[x] = u;
+            // row statistics of the 64 queries, 2 per lane; padded rows get
             // LSE = +inf (so P = 0) and D = 0
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int q = lane * 4 + e;
-                const int i = t * C::BQ + q;
+            for (int e = 0; e < 2; ++e) {
+                const int q = lane * 2 + e;
+                const int i = u * C::BS + q;
                 const bool v = i < N;
-                L2s[s * 128 + q] = v ? lse[(size_t)bh * N + i] * kLog2e : INFINITY;
-                Ds[s * 128 + q] = v ? Drow[(size_t)bh * N + i] : 0.f;
+                L2s[s * 64 + q] = v ? lse[(size_t)bh * N + i] * kLog2e : INFINITY;
+                Ds[s * 64 + q] = v ? Drow[(size_t)bh * N + i] : 0.f;
             }
-            mbar_arrive(sy.bar(B_QF0 + s));
+            mbar_arrive(sy.bar(B_QF + s));
+            if (++s == C::NST) { s = 0; ph ^= 1; }
+        }
+        __syncwarp();
+        if (*sy.abort && lane == 0) {
+            // let this CTA's own copies land before its shared memory is released
+            wait_drain(sy.bar(B_KV), 0);
+#pragma unroll
+            for (int x = 0; x < C::NST; ++x)
+                if (last_issued[x] >= 0) wait_drain(sy.bar(B_QF + x), (last_issued[x] / C::NST) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t ID_S = idesc_bf16(128, 128, 0, 0);   // S^T, dP^T
-            constexpr uint32_t ID_KN = idesc_bf16(128, D, 0, 1);    // dV, dK: A K-major, B MN-major
-            constexpr uint32_t ID_DQ = idesc_bf16(128, D, 1, 1);    // dQ: A, B MN-major
-            const uint32_t sK = sb + C::OFF_K, sVL = sb + C::OFF_VL, sVH = sb + C::OFF_VH;
-            const uint32_t sPT = sb + C::OFF_PT, sDST = sb + C::OFF_DST;
-            auto issue_s_dp = [&](int s) {
-                const uint32_t sQ = sb + C::OFF_STAGE + s * C::STAGE;
-                const uint32_t sGL = sQ + C::TILE, sGH = sQ + 2 * C::TILE;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16_ss(tmem + C::C_S, smem_desc(sK + 32 * kk, 16, 8 * C::ROWB, C::SW),
-                                smem_desc(sQ + 32 * kk, 16, 8 * C::ROWB, C::SW), ID_S, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16_ss(tmem + C::C_DP, smem_desc(sVL + 32 * kk, 16, 8 * C::ROWB, C::SW),
-                                smem_desc(sGL + 32 * kk, 16, 8 * C::ROWB, C::SW), ID_S, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16_ss(tmem + C::C_DP, smem_desc(sVH + 32 * kk, 16, 8 * C::ROWB, C::SW),
-                                smem_desc(sGH + 32 * kk, 16, 8 * C::ROWB, C::SW), ID_S, 1);
-            };
-            bool ok = wait_bounded(sy, sy.bar(B_KV), 0, 1, -1) && wait_bounded(sy, sy.bar(B_QF0), 0, 1, 0);
-            if (ok) {
+            constexpr uint32_t ID_S = idesc_bf16(128, 64, 0, 0);     // S^T, dP^T: 64 queries
+            constexpr uint32_t ID_DV = idesc_bf16(128, 2 * D, 0, 1); // dV_lo | dV_hi: B MN-major
+            constexpr uint32_t ID_DK = idesc_bf16(128, D, 0, 1);     // dK: A K-major, B MN-major
+            constexpr uint32_t ID_DQ = idesc_bf16(128, D, 1, 1);     // dQ: A, B MN-major
+            constexpr uint32_t SBO = 8 * C::ROWB;
+            constexpr uint32_t KSTEP = (16 * C::ROWB) >> 4;          // 16 rows, in descriptor address units
+            // every descriptor is built once; an MMA adds its k-step offset to the address field
+            const uint64_t dK = smem_desc(sb + C::OFF_K, 16, SBO, C::SW);
+            const uint64_t dVL = smem_desc(sb + C::OFF_VL, 16, SBO, C::SW);
+            const uint64_t dVH = smem_desc(sb + C::OFF_VH, 16, SBO, C::SW);
+            const uint64_t dStage0 = smem_desc(sb + C::OFF_STAGE, 16, SBO, C::SW);
+            const uint64_t dStage0mn = smem_desc(sb + C::OFF_STAGE + C::QTILE, C::QTILE, SBO, C::SW);
+            const uint64_t dDS0 = smem_desc(sb + C::OFF_DS, 16, 1024, 2);
+            const uint64_t dDS0mn = smem_desc(sb + C::OFF_DS, 16384, 1024, 2);
+            const uint64_t dP0 = smem_desc(sb + C::OFF_P, 16, 1024, 2);
+            constexpr uint32_t STAGE_U = C::STAGE >> 4, QTILE_U = C::QTILE >> 4, BLK_U = 16384 >> 4;
+
+            auto issue_s_dp = [&](int u) -> bool {
+                const int s = u % C::NST;
+                if (!wait_bounded(sy, sy.bar(B_QF + s), (u / C::NST) & 1, 1, u)) return false;
                 tc_fence_after();
-                issue_s_dp(0);
-                mma_commit(sy.bar(B_SF));
-            }
-            for (int t = 0; t < nqt && ok; ++t) {
-                const int s = t & 1;
-                ok = wait_bounded(sy, sy.bar(B_PF), t & 1, 1, t);
-                if (ok && t > 0) ok = wait_bounded(sy, sy.bar(B_DQE), (t - 1) & 1, 1, t);
+                const uint64_t dQs = dStage0 + STAGE_U * s;
+                const uint32_t tS = tmem + 128u * (u & 1), tDP = tS + 64;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) mma_bf16_ss(tS, dK + 2 * kk, dQs + 2 * kk, ID_S, kk);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16_ss(tDP, dVL + 2 * kk, dQs + QTILE_U + 2 * kk, ID_S, kk);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16_ss(tDP, dVH + 2 * kk, dQs + 2 * QTILE_U + 2 * kk, ID_S, 1);
+                mma_commit(sy.bar(B_SF + (u & 1)));
+                return true;
+            };
+            // dV, dK of sub-tile u (A = P^T, dS^T over 64 queries = 4 k-steps)
+            auto issue_dv_dk = [&](int u) {
+                const int s = u % C::NST;
+                const uint64_t dGmn = dStage0mn + STAGE_U * s;      // [dO_lo | dO_hi], MN-major
+                const uint64_t dQmn = dStage0 + STAGE_U * s;        // Q rows, MN-major
+                const uint64_t dDS = dDS0 + BLK_U * (u & 3);
+#pragma unroll
+                for (int kk = 0; kk < C::BS / 16; ++kk) {
+                    const uint32_t acc = (u > 0 || kk > 0) ? 1u : 0u;
+                    if constexpr (C::kPT)
+                        mma_bf16_ts(tmem + C::C_DV, tmem + C::C_P + 32 * (u & 3) + 8 * kk, dGmn + KSTEP * kk, ID_DV,
+                                    acc);
+                    else
+                        mma_bf16_ss(tmem + C::C_DV, dP0 + BLK_U * (u & 1) + 2 * kk, dGmn + KSTEP * kk, ID_DV, acc);
+                    mma_bf16_ss(tmem + C::C_DK, dDS + 2 * kk, dQmn + KSTEP * kk, ID_DK, acc);
+                }
+                mma_commit(sy.bar(B_QE + s));
+            };
+            // dQ of the 128-query group g: A = dS (queries x keys) read MN-major from the
+            // pair's two dS^T blocks (16 KB apart); B = K_j rows (MN-major)
+            auto issue_dq = [&](int g) {
+                const uint64_t dA = dDS0mn + BLK_U * ((2 * g) & 3);
+#pragma unroll
+                for (int kk = 0; kk < C::BM / 16; ++kk)
+                    mma_bf16_ss(tmem + C::C_DQ, dA + 128 * kk, dK + KSTEP * kk, ID_DQ, kk);
+                mma_commit(sy.bar(B_DQF));
+            };
+
+            bool ok = wait_bounded(sy, sy.bar(B_KV), 0, 1, -1);
+            if (ok) ok = issue_s_dp(0);
+            if (ok && nsub > 1) ok = issue_s_dp(1);
+            for (int u = 0; u < nsub && ok; ++u) {
+                const int b = u & 1;
+                ok = wait_bounded(sy, sy.bar(B_PF + b), (u >> 1) & 1, 1, u);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t sQ = sb + C::OFF_STAGE + s * C::STAGE;
-                const uint32_t sGL = sQ + C::TILE, sGH = sQ + 2 * C::TILE;
-#pragma unroll
-                for (int kk = 0; kk < C::BQ / 16; ++kk) {
-                    // A = P^T / dS^T (K-major, 2 blocks of 64 queries); B = [16 queries, D] rows (MN-major)
-                    const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    const uint32_t boff = kk * 16 * C::ROWB;
-                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-                    mma_bf16_ss(tmem + C::C_DVL, smem_desc(sPT + aoff, 16, 1024, 2),
-                                smem_desc(sGL + boff, 16, 8 * C::ROWB, C::SW), ID_KN, acc);
-                    mma_bf16_ss(tmem + C::C_DVH, smem_desc(sPT + aoff, 16, 1024, 2),
-                                smem_desc(sGH + boff, 16, 8 * C::ROWB, C::SW), ID_KN, acc);
-                    mma_bf16_ss(tmem + C::C_DK, smem_desc(sDST + aoff, 16, 1024, 2),
-                                smem_desc(sQ + boff, 16, 8 * C::ROWB, C::SW), ID_KN, acc);
-                }
-#pragma unroll
-                for (int kk = 0; kk < C::BM / 16; ++kk) {
-                    // A = dS (queries x keys): the dS^T buffer read MN-major, two 64-query atoms
-                    // 16 KB apart; B = K_j rows kk*16.. (MN-major)
-                    mma_bf16_ss(tmem + C::C_DQ, smem_desc(sDST + kk * 2048, 16384, 1024, 2),
-                                smem_desc(sK + kk * 16 * C::ROWB, 16, 8 * C::ROWB, C::SW), ID_DQ, kk > 0);
-                }
-                mma_commit(sy.bar(B_QE0 + s));
-                mma_commit(sy.bar(B_DQF));
-                if (t + 1 < nqt) {
-                    const int s1 = (t + 1) & 1;
-                    ok = wait_bounded(sy, sy.bar(B_QF0 + s1), ((t + 1) >> 1) & 1, 1, t + 1);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s_dp(s1);
-                    mma_commit(sy.bar(B_SF));
+                const bool pair_done = b == 1 || u == nsub - 1;
+                if constexpr (C::kPT) {
+                    // S/dP of u+2 first: the next softmax of this warpgroup starts sooner
+                    if (u + 2 < nsub && !(ok = issue_s_dp(u + 2))) break;
+                    issue_dv_dk(u);
+                    if (pair_done) {
+                        if (u >= 2) ok = wait_bounded(sy, sy.bar(B_DQE), ((u >> 1) - 1) & 1, 1, u);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_dq(u >> 1);
+                    }
+                } else {
+                    // P^T's 2-block shared ring: dV/dK(u) must read P(u) before S/dP(u+2)
+                    // lets the next softmax of this warpgroup overwrite it
+                    issue_dv_dk(u);
+                    if (pair_done) {
+                        if (u >= 2) ok = wait_bounded(sy, sy.bar(B_DQE), ((u >> 1) - 1) & 1, 1, u);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_dq(u >> 1);
+                    }
+                    if (u + 2 < nsub && !(ok = issue_s_dp(u + 2))) break;
                 }
             }
-            if (ok) {
-                mma_commit(sy.bar(B_ACC));
-            } else {
-                // aborted: let the MMAs already issued finish before TMEM is freed
-                mma_commit(sy.bar(B_ACC));
-                wait_drain(sy.bar(B_ACC), 0);
-            }
+            // all MMAs done (also on abort, before TMEM is freed)
+            mma_commit(sy.bar(B_ACC));
+            if (!ok) wait_drain(sy.bar(B_ACC), 0);
         }
         __syncwarp();
-    } else if (warp < 6) {
-        // ------------------------------------------------------------ softmax gradient
+    } else if (warp < 10) {
+        // ------------------------------------------------------------ softmax-gradient warpgroups
+        const int grp = (warp - 2) >> 2;         // 0: even sub-tiles, 1: odd
         const int q4 = warp & 3;                 // TMEM lane quarter of this warp
         const int jl = q4 * 32 + lane;           // key row within the tile
         const bool kvalid = k0 + jl < N;
+        const bool full = k0 + C::BM <= N;       // uniform: no padded keys in this tile
         const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
-        const float* L2s = reinterpret_cast<const float*>(smem + C::OFF_L2);
-        const float* Ds = reinterpret_cast<const float*>(smem + C::OFF_DD);
-        const uint32_t pt_row = sb + C::OFF_PT + jl * 128;
-        const uint32_t ds_row = sb + C::OFF_DST + jl * 128;
         bool ok = true;
-        for (int t = 0; t < nqt; ++t) {
-            const int s = t & 1;
-            // S/dP of tile t in TMEM; the row statistics of stage s written
-            ok = warp_wait(sy, sy.bar(B_SF), t & 1, 2, t) && warp_wait(sy, sy.bar(B_QF0 + s), (t >> 1) & 1, 2, t);
+        for (int u = grp; u < nsub; u += 2) {
+            const int s = u % C::NST;
+            ok = warp_wait(sy, sy.bar(B_SF + grp), (u >> 1) & 1, 2, u) &&
+                 warp_wait(sy, sy.bar(B_QF + s), (u / C::NST) & 1, 2, u);
             if (!ok) break;
             tc_fence_after();
+            const float* L2s = reinterpret_cast<const float*>(smem + C::OFF_L2) + s * 64;
+            const float* Ds = reinterpret_cast<const float*>(smem + C::OFF_DD) + s * 64;
+            const uint32_t ds_row = sb + C::OFF_DS + 16384 * (u & 3) + jl * 128;
+            const uint32_t p_row = sb + C::OFF_P + 16384 * grp + jl * 128;
+            const uint32_t tS = trow + 128u * grp, tDP = tS + 64;
 #pragma unroll 1
-            for (int c = 0; c < C::BQ / 32; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t sr[32], pr[32];
-                tmem_ld_32x32b_x32(trow + C::C_S + 32 * c, sr);
-                tmem_ld_32x32b_x32(trow + C::C_DP + 32 * c, pr);
+                tmem_ld_32x32b_x32(tS + 32 * c, sr);
+                tmem_ld_32x32b_x32(tDP + 32 * c, pr);
                 tmem_wait_ld();
                 uint32_t pk[16], dk[16];
+                if (full)
+                    softmax_vals<false>(sr, pr, L2s + 32 * c, Ds + 32 * c, scale_log2, kvalid, pk, dk);
+                else
+                    softmax_vals<true>(sr, pr, L2s + 32 * c, Ds + 32 * c, scale_log2, kvalid, pk, dk);
+                if constexpr (C::kPT) tmem_st_32x32b_x16(trow + C::C_P + 32 * (u & 3) + 16 * c, pk);
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4*>(L2s + s * 128 + 32 * c + e);
-                    const float4 d4 = *reinterpret_cast<const float4*>(Ds + s * 128 + 32 * c + e);
-                    float p0 = exp2f(fmaf(__uint_as_float(sr[e + 0]), scale_log2, -l4.x));
-                    float p1 = exp2f(fmaf(__uint_as_float(sr[e + 1]), scale_log2, -l4.y));
-                    float p2 = exp2f(fmaf(__uint_as_float(sr[e + 2]), scale_log2, -l4.z));
-                    float p3 = exp2f(fmaf(__uint_as_float(sr[e + 3]), scale_log2, -l4.w));
-                    if (!kvalid) p0 = p1 = p2 = p3 = 0.f;
-                    const float g0 = p0 * (__uint_as_float(pr[e + 0]) - d4.x);
-                    const float g1 = p1 * (__uint_as_float(pr[e + 1]) - d4.y);
-                    const float g2 = p2 * (__uint_as_float(pr[e + 2]) - d4.z);
-                    const float g3 = p3 * (__uint_as_float(pr[e + 3]) - d4.w);
-                    pk[e / 2] = pack_bf16x2(p0, p1);
-                    pk[e / 2 + 1] = pack_bf16x2(p2, p3);
-                    dk[e / 2] = pack_bf16x2(g0, g1);
-                    dk[e / 2 + 1] = pack_bf16x2(g2, g3);
-                }
-                // 32 queries = four 16-byte chunks of row jl; 128B-swizzled position
-                const uint32_t blk = (c >> 1) * 16384;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t ch = (uint32_t)(((c & 1) * 4 + u) ^ (jl & 7)) << 4;
-                    st_shared_v4(pt_row + blk + ch, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-                    st_shared_v4(ds_row + blk + ch, dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+                for (int v = 0; v < 4; ++v) {
+                    const uint32_t ch = (uint32_t)((c * 4 + v) ^ (jl & 7)) << 4;
+                    st_shared_v4(ds_row + ch, dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
+                    if constexpr (!C::kPT)
+                        st_shared_v4(p_row + ch, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
                 }
             }
+            if constexpr (C::kPT) tmem_wait_st();
             tc_fence_before();
             fence_proxy_async_smem();
-            mbar_arrive(sy.bar(B_PF));
+            mbar_arrive(sy.bar(B_PF + grp));
         }
-        // epilogue: dV_lo, dV_hi, dK rows of this thread's key
-        if (ok) ok = warp_wait(sy, sy.bar(B_ACC), 0, 2, nqt);
-        if (ok) {
-            tc_fence_after();
-            uint32_t v[D];
-            const size_t sec = (size_t)N * D;
-            bf16* out = d_packed + (size_t)bh * 4 * sec + (size_t)(k0 + jl) * D;
+        // epilogue (warpgroup 0): dK, dV_lo, dV_hi rows of this thread's key
+        if (grp == 0) {
+            if (ok) ok = warp_wait(sy, sy.bar(B_ACC), 0, 2, nsub);
+            if (ok) {
+                tc_fence_after();
+                uint32_t v[D];
+                const size_t sec = (size_t)N * D;
+                bf16* out = d_packed + (size_t)bh * 4 * sec + (size_t)(k0 + jl) * D;
 #pragma unroll
-            for (int which = 0; which < 3; ++which) {
-                const uint32_t col = which == 0 ? C::C_DK : which == 1 ? C::C_DVL : C::C_DVH;
-                const float mul = which == 0 ? scale : 1.f;
-                tmem_ld_row<D>(trow + col, v);
-                tmem_wait_ld();
-                if (kvalid) {
-                    bf16* o = out + (size_t)(1 + which) * sec;
+                for (int which = 0; which < 3; ++which) {
+                    const uint32_t col = which == 0 ? C::C_DK : C::C_DV + (which - 1) * D;
+                    const float mul = which == 0 ? scale : 1.f;
+                    tmem_ld_row<D>(trow + col, v);
+                    tmem_wait_ld();
+                    if (kvalid) {
+                        bf16* o = out + (size_t)(1 + which) * sec;
 #pragma unroll
-                    for (int e = 0; e < D; e += 8) {
-                        uint4 u;
-                        u.x = pack_bf16x2(__uint_as_float(v[e + 0]) * mul, __uint_as_float(v[e + 1]) * mul);
-                        u.y = pack_bf16x2(__uint_as_float(v[e + 2]) * mul, __uint_as_float(v[e + 3]) * mul);
-                        u.z = pack_bf16x2(__uint_as_float(v[e + 4]) * mul, __uint_as_float(v[e + 5]) * mul);
-                        u.w = pack_bf16x2(__uint_as_float(v[e + 6]) * mul, __uint_as_float(v[e + 7]) * mul);
-                        *reinterpret_cast<uint4*>(o + e) = u;
+                        for (int e = 0; e < D; e += 8) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(v[e + 0]) * mul, __uint_as_float(v[e + 1]) * mul);
+                            w.y = pack_bf16x2(__uint_as_float(v[e + 2]) * mul, __uint_as_float(v[e + 3]) * mul);
+                            w.z = pack_bf16x2(__uint_as_float(v[e + 4]) * mul, __uint_as_float(v[e + 5]) * mul);
+                            w.w = pack_bf16x2(__uint_as_float(v[e + 6]) * mul, __uint_as_float(v[e + 7]) * mul);
+                            *reinterpret_cast<uint4*>(o + e) = w;
+                        }
                     }
                 }
             }
@@ -379,17 +476,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_cons
     } else {
         // ------------------------------------------------------------ dQ drain
         const int q4 = warp & 3;
-        const int il = q4 * 32 + lane;           // query row within the tile
+        const int il = q4 * 32 + lane;           // query row within the 128-query group
         const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
-        for (int t = 0; t < nqt; ++t) {
-            if (!warp_wait(sy, sy.bar(B_DQF), t & 1, 3, t)) break;
+        for (int g = 0; g < ngrp; ++g) {
+            if (!warp_wait(sy, sy.bar(B_DQF), g & 1, 3, g)) break;
             tc_fence_after();
             uint32_t v[D];
             tmem_ld_row<D>(trow + C::C_DQ, v);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(sy.bar(B_DQE));
-            const int i = t * C::BQ + il;
+            const int i = g * 128 + il;
             if (i < N) {
                 float4* dst = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * N + i) * D);
 #pragma unroll
@@ -402,13 +499,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_packed, const __grid_cons
 
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
-    __syncthreads();
-    if (*sy.abort && warp == 0 && lane == 0) {
-        // let this CTA's own copies land before its shared memory is released
-        wait_drain(sy.bar(B_KV), 0);
-        for (int s = 0; s < 2; ++s)
-            if (last_issued[s] >= 0) wait_drain(sy.bar(B_QF0 + s), (last_issued[s] >> 1) & 1);
-    }
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
@@ -488,12 +578,12 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode(std::string* err) {
     return fn;
 }
 
-// 3-D map over a [Z, N, D] bf16 tensor, box [1, 128, D], swizzle matching D.
+// 3-D map over a [Z, N, D] bf16 tensor, box [1, rows, D], swizzle matching D.
 bool encode_3d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* base, int D, int N, long long Z,
-               std::string* err) {
+               int rows, std::string* err) {
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)Z};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)D, 128u, 1u};
+    const cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)rows, 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUtensorMapSwizzle sw = D == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : D == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -512,17 +602,21 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 template <int D>
 int launch(const BwdArgs& a, std::string* err) {
-    using C = Cfg<D>;
+    using M = Cfg<D>;
     auto enc = get_encode(err);
     if (!enc) return PSA_ERR_CUDA;
-    CUtensorMap tm_packed, tm_lo, tm_hi;
-    if (!encode_3d(enc, &tm_packed, a.packed, D, a.N, a.BH * 4, err) ||
-        !encode_3d(enc, &tm_lo, a.do_lo, D, a.N, a.BH, err) || !encode_3d(enc, &tm_hi, a.do_hi, D, a.N, a.BH, err))
+    // K/V tiles: 128 rows; Q/dO sub-tiles: 64 rows (the byte counts the
+    // kernel's barriers expect)
+    CUtensorMap tm_kv, tm_q, tm_lo, tm_hi;
+    if (!encode_3d(enc, &tm_kv, a.packed, D, a.N, a.BH * 4, M::BM, err) ||
+        !encode_3d(enc, &tm_q, a.packed, D, a.N, a.BH * 4, M::BS, err) ||
+        !encode_3d(enc, &tm_lo, a.do_lo, D, a.N, a.BH, M::BS, err) ||
+        !encode_3d(enc, &tm_hi, a.do_hi, D, a.N, a.BH, M::BS, err))
         return PSA_ERR_CUDA;
     static std::once_flag attr_once;
     static cudaError_t attr_st = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_st = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        attr_st = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, M::SMEM);
     });
     if (attr_st != cudaSuccess) {
         *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(attr_st);
@@ -531,8 +625,7 @@ int launch(const BwdArgs& a, std::string* err) {
     const long long rows = a.BH * a.N;
     float* Drow = static_cast<float*>(a.workspace);
     float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + align256((size_t)rows * 4));
-    const int nkt = (a.N + C::BM - 1) / C::BM;
-    const int nqt = (a.N + C::BQ - 1) / C::BQ;
+    const int nkt = (a.N + M::BM - 1) / M::BM;
     const long long grid = a.BH * nkt;
     const long long pre_grid = (rows + 256 / (D / 8) - 1) / (256 / (D / 8));
     const long long fin_grid = (rows * (D / 8) + 255) / 256;
@@ -551,8 +644,8 @@ int launch(const BwdArgs& a, std::string* err) {
     }
     {
         ProfScope prof(kSlotMain, a.stream);
-        bwd_main_kernel<D><<<(unsigned)grid, kThreads, C::SMEM, a.stream>>>(
-            tm_packed, tm_lo, tm_hi, a.lse, Drow, dq_acc, dp, a.N, nkt, nqt, a.scale, a.scale * kLog2e);
+        bwd_main_kernel<D><<<(unsigned)grid, kThreads, M::SMEM, a.stream>>>(
+            tm_kv, tm_q, tm_lo, tm_hi, a.lse, Drow, dq_acc, dp, a.N, nkt, a.scale, a.scale * kLog2e);
     }
     {
         ProfScope prof(kSlotDq, a.stream);
