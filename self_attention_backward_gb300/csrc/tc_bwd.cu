@@ -118,8 +118,9 @@ struct Sync {
 __device__ __noinline__ bool wait_slow(const Sync& s, uint32_t bar, uint32_t parity, int role, int tile) {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 15) == 15) {
+        // the thread may be suspended in hardware between polls (up to 0.2 ms)
+        if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
+        if ((it & 3) == 3) {
             if (*s.abort) return false;
             const uint64_t now = globaltimer_ns();
             if (t0 == 0) {
@@ -317,10 +318,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             const uint64_t dP0 = smem_desc(sb + C::OFF_P, 16, 1024, 2);
             constexpr uint32_t STAGE_U = C::STAGE >> 4, QTILE_U = C::QTILE >> 4, BLK_U = 16384 >> 4;
 
-            auto issue_s_dp = [&](int u) -> bool {
+            // S^T(u), dP^T(u) into TMEM buffer u & 1.  Its Q/dO stage is known to be
+            // loaded: the prologue waits for it, later the softmax warpgroup that
+            // arrives PF(u-2) has waited for it first.
+            auto issue_s_dp = [&](int u) {
                 const int s = u % C::NST;
-                if (!wait_bounded(sy, sy.bar(B_QF + s), (u / C::NST) & 1, 1, u)) return false;
-                tc_fence_after();
                 const uint64_t dQs = dStage0 + STAGE_U * s;
                 const uint32_t tS = tmem + 128u * (u & 1), tDP = tS + 64;
 #pragma unroll
@@ -332,7 +334,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_bf16_ss(tDP, dVH + 2 * kk, dQs + 2 * QTILE_U + 2 * kk, ID_S, 1);
                 mma_commit(sy.bar(B_SF + (u & 1)));
-                return true;
             };
             // dV, dK of sub-tile u (A = P^T, dS^T over 64 queries = 4 k-steps)
             auto issue_dv_dk = [&](int u) {
@@ -362,9 +363,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 mma_commit(sy.bar(B_DQF));
             };
 
-            bool ok = wait_bounded(sy, sy.bar(B_KV), 0, 1, -1);
-            if (ok) ok = issue_s_dp(0);
-            if (ok && nsub > 1) ok = issue_s_dp(1);
+            bool ok = wait_bounded(sy, sy.bar(B_KV), 0, 1, -1) && wait_bounded(sy, sy.bar(B_QF), 0, 1, 0) &&
+                      (nsub < 2 || wait_bounded(sy, sy.bar(B_QF + 1), 0, 1, 1));
+            if (ok) {
+                tc_fence_after();
+                issue_s_dp(0);
+                if (nsub > 1) issue_s_dp(1);
+            }
+            // One barrier per sub-tile: PF(u) also certifies that the Q/dO stage of
+            // u+2 is loaded and, when u closes a 128-query group, that the dQ drain
+            // has emptied the dQ accumulator (the softmax warpgroup waited for both).
             for (int u = 0; u < nsub && ok; ++u) {
                 const int b = u & 1;
                 ok = wait_bounded(sy, sy.bar(B_PF + b), (u >> 1) & 1, 1, u);
@@ -373,25 +381,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 const bool pair_done = b == 1 || u == nsub - 1;
                 if constexpr (C::kPT) {
                     // S/dP of u+2 first: the next softmax of this warpgroup starts sooner
-                    if (u + 2 < nsub && !(ok = issue_s_dp(u + 2))) break;
+                    if (u + 2 < nsub) issue_s_dp(u + 2);
                     issue_dv_dk(u);
-                    if (pair_done) {
-                        if (u >= 2) ok = wait_bounded(sy, sy.bar(B_DQE), ((u >> 1) - 1) & 1, 1, u);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_dq(u >> 1);
-                    }
+                    if (pair_done) issue_dq(u >> 1);
                 } else {
                     // P^T's 2-block shared ring: dV/dK(u) must read P(u) before S/dP(u+2)
                     // lets the next softmax of this warpgroup overwrite it
                     issue_dv_dk(u);
-                    if (pair_done) {
-                        if (u >= 2) ok = wait_bounded(sy, sy.bar(B_DQE), ((u >> 1) - 1) & 1, 1, u);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_dq(u >> 1);
-                    }
-                    if (u + 2 < nsub && !(ok = issue_s_dp(u + 2))) break;
+                    if (pair_done) issue_dq(u >> 1);
+                    if (u + 2 < nsub) issue_s_dp(u + 2);
                 }
             }
             // all MMAs done (also on abort, before TMEM is freed)
@@ -442,7 +440,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             if constexpr (C::kPT) tmem_wait_st();
             tc_fence_before();
             fence_proxy_async_smem();
+            // stand-in waits for the MMA issuer (see its loop): the stage of u+2 is
+            // loaded, and the dQ accumulator is free before this group's dQ MMA
+            if (u + 2 < nsub)
+                ok = warp_wait(sy, sy.bar(B_QF + (u + 2) % C::NST), ((u + 2) / C::NST) & 1, 2, u);
+            if (ok && ((u & 1) == 1 || u == nsub - 1) && u >= 2)
+                ok = warp_wait(sy, sy.bar(B_DQE), ((u >> 1) - 1) & 1, 2, u);
             mbar_arrive(sy.bar(B_PF + grp));
+            if (!ok) break;
         }
         // epilogue (warpgroup 0): dK, dV_lo, dV_hi rows of this thread's key
         if (grp == 0) {
