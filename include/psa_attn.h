@@ -157,6 +157,17 @@ size_t psa_attn_bwd_workspace_bytes_algo(int B, int heads, int N, int head_dim, 
 int psa_attn_sync_status(void* stream);
 
 /*
+ * Failure-detection self-test (the pages have no counterpart).  Launches, on
+ * `stream`, one small kernel that waits -- through the same bounded device-side
+ * wait the backward kernels use -- on a barrier nothing ever arrives on, with
+ * a 20 ms limit.  The wait gives up, records the timeout in the device error
+ * word and the kernel exits normally; no fault, no trap, and the CUDA context
+ * stays usable.  A following psa_attn_sync_status(stream) returns
+ * PSA_ERR_TIMEOUT and clears the word.  Returns 0 if the launch succeeded.
+ */
+int psa_attn_selftest_wait_timeout(void* stream);
+
+/*
  * Kernel timing (instrumentation; it changes no result and skips no work).
  * While enabled, every launch this library makes records a pair of CUDA events
  * around itself on the call's stream, tagged with a slot: 0 = forward,

@@ -31,6 +31,7 @@ _SIGS = {
     "psa_attn_bwd_noalloc": ([_vp] * 7 + [_i, _i, _i, _i, _f, _i, _vp], _i),
     "psa_attn_bwd_noalloc_max_rows": ([], ctypes.c_longlong),
     "psa_attn_sync_status": ([_vp], _i),
+    "psa_attn_selftest_wait_timeout": ([_vp], _i),
     "psa_attn_profile_enable": ([_i], _i),
     "psa_attn_profile_read": ([ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int), _i], _i),
     "psa_attn_profile_slot_name": ([_i], ctypes.c_char_p),
@@ -151,6 +152,11 @@ def psa_attn_bwd_noalloc_max_rows() -> int:
 
 def psa_attn_sync_status(stream=None, check=True) -> int:
     rc = lib().psa_attn_sync_status(_stream(stream))
+    return _check(rc) if check else rc
+
+
+def psa_attn_selftest_wait_timeout(stream=None, check=True) -> int:
+    rc = lib().psa_attn_selftest_wait_timeout(_stream(stream))
     return _check(rc) if check else rc
 
 

@@ -277,6 +277,12 @@ int psa_attn_profile_read(float* total_ms, int* launches, int n_slots) {
     return rc ? rc : psa::kNumSlots;
 }
 
+int psa_attn_selftest_wait_timeout(void* stream) {
+    std::string err;
+    const int rc = psa::tc_wait_selftest((cudaStream_t)stream, &err);
+    return rc ? fail(rc, "%s", err.c_str()) : ok();
+}
+
 int psa_attn_sync_status(void* stream) {
     const cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return fail(PSA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));

@@ -47,6 +47,8 @@ bool tc_supported(int dtype, int d);
 size_t tc_workspace_bytes(long long BH, int N, int d);
 // Returns 0 or a psa_status; `err` receives a message on failure.
 int tc_bwd_launch(const BwdArgs& a, std::string* err);
+// Launches a kernel whose bounded wait is made to run out (20 ms).
+int tc_wait_selftest(cudaStream_t stream, std::string* err);
 // Reads and clears the device-side timeout flag of the tensor-core kernels
 // (call after the stream is synchronised).  Returns 1 if a wait gave up.
 int tc_take_device_error(std::string* err);

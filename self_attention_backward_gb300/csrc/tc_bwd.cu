@@ -115,7 +115,8 @@ struct Sync {
 
 // Bounded wait on a barrier phase, by one thread.  Returns false on timeout or
 // when another thread of the CTA has already aborted.
-__device__ __noinline__ bool wait_slow(const Sync& s, uint32_t bar, uint32_t parity, int role, int tile) {
+__device__ __noinline__ bool wait_slow(const Sync& s, uint32_t bar, uint32_t parity, int role, int tile,
+                                       uint64_t limit_ns = kTimeoutNs) {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
         // the thread may be suspended in hardware between polls (up to 0.2 ms)
@@ -125,7 +126,7 @@ __device__ __noinline__ bool wait_slow(const Sync& s, uint32_t bar, uint32_t par
             const uint64_t now = globaltimer_ns();
             if (t0 == 0) {
                 t0 = now;
-            } else if (now - t0 > kTimeoutNs) {
+            } else if (now - t0 > limit_ns) {
                 *s.abort = 1;
                 atomicCAS(&g_tc_error, 0, ((1 + role) << 24) | (tile & 0xFFFFFF));
                 return false;
@@ -509,6 +510,25 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
+// ---------------------------------------------------------------- bounded-wait self-test
+// One CTA waits, through the same bounded wait as the backward kernel, on a
+// barrier that nothing arrives on, with a short limit: the wait gives up, the
+// device error word is set, and the kernel returns normally.
+__global__ void wait_selftest_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        Sync sy{smem_u32(&bar), &abort_flag};
+        wait_slow(sy, smem_u32(&bar), 0, 4, 0, limit_ns);
+    }
+}
+
 // ---------------------------------------------------------------- D and dQ-accumulator reset
 template <int D>
 __global__ void __launch_bounds__(256)
@@ -682,15 +702,25 @@ int tc_bwd_launch(const BwdArgs& a, std::string* err) {
     }
 }
 
+int tc_wait_selftest(cudaStream_t stream, std::string* err) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(20000000ull);  // 20 ms
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        *err = std::string("self-test launch: ") + cudaGetErrorString(e);
+        return PSA_ERR_CUDA;
+    }
+    return PSA_OK;
+}
+
 int tc_take_device_error(std::string* err) {
     int v = 0;
     cudaError_t e = cudaMemcpyFromSymbol(&v, g_tc_error, sizeof(int));
     if (e != cudaSuccess || v == 0) return 0;
     const int zero = 0;
     cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(int));
-    static const char* roles[] = {"?", "producer", "mma", "softmax", "dq"};
+    static const char* roles[] = {"?", "producer", "mma", "softmax", "dq", "self-test"};
     const int role = (v >> 24) & 0xff;
-    *err = std::string("tensor-core backward: a bounded wait gave up (") + roles[role < 5 ? role : 0] +
+    *err = std::string("tensor-core backward: a bounded wait gave up (") + roles[role < 6 ? role : 0] +
            " warp, query tile " + std::to_string(v & 0xFFFFFF) + ")";
     return 1;
 }

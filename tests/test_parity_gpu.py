@@ -124,3 +124,18 @@ def test_overwrites_d_packed_and_stream_arg():
 
 def test_sync_status_ok():
     assert B.psa_attn_sync_status() == 0
+
+
+def test_bounded_wait_timeout_is_reported_and_context_survives():
+    """A device-side wait that nothing satisfies gives up after its limit and
+    is reported as PSA_ERR_TIMEOUT by psa_attn_sync_status; the context stays
+    usable and the flag is cleared."""
+    assert B.psa_attn_sync_status() == 0
+    B.psa_attn_selftest_wait_timeout()
+    rc = B.psa_attn_sync_status(check=False)
+    assert rc == B.PSA_ERR_TIMEOUT, (rc, B.psa_attn_last_error())
+    assert "gave up" in B.psa_attn_last_error()
+    assert B.psa_attn_sync_status() == 0        # cleared
+    inp = make_custom(BH=1, N=70, d=32, dtype="bf16", seed=81)
+    errs = compare(gpu_fwd_bwd(inp, B.PSA_ALGO_TC), oracle_fwd_bwd(inp), "bf16")
+    assert_within(errs, "bf16")
