@@ -77,7 +77,8 @@ struct Cfg {
     static constexpr int ROWB = D * 2;             // bytes per [*, D] bf16 row
     static constexpr int KTILE = BM * ROWB;        // [128, D] tile
     static constexpr int QTILE = BS * ROWB;        // [64, D] tile
-    static constexpr int NST = kPT ? 4 : 3;        // Q/dO stages
+    static constexpr int NB = kPT ? 3 : 2;         // S^T/dP^T buffers in TMEM
+    static constexpr int NST = kPT ? 6 : 3;        // Q/dO stages
     static constexpr uint32_t SW = D == 64 ? 2u : D == 32 ? 4u : 6u;  // swizzle code of [*, D] tiles
     static constexpr int OFF_K = 0;
     static constexpr int OFF_VL = KTILE;
@@ -94,18 +95,19 @@ struct Cfg {
     // + 1 KB to align the base to 1024; at least 116 KB so that one CTA owns
     // an SM (its TMEM allocation is all 512 columns)
     static constexpr int SMEM = (USED + 1024) > 118784 ? (USED + 1024) : 118784;
-    // TMEM columns (fp32): buffer b = [128b, 128b+128): S^T (64), dP^T (64);
-    // then P^T ring (4 x 32 columns of bf16 pairs, d <= 32 only), dV_lo|dV_hi, dK, dQ
-    static constexpr uint32_t C_P = 256;
-    static constexpr uint32_t C_DV = kPT ? 384 : 256;
+    // TMEM columns (fp32): buffer b = [128b, 128b+128): S^T (64), dP^T (64)
+    // (for d <= 32, P^T is written over the first 32 columns of its S^T as bf16
+    // pairs); then dV_lo|dV_hi, dK, dQ
+    static constexpr uint32_t C_DV = 128 * NB;
     static constexpr uint32_t C_DK = C_DV + 2 * D, C_DQ = C_DV + 3 * D;
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(C_DQ + D <= TMEM_COLS, "TMEM budget");
     static_assert(USED + 1024 <= 232448, "shared memory budget");
 };
 
-// barrier indices
-enum { B_KV = 0, B_SF = 1, B_PF = 3, B_DQF = 5, B_DQE = 6, B_ACC = 7, B_QF = 8, B_QE = 12 };
+// barrier indices (SF: one per S/dP buffer; PF: one per softmax warpgroup;
+// QF/QE: one per Q/dO stage)
+enum { B_KV = 0, B_SF = 1, B_PF = 4, B_DQF = 6, B_DQE = 7, B_ACC = 8, B_QF = 9, B_QE = 15 };
 
 struct Sync {
     uint32_t bar0;
@@ -220,8 +222,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
 
     if (threadIdx.x == 0) {
         mbar_init(sy.bar(B_KV), 1);
-        mbar_init(sy.bar(B_SF), 1);
-        mbar_init(sy.bar(B_SF + 1), 1);
+        for (int b = 0; b < C::NB; ++b) mbar_init(sy.bar(B_SF + b), 1);
         mbar_init(sy.bar(B_PF), 128);
         mbar_init(sy.bar(B_PF + 1), 128);
         mbar_init(sy.bar(B_DQF), 1);
@@ -325,7 +326,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             auto issue_s_dp = [&](int u) {
                 const int s = u % C::NST;
                 const uint64_t dQs = dStage0 + STAGE_U * s;
-                const uint32_t tS = tmem + 128u * (u & 1), tDP = tS + 64;
+                const uint32_t tS = tmem + 128u * (u % C::NB), tDP = tS + 64;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) mma_bf16_ss(tS, dK + 2 * kk, dQs + 2 * kk, ID_S, kk);
 #pragma unroll
@@ -334,7 +335,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_bf16_ss(tDP, dVH + 2 * kk, dQs + 2 * QTILE_U + 2 * kk, ID_S, 1);
-                mma_commit(sy.bar(B_SF + (u & 1)));
+                mma_commit(sy.bar(B_SF + u % C::NB));
             };
             // dV, dK of sub-tile u (A = P^T, dS^T over 64 queries = 4 k-steps)
             auto issue_dv_dk = [&](int u) {
@@ -346,7 +347,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 for (int kk = 0; kk < C::BS / 16; ++kk) {
                     const uint32_t acc = (u > 0 || kk > 0) ? 1u : 0u;
                     if constexpr (C::kPT)
-                        mma_bf16_ts(tmem + C::C_DV, tmem + C::C_P + 32 * (u & 3) + 8 * kk, dGmn + KSTEP * kk, ID_DV,
+                        mma_bf16_ts(tmem + C::C_DV, tmem + 128u * (u % C::NB) + 8 * kk, dGmn + KSTEP * kk, ID_DV,
                                     acc);
                     else
                         mma_bf16_ss(tmem + C::C_DV, dP0 + BLK_U * (u & 1) + 2 * kk, dGmn + KSTEP * kk, ID_DV, acc);
@@ -364,15 +365,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 mma_commit(sy.bar(B_DQF));
             };
 
-            bool ok = wait_bounded(sy, sy.bar(B_KV), 0, 1, -1) && wait_bounded(sy, sy.bar(B_QF), 0, 1, 0) &&
-                      (nsub < 2 || wait_bounded(sy, sy.bar(B_QF + 1), 0, 1, 1));
+            bool ok = wait_bounded(sy, sy.bar(B_KV), 0, 1, -1);
+            for (int u = 0; u < C::NB && u < nsub && ok; ++u)
+                ok = wait_bounded(sy, sy.bar(B_QF + u), 0, 1, u);
             if (ok) {
                 tc_fence_after();
-                issue_s_dp(0);
-                if (nsub > 1) issue_s_dp(1);
+                for (int u = 0; u < C::NB && u < nsub; ++u) issue_s_dp(u);
             }
             // One barrier per sub-tile: PF(u) also certifies that the Q/dO stage of
-            // u+2 is loaded and, when u closes a 128-query group, that the dQ drain
+            // u+NB is loaded and, when u closes a 128-query group, that the dQ drain
             // has emptied the dQ accumulator (the softmax warpgroup waited for both).
             for (int u = 0; u < nsub && ok; ++u) {
                 const int b = u & 1;
@@ -381,10 +382,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 tc_fence_after();
                 const bool pair_done = b == 1 || u == nsub - 1;
                 if constexpr (C::kPT) {
-                    // S/dP of u+2 first: the next softmax of this warpgroup starts sooner
-                    if (u + 2 < nsub) issue_s_dp(u + 2);
+                    // P(u) lives in S/dP buffer u % 3: dV(u) reads it before S/dP(u+3)
+                    // reuses the buffer; the other two buffers keep the softmax fed
                     issue_dv_dk(u);
                     if (pair_done) issue_dq(u >> 1);
+                    if (u + C::NB < nsub) issue_s_dp(u + C::NB);
                 } else {
                     // P^T's 2-block shared ring: dV/dK(u) must read P(u) before S/dP(u+2)
                     // lets the next softmax of this warpgroup overwrite it
@@ -409,7 +411,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         bool ok = true;
         for (int u = grp; u < nsub; u += 2) {
             const int s = u % C::NST;
-            ok = warp_wait(sy, sy.bar(B_SF + grp), (u >> 1) & 1, 2, u) &&
+            const int buf = u % C::NB;
+            ok = warp_wait(sy, sy.bar(B_SF + buf), (u / C::NB) & 1, 2, u) &&
                  warp_wait(sy, sy.bar(B_QF + s), (u / C::NST) & 1, 2, u);
             if (!ok) break;
             tc_fence_after();
@@ -417,7 +420,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             const float* Ds = reinterpret_cast<const float*>(smem + C::OFF_DD) + s * 64;
             const uint32_t ds_row = sb + C::OFF_DS + 16384 * (u & 3) + jl * 128;
             const uint32_t p_row = sb + C::OFF_P + 16384 * grp + jl * 128;
-            const uint32_t tS = trow + 128u * grp, tDP = tS + 64;
+            const uint32_t tS = trow + 128u * buf, tDP = tS + 64;
 #pragma unroll 1
             for (int c = 0; c < 2; ++c) {
                 uint32_t sr[32], pr[32];
@@ -429,7 +432,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                     softmax_vals<false>(sr, pr, L2s + 32 * c, Ds + 32 * c, scale_log2, kvalid, pk, dk);
                 else
                     softmax_vals<true>(sr, pr, L2s + 32 * c, Ds + 32 * c, scale_log2, kvalid, pk, dk);
-                if constexpr (C::kPT) tmem_st_32x32b_x16(trow + C::C_P + 32 * (u & 3) + 16 * c, pk);
+                // P over the S^T columns already read (chunk c's S is in registers)
+                if constexpr (C::kPT) tmem_st_32x32b_x16(tS + 16 * c, pk);
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     const uint32_t ch = (uint32_t)((c * 4 + v) ^ (jl & 7)) << 4;
@@ -443,8 +447,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             fence_proxy_async_smem();
             // stand-in waits for the MMA issuer (see its loop): the stage of u+2 is
             // loaded, and the dQ accumulator is free before this group's dQ MMA
-            if (u + 2 < nsub)
-                ok = warp_wait(sy, sy.bar(B_QF + (u + 2) % C::NST), ((u + 2) / C::NST) & 1, 2, u);
+            if (u + C::NB < nsub)
+                ok = warp_wait(sy, sy.bar(B_QF + (u + C::NB) % C::NST), ((u + C::NB) / C::NST) & 1, 2, u);
             if (ok && ((u & 1) == 1 || u == nsub - 1) && u >= 2)
                 ok = warp_wait(sy, sy.bar(B_DQE), ((u >> 1) - 1) & 1, 2, u);
             mbar_arrive(sy.bar(B_PF + grp));
