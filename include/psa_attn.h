@@ -73,6 +73,13 @@ int psa_attn_fwd(const void* packed, void* o_lo, void* o_hi, float* lse,
                  int B, int heads, int N, int head_dim, float scale,
                  int dtype, void* stream);
 
+/* Like psa_attn_fwd, with an explicit kernel choice (psa_algo): the
+ * tensor-core forward (bf16 storage) or the CUDA-core forward (any storage).
+ * PSA_ALGO_TC returns PSA_ERR_UNSUPPORTED for fp32 storage. */
+int psa_attn_fwd_algo(const void* packed, void* o_lo, void* o_hi, float* lse,
+                      int B, int heads, int N, int head_dim, float scale,
+                      int dtype, int algo, void* stream);
+
 /*
  * Bytes of device workspace psa_attn_bwd needs for these sizes and the kernel
  * AUTO would pick (fp32 row statistics D and, on the tensor-core path, an fp32

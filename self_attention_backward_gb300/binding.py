@@ -24,6 +24,7 @@ PSA_ALGO_AUTO, PSA_ALGO_SIMT, PSA_ALGO_TC = 0, 1, 2
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _SIGS = {
     "psa_attn_fwd": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp], _i),
+    "psa_attn_fwd_algo": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
     "psa_attn_bwd_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
     "psa_attn_bwd_workspace_bytes_algo": ([_i, _i, _i, _i, _i, _i], _sz),
     "psa_attn_bwd": ([_vp] * 8 + [_sz, _i, _i, _i, _i, _f, _i, _vp], _i),
@@ -115,10 +116,10 @@ def psa_attn_version() -> int:
 
 
 def psa_attn_fwd(packed, o_lo, o_hi, lse, B, heads, N, head_dim, scale, dtype=None, stream=None,
-                 check=True) -> int:
+                 check=True, algo=PSA_ALGO_AUTO) -> int:
     dtype = _dtype_code(packed) if dtype is None else dtype
-    rc = lib().psa_attn_fwd(_ptr(packed), _ptr(o_lo), _ptr(o_hi), _ptr(lse), B, heads, N, head_dim,
-                            float(scale), dtype, _stream(stream))
+    rc = lib().psa_attn_fwd_algo(_ptr(packed), _ptr(o_lo), _ptr(o_hi), _ptr(lse), B, heads, N, head_dim,
+                                 float(scale), dtype, algo, _stream(stream))
     return _check(rc) if check else rc
 
 
@@ -185,7 +186,7 @@ def _torch_dtype(dtype):
     return {PSA_F32: torch.float32, PSA_BF16: torch.bfloat16}[dtype]
 
 
-def attn_fwd(packed, scale: float, stream=None):
+def attn_fwd(packed, scale: float, stream=None, algo=PSA_ALGO_AUTO):
     """Allocates O_lo, O_hi, LSE on packed's device and runs psa_attn_fwd.
 
     packed: [BH, 4, N, d] CUDA tensor (fp32 or bf16).  B is taken as BH, heads 1.
@@ -196,7 +197,7 @@ def attn_fwd(packed, scale: float, stream=None):
     o_lo = torch.empty((BH, N, d), dtype=packed.dtype, device=packed.device)
     o_hi = torch.empty_like(o_lo)
     lse = torch.empty((BH, N), dtype=torch.float32, device=packed.device)
-    psa_attn_fwd(packed, o_lo, o_hi, lse, BH, 1, N, d, scale, stream=stream)
+    psa_attn_fwd(packed, o_lo, o_hi, lse, BH, 1, N, d, scale, stream=stream, algo=algo)
     return o_lo, o_hi, lse
 
 

@@ -178,16 +178,31 @@ int psa_attn_version(void) { return 100; }
 
 const char* psa_attn_last_error(void) { return g_last_error.c_str(); }
 
-int psa_attn_fwd(const void* packed, void* o_lo, void* o_hi, float* lse, int B, int heads, int N, int head_dim,
-                 float scale, int dtype, void* stream) {
+int psa_attn_fwd_algo(const void* packed, void* o_lo, void* o_hi, float* lse, int B, int heads, int N,
+                      int head_dim, float scale, int dtype, int algo, void* stream) {
     Shape s;
     int rc = check_shape(B, heads, N, head_dim, scale, dtype, &s);
     if (rc) return rc;
+    if (algo != PSA_ALGO_AUTO && algo != PSA_ALGO_SIMT && algo != PSA_ALGO_TC)
+        return fail(PSA_ERR_ARG, "algo %d is not a psa_algo", algo);
+    if (algo == PSA_ALGO_AUTO) algo = psa::tc_fwd_supported(dtype, head_dim) ? PSA_ALGO_TC : PSA_ALGO_SIMT;
+    if (algo == PSA_ALGO_TC && !psa::tc_fwd_supported(dtype, head_dim))
+        return fail(PSA_ERR_UNSUPPORTED, "no tensor-core forward for dtype %d, head_dim %d", dtype, head_dim);
     if (s.empty) return ok();
     rc = check_ptrs({{"packed", packed}, {"o_lo", o_lo}, {"o_hi", o_hi}, {"lse", lse}});
     if (rc) return rc;
+    if (algo == PSA_ALGO_TC) {
+        std::string err;
+        rc = psa::tc_fwd_launch(packed, o_lo, o_hi, lse, s.BH, N, head_dim, scale, (cudaStream_t)stream, &err);
+        return rc ? fail(rc, "%s", err.c_str()) : ok();
+    }
     rc = PSA_DISPATCH(dtype, head_dim, launch_fwd, packed, o_lo, o_hi, lse, s.BH, N, scale, (cudaStream_t)stream);
     return rc ? rc : ok();
+}
+
+int psa_attn_fwd(const void* packed, void* o_lo, void* o_hi, float* lse, int B, int heads, int N, int head_dim,
+                 float scale, int dtype, void* stream) {
+    return psa_attn_fwd_algo(packed, o_lo, o_hi, lse, B, heads, N, head_dim, scale, dtype, PSA_ALGO_AUTO, stream);
 }
 
 size_t psa_attn_bwd_workspace_bytes_algo(int B, int heads, int N, int head_dim, int dtype, int algo) {
@@ -288,6 +303,7 @@ int psa_attn_sync_status(void* stream) {
     if (e != cudaSuccess) return fail(PSA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
     std::string err;
     if (psa::tc_take_device_error(&err)) return fail(PSA_ERR_TIMEOUT, "%s", err.c_str());
+    if (psa::tc_fwd_take_device_error(&err)) return fail(PSA_ERR_TIMEOUT, "%s", err.c_str());
     return ok();
 }
 

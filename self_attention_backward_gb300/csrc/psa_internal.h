@@ -42,6 +42,12 @@ class ProfScope {
     cudaEvent_t a_ = nullptr, b_ = nullptr;
 };
 
+// Tensor-core (tcgen05) forward: tc_fwd.cu.
+bool tc_fwd_supported(int dtype, int d);
+int tc_fwd_launch(const void* packed, void* o_lo, void* o_hi, float* lse, long long BH, int N, int d, float scale,
+                  cudaStream_t stream, std::string* err);
+int tc_fwd_take_device_error(std::string* err);
+
 // Tensor-core (tcgen05) backward: tc_bwd.cu.
 bool tc_supported(int dtype, int d);
 size_t tc_workspace_bytes(long long BH, int N, int d);

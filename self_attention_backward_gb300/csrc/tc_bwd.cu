@@ -55,6 +55,7 @@
 #include "psa_attn.h"
 #include "psa_internal.h"
 #include "tc_ptx.cuh"
+#include "tc_sync.cuh"
 
 #pragma nv_diag_suppress 177  // per-variant tile constants not all used by every head_dim
 
@@ -66,7 +67,6 @@ using bf16 = __nv_bfloat16;
 
 __device__ int g_tc_error = 0;  // 0 = fine; else (1 + role) << 24 | tile
 
-constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr int kThreads = 448;
 
 template <int D>
@@ -109,74 +109,6 @@ struct Cfg {
 // QF/QE: one per Q/dO stage)
 enum { B_KV = 0, B_SF = 1, B_PF = 4, B_DQF = 6, B_DQE = 7, B_ACC = 8, B_QF = 9, B_QE = 15 };
 
-struct Sync {
-    uint32_t bar0;
-    volatile int* abort;
-    __device__ uint32_t bar(int i) const { return bar0 + 8u * i; }
-};
-
-// Bounded wait on a barrier phase, by one thread.  Returns false on timeout or
-// when another thread of the CTA has already aborted.
-__device__ __noinline__ bool wait_slow(const Sync& s, uint32_t bar, uint32_t parity, int role, int tile,
-                                       uint64_t limit_ns = kTimeoutNs) {
-    uint64_t t0 = 0;
-    for (uint32_t it = 0;; ++it) {
-        // the thread may be suspended in hardware between polls (up to 0.2 ms)
-        if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
-        if ((it & 3) == 3) {
-            if (*s.abort) return false;
-            const uint64_t now = globaltimer_ns();
-            if (t0 == 0) {
-                t0 = now;
-            } else if (now - t0 > limit_ns) {
-                *s.abort = 1;
-                atomicCAS(&g_tc_error, 0, ((1 + role) << 24) | (tile & 0xFFFFFF));
-                return false;
-            }
-        }
-    }
-}
-// Fast path first (the phase is often already complete), then the bounded loop.
-__device__ __forceinline__ bool wait_bounded(const Sync& s, uint32_t bar, uint32_t parity, int role, int tile) {
-    if (mbar_try_wait(bar, parity)) return true;
-    return wait_slow(s, bar, parity, role, tile);
-}
-
-// Whole-warp wait: every lane waits, the warp agrees on the outcome.
-__device__ __forceinline__ bool warp_wait(const Sync& s, uint32_t bar, uint32_t parity, int role, int tile) {
-    const bool ok = wait_bounded(s, bar, parity, role, tile);
-    return __all_sync(0xffffffffu, ok);
-}
-
-// Wait without the abort short-cut (used only to drain work after an abort).
-__device__ bool wait_drain(uint32_t bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (globaltimer_ns() - t0 > kTimeoutNs) return false;
-    return true;
-}
-
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-template <int D>
-__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, uint32_t* v) {
-    if constexpr (D == 16) {
-        tmem_ld_32x32b_x16(taddr, v);
-    } else {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + 32 * c, r);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[32 * c + e] = r[e];
-        }
-    }
-}
-
 // P and dS of one 32-query chunk of this thread's key row, packed to bf16
 // pairs: P = exp2(S * scale*log2e - L), dS = P (dP - D).
 template <bool MASK>
@@ -211,7 +143,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
-    Sync sy{sb + C::OFF_BAR, reinterpret_cast<volatile int*>(smem + C::OFF_MISC)};
+    Sync sy{sb + C::OFF_BAR, reinterpret_cast<volatile int*>(smem + C::OFF_MISC), &g_tc_error};
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 16);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -528,7 +460,7 @@ __global__ void wait_selftest_kernel(uint64_t limit_ns) {
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        Sync sy{smem_u32(&bar), &abort_flag};
+        Sync sy{smem_u32(&bar), &abort_flag, &g_tc_error};
         wait_slow(sy, smem_u32(&bar), 0, 4, 0, limit_ns);
     }
 }

@@ -139,3 +139,34 @@ def test_bounded_wait_timeout_is_reported_and_context_survives():
     inp = make_custom(BH=1, N=70, d=32, dtype="bf16", seed=81)
     errs = compare(gpu_fwd_bwd(inp, B.PSA_ALGO_TC), oracle_fwd_bwd(inp), "bf16")
     assert_within(errs, "bf16")
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("N", [1, 100, 128, 300])
+def test_tensor_core_forward_matches_oracle(N, d):
+    """The tensor-core forward (bf16) against the oracle's O and LSE, and the
+    CUDA-core forward on the same inputs."""
+    import torch
+    from gpu_helpers import to_device, TOL, TOL_LSE
+    inp = make_custom(BH=3, N=N, d=d, dtype="bf16", seed=2000 + N + d)
+    ref = oracle_fwd_bwd(inp)
+    packed = to_device(inp.packed, "bf16")
+    for algo in (B.PSA_ALGO_TC, B.PSA_ALGO_SIMT):
+        o_lo, o_hi, lse = B.attn_fwd(packed, inp.scale, algo=algo)
+        B.psa_attn_sync_status()
+        assert rel_err(o_lo.double().cpu().numpy(), ref["o_lo"]) <= TOL["bf16"]
+        assert rel_err(o_hi.double().cpu().numpy(), ref["o_hi"]) <= TOL["bf16"]
+        assert rel_err(lse.double().cpu().numpy(), ref["lse"]) <= TOL_LSE
+
+
+def test_tensor_core_forward_full_size_sampled():
+    """Tensor-core forward at the N=6400, d=32 workload size (sampled slices)."""
+    from gpu_helpers import to_device, TOL, TOL_LSE
+    inp = make_inputs("psa_bf16_b8_h2_n6400_d32")
+    ref = oracle_fwd_bwd(inp, [3])
+    packed = to_device(inp.packed, "bf16")
+    o_lo, o_hi, lse = B.attn_fwd(packed, inp.scale, algo=B.PSA_ALGO_TC)
+    B.psa_attn_sync_status()
+    assert rel_err(o_lo[3].double().cpu().numpy(), ref["o_lo"][0]) <= TOL["bf16"]
+    assert rel_err(o_hi[3].double().cpu().numpy(), ref["o_hi"][0]) <= TOL["bf16"]
+    assert rel_err(lse[3].double().cpu().numpy(), ref["lse"][0]) <= TOL_LSE
