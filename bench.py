@@ -45,6 +45,28 @@ def metric_flops(w) -> float:
     return 12.0 * w.N * w.N * w.d * w.BH
 
 
+# Per-launch FLOPs of each kernel, in units of N^2*d per (batch, head).  The
+# fused tensor-core kernel does the whole backward: the metric's 12 (it
+# executes 14).  The two-pass dK/dV kernel executes S (2), dP (4), dV (4) and
+# dK (2); the dQ pass S (2), dP (4) and dQ (2).  The CUDA-core dK/dV and dQ
+# kernels are credited with the metric's terms they produce.
+KERNEL_FLOPS = {
+    "tc": {"bwd_main": 12.0},
+    "tc2": {"bwd_main": 12.0, "bwd_dq": 8.0},
+    "simt": {"bwd_main": 10.0, "bwd_dq": 2.0},
+}
+# executed FLOPs of one backward, same units
+EXECUTED = {"tc": 14.0, "tc2": 20.0, "simt": 20.0}
+
+
+def resolved_algo(B, name: str, w) -> str:
+    """The kernel family a run with --algo `name` uses on workload w."""
+    if name != "auto":
+        return name
+    tc = B.psa_attn_bwd_workspace_bytes(1, 1, 16, w.d, 1 if w.dtype == "bf16" else 0, B.PSA_ALGO_TC) > 0
+    return "tc" if tc else "simt"
+
+
 def alg_bytes(w) -> float:
     """Algorithmic HBM bytes of one backward: read Q, K, V_lo, V_hi, O_lo, O_hi,
     dO_lo, dO_hi and LSE (fp32); write dQ, dK, dV_lo, dV_hi."""
@@ -278,7 +300,8 @@ def run_ours(args, w):
     from self_attention_backward_gb300.build import build
     build()
     from self_attention_backward_gb300 import binding as B
-    algo = {"auto": B.PSA_ALGO_AUTO, "simt": B.PSA_ALGO_SIMT, "tc": B.PSA_ALGO_TC}[args.algo]
+    algo = {"auto": B.PSA_ALGO_AUTO, "simt": B.PSA_ALGO_SIMT, "tc": B.PSA_ALGO_TC,
+            "tc2": B.PSA_ALGO_TC_2PASS}[args.algo]
     peaks, peaks_src = read_peaks()
 
     bufs = device_inputs(w, device)
@@ -309,11 +332,10 @@ def run_ours(args, w):
     dom_ms = prof[dom][0] / prof[dom][1]
     t_roof, bound = roofline_time_s(w, peaks)
     # algorithmic work of the dominant kernel per launch
-    used_algo = "tc" if (algo == B.PSA_ALGO_TC or (algo == B.PSA_ALGO_AUTO and B.psa_attn_bwd_workspace_bytes(
-        1, 1, 16, w.d, 1 if w.dtype == "bf16" else 0, B.PSA_ALGO_TC) > 0)) else "simt"
+    used_algo = resolved_algo(B, args.algo, w)
     if bound == "tensor":
-        share = {"bwd_main": 12.0 if used_algo == "tc" else 10.0, "bwd_dq": 2.0}.get(dom, 0.0)
-        achieved = share / 12.0 * metric_flops(w) / (dom_ms * 1e-3) / 1e12
+        share = KERNEL_FLOPS[used_algo].get(dom, 0.0)
+        achieved = share * w.BH * w.N * w.N * w.d / (dom_ms * 1e-3) / 1e12
         peak, unit = tensor_peak(peaks, w.dtype), "TFLOP/s"
         peak_note = f"bf16_tflops (burst) of {peaks_src}"
     else:
@@ -331,7 +353,7 @@ def run_ours(args, w):
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic, "kernel": dom, "peak_source": peak_note},
         "step_roofline_frac": t_roof / (ms * 1e-3),
-        "executed_tflops": value * 14.0 / 12.0 if used_algo == "tc" else value * 20.0 / 12.0,
+        "executed_tflops": value * EXECUTED[used_algo] / 12.0,
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]},
         "gpu_launches": launches,
         "wall_s_timed_region": wall,
@@ -405,7 +427,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE)
-    ap.add_argument("--algo", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--algo", choices=["auto", "simt", "tc", "tc2"], default="auto")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")

@@ -56,8 +56,16 @@ typedef enum {
 } psa_status;
 
 /* Backward kernel choice.  AUTO picks the tensor-core (tcgen05) path where it
- * exists for the (dtype, head_dim) and the CUDA-core (SIMT) path elsewhere. */
-typedef enum { PSA_ALGO_AUTO = 0, PSA_ALGO_SIMT = 1, PSA_ALGO_TC = 2 } psa_algo;
+ * exists for the (dtype, head_dim) and the CUDA-core (SIMT) path elsewhere.
+ *   PSA_ALGO_TC        one key-outer pass; dQ partial sums are added to an
+ *                      fp32 accumulator with atomics, so the rounding of dQ
+ *                      can differ from run to run.
+ *   PSA_ALGO_TC_2PASS  a key-outer dK/dV pass and a query-outer dQ pass
+ *                      ("Struct PsaFa2Backward" description: dQ by iterating
+ *                      over keys, dK/dV by iterating over queries); no atomics,
+ *                      bit-for-bit reproducible.  Backward only (the forward
+ *                      entry points reject it). */
+typedef enum { PSA_ALGO_AUTO = 0, PSA_ALGO_SIMT = 1, PSA_ALGO_TC = 2, PSA_ALGO_TC_2PASS = 3 } psa_algo;
 
 /*
  * psa_attn_fwd -- PSA forward: O_lo = P V_lo, O_hi = P V_hi and LSE.
@@ -110,8 +118,8 @@ int psa_attn_bwd(const void* packed, const void* o_lo, const void* o_hi, const f
                  int dtype, void* stream);
 
 /* Like psa_attn_bwd, with an explicit kernel choice (psa_algo).  PSA_ALGO_TC
- * returns PSA_ERR_UNSUPPORTED where no tensor-core kernel exists for the
- * (dtype, head_dim). */
+ * and PSA_ALGO_TC_2PASS return PSA_ERR_UNSUPPORTED where no tensor-core kernel
+ * exists for the (dtype, head_dim). */
 int psa_attn_bwd_algo(const void* packed, const void* o_lo, const void* o_hi, const float* lse,
                       const void* do_lo, const void* do_hi, void* d_packed,
                       void* workspace, size_t workspace_bytes,

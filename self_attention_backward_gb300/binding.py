@@ -19,7 +19,7 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "psa_attn.h")
 PSA_F32, PSA_BF16 = 0, 1
 PSA_OK, PSA_ERR_ARG, PSA_ERR_ALIGN, PSA_ERR_UNSUPPORTED = 0, -1, -2, -3
 PSA_ERR_WORKSPACE, PSA_ERR_CUDA, PSA_ERR_TIMEOUT = -4, -5, -6
-PSA_ALGO_AUTO, PSA_ALGO_SIMT, PSA_ALGO_TC = 0, 1, 2
+PSA_ALGO_AUTO, PSA_ALGO_SIMT, PSA_ALGO_TC, PSA_ALGO_TC_2PASS = 0, 1, 2, 3
 
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _SIGS = {

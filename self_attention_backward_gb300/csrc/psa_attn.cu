@@ -152,6 +152,10 @@ size_t simt_workspace_bytes(long long BH, int N) { return (size_t)BH * (size_t)N
                       : (d) == 32 ? FN<__nv_bfloat16, 32>(__VA_ARGS__)                           \
                                   : FN<__nv_bfloat16, 64>(__VA_ARGS__)))
 
+bool is_bwd_algo(int algo) {
+    return algo == PSA_ALGO_AUTO || algo == PSA_ALGO_SIMT || algo == PSA_ALGO_TC || algo == PSA_ALGO_TC_2PASS;
+}
+
 int resolve_algo(int dtype, int d, int algo) {
     if (algo == PSA_ALGO_AUTO) return psa::tc_supported(dtype, d) ? PSA_ALGO_TC : PSA_ALGO_SIMT;
     return algo;
@@ -162,6 +166,7 @@ size_t workspace_for(const Shape& s, int dtype, int algo) {
     algo = resolve_algo(dtype, s.d, algo);
     if (algo == PSA_ALGO_SIMT) return simt_workspace_bytes(s.BH, s.N);
     if (algo == PSA_ALGO_TC && psa::tc_supported(dtype, s.d)) return psa::tc_workspace_bytes(s.BH, s.N, s.d);
+    if (algo == PSA_ALGO_TC_2PASS && psa::tc_supported(dtype, s.d)) return psa::tc_two_pass_workspace_bytes(s.BH, s.N);
     return 0;
 }
 
@@ -211,7 +216,7 @@ size_t psa_attn_bwd_workspace_bytes_algo(int B, int heads, int N, int head_dim, 
     const int rc = check_shape(B, heads, N, head_dim, 1.0f, dtype, &s);
     g_last_error = keep;
     if (rc) return 0;
-    if (algo != PSA_ALGO_AUTO && algo != PSA_ALGO_SIMT && algo != PSA_ALGO_TC) return 0;
+    if (!is_bwd_algo(algo)) return 0;
     return workspace_for(s, dtype, algo);
 }
 
@@ -225,10 +230,9 @@ int psa_attn_bwd_algo(const void* packed, const void* o_lo, const void* o_hi, co
     Shape s;
     int rc = check_shape(B, heads, N, head_dim, scale, dtype, &s);
     if (rc) return rc;
-    if (algo != PSA_ALGO_AUTO && algo != PSA_ALGO_SIMT && algo != PSA_ALGO_TC)
-        return fail(PSA_ERR_ARG, "algo %d is not a psa_algo", algo);
+    if (!is_bwd_algo(algo)) return fail(PSA_ERR_ARG, "algo %d is not a psa_algo", algo);
     algo = resolve_algo(dtype, head_dim, algo);
-    if (algo == PSA_ALGO_TC && !psa::tc_supported(dtype, head_dim))
+    if ((algo == PSA_ALGO_TC || algo == PSA_ALGO_TC_2PASS) && !psa::tc_supported(dtype, head_dim))
         return fail(PSA_ERR_UNSUPPORTED, "no tensor-core backward for dtype %d, head_dim %d", dtype, head_dim);
     if (s.empty) return ok();
     rc = check_ptrs({{"packed", packed}, {"o_lo", o_lo}, {"o_hi", o_hi}, {"lse", lse}, {"do_lo", do_lo},
@@ -242,9 +246,9 @@ int psa_attn_bwd_algo(const void* packed, const void* o_lo, const void* o_hi, co
     }
     psa::BwdArgs a{packed, o_lo, o_hi, lse, do_lo, do_hi, d_packed, workspace, workspace_bytes,
                    s.BH, N, head_dim, scale, dtype, (cudaStream_t)stream};
-    if (algo == PSA_ALGO_TC) {
+    if (algo == PSA_ALGO_TC || algo == PSA_ALGO_TC_2PASS) {
         std::string err;
-        rc = psa::tc_bwd_launch(a, &err);
+        rc = algo == PSA_ALGO_TC ? psa::tc_bwd_launch(a, &err) : psa::tc_two_pass_launch(a, &err);
         if (rc) return fail(rc, "%s", err.c_str());
         return ok();
     }
@@ -304,6 +308,7 @@ int psa_attn_sync_status(void* stream) {
     std::string err;
     if (psa::tc_take_device_error(&err)) return fail(PSA_ERR_TIMEOUT, "%s", err.c_str());
     if (psa::tc_fwd_take_device_error(&err)) return fail(PSA_ERR_TIMEOUT, "%s", err.c_str());
+    if (psa::tc_dq_take_device_error(&err)) return fail(PSA_ERR_TIMEOUT, "%s", err.c_str());
     return ok();
 }
 

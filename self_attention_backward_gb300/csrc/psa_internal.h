@@ -53,6 +53,13 @@ bool tc_supported(int dtype, int d);
 size_t tc_workspace_bytes(long long BH, int N, int d);
 // Returns 0 or a psa_status; `err` receives a message on failure.
 int tc_bwd_launch(const BwdArgs& a, std::string* err);
+// Two-pass tensor-core backward (no atomics, reproducible bit for bit): D,
+// the key-outer dK/dV pass (tc_bwd.cu), the query-outer dQ pass (tc_dq.cu).
+size_t tc_two_pass_workspace_bytes(long long BH, int N);
+int tc_two_pass_launch(const BwdArgs& a, std::string* err);
+// The query-outer dQ pass alone; `Drow` = [BH*N] fp32 row statistics D.
+int tc_dq_launch(const BwdArgs& a, const float* Drow, std::string* err);
+int tc_dq_take_device_error(std::string* err);
 // Launches a kernel whose bounded wait is made to run out (20 ms).
 int tc_wait_selftest(cudaStream_t stream, std::string* err);
 // Reads and clears the device-side timeout flag of the tensor-core kernels

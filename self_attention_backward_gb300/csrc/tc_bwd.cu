@@ -446,6 +446,255 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
+// ---------------------------------------------------------------- dK/dV pass (deterministic mode)
+// The key-outer pass without its dQ work: the same walk over 64-query
+// sub-tiles, but P^T and dS^T both stay in TMEM (P over the S^T columns, dS
+// over the dP^T columns) as the A operands of the dV and dK MMAs, so the
+// softmax warps issue no shared-memory stores; dK and dV accumulate in TMEM in
+// a fixed order.  dQ comes from the query-outer pass (tc_dq.cu).
+template <int D>
+struct CfgS {
+    static constexpr int BM = 128, BS = 64;
+    static constexpr int ROWB = D * 2;
+    static constexpr int KTILE = BM * ROWB, QTILE = BS * ROWB;
+    static constexpr int NB = D <= 32 ? 3 : 2;    // S^T/dP^T buffers in TMEM
+    static constexpr int NST = D <= 32 ? 6 : 4;   // Q/dO stages (> NB)
+    static constexpr uint32_t SW = D == 64 ? 2u : D == 32 ? 4u : 6u;
+    static constexpr int OFF_K = 0, OFF_VL = KTILE, OFF_VH = 2 * KTILE;
+    static constexpr int OFF_STAGE = 3 * KTILE, STAGE = 3 * QTILE;
+    static constexpr int OFF_L2 = OFF_STAGE + NST * STAGE;
+    static constexpr int OFF_DD = OFF_L2 + NST * 256;
+    static constexpr int OFF_BAR = OFF_DD + NST * 256;
+    static constexpr int OFF_MISC = OFF_BAR + 256;
+    static constexpr int USED = OFF_MISC + 64;
+    static constexpr int SMEM = (USED + 1024) > 118784 ? (USED + 1024) : 118784;
+    static constexpr uint32_t C_DV = 128 * NB, C_DK = C_DV + 2 * D;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(C_DK + D <= TMEM_COLS, "TMEM budget");
+    static_assert(NST > NB, "the softmax's wait for the stage of u+NB would wait on its own release");
+    static_assert(USED + 1024 <= 232448, "shared memory budget");
+};
+constexpr int kThreadsS = 320;
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsS, 1)
+bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
+                const __grid_constant__ CUtensorMap tm_do_lo, const __grid_constant__ CUtensorMap tm_do_hi,
+                const float* __restrict__ lse, const float* __restrict__ Drow, bf16* __restrict__ d_packed, int N,
+                int nkt, float scale, float scale_log2) {
+    using C = CfgS<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    Sync sy{sb + C::OFF_BAR, reinterpret_cast<volatile int*>(smem + C::OFF_MISC), &g_tc_error};
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 16);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / nkt, kt = blockIdx.x % nkt;
+    const int k0 = kt * C::BM;
+    const int nsub = (N + C::BS - 1) / C::BS;
+
+    if (threadIdx.x == 0) {
+        mbar_init(sy.bar(B_KV), 1);
+        for (int b = 0; b < C::NB; ++b) mbar_init(sy.bar(B_SF + b), 1);
+        mbar_init(sy.bar(B_PF), 128);
+        mbar_init(sy.bar(B_PF + 1), 128);
+        mbar_init(sy.bar(B_ACC), 1);
+        for (int s = 0; s < C::NST; ++s) {
+            mbar_init(sy.bar(B_QF + s), 32);
+            mbar_init(sy.bar(B_QE + s), 1);
+        }
+        *sy.abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tm_kv);
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_do_lo);
+        tma_prefetch_desc(&tm_do_hi);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int last_issued[C::NST];
+#pragma unroll
+        for (int s = 0; s < C::NST; ++s) last_issued[s] = -1;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(sy.bar(B_KV), 3 * C::KTILE);
+            tma_load_3d(sb + C::OFF_K, &tm_kv, 0, k0, bh * 4 + 1, sy.bar(B_KV));
+            tma_load_3d(sb + C::OFF_VL, &tm_kv, 0, k0, bh * 4 + 2, sy.bar(B_KV));
+            tma_load_3d(sb + C::OFF_VH, &tm_kv, 0, k0, bh * 4 + 3, sy.bar(B_KV));
+        }
+        float* L2s = reinterpret_cast<float*>(smem + C::OFF_L2);
+        float* Ds = reinterpret_cast<float*>(smem + C::OFF_DD);
+        int s = 0, ph = 0;
+        for (int u = 0; u < nsub; ++u) {
+            if (!warp_wait(sy, sy.bar(B_QE + s), ph ^ 1, 0, u)) break;
+            if (lane == 0) {
+                const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE;
+                mbar_expect_tx(sy.bar(B_QF + s), 3 * C::QTILE);
+                tma_load_3d(st, &tm_q, 0, u * C::BS, bh * 4 + 0, sy.bar(B_QF + s));
+                tma_load_3d(st + C::QTILE, &tm_do_lo, 0, u * C::BS, bh, sy.bar(B_QF + s));
+                tma_load_3d(st + 2 * C::QTILE, &tm_do_hi, 0, u * C::BS, bh, sy.bar(B_QF + s));
+            }
+#pragma unroll
+            for (int x = 0; x < C::NST; ++x)
+                if (x == s) last_issued[x] = u;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int q = lane * 2 + e;
+                const int i = u * C::BS + q;
+                const bool v = i < N;
+                L2s[s * 64 + q] = v ? lse[(size_t)bh * N + i] * kLog2e : INFINITY;
+                Ds[s * 64 + q] = v ? Drow[(size_t)bh * N + i] : 0.f;
+            }
+            mbar_arrive(sy.bar(B_QF + s));
+            if (++s == C::NST) { s = 0; ph ^= 1; }
+        }
+        __syncwarp();
+        if (*sy.abort && lane == 0) {
+            wait_drain(sy.bar(B_KV), 0);
+#pragma unroll
+            for (int x = 0; x < C::NST; ++x)
+                if (last_issued[x] >= 0) wait_drain(sy.bar(B_QF + x), (last_issued[x] / C::NST) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t ID_S = idesc_bf16(128, 64, 0, 0);
+            constexpr uint32_t ID_DV = idesc_bf16(128, 2 * D, 0, 1);
+            constexpr uint32_t ID_DK = idesc_bf16(128, D, 0, 1);
+            constexpr uint32_t SBO = 8 * C::ROWB;
+            constexpr uint32_t KSTEP = (16 * C::ROWB) >> 4;
+            constexpr uint32_t STAGE_U = C::STAGE >> 4, QTILE_U = C::QTILE >> 4;
+            const uint64_t dK = smem_desc(sb + C::OFF_K, 16, SBO, C::SW);
+            const uint64_t dVL = smem_desc(sb + C::OFF_VL, 16, SBO, C::SW);
+            const uint64_t dVH = smem_desc(sb + C::OFF_VH, 16, SBO, C::SW);
+            const uint64_t dStage0 = smem_desc(sb + C::OFF_STAGE, 16, SBO, C::SW);
+            const uint64_t dStage0mn = smem_desc(sb + C::OFF_STAGE + C::QTILE, C::QTILE, SBO, C::SW);
+            auto issue_s_dp = [&](int u) {
+                const int s = u % C::NST;
+                const uint64_t dQs = dStage0 + STAGE_U * s;
+                const uint32_t tS = tmem + 128u * (u % C::NB), tDP = tS + 64;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) mma_bf16_ss(tS, dK + 2 * kk, dQs + 2 * kk, ID_S, kk);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16_ss(tDP, dVL + 2 * kk, dQs + QTILE_U + 2 * kk, ID_S, kk);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16_ss(tDP, dVH + 2 * kk, dQs + 2 * QTILE_U + 2 * kk, ID_S, 1);
+                mma_commit(sy.bar(B_SF + u % C::NB));
+            };
+            bool ok = wait_bounded(sy, sy.bar(B_KV), 0, 1, -1);
+            for (int u = 0; u < C::NB && u < nsub && ok; ++u) ok = wait_bounded(sy, sy.bar(B_QF + u), 0, 1, u);
+            if (ok) {
+                tc_fence_after();
+                for (int u = 0; u < C::NB && u < nsub; ++u) issue_s_dp(u);
+            }
+            for (int u = 0; u < nsub && ok; ++u) {
+                const int b = u % C::NB, s = u % C::NST;
+                ok = wait_bounded(sy, sy.bar(B_PF + (u & 1)), (u >> 1) & 1, 1, u);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t dGmn = dStage0mn + STAGE_U * s;
+                const uint64_t dQmn = dStage0 + STAGE_U * s;
+                const uint32_t tP = tmem + 128u * b, tDS = tP + 64;
+#pragma unroll
+                for (int kk = 0; kk < C::BS / 16; ++kk) {
+                    const uint32_t acc = (u > 0 || kk > 0) ? 1u : 0u;
+                    mma_bf16_ts(tmem + C::C_DV, tP + 8 * kk, dGmn + KSTEP * kk, ID_DV, acc);
+                    mma_bf16_ts(tmem + C::C_DK, tDS + 8 * kk, dQmn + KSTEP * kk, ID_DK, acc);
+                }
+                mma_commit(sy.bar(B_QE + s));
+                if (u + C::NB < nsub) issue_s_dp(u + C::NB);
+            }
+            mma_commit(sy.bar(B_ACC));
+            if (!ok) wait_drain(sy.bar(B_ACC), 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax-gradient warpgroups
+        const int grp = (warp - 2) >> 2;
+        const int q4 = warp & 3;
+        const int jl = q4 * 32 + lane;
+        const bool kvalid = k0 + jl < N;
+        const bool full = k0 + C::BM <= N;
+        const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+        bool ok = true;
+        for (int u = grp; u < nsub; u += 2) {
+            const int s = u % C::NST, buf = u % C::NB;
+            ok = warp_wait(sy, sy.bar(B_SF + buf), (u / C::NB) & 1, 2, u) &&
+                 warp_wait(sy, sy.bar(B_QF + s), (u / C::NST) & 1, 2, u);
+            if (!ok) break;
+            tc_fence_after();
+            const float* L2s = reinterpret_cast<const float*>(smem + C::OFF_L2) + s * 64;
+            const float* Ds = reinterpret_cast<const float*>(smem + C::OFF_DD) + s * 64;
+            const uint32_t tS = trow + 128u * buf, tDP = tS + 64;
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+                uint32_t sr[32], pr[32];
+                tmem_ld_32x32b_x32(tS + 32 * c, sr);
+                tmem_ld_32x32b_x32(tDP + 32 * c, pr);
+                tmem_wait_ld();
+                uint32_t pk[16], dk[16];
+                if (full)
+                    softmax_vals<false>(sr, pr, L2s + 32 * c, Ds + 32 * c, scale_log2, kvalid, pk, dk);
+                else
+                    softmax_vals<true>(sr, pr, L2s + 32 * c, Ds + 32 * c, scale_log2, kvalid, pk, dk);
+                // P over the S^T columns, dS over the dP^T columns (chunk c's values are in registers)
+                tmem_st_32x32b_x16(tS + 16 * c, pk);
+                tmem_st_32x32b_x16(tDP + 16 * c, dk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            if (u + C::NB < nsub)
+                ok = warp_wait(sy, sy.bar(B_QF + (u + C::NB) % C::NST), ((u + C::NB) / C::NST) & 1, 2, u);
+            mbar_arrive(sy.bar(B_PF + grp));
+            if (!ok) break;
+        }
+        if (grp == 0) {
+            if (ok) ok = warp_wait(sy, sy.bar(B_ACC), 0, 2, nsub);
+            if (ok) {
+                tc_fence_after();
+                uint32_t v[D];
+                const size_t sec = (size_t)N * D;
+                bf16* out = d_packed + (size_t)bh * 4 * sec + (size_t)(k0 + jl) * D;
+#pragma unroll
+                for (int which = 0; which < 3; ++which) {
+                    const uint32_t col = which == 0 ? C::C_DK : C::C_DV + (which - 1) * D;
+                    const float mul = which == 0 ? scale : 1.f;
+                    tmem_ld_row<D>(trow + col, v);
+                    tmem_wait_ld();
+                    if (kvalid) {
+                        bf16* o = out + (size_t)(1 + which) * sec;
+#pragma unroll
+                        for (int e = 0; e < D; e += 8) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(v[e + 0]) * mul, __uint_as_float(v[e + 1]) * mul);
+                            w.y = pack_bf16x2(__uint_as_float(v[e + 2]) * mul, __uint_as_float(v[e + 3]) * mul);
+                            w.z = pack_bf16x2(__uint_as_float(v[e + 4]) * mul, __uint_as_float(v[e + 5]) * mul);
+                            w.w = pack_bf16x2(__uint_as_float(v[e + 6]) * mul, __uint_as_float(v[e + 7]) * mul);
+                            *reinterpret_cast<uint4*>(o + e) = w;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
 // ---------------------------------------------------------------- bounded-wait self-test
 // One CTA waits, through the same bounded wait as the backward kernel, on a
 // barrier that nothing arrives on, with a short limit: the wait gives up, the
@@ -494,9 +743,11 @@ pre_kernel(const bf16* __restrict__ o_lo, const bf16* __restrict__ o_hi, const b
             acc = fmaf(fc.x, fd.x, acc);
             acc = fmaf(fc.y, fd.y, acc);
         }
-        float4* z = reinterpret_cast<float4*>(dq_acc + (size_t)row * D);
+        if (dq_acc) {  // null in the two-pass mode, which has no dQ accumulator
+            float4* z = reinterpret_cast<float4*>(dq_acc + (size_t)row * D);
 #pragma unroll
-        for (int k = part; k < D / 4; k += TPR) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k = part; k < D / 4; k += TPR) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
 #pragma unroll
     for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, TPR);
@@ -620,6 +871,57 @@ int launch(const BwdArgs& a, std::string* err) {
     return PSA_OK;
 }
 
+// Two-pass mode: D, then the key-outer dK/dV pass, then the query-outer dQ
+// pass (tc_dq.cu).  Every output element is summed in one fixed order.
+template <int D>
+int launch_two_pass(const BwdArgs& a, std::string* err) {
+    using M = CfgS<D>;
+    auto enc = get_encode(err);
+    if (!enc) return PSA_ERR_CUDA;
+    CUtensorMap tm_kv, tm_q, tm_lo, tm_hi;
+    if (!encode_3d(enc, &tm_kv, a.packed, D, a.N, a.BH * 4, M::BM, err) ||
+        !encode_3d(enc, &tm_q, a.packed, D, a.N, a.BH * 4, M::BS, err) ||
+        !encode_3d(enc, &tm_lo, a.do_lo, D, a.N, a.BH, M::BS, err) ||
+        !encode_3d(enc, &tm_hi, a.do_hi, D, a.N, a.BH, M::BS, err))
+        return PSA_ERR_CUDA;
+    static std::once_flag attr_once;
+    static cudaError_t attr_st = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_st = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, M::SMEM);
+    });
+    if (attr_st != cudaSuccess) {
+        *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(attr_st);
+        return PSA_ERR_CUDA;
+    }
+    const long long rows = a.BH * a.N;
+    float* Drow = static_cast<float*>(a.workspace);
+    const int nkt = (a.N + M::BM - 1) / M::BM;
+    const long long grid = a.BH * nkt;
+    const long long pre_grid = (rows + 256 / (D / 8) - 1) / (256 / (D / 8));
+    if (grid > 0x7fffffffll || pre_grid > 0x7fffffffll) {
+        *err = "grid too large";
+        return PSA_ERR_UNSUPPORTED;
+    }
+    bf16* dp = static_cast<bf16*>(a.d_packed);
+    {
+        ProfScope prof(kSlotPre, a.stream);
+        pre_kernel<D><<<(unsigned)pre_grid, 256, 0, a.stream>>>(
+            static_cast<const bf16*>(a.o_lo), static_cast<const bf16*>(a.o_hi), static_cast<const bf16*>(a.do_lo),
+            static_cast<const bf16*>(a.do_hi), Drow, nullptr, rows);
+    }
+    {
+        ProfScope prof(kSlotMain, a.stream);
+        bwd_dkdv_kernel<D><<<(unsigned)grid, kThreadsS, M::SMEM, a.stream>>>(
+            tm_kv, tm_q, tm_lo, tm_hi, a.lse, Drow, dp, a.N, nkt, a.scale, a.scale * kLog2e);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        *err = std::string("tensor-core dK/dV launch: ") + cudaGetErrorString(e);
+        return PSA_ERR_CUDA;
+    }
+    return tc_dq_launch(a, Drow, err);
+}
+
 }  // namespace
 
 bool tc_supported(int dtype, int d) { return dtype == PSA_BF16 && (d == 16 || d == 32 || d == 64); }
@@ -627,6 +929,17 @@ bool tc_supported(int dtype, int d) { return dtype == PSA_BF16 && (d == 16 || d 
 size_t tc_workspace_bytes(long long BH, int N, int d) {
     const size_t rows = (size_t)BH * (size_t)N;
     return align256(rows * 4) + rows * (size_t)d * 4;
+}
+
+size_t tc_two_pass_workspace_bytes(long long BH, int N) { return align256((size_t)BH * (size_t)N * 4); }
+
+int tc_two_pass_launch(const BwdArgs& a, std::string* err) {
+    switch (a.d) {
+        case 16: return launch_two_pass<16>(a, err);
+        case 32: return launch_two_pass<32>(a, err);
+        case 64: return launch_two_pass<64>(a, err);
+        default: *err = "unsupported head_dim"; return PSA_ERR_UNSUPPORTED;
+    }
 }
 
 int tc_bwd_launch(const BwdArgs& a, std::string* err) {

@@ -90,6 +90,19 @@ def test_bwd_bad_algo(lib):
 
 def test_bwd_tc_unsupported_for_fp32(lib):
     assert _bwd(algo=B.PSA_ALGO_TC, dtype=B.PSA_F32, workspace_bytes=1 << 20) == B.PSA_ERR_UNSUPPORTED
+    assert _bwd(algo=B.PSA_ALGO_TC_2PASS, dtype=B.PSA_F32, workspace_bytes=1 << 20) == B.PSA_ERR_UNSUPPORTED
+    assert _bwd(algo=B.PSA_ALGO_TC_2PASS + 1, workspace_bytes=1 << 20) == B.PSA_ERR_ARG
+
+
+def test_two_pass_workspace_and_forward_rejects_it(lib):
+    # the two-pass backward keeps only D (fp32 per query row, 256-byte aligned)
+    assert B.psa_attn_bwd_workspace_bytes(2, 3, 100, 32, B.PSA_BF16, B.PSA_ALGO_TC_2PASS) == 2560
+    assert B.psa_attn_bwd_workspace_bytes(1, 1, 100, 32, B.PSA_BF16, B.PSA_ALGO_TC_2PASS) == 512
+    assert B.psa_attn_bwd_workspace_bytes(1, 1, 100, 32, B.PSA_F32, B.PSA_ALGO_TC_2PASS) == 0
+    # the fused mode also holds an fp32 dQ accumulator
+    assert B.psa_attn_bwd_workspace_bytes(1, 1, 100, 32, B.PSA_BF16, B.PSA_ALGO_TC) == 512 + 100 * 32 * 4
+    rc = B.lib().psa_attn_fwd_algo(FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 16, 1.0, B.PSA_BF16, B.PSA_ALGO_TC_2PASS, None)
+    assert rc == B.PSA_ERR_ARG
 
 
 def test_workspace_bytes(lib):

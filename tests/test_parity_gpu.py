@@ -26,7 +26,7 @@ def _built():
 def algos_for(dtype, d):
     out = [B.PSA_ALGO_SIMT]
     if B.psa_attn_bwd_workspace_bytes(1, 1, 16, d, {"f32": 0, "bf16": 1}[dtype], B.PSA_ALGO_TC) > 0:
-        out.append(B.PSA_ALGO_TC)
+        out += [B.PSA_ALGO_TC, B.PSA_ALGO_TC_2PASS]
     return out
 
 
@@ -51,7 +51,7 @@ def _ref(name):
 
 
 @pytest.mark.parametrize("name", list(SAMPLED))
-@pytest.mark.parametrize("algo", [B.PSA_ALGO_SIMT, B.PSA_ALGO_TC])
+@pytest.mark.parametrize("algo", [B.PSA_ALGO_SIMT, B.PSA_ALGO_TC, B.PSA_ALGO_TC_2PASS])
 def test_workload_parity(name, algo):
     w = WORKLOADS[name]
     if algo not in algos_for(w.dtype, w.d):
@@ -99,11 +99,27 @@ def test_dv_sums_match_do_sums(dtype):
             assert rel_err(g[:, h].sum(axis=1), ref) < (1e-4 if dtype == "f32" else 2e-2)
 
 
-def test_simt_is_deterministic():
-    inp = make_custom(BH=2, N=257, d=32, dtype="bf16", seed=79)
-    a = gpu_fwd_bwd(inp, B.PSA_ALGO_SIMT)["d_packed"]
-    b = gpu_fwd_bwd(inp, B.PSA_ALGO_SIMT)["d_packed"]
-    np.testing.assert_array_equal(a, b)
+@pytest.mark.parametrize("algo", [B.PSA_ALGO_SIMT, B.PSA_ALGO_TC_2PASS])
+def test_atomic_free_modes_are_deterministic(algo):
+    """The CUDA-core and two-pass tensor-core backwards sum every output in a
+    fixed order: repeated runs agree bit for bit (many key and query tiles, a
+    ragged tail)."""
+    for d in (16, 32, 64):
+        inp = make_custom(BH=3, N=777, d=d, dtype="bf16", seed=79 + d)
+        a = gpu_fwd_bwd(inp, algo)["d_packed"]
+        for _ in range(2):
+            np.testing.assert_array_equal(a, gpu_fwd_bwd(inp, algo)["d_packed"])
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+def test_two_pass_matches_fused_tensor_core(d):
+    """The two tensor-core modes compute the same products with the same bf16
+    roundings of P and dS; they differ only in fp32 summation order."""
+    inp = make_custom(BH=2, N=1000, d=d, dtype="bf16", seed=90 + d)
+    a = gpu_fwd_bwd(inp, B.PSA_ALGO_TC)["d_packed"]
+    b = gpu_fwd_bwd(inp, B.PSA_ALGO_TC_2PASS)["d_packed"]
+    for sec in range(4):
+        assert rel_err(b[:, sec], a[:, sec]) < 1e-2, sec
 
 
 def test_overwrites_d_packed_and_stream_arg():
