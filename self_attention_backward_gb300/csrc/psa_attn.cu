@@ -248,7 +248,12 @@ int psa_attn_bwd_algo(const void* packed, const void* o_lo, const void* o_hi, co
                    s.BH, N, head_dim, scale, dtype, (cudaStream_t)stream};
     if (algo == PSA_ALGO_TC || algo == PSA_ALGO_TC_2PASS) {
         std::string err;
-        rc = algo == PSA_ALGO_TC ? psa::tc_bwd_launch(a, &err) : psa::tc_two_pass_launch(a, &err);
+        if (algo == PSA_ALGO_TC)
+            rc = psa::tc_bwd_launch(a, &err);
+        else if (psa::tc_pair_supported(dtype, head_dim))
+            rc = psa::tc_pair_launch(a, &err);
+        else
+            rc = psa::tc_two_pass_launch(a, &err);
         if (rc) return fail(rc, "%s", err.c_str());
         return ok();
     }
@@ -309,6 +314,7 @@ int psa_attn_sync_status(void* stream) {
     if (psa::tc_take_device_error(&err)) return fail(PSA_ERR_TIMEOUT, "%s", err.c_str());
     if (psa::tc_fwd_take_device_error(&err)) return fail(PSA_ERR_TIMEOUT, "%s", err.c_str());
     if (psa::tc_dq_take_device_error(&err)) return fail(PSA_ERR_TIMEOUT, "%s", err.c_str());
+    if (psa::tc_pair_take_device_error(&err)) return fail(PSA_ERR_TIMEOUT, "%s", err.c_str());
     return ok();
 }
 

@@ -57,6 +57,13 @@ int tc_bwd_launch(const BwdArgs& a, std::string* err);
 // the key-outer dK/dV pass (tc_bwd.cu), the query-outer dQ pass (tc_dq.cu).
 size_t tc_two_pass_workspace_bytes(long long BH, int N);
 int tc_two_pass_launch(const BwdArgs& a, std::string* err);
+// D = rowsum(dO_lo o O_lo + dO_hi o O_hi) into `Drow` ([BH*N] fp32), bf16 inputs.
+int tc_pre_d_launch(const BwdArgs& a, float* Drow, std::string* err);
+// Two-pass backward on SM pairs (cta_group::2, tc_pair.cu), head_dim 32 or 64;
+// same workspace as tc_two_pass_launch.
+bool tc_pair_supported(int dtype, int d);
+int tc_pair_launch(const BwdArgs& a, std::string* err);
+int tc_pair_take_device_error(std::string* err);
 // The query-outer dQ pass alone; `Drow` = [BH*N] fp32 row statistics D.
 int tc_dq_launch(const BwdArgs& a, const float* Drow, std::string* err);
 int tc_dq_take_device_error(std::string* err);

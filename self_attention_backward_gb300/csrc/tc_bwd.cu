@@ -105,9 +105,15 @@ struct Cfg {
     static_assert(USED + 1024 <= 232448, "shared memory budget");
 };
 
-// barrier indices (SF: one per S/dP buffer; PF: one per softmax warpgroup;
-// QF/QE: one per Q/dO stage)
-enum { B_KV = 0, B_SF = 1, B_PF = 4, B_DQF = 6, B_DQE = 7, B_ACC = 8, B_QF = 9, B_QE = 15 };
+// barrier indices (SF: one per S/dP buffer; PF: softmax done, a ring of 4 over
+// the sub-tiles; QF/QE: one per Q/dO stage).  A warp starts sub-tile u only
+// after S/dP(u) was issued, which followed the issuer's wait on PF(u - NB); so
+// with NB <= 3 no warp runs 4 sub-tiles ahead of a slower one and a PF barrier
+// never gets arrivals for two of its phases at once (a ring of 2 would allow a
+// warp two sub-tiles ahead to complete a slower warp's phase).
+enum { B_KV = 0, B_SF = 1, B_PF = 4, B_DQF = 8, B_DQE = 9, B_ACC = 10, B_QF = 11, B_QE = 17 };
+constexpr int kPfRing = 4;
+static_assert(B_QE + 6 <= 32, "barrier area holds 32 barriers");
 
 // P and dS of one 32-query chunk of this thread's key row, packed to bf16
 // pairs: P = exp2(S * scale*log2e - L), dS = P (dP - D).
@@ -155,8 +161,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
     if (threadIdx.x == 0) {
         mbar_init(sy.bar(B_KV), 1);
         for (int b = 0; b < C::NB; ++b) mbar_init(sy.bar(B_SF + b), 1);
-        mbar_init(sy.bar(B_PF), 128);
-        mbar_init(sy.bar(B_PF + 1), 128);
+        for (int x = 0; x < kPfRing; ++x) mbar_init(sy.bar(B_PF + x), 128);
         mbar_init(sy.bar(B_DQF), 1);
         mbar_init(sy.bar(B_DQE), 128);
         mbar_init(sy.bar(B_ACC), 1);
@@ -309,7 +314,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             // has emptied the dQ accumulator (the softmax warpgroup waited for both).
             for (int u = 0; u < nsub && ok; ++u) {
                 const int b = u & 1;
-                ok = wait_bounded(sy, sy.bar(B_PF + b), (u >> 1) & 1, 1, u);
+                ok = wait_bounded(sy, sy.bar(B_PF + u % kPfRing), (u / kPfRing) & 1, 1, u);
                 if (!ok) break;
                 tc_fence_after();
                 const bool pair_done = b == 1 || u == nsub - 1;
@@ -383,7 +388,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 ok = warp_wait(sy, sy.bar(B_QF + (u + C::NB) % C::NST), ((u + C::NB) / C::NST) & 1, 2, u);
             if (ok && ((u & 1) == 1 || u == nsub - 1) && u >= 2)
                 ok = warp_wait(sy, sy.bar(B_DQE), ((u >> 1) - 1) & 1, 2, u);
-            mbar_arrive(sy.bar(B_PF + grp));
+            mbar_arrive(sy.bar(B_PF + u % kPfRing));
             if (!ok) break;
         }
         // epilogue (warpgroup 0): dK, dV_lo, dV_hi rows of this thread's key
@@ -497,8 +502,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
     if (threadIdx.x == 0) {
         mbar_init(sy.bar(B_KV), 1);
         for (int b = 0; b < C::NB; ++b) mbar_init(sy.bar(B_SF + b), 1);
-        mbar_init(sy.bar(B_PF), 128);
-        mbar_init(sy.bar(B_PF + 1), 128);
+        for (int x = 0; x < kPfRing; ++x) mbar_init(sy.bar(B_PF + x), 128);
         mbar_init(sy.bar(B_ACC), 1);
         for (int s = 0; s < C::NST; ++s) {
             mbar_init(sy.bar(B_QF + s), 32);
@@ -600,7 +604,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             }
             for (int u = 0; u < nsub && ok; ++u) {
                 const int b = u % C::NB, s = u % C::NST;
-                ok = wait_bounded(sy, sy.bar(B_PF + (u & 1)), (u >> 1) & 1, 1, u);
+                ok = wait_bounded(sy, sy.bar(B_PF + u % kPfRing), (u / kPfRing) & 1, 1, u);
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t dGmn = dStage0mn + STAGE_U * s;
@@ -656,7 +660,7 @@ bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             tc_fence_before();
             if (u + C::NB < nsub)
                 ok = warp_wait(sy, sy.bar(B_QF + (u + C::NB) % C::NST), ((u + C::NB) / C::NST) & 1, 2, u);
-            mbar_arrive(sy.bar(B_PF + grp));
+            mbar_arrive(sy.bar(B_PF + u % kPfRing));
             if (!ok) break;
         }
         if (grp == 0) {
@@ -932,6 +936,35 @@ size_t tc_workspace_bytes(long long BH, int N, int d) {
 }
 
 size_t tc_two_pass_workspace_bytes(long long BH, int N) { return align256((size_t)BH * (size_t)N * 4); }
+
+int tc_pre_d_launch(const BwdArgs& a, float* Drow, std::string* err) {
+    const long long rows = a.BH * a.N;
+    const int rpb = 256 / (a.d / 8);
+    const long long grid = (rows + rpb - 1) / rpb;
+    if (grid > 0x7fffffffll) {
+        *err = "grid too large";
+        return PSA_ERR_UNSUPPORTED;
+    }
+    const bf16* o_lo = static_cast<const bf16*>(a.o_lo);
+    const bf16* o_hi = static_cast<const bf16*>(a.o_hi);
+    const bf16* do_lo = static_cast<const bf16*>(a.do_lo);
+    const bf16* do_hi = static_cast<const bf16*>(a.do_hi);
+    {
+        ProfScope prof(kSlotPre, a.stream);
+        switch (a.d) {
+            case 16: pre_kernel<16><<<(unsigned)grid, 256, 0, a.stream>>>(o_lo, o_hi, do_lo, do_hi, Drow, nullptr, rows); break;
+            case 32: pre_kernel<32><<<(unsigned)grid, 256, 0, a.stream>>>(o_lo, o_hi, do_lo, do_hi, Drow, nullptr, rows); break;
+            case 64: pre_kernel<64><<<(unsigned)grid, 256, 0, a.stream>>>(o_lo, o_hi, do_lo, do_hi, Drow, nullptr, rows); break;
+            default: *err = "unsupported head_dim"; return PSA_ERR_UNSUPPORTED;
+        }
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        *err = std::string("row-statistics launch: ") + cudaGetErrorString(e);
+        return PSA_ERR_CUDA;
+    }
+    return PSA_OK;
+}
 
 int tc_two_pass_launch(const BwdArgs& a, std::string* err) {
     switch (a.d) {

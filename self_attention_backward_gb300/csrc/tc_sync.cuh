@@ -50,6 +50,32 @@ __device__ __forceinline__ bool wait_bounded(const Sync& s, uint32_t bar, uint32
     return wait_slow(s, bar, parity, role, tile);
 }
 
+// The same bounded wait with cluster-scope acquire, for barriers that the
+// peer CTA of a pair arrives on.
+static __device__ __noinline__ bool wait_slow_cluster(const Sync& s, uint32_t bar, uint32_t parity, int role,
+                                                      int tile) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 15) == 15) {
+            if (*s.abort) return false;
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kTimeoutNs) {
+                *s.abort = 1;
+                atomicCAS(s.err, 0, ((1 + role) << 24) | (tile & 0xFFFFFF));
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ bool wait_bounded_cluster(const Sync& s, uint32_t bar, uint32_t parity, int role,
+                                                     int tile) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    return wait_slow_cluster(s, bar, parity, role, tile);
+}
+
 // Whole-warp wait: every lane waits, the warp agrees on the outcome.
 __device__ __forceinline__ bool warp_wait(const Sync& s, uint32_t bar, uint32_t parity, int role, int tile) {
     const bool ok = wait_bounded(s, bar, parity, role, tile);
