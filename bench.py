@@ -106,7 +106,7 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_slot: str, workload: str):
+def recorded_traffic(kernel_slot: str, workload: str, algo: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -115,7 +115,7 @@ def recorded_traffic(kernel_slot: str, workload: str):
             rec = json.load(f)
     except Exception:
         return None
-    e = rec.get(workload, {}).get(kernel_slot)
+    e = rec.get(workload, {}).get(algo, {}).get(kernel_slot)
     if not e or e.get("source_hash") != source_hash():
         return None
     return float(e["dram_bytes_per_launch"])
@@ -342,7 +342,7 @@ def run_ours(args, w):
         achieved = alg_bytes(w) / (dom_ms * 1e-3) / 1e9
         peak, unit = peaks["hbm_gbs"], "GB/s"
         peak_note = f"hbm_gbs of {peaks_src}"
-    traffic = recorded_traffic(dom, w.name)
+    traffic = recorded_traffic(dom, w.name, used_algo)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
