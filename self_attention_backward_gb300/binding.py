@@ -234,11 +234,17 @@ def attn_bwd(packed, o_lo, o_hi, lse, do_lo, do_hi, scale: float, d_packed=None,
 
 class HostBwd:
     """psa_attn_bwd on HOST tensors: copies the inputs host->device, runs the
-    backward, copies d_packed device->host, all on one stream.  Host tensors
-    should be pinned for asynchronous copies.  Device staging buffers and the
-    workspace are allocated once, for one shape."""
+    backward, copies d_packed device->host.  Host tensors should be pinned for
+    asynchronous copies.  Device staging buffers and the workspace are
+    allocated once, for one shape.
 
-    def __init__(self, BH: int, N: int, d: int, dtype: int, device="cuda", algo=PSA_ALGO_AUTO):
+    The (batch*head) slices are independent, so the work is split into
+    `chunks` groups of slices and pipelined over three streams: the copy of
+    group c+1 to the device and the copy of group c-1 back to the host run
+    while the backward of group c runs on the caller's stream.  The call
+    returns with the caller's stream ordered after the last copy back."""
+
+    def __init__(self, BH: int, N: int, d: int, dtype: int, device="cuda", algo=PSA_ALGO_AUTO, chunks=None):
         import torch
         tdt = _torch_dtype(dtype)
         self.shape = (BH, N, d)
@@ -250,8 +256,20 @@ class HostBwd:
         self.do_hi = torch.empty_like(self.o_lo)
         self.lse = torch.empty((BH, N), dtype=torch.float32, device=device)
         self.d_packed = torch.empty_like(self.packed)
-        self.ws_bytes = psa_attn_bwd_workspace_bytes(BH, 1, N, d, dtype, algo)
+        if chunks is None:
+            # two groups: more would shrink each launch's grid below a few waves
+            chunks = 2 if BH >= 4 else 1
+        if N % 4:
+            chunks = 1  # every slice of `lse` must start on a 16-byte boundary
+        chunks = max(1, min(int(chunks), BH))
+        self.bounds = [(BH * c // chunks, BH * (c + 1) // chunks) for c in range(chunks)]
+        self.ws_bytes = max(psa_attn_bwd_workspace_bytes(b1 - b0, 1, N, d, dtype, algo) for b0, b1 in self.bounds)
         self.ws = BwdWorkspace(device).get(self.ws_bytes)
+        self.s_in = torch.cuda.Stream(device=device)
+        self.s_out = torch.cuda.Stream(device=device)
+        self.ev_in = [torch.cuda.Event() for _ in self.bounds]
+        self.ev_k = [torch.cuda.Event() for _ in self.bounds]
+        self.ev_done = torch.cuda.Event()
 
     def h2d_bytes(self) -> int:
         ts = (self.packed, self.o_lo, self.o_hi, self.lse, self.do_lo, self.do_hi)
@@ -261,12 +279,27 @@ class HostBwd:
         return self.d_packed.numel() * self.d_packed.element_size()
 
     def __call__(self, packed, o_lo, o_hi, lse, do_lo, do_hi, scale: float, out, stream=None):
-        BH, N, d = self.shape
-        for dst, src in ((self.packed, packed), (self.o_lo, o_lo), (self.o_hi, o_hi), (self.lse, lse),
-                         (self.do_lo, do_lo), (self.do_hi, do_hi)):
-            dst.copy_(src, non_blocking=True)
-        psa_attn_bwd(self.packed, self.o_lo, self.o_hi, self.lse, self.do_lo, self.do_hi, self.d_packed,
-                     self.ws, self.ws_bytes, BH, 1, N, d, scale, dtype=self.dtype, stream=stream,
-                     algo=self.algo)
-        out.copy_(self.d_packed, non_blocking=True)
+        import torch
+        _, N, d = self.shape
+        main = stream if stream is not None else torch.cuda.current_stream()
+        # the staging buffers and d_packed are free once the caller's stream got here
+        self.s_in.wait_stream(main)
+        self.s_out.wait_stream(main)
+        pairs = ((self.packed, packed), (self.o_lo, o_lo), (self.o_hi, o_hi), (self.lse, lse),
+                 (self.do_lo, do_lo), (self.do_hi, do_hi))
+        for c, (b0, b1) in enumerate(self.bounds):
+            with torch.cuda.stream(self.s_in):
+                for dst, src in pairs:
+                    dst[b0:b1].copy_(src[b0:b1], non_blocking=True)
+                self.ev_in[c].record(self.s_in)
+            main.wait_event(self.ev_in[c])
+            psa_attn_bwd(self.packed[b0:b1], self.o_lo[b0:b1], self.o_hi[b0:b1], self.lse[b0:b1],
+                         self.do_lo[b0:b1], self.do_hi[b0:b1], self.d_packed[b0:b1], self.ws, self.ws_bytes,
+                         b1 - b0, 1, N, d, scale, dtype=self.dtype, stream=main, algo=self.algo)
+            self.ev_k[c].record(main)
+            self.s_out.wait_event(self.ev_k[c])
+            with torch.cuda.stream(self.s_out):
+                out[b0:b1].copy_(self.d_packed[b0:b1], non_blocking=True)
+        self.ev_done.record(self.s_out)
+        main.wait_event(self.ev_done)
         return out

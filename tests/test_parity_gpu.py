@@ -186,3 +186,29 @@ def test_tensor_core_forward_full_size_sampled():
     assert rel_err(o_lo[3].double().cpu().numpy(), ref["o_lo"][0]) <= TOL["bf16"]
     assert rel_err(o_hi[3].double().cpu().numpy(), ref["o_hi"][0]) <= TOL["bf16"]
     assert rel_err(lse[3].double().cpu().numpy(), ref["lse"][0]) <= TOL_LSE
+
+
+@pytest.mark.parametrize("chunks", [1, 3])
+def test_host_buffers_pipelined_match_device_path(chunks):
+    """HostBwd (host tensors in, host d_packed out, slices pipelined over
+    streams in `chunks` groups) gives the device path's result: bit for bit in
+    the two-pass mode, and within tolerance of the oracle."""
+    import torch
+    from gpu_helpers import to_device, TOL
+    inp = make_custom(BH=6, N=132, d=32, dtype="bf16", seed=95)
+    dev = gpu_fwd_bwd(inp, B.PSA_ALGO_TC_2PASS)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).pin_memory()  # noqa: E731
+    packed, do_lo, do_hi = pin(inp.packed), pin(inp.do_lo), pin(inp.do_hi)
+    o_lo, o_hi, lse = B.attn_fwd(to_device(inp.packed, "bf16"), inp.scale)
+    o_lo, o_hi, lse = o_lo.cpu().pin_memory(), o_hi.cpu().pin_memory(), lse.cpu().pin_memory()
+    out = torch.empty(packed.shape, dtype=torch.bfloat16).pin_memory()
+    runner = B.HostBwd(6, 132, 32, B.PSA_BF16, algo=B.PSA_ALGO_TC_2PASS, chunks=chunks)
+    assert len(runner.bounds) == chunks
+    for _ in range(2):  # the second call reuses the staging buffers
+        runner(packed, o_lo, o_hi, lse, do_lo, do_hi, inp.scale, out)
+    torch.cuda.synchronize()
+    B.psa_attn_sync_status()
+    got = out.double().numpy()
+    np.testing.assert_array_equal(got, dev["d_packed"])
+    ref = oracle_fwd_bwd(inp)["d_packed"]
+    assert rel_err(got, ref) < TOL["bf16"]
