@@ -1,0 +1,226 @@
+"""ncu evidence harness for the backward kernels.
+
+On a machine with the GPU it runs the benchmark once plainly, then twice under
+Nsight Compute (`--clock-control none` always):
+
+1. the launch list (`gpu__time_duration.sum` only, one pass per launch) of the
+   whole benchmark command;
+2. one backward step's kernels with DRAM bytes, duration and tensor-pipe
+   utilisation (a handful of passes per launch, a few launches);
+
+and writes Markdown summaries: per kernel its launches, total time and share,
+and per captured launch its DRAM traffic, achieved DRAM bandwidth against the
+measured HBM peak, and tensor-pipe busy fraction.  The summarising half reads
+ncu's `--csv` output and runs anywhere.
+
+    python -m self_attention_backward_gb300.ncu_harness run --out DIR [--algo tc|tc2|simt|auto]
+    python -m self_attention_backward_gb300.ncu_harness launches DIR/launches.csv
+    python -m self_attention_backward_gb300.ncu_harness kernels DIR/kernels.csv
+
+ncu's per-launch times are cold-cache and serialised: compare shares, not
+absolute times, with the benchmark's CUDA-event numbers.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import json
+import os
+import subprocess
+import sys
+from collections import OrderedDict
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+KERNEL_METRICS = ["gpu__time_duration.sum", "dram__bytes_read.sum", "dram__bytes_write.sum",
+                  "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active"]
+BACKWARD_KERNELS = "regex:bwd_main_kernel|pair_kernel|dkdv_kernel|dq_kernel|pre_kernel|dq_finalize"
+
+_TIME_SCALE_US = {"ns": 1e-3, "nsecond": 1e-3, "us": 1.0, "usecond": 1.0, "ms": 1e3, "msecond": 1e3,
+                  "s": 1e6, "second": 1e6}
+_BYTE_SCALE = {"byte": 1.0, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "tbyte": 1e12}
+
+
+def _number(text: str) -> float:
+    return float(text.replace(",", "").strip())
+
+
+def read_metric_rows(path: str):
+    """Rows of an ncu `--csv` metrics log: (launch id, kernel, metric, unit, value)."""
+    with open(path, newline="") as f:
+        lines = [ln for ln in f if ln.startswith('"')]   # ncu may prepend its own log lines
+    rows = list(csv.reader(lines))
+    if not rows:
+        return []
+    hdr = rows[0]
+    idx = {k: hdr.index(k) for k in ("ID", "Kernel Name", "Metric Name", "Metric Unit", "Metric Value")}
+    out = []
+    for r in rows[1:]:
+        if len(r) < len(hdr):
+            continue
+        try:
+            val = _number(r[idx["Metric Value"]])
+        except ValueError:
+            continue
+        out.append((r[idx["ID"]], r[idx["Kernel Name"]], r[idx["Metric Name"]], r[idx["Metric Unit"]], val))
+    return out
+
+
+def short_name(kernel: str) -> str:
+    """`void psa::<unnamed>::bwd_main_kernel<32>(CUtensorMap_st, ...)` -> `bwd_main_kernel<32>`."""
+    s = kernel.strip()
+    if s.startswith("void "):
+        s = s[5:]
+    s = s.replace("(anonymous namespace)", "")
+    depth, cut, last = 0, len(s), 0
+    for i, ch in enumerate(s):
+        if ch == "<":
+            depth += 1
+        elif ch == ">":
+            depth = max(0, depth - 1)
+        elif ch == "(" and depth == 0:
+            cut = i
+            break
+        elif ch == ":" and depth == 0 and s[i:i + 2] == "::":
+            last = i + 2
+    return s[last:cut].strip()
+
+
+def time_us(value: float, unit: str) -> float:
+    return value * _TIME_SCALE_US[unit.strip().lower()]
+
+
+def nbytes(value: float, unit: str) -> float:
+    return value * _BYTE_SCALE[unit.strip().lower()]
+
+
+def summarize_launches(rows):
+    """Per kernel: launches, total microseconds, share of the listed time."""
+    agg: "OrderedDict[str, list]" = OrderedDict()
+    for _, kernel, metric, unit, val in rows:
+        if metric != "gpu__time_duration.sum":
+            continue
+        a = agg.setdefault(short_name(kernel), [0, 0.0])
+        a[0] += 1
+        a[1] += time_us(val, unit)
+    total = sum(t for _, t in agg.values())
+    table = [(k, n, t, 100.0 * t / total if total else 0.0, t / n) for k, (n, t) in agg.items()]
+    table.sort(key=lambda x: -x[2])
+    return table, total
+
+
+def summarize_kernels(rows, hbm_gbs: float):
+    """Per captured launch: duration, DRAM bytes, achieved GB/s and its fraction
+    of `hbm_gbs`, tensor-pipe busy percentage."""
+    per: "OrderedDict[str, dict]" = OrderedDict()
+    for lid, kernel, metric, unit, val in rows:
+        d = per.setdefault(lid, {"kernel": short_name(kernel)})
+        if metric == "gpu__time_duration.sum":
+            d["us"] = time_us(val, unit)
+        elif metric == "dram__bytes_read.sum":
+            d["read"] = nbytes(val, unit)
+        elif metric == "dram__bytes_write.sum":
+            d["write"] = nbytes(val, unit)
+        elif metric.startswith("sm__pipe_tensor_cycles_active"):
+            d["tensor_pct"] = val
+    out = []
+    for lid, d in per.items():
+        traffic = d.get("read", 0.0) + d.get("write", 0.0)
+        gbs = traffic / (d["us"] * 1e-6) / 1e9 if d.get("us") else 0.0
+        out.append({"id": lid, "kernel": d["kernel"], "us": d.get("us", 0.0), "dram_read": d.get("read", 0.0),
+                    "dram_write": d.get("write", 0.0), "gbs": gbs, "hbm_frac": gbs / hbm_gbs if hbm_gbs else 0.0,
+                    "tensor_pct": d.get("tensor_pct")})
+    return out
+
+
+def launches_markdown(table, total) -> str:
+    lines = ["| kernel | launches | total (us) | share | per launch (us) |", "|---|---|---|---|---|"]
+    for k, n, t, share, per in table:
+        lines.append(f"| {k} | {n} | {t:.1f} | {share:.1f} % | {per:.1f} |")
+    lines.append(f"| all | {sum(r[1] for r in table)} | {total:.1f} | 100 % | |")
+    return "\n".join(lines)
+
+
+def kernels_markdown(items, hbm_gbs: float) -> str:
+    lines = [f"| launch | kernel | time (us) | DRAM read (MB) | DRAM write (MB) | achieved GB/s | of {hbm_gbs:.0f} GB/s "
+             "| tensor pipe busy |", "|---|---|---|---|---|---|---|---|"]
+    for it in items:
+        tp = "n/a" if it["tensor_pct"] is None else f"{it['tensor_pct']:.1f} %"
+        lines.append(f"| {it['id']} | {it['kernel']} | {it['us']:.1f} | {it['dram_read'] / 1e6:.2f} | "
+                     f"{it['dram_write'] / 1e6:.2f} | {it['gbs']:.0f} | {100 * it['hbm_frac']:.1f} % | {tp} |")
+    return "\n".join(lines)
+
+
+def measured_hbm_gbs() -> float:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"])
+    except Exception:
+        return 6800.0   # the profiling recipe's fallback
+
+
+def _run(cmd, log_path: str) -> int:
+    with open(log_path, "w") as log:
+        return subprocess.call(cmd, cwd=ROOT, stdout=log, stderr=subprocess.STDOUT)
+
+
+def run(out_dir: str, algo: str, workload: str | None) -> int:
+    os.makedirs(out_dir, exist_ok=True)
+    bench = [sys.executable, "bench.py", "--steps", "2", "--warmup", "3", "--no-cpu", "--no-secondary",
+             "--algo", algo]
+    if workload:
+        bench += ["--workload", workload]
+    # the same command must exit 0 without ncu before ncu runs it
+    if _run(bench, os.path.join(out_dir, "plain.log")) != 0:
+        print("plain benchmark run failed; see plain.log", file=sys.stderr)
+        return 1
+    launches = os.path.join(out_dir, "launches.csv")
+    rc = _run(["ncu", "--metrics", "gpu__time_duration.sum", "--clock-control", "none", "-c", "400", "--csv",
+               "--log-file", launches] + bench, os.path.join(out_dir, "ncu_launches.log"))
+    if rc != 0:
+        return rc
+    # one backward step's kernels: skip the warm-up steps' launches (at most 3
+    # backward kernels per step; 3 warm-up steps)
+    kernels = os.path.join(out_dir, "kernels.csv")
+    rc = _run(["ncu", "--metrics", ",".join(KERNEL_METRICS), "--clock-control", "none", "-k", BACKWARD_KERNELS,
+               "-s", "9", "-c", "3", "--csv", "--log-file", kernels] + bench,
+              os.path.join(out_dir, "ncu_kernels.log"))
+    if rc != 0:
+        return rc
+    hbm = measured_hbm_gbs()
+    table, total = summarize_launches(read_metric_rows(launches))
+    items = summarize_kernels(read_metric_rows(kernels), hbm)
+    text = ("# ncu evidence: " + " ".join(bench[1:]) + "\n\n## Launch list (cold-cache, serialised)\n\n" +
+            launches_markdown(table, total) + "\n\n## One backward step\n\n" + kernels_markdown(items, hbm) + "\n")
+    with open(os.path.join(out_dir, "summary.md"), "w") as f:
+        f.write(text)
+    print(text)
+    return 0
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    sub = ap.add_subparsers(dest="cmd", required=True)
+    r = sub.add_parser("run")
+    r.add_argument("--out", required=True)
+    r.add_argument("--algo", default="auto", choices=["auto", "tc", "tc2", "simt"])
+    r.add_argument("--workload", default=None)
+    la = sub.add_parser("launches")
+    la.add_argument("csv")
+    ke = sub.add_parser("kernels")
+    ke.add_argument("csv")
+    ke.add_argument("--hbm-gbs", type=float, default=None)
+    a = ap.parse_args(argv)
+    if a.cmd == "run":
+        return run(a.out, a.algo, a.workload)
+    if a.cmd == "launches":
+        table, total = summarize_launches(read_metric_rows(a.csv))
+        print(launches_markdown(table, total))
+        return 0
+    hbm = a.hbm_gbs or measured_hbm_gbs()
+    print(kernels_markdown(summarize_kernels(read_metric_rows(a.csv), hbm), hbm))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
