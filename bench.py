@@ -96,13 +96,21 @@ def roofline_time_s(w, peaks) -> tuple[float, str]:
     return (t_t, "tensor") if t_t >= t_m else (t_m, "hbm")
 
 
-def source_hash() -> str:
+# Sources each kernel family's code comes from (the traffic record is tied to
+# their contents; a change elsewhere, such as the forward, leaves it valid).
+TRAFFIC_SOURCES = {
+    "tc": ["tc_bwd.cu", "tc_ptx.cuh", "tc_sync.cuh", "common.cuh", "psa_internal.h"],
+    "tc2": ["tc_pair.cu", "tc_bwd.cu", "tc_dq.cu", "tc_ptx.cuh", "tc_sync.cuh", "common.cuh", "psa_internal.h"],
+    "simt": ["simt_kernels.cuh", "psa_attn.cu", "common.cuh", "psa_internal.h"],
+}
+
+
+def source_hash(algo: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "self_attention_backward_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in sorted(TRAFFIC_SOURCES.get(algo, os.listdir(csrc))):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -116,7 +124,7 @@ def recorded_traffic(kernel_slot: str, workload: str, algo: str):
     except Exception:
         return None
     e = rec.get(workload, {}).get(algo, {}).get(kernel_slot)
-    if not e or e.get("source_hash") != source_hash():
+    if not e or e.get("source_hash") != source_hash(algo):
         return None
     return float(e["dram_bytes_per_launch"])
 
@@ -377,6 +385,7 @@ def run_ours(args, w):
 
     if rank == 0:
         line["e2e"] = run_e2e(w, args, device, algo)
+        line["forward"] = time_forward(w, bufs, flush, args.steps)
     if rank == 0 and world == 1 and not args.no_cpu:
         v, n, t = oracle_sample(w, args.cpu_budget)
         import oracle
@@ -388,6 +397,27 @@ def run_ours(args, w):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def time_forward(w, bufs, flush, steps):
+    """psa_attn_fwd on the same workload (support for the backward, outside the
+    timed step): CUDA-event time per call, L2 flushed before each call, and
+    TFLOP/s counting 6 N^2 d per (batch, head) (S and the two P V products)."""
+    import torch
+    from self_attention_backward_gb300 import binding as B
+    packed = bufs[0]
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        B.attn_fwd(packed, w.scale)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(st)
+        B.attn_fwd(packed, w.scale)
+        b.record(st)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    return {"ms": ms, "tflops": 6.0 * w.BH * w.N * w.N * w.d / (ms * 1e-3) / 1e12, "flops_per_bh": "6 N^2 d"}
 
 
 def run_e2e(w, args, device, algo):

@@ -6,21 +6,29 @@
 // decomposition).  As in the backward, lo and hi run as one attention with a
 // 2d-wide value [V_lo | V_hi].
 //
-// One CTA per (batch*head, 128-query tile), two passes over 128-key tiles:
-//   pass 1: S = Q K_j^T (M = 128 queries, N = 128 keys) -> per query row the
-//           running max and sum of exp2(S * scale*log2e) -> LSE;
-//   pass 2: S again, P = exp2(S * scale*log2e - LSE*log2e) (already
-//           normalised) written over S in TMEM as bf16 pairs, then
-//           [O_lo | O_hi] += P [V_lo,j | V_hi,j] with P as the MMA's A operand
-//           from TMEM (one N = 2d MMA per 16-key step).
-// Two passes recompute S once more than an online softmax would, and in
-// exchange O never needs rescaling.
+// One CTA per (batch*head, 128-query tile), one pass over 64-key tiles j with
+// an online softmax (per query row a running max m and sum l, log2 domain):
+//   S = Q K_j^T                      (M = 128 queries, N = 64 keys, K = d)
+//   m' = max(m, max_k S c) if that exceeds m by more than 8, else m
+//        (a stale max keeps P <= 2^8; when m moves, l and O are scaled by
+//        exp2(m - m'), O read and written back in TMEM)
+//   P = exp2(S c - m) written over S in TMEM as bf16 pairs,  l += sum P
+//   [O_lo | O_hi] += P [V_lo,j | V_hi,j]   (A = P from TMEM, N = 2d)
+// and at the end O / l and LSE = (m + log2 l) ln 2.  c = scale log2(e).
 //
 // Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer (one
 // thread) and TMEM owner, warps 2-5 softmax (one query row per thread, the
-// warp's TMEM lane quarter).  S is double-buffered in TMEM; K (and in pass 2
-// V_lo, V_hi) tiles are double-buffered in shared memory.  All waits are
-// bounded (tc_sync.cuh).
+// warp's TMEM lane quarter).  A CTA holds 256 TMEM columns (two 64-column S
+// buffers, then O), so two CTAs share an SM.  S(j+1) is computed while the
+// softmax works on S(j), and S(j+2) once P(j) V_j has read P(j); the other
+// CTA's softmax and MMAs fill the remaining gaps of the tensor pipe and the
+// exp2 unit.  A row max that moves by more than 2^8 makes the softmax rescale
+// O, after waiting for P(j-1) V_{j-1} to finish (rare after the first tiles).
+// K tiles rotate through two
+// shared-memory stages, [V_lo | V_hi] through two (d <= 32) or one (d = 64,
+// for two CTAs to fit an SM's shared memory); the softmax warps wait for the
+// next K and the current V before they release P, so the issuing thread waits
+// once per key tile.  All waits are bounded (tc_sync.cuh).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -44,31 +52,38 @@ using bf16 = __nv_bfloat16;
 __device__ int g_fwd_error = 0;
 
 constexpr int kFwdThreads = 192;
+constexpr float kRescaleLog2 = 8.f;   // keep a stale row max while the new one is at most 2^8 larger
 
 template <int D>
 struct FwdCfg {
     static constexpr int BQ = 128;                 // queries per CTA (MMA M)
-    static constexpr int BK = 128;                 // keys per tile
+    static constexpr int BK = 64;                  // keys per tile
     static constexpr int ROWB = D * 2;
-    static constexpr int TILE = 128 * ROWB;        // [128, D] bf16 tile
+    static constexpr int TILE = 128 * ROWB;        // [128, D] bf16 tile (Q)
+    static constexpr int KT = BK * ROWB;           // [64, D] bf16 tile (K, V_lo, V_hi)
     static constexpr uint32_t SW = D == 64 ? 2u : D == 32 ? 4u : 6u;
+    static constexpr int NK = 2;                   // K stages
+    static constexpr int NV = 2;                   // [V_lo | V_hi] stages
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_STAGE = TILE;         // stage s: K, V_lo, V_hi at +s*STAGE
-    static constexpr int STAGE = 3 * TILE;
-    static constexpr int OFF_BAR = OFF_STAGE + 2 * STAGE;
+    static constexpr int OFF_K = TILE;             // K stage s at +s*KT
+    static constexpr int OFF_V = OFF_K + NK * KT;  // V stage s: V_lo, V_hi at +s*2*KT
+    static constexpr int OFF_BAR = OFF_V + NV * 2 * KT;
     static constexpr int OFF_MISC = OFF_BAR + 128;
     static constexpr int USED = OFF_MISC + 64;
-    static constexpr int SMEM = (USED + 1024) > 118784 ? (USED + 1024) : 118784;  // one CTA per SM
-    static constexpr uint32_t C_O = 256;          // S buffers at 0 and 128; O_lo | O_hi at 256
-    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int SMEM = USED + 1024;       // two CTAs per SM
+    static constexpr uint32_t C_O = 128;           // S buffers at 0 and 64; O_lo | O_hi at 128
+    static constexpr uint32_t TMEM_COLS = 256;
+    static_assert(C_O + 2 * D <= TMEM_COLS, "TMEM budget");
+    static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
 };
 
-// barriers: Q loaded, stage full[2], stage empty[2], S ready[2], S done[2], O ready
-enum { F_Q = 0, F_FULL = 1, F_EMPTY = 3, F_SF = 5, F_SD = 7, F_ACC = 9 };
+// barriers: Q loaded, O final, S ready[2], P written[2] (softmax done), K full/empty[2],
+// V full/empty[2], O updated (after each P V)
+enum { F_Q = 0, F_ACC = 1, F_SF = 2, F_PF = 4, F_KF = 6, F_KE = 8, F_VF = 10, F_VE = 12, F_OD = 14 };
 
 template <int D>
-__global__ void __launch_bounds__(kFwdThreads, 1)
-fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, bf16* __restrict__ o_lo, bf16* __restrict__ o_hi,
+__global__ void __launch_bounds__(kFwdThreads, 2)
+fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CUtensorMap tm_kv, bf16* __restrict__ o_lo, bf16* __restrict__ o_hi,
            float* __restrict__ lse, int N, int nqt, float scale_log2) {
     using C = FwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -81,20 +96,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, bf16* __restrict__ o_lo, b
     const int bh = blockIdx.x / nqt, qt = blockIdx.x % nqt;
     const int q0 = qt * C::BQ;
     const int nk = (N + C::BK - 1) / C::BK;
-    const int total = 2 * nk;                      // pass 1 tiles, then pass 2 tiles
 
     if (threadIdx.x == 0) {
         mbar_init(sy.bar(F_Q), 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(sy.bar(F_FULL + s), 1);
-            mbar_init(sy.bar(F_EMPTY + s), 1);
-            mbar_init(sy.bar(F_SF + s), 1);
-            mbar_init(sy.bar(F_SD + s), 128);
-        }
         mbar_init(sy.bar(F_ACC), 1);
+        mbar_init(sy.bar(F_OD), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(sy.bar(F_SF + s), 1);
+            mbar_init(sy.bar(F_PF + s), 128);
+            mbar_init(sy.bar(F_KF + s), 1);
+            mbar_init(sy.bar(F_KE + s), 1);
+            mbar_init(sy.bar(F_VF + s), 1);
+            mbar_init(sy.bar(F_VE + s), 1);
+        }
         *sy.abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_pk);
+        tma_prefetch_desc(&tm_kv);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -108,70 +126,84 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, bf16* __restrict__ o_lo, b
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int last[2] = {-1, -1};
+            int lastk[C::NK], lastv[C::NV];
+#pragma unroll
+            for (int x = 0; x < C::NK; ++x) lastk[x] = -1;
+#pragma unroll
+            for (int x = 0; x < C::NV; ++x) lastv[x] = -1;
             mbar_arrive_expect_tx(sy.bar(F_Q), C::TILE);
             tma_load_3d(sb + C::OFF_Q, &tm_pk, 0, q0, bh * 4 + 0, sy.bar(F_Q));
-            for (int it = 0; it < total; ++it) {
-                const int s = it & 1, j = it < nk ? it : it - nk;
-                const bool pass2 = it >= nk;
-                if (!wait_bounded(sy, sy.bar(F_EMPTY + s), ((it >> 1) & 1) ^ 1, 0, it)) break;
-                const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE;
-                mbar_arrive_expect_tx(sy.bar(F_FULL + s), (pass2 ? 3 : 1) * C::TILE);
-                tma_load_3d(st, &tm_pk, 0, j * C::BK, bh * 4 + 1, sy.bar(F_FULL + s));
-                if (pass2) {
-                    tma_load_3d(st + C::TILE, &tm_pk, 0, j * C::BK, bh * 4 + 2, sy.bar(F_FULL + s));
-                    tma_load_3d(st + 2 * C::TILE, &tm_pk, 0, j * C::BK, bh * 4 + 3, sy.bar(F_FULL + s));
-                }
-                last[s] = it;
+            for (int j = 0; j < nk; ++j) {
+                const int sk = j % C::NK, sv = j % C::NV;
+                if (!wait_bounded(sy, sy.bar(F_KE + sk), ((j / C::NK) & 1) ^ 1, 0, j)) break;
+                mbar_arrive_expect_tx(sy.bar(F_KF + sk), C::KT);
+                tma_load_3d(sb + C::OFF_K + sk * C::KT, &tm_kv, 0, j * C::BK, bh * 4 + 1, sy.bar(F_KF + sk));
+#pragma unroll
+                for (int x = 0; x < C::NK; ++x)
+                    if (x == sk) lastk[x] = j;
+                if (!wait_bounded(sy, sy.bar(F_VE + sv), ((j / C::NV) & 1) ^ 1, 0, j)) break;
+                const uint32_t vs = sb + C::OFF_V + sv * 2 * C::KT;
+                mbar_arrive_expect_tx(sy.bar(F_VF + sv), 2 * C::KT);
+                tma_load_3d(vs, &tm_kv, 0, j * C::BK, bh * 4 + 2, sy.bar(F_VF + sv));
+                tma_load_3d(vs + C::KT, &tm_kv, 0, j * C::BK, bh * 4 + 3, sy.bar(F_VF + sv));
+#pragma unroll
+                for (int x = 0; x < C::NV; ++x)
+                    if (x == sv) lastv[x] = j;
             }
             if (*sy.abort) {
                 wait_drain(sy.bar(F_Q), 0);
-                for (int s = 0; s < 2; ++s)
-                    if (last[s] >= 0) wait_drain(sy.bar(F_FULL + s), (last[s] >> 1) & 1);
+#pragma unroll
+                for (int x = 0; x < C::NK; ++x)
+                    if (lastk[x] >= 0) wait_drain(sy.bar(F_KF + x), (lastk[x] / C::NK) & 1);
+#pragma unroll
+                for (int x = 0; x < C::NV; ++x)
+                    if (lastv[x] >= 0) wait_drain(sy.bar(F_VF + x), (lastv[x] / C::NV) & 1);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t ID_S = idesc_bf16(128, 128, 0, 0);
+            constexpr uint32_t ID_S = idesc_bf16(128, 64, 0, 0);
             constexpr uint32_t ID_O = idesc_bf16(128, 2 * D, 0, 1);   // A = P (TMEM), B = [V_lo | V_hi] MN-major
             constexpr uint32_t SBO = 8 * C::ROWB;
             constexpr uint32_t KSTEP = (16 * C::ROWB) >> 4;
             const uint64_t dQ = smem_desc(sb + C::OFF_Q, 16, SBO, C::SW);
-            const uint64_t dStage0 = smem_desc(sb + C::OFF_STAGE, 16, SBO, C::SW);
-            const uint64_t dV0 = smem_desc(sb + C::OFF_STAGE + C::TILE, C::TILE, SBO, C::SW);
-            constexpr uint32_t STAGE_U = C::STAGE >> 4;
-            auto issue_s = [&](int it) -> bool {
-                const int s = it & 1;
-                if (!wait_bounded(sy, sy.bar(F_FULL + s), (it >> 1) & 1, 1, it)) return false;
-                tc_fence_after();
-                const uint64_t dK = dStage0 + STAGE_U * s;
+            const uint64_t dK0 = smem_desc(sb + C::OFF_K, 16, SBO, C::SW);
+            const uint64_t dV0 = smem_desc(sb + C::OFF_V, C::KT, SBO, C::SW);
+            constexpr uint32_t KT_U = C::KT >> 4;
+            // S(j) = Q K_j^T into buffer j & 1; K_j is known to be loaded (the
+            // prologue waits for K_0 and K_1; the softmax warps wait for K_{j+2}
+            // before releasing P(j))
+            auto issue_s = [&](int j) {
+                const int sk = j % C::NK;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16_ss(tmem + 128u * s, dQ + 2 * kk, dK + 2 * kk, ID_S, kk);
-                mma_commit(sy.bar(F_SF + s));
-                if (it < nk) mma_commit(sy.bar(F_EMPTY + s));    // pass 1: the stage held only K
-                return true;
+                    mma_bf16_ss(tmem + 64u * (j & 1), dQ + 2 * kk, dK0 + KT_U * sk + 2 * kk, ID_S, kk);
+                mma_commit(sy.bar(F_SF + (j & 1)));
+                mma_commit(sy.bar(F_KE + sk));
             };
             bool ok = wait_bounded(sy, sy.bar(F_Q), 0, 1, -1);
-            if (ok) ok = issue_s(0);
-            if (ok && total > 1) ok = issue_s(1);
-            for (int it = 0; it < total && ok; ++it) {
-                const int s = it & 1;
-                // softmax is done with S buffer s (pass 1: statistics read; pass 2: P written)
-                ok = wait_bounded(sy, sy.bar(F_SD + s), (it >> 1) & 1, 1, it);
+            for (int j = 0; j < 2 && j < nk && ok; ++j) ok = wait_bounded(sy, sy.bar(F_KF + j), 0, 1, j);
+            if (ok) {
+                tc_fence_after();
+                for (int j = 0; j < 2 && j < nk; ++j) issue_s(j);
+            }
+            for (int j = 0; j < nk && ok; ++j) {
+                // P(j) written over S(j), O rescaled if a row max moved, V_j and
+                // K_{j+2} loaded (the softmax warps waited for both)
+                ok = wait_bounded(sy, sy.bar(F_PF + (j & 1)), (j >> 1) & 1, 1, j);
                 if (!ok) break;
                 tc_fence_after();
-                if (it >= nk) {
-                    const uint64_t dV = dV0 + STAGE_U * s;
+                const uint64_t dV = dV0 + 2 * KT_U * (j % C::NV);
 #pragma unroll
-                    for (int kk = 0; kk < C::BK / 16; ++kk)
-                        mma_bf16_ts(tmem + C::C_O, tmem + 128u * s + 8 * kk, dV + KSTEP * kk, ID_O,
-                                    (it > nk || kk > 0) ? 1u : 0u);
-                    mma_commit(sy.bar(F_EMPTY + s));
-                }
-                if (it + 2 < total) ok = issue_s(it + 2);
+                for (int kk = 0; kk < C::BK / 16; ++kk)
+                    mma_bf16_ts(tmem + C::C_O, tmem + 64u * (j & 1) + 8 * kk, dV + KSTEP * kk, ID_O,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(sy.bar(F_VE + j % C::NV));
+                mma_commit(sy.bar(F_OD));
+                // S(j+2) overwrites P(j): issued after P(j) V_j, the pipe keeps issue order
+                if (j + 2 < nk) issue_s(j + 2);
             }
             mma_commit(sy.bar(F_ACC));
             if (!ok) wait_drain(sy.bar(F_ACC), 0);
@@ -182,51 +214,73 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, bf16* __restrict__ o_lo, b
         const int q4 = warp & 3;
         const int il = q4 * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
-        float m = -INFINITY, l = 0.f, L2 = 0.f;   // log2-domain running max and sum; then LSE * log2(e)
+        float m = -INFINITY, l = 0.f;              // log2-domain row max in use and row sum
         bool ok = true;
-        for (int it = 0; it < total; ++it) {
-            const int s = it & 1, j = it < nk ? it : it - nk;
-            ok = warp_wait(sy, sy.bar(F_SF + s), (it >> 1) & 1, 2, it);
+        for (int j = 0; j < nk; ++j) {
+            const uint32_t tS = trow + 64u * (j & 1);
+            ok = warp_wait(sy, sy.bar(F_SF + (j & 1)), (j >> 1) & 1, 2, j);
             if (!ok) break;
             tc_fence_after();
             const int nvalid = N - j * C::BK;      // keys of this tile that exist (>= 1)
-            const uint32_t tS = trow + 128u * s;
-            if (it == nk) L2 = m + __log2f(l);
-#pragma unroll 1
-            for (int c = 0; c < C::BK / 32; ++c) {
-                uint32_t sr[32];
-                tmem_ld_32x32b_x32(tS + 32 * c, sr);
-                tmem_wait_ld();
-                if (it < nk) {
-                    float mt = m;
+            uint32_t sr[C::BK];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (32 * c + e < nvalid) mt = fmaxf(mt, __uint_as_float(sr[e]) * scale_log2);
-                    l *= ex2_approx(m - mt);
-                    m = mt;
+            for (int c = 0; c < C::BK / 32; ++c)
+                tmem_ld_32x32b_x32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
+            tmem_wait_ld();
+            float mt = -INFINITY;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (32 * c + e < nvalid) l += ex2_approx(fmaf(__uint_as_float(sr[e]), scale_log2, -m));
-                } else {
-                    uint32_t pk[16];
+            for (int e = 0; e < C::BK; ++e)
+                if (e < nvalid) mt = fmaxf(mt, __uint_as_float(sr[e]));
+            mt *= scale_log2;
+            const bool move = mt > m + kRescaleLog2;
+            const float m_new = move ? mt : m;
+            const float alpha = move ? ex2_approx(m - m_new) : 1.f;   // 0 on the first tile
+            l *= alpha;
+            if (j > 0 && __any_sync(0xffffffffu, move)) {
+                // O *= alpha on this warp's rows, once P(j-1) V_{j-1} has finished
+                // (every lane loads and stores: .sync.aligned)
+                ok = warp_wait(sy, sy.bar(F_OD), (j - 1) & 1, 2, j);
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float p0 = ex2_approx(fmaf(__uint_as_float(sr[e]), scale_log2, -L2));
-                        float p1 = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), scale_log2, -L2));
-                        if (32 * c + e >= nvalid) p0 = 0.f;
-                        if (32 * c + e + 1 >= nvalid) p1 = 0.f;
-                        pk[e / 2] = pack_bf16x2(p0, p1);
-                    }
-                    // P over the S columns already read
-                    tmem_st_32x32b_x16(tS + 16 * c, pk);
+                for (int h = 0; h < 2 * D; h += 32) {
+                    uint32_t o[32];
+                    tmem_ld_32x32b_x32(trow + C::C_O + h, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st_32x32b_x16(trow + C::C_O + h, o);
+                    tmem_st_32x32b_x16(trow + C::C_O + h + 16, o + 16);
                 }
+                tmem_wait_st();
             }
-            if (it >= nk) tmem_wait_st();
+            m = m_new;
+#pragma unroll
+            for (int c = 0; c < C::BK / 32; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const int k = 32 * c + e;
+                    float p0 = ex2_approx(fmaf(__uint_as_float(sr[k]), scale_log2, -m));
+                    float p1 = ex2_approx(fmaf(__uint_as_float(sr[k + 1]), scale_log2, -m));
+                    if (k >= nvalid) p0 = 0.f;
+                    if (k + 1 >= nvalid) p1 = 0.f;
+                    l += p0 + p1;
+                    pk[e / 2] = pack_bf16x2(p0, p1);
+                }
+                // P over the S columns (all of S is in registers)
+                tmem_st_32x32b_x16(tS + 16 * c, pk);
+            }
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(sy.bar(F_SD + s));
+            // stand-in waits for the issuer: V_j and K_{j+2} are in shared memory
+            ok = warp_wait(sy, sy.bar(F_VF + j % C::NV), (j / C::NV) & 1, 2, j);
+            if (ok && j + 2 < nk)
+                ok = warp_wait(sy, sy.bar(F_KF + (j + 2) % C::NK), ((j + 2) / C::NK) & 1, 2, j);
+            mbar_arrive(sy.bar(F_PF + (j & 1)));
+            if (!ok) break;
         }
-        if (ok && total == nk) L2 = m + __log2f(l);
-        if (ok) ok = warp_wait(sy, sy.bar(F_ACC), 0, 2, total);
+        if (ok) ok = warp_wait(sy, sy.bar(F_ACC), 0, 2, nk);
         if (ok) {
             // TMEM loads are warp-collective (.sync.aligned): every lane loads,
             // only rows that exist are stored
@@ -234,7 +288,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, bf16* __restrict__ o_lo, b
             const int i = q0 + il;
             const bool valid = i < N;
             const size_t row = (size_t)bh * N + (valid ? i : 0);
-            if (valid) lse[row] = L2 * kLn2;
+            if (valid) lse[row] = (m + __log2f(l)) * kLn2;
+            const float inv_l = 1.f / l;
             uint32_t v[D];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -245,10 +300,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, bf16* __restrict__ o_lo, b
 #pragma unroll
                     for (int e = 0; e < D; e += 8) {
                         uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(v[e + 0]), __uint_as_float(v[e + 1]));
-                        w.y = pack_bf16x2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-                        w.z = pack_bf16x2(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
-                        w.w = pack_bf16x2(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+                        w.x = pack_bf16x2(__uint_as_float(v[e + 0]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
+                        w.y = pack_bf16x2(__uint_as_float(v[e + 2]) * inv_l, __uint_as_float(v[e + 3]) * inv_l);
+                        w.z = pack_bf16x2(__uint_as_float(v[e + 4]) * inv_l, __uint_as_float(v[e + 5]) * inv_l);
+                        w.w = pack_bf16x2(__uint_as_float(v[e + 6]) * inv_l, __uint_as_float(v[e + 7]) * inv_l);
                         *reinterpret_cast<uint4*>(o + e) = w;
                     }
                 }
@@ -283,20 +338,23 @@ int launch_fwd(const void* packed, void* o_lo, void* o_hi, float* lse, long long
     using C = FwdCfg<D>;
     auto enc = get_encode_fwd(err);
     if (!enc) return PSA_ERR_CUDA;
-    CUtensorMap tm;
+    // two maps over packed [BH*4, N, D]: 128-row boxes (Q) and 64-row boxes (K, V)
+    CUtensorMap tm, tm_kv;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)(BH * 4)};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)D, 128u, 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUtensorMapSwizzle sw = D == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : D == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
                                             : CU_TENSOR_MAP_SWIZZLE_32B;
-    const CUresult r = enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(packed), dims, strides, box,
-                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        *err = "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")";
-        return PSA_ERR_CUDA;
+    for (int which = 0; which < 2; ++which) {
+        const cuuint32_t box[3] = {(cuuint32_t)D, which == 0 ? (cuuint32_t)C::BQ : (cuuint32_t)C::BK, 1u};
+        const CUresult r = enc(which == 0 ? &tm : &tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                               const_cast<void*>(packed), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            *err = "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")";
+            return PSA_ERR_CUDA;
+        }
     }
     static std::once_flag attr_once;
     static cudaError_t attr_st = cudaSuccess;
@@ -316,7 +374,7 @@ int launch_fwd(const void* packed, void* o_lo, void* o_hi, float* lse, long long
     {
         ProfScope prof(kSlotFwd, stream);
         fwd_kernel<D><<<(unsigned)grid, kFwdThreads, C::SMEM, stream>>>(
-            tm, static_cast<bf16*>(o_lo), static_cast<bf16*>(o_hi), lse, N, nqt, scale * kLog2e);
+            tm, tm_kv, static_cast<bf16*>(o_lo), static_cast<bf16*>(o_hi), lse, N, nqt, scale * kLog2e);
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
