@@ -99,8 +99,9 @@ def roofline_time_s(w, peaks) -> tuple[float, str]:
 # Sources each kernel family's code comes from (the traffic record is tied to
 # their contents; a change elsewhere, such as the forward, leaves it valid).
 TRAFFIC_SOURCES = {
-    "tc": ["tc_bwd.cu", "tc_ptx.cuh", "tc_sync.cuh", "common.cuh", "psa_internal.h"],
-    "tc2": ["tc_pair.cu", "tc_bwd.cu", "tc_dq.cu", "tc_ptx.cuh", "tc_sync.cuh", "common.cuh", "psa_internal.h"],
+    "tc": ["tc_bwd.cu", "tc_tmap.cu", "tc_ptx.cuh", "tc_sync.cuh", "common.cuh", "psa_internal.h"],
+    "tc2": ["tc_pair.cu", "tc_bwd.cu", "tc_dq.cu", "tc_tmap.cu", "tc_ptx.cuh", "tc_sync.cuh", "common.cuh",
+            "psa_internal.h"],
     "simt": ["simt_kernels.cuh", "psa_attn.cu", "common.cuh", "psa_internal.h"],
 }
 

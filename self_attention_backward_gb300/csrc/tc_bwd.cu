@@ -56,6 +56,7 @@
 #include "psa_internal.h"
 #include "tc_ptx.cuh"
 #include "tc_sync.cuh"
+#include "tc_tmap.h"
 
 #pragma nv_diag_suppress 177  // per-variant tile constants not all used by every head_dim
 
@@ -780,54 +781,18 @@ dq_finalize_kernel(const float* __restrict__ dq_acc, bf16* __restrict__ d_packed
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encode(std::string* err) {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    static cudaError_t st = cudaSuccess;
-    std::call_once(once, [] {
-        cudaDriverEntryPointQueryResult q;
-        void* p = nullptr;
-        st = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
-        if (st == cudaSuccess && q == cudaDriverEntryPointSuccess) fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    if (!fn) *err = std::string("cuTensorMapEncodeTiled unavailable: ") + cudaGetErrorString(st);
-    return fn;
-}
-
-// 3-D map over a [Z, N, D] bf16 tensor, box [1, rows, D], swizzle matching D.
-bool encode_3d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* base, int D, int N, long long Z,
-               int rows, std::string* err) {
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)Z};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)rows, 1u};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    const CUtensorMapSwizzle sw = D == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
-                                  : D == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                            : CU_TENSOR_MAP_SWIZZLE_32B;
-    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        *err = "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")";
-        return false;
-    }
-    return true;
-}
-
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 template <int D>
 int launch(const BwdArgs& a, std::string* err) {
     using M = Cfg<D>;
-    auto enc = get_encode(err);
-    if (!enc) return PSA_ERR_CUDA;
     // K/V tiles: 128 rows; Q/dO sub-tiles: 64 rows (the byte counts the
     // kernel's barriers expect)
     CUtensorMap tm_kv, tm_q, tm_lo, tm_hi;
-    if (!encode_3d(enc, &tm_kv, a.packed, D, a.N, a.BH * 4, M::BM, err) ||
-        !encode_3d(enc, &tm_q, a.packed, D, a.N, a.BH * 4, M::BS, err) ||
-        !encode_3d(enc, &tm_lo, a.do_lo, D, a.N, a.BH, M::BS, err) ||
-        !encode_3d(enc, &tm_hi, a.do_hi, D, a.N, a.BH, M::BS, err))
+    if (!encode_bf16_rows(&tm_kv, a.packed, D, a.N, a.BH * 4, M::BM, D, err) ||
+        !encode_bf16_rows(&tm_q, a.packed, D, a.N, a.BH * 4, M::BS, D, err) ||
+        !encode_bf16_rows(&tm_lo, a.do_lo, D, a.N, a.BH, M::BS, D, err) ||
+        !encode_bf16_rows(&tm_hi, a.do_hi, D, a.N, a.BH, M::BS, D, err))
         return PSA_ERR_CUDA;
     static std::once_flag attr_once;
     static cudaError_t attr_st = cudaSuccess;
@@ -880,13 +845,11 @@ int launch(const BwdArgs& a, std::string* err) {
 template <int D>
 int launch_two_pass(const BwdArgs& a, std::string* err) {
     using M = CfgS<D>;
-    auto enc = get_encode(err);
-    if (!enc) return PSA_ERR_CUDA;
     CUtensorMap tm_kv, tm_q, tm_lo, tm_hi;
-    if (!encode_3d(enc, &tm_kv, a.packed, D, a.N, a.BH * 4, M::BM, err) ||
-        !encode_3d(enc, &tm_q, a.packed, D, a.N, a.BH * 4, M::BS, err) ||
-        !encode_3d(enc, &tm_lo, a.do_lo, D, a.N, a.BH, M::BS, err) ||
-        !encode_3d(enc, &tm_hi, a.do_hi, D, a.N, a.BH, M::BS, err))
+    if (!encode_bf16_rows(&tm_kv, a.packed, D, a.N, a.BH * 4, M::BM, D, err) ||
+        !encode_bf16_rows(&tm_q, a.packed, D, a.N, a.BH * 4, M::BS, D, err) ||
+        !encode_bf16_rows(&tm_lo, a.do_lo, D, a.N, a.BH, M::BS, D, err) ||
+        !encode_bf16_rows(&tm_hi, a.do_hi, D, a.N, a.BH, M::BS, D, err))
         return PSA_ERR_CUDA;
     static std::once_flag attr_once;
     static cudaError_t attr_st = cudaSuccess;

@@ -30,6 +30,7 @@
 #include "psa_internal.h"
 #include "tc_ptx.cuh"
 #include "tc_sync.cuh"
+#include "tc_tmap.h"
 
 namespace psa {
 namespace {
@@ -265,50 +266,14 @@ dq_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_constant__ C
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_dq(std::string* err) {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    static cudaError_t st = cudaSuccess;
-    std::call_once(once, [] {
-        cudaDriverEntryPointQueryResult q;
-        void* p = nullptr;
-        st = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
-        if (st == cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    if (!fn) *err = std::string("cuTensorMapEncodeTiled unavailable: ") + cudaGetErrorString(st);
-    return fn;
-}
-
-bool encode_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* base, int D, int N, long long Z,
-                int rows, std::string* err) {
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)Z};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)rows, 1u};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    const CUtensorMapSwizzle sw = D == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
-                                  : D == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                            : CU_TENSOR_MAP_SWIZZLE_32B;
-    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        *err = "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")";
-        return false;
-    }
-    return true;
-}
-
 template <int D>
 int launch_dq(const BwdArgs& a, const float* Drow, std::string* err) {
     using C = DqCfg<D>;
-    auto enc = get_encode_dq(err);
-    if (!enc) return PSA_ERR_CUDA;
     CUtensorMap tq, tk, tlo, thi;
-    if (!encode_map(enc, &tq, a.packed, D, a.N, a.BH * 4, C::BQ, err) ||
-        !encode_map(enc, &tk, a.packed, D, a.N, a.BH * 4, C::BK, err) ||
-        !encode_map(enc, &tlo, a.do_lo, D, a.N, a.BH, C::BQ, err) ||
-        !encode_map(enc, &thi, a.do_hi, D, a.N, a.BH, C::BQ, err))
+    if (!encode_bf16_rows(&tq, a.packed, D, a.N, a.BH * 4, C::BQ, D, err) ||
+        !encode_bf16_rows(&tk, a.packed, D, a.N, a.BH * 4, C::BK, D, err) ||
+        !encode_bf16_rows(&tlo, a.do_lo, D, a.N, a.BH, C::BQ, D, err) ||
+        !encode_bf16_rows(&thi, a.do_hi, D, a.N, a.BH, C::BQ, D, err))
         return PSA_ERR_CUDA;
     static std::once_flag attr_once;
     static cudaError_t attr_st = cudaSuccess;

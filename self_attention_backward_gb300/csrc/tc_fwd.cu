@@ -42,6 +42,7 @@
 #include "psa_internal.h"
 #include "tc_ptx.cuh"
 #include "tc_sync.cuh"
+#include "tc_tmap.h"
 
 namespace psa {
 namespace {
@@ -317,45 +318,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CU
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fwd(std::string* err) {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    static cudaError_t st = cudaSuccess;
-    std::call_once(once, [] {
-        cudaDriverEntryPointQueryResult q;
-        void* p = nullptr;
-        st = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
-        if (st == cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    if (!fn) *err = std::string("cuTensorMapEncodeTiled unavailable: ") + cudaGetErrorString(st);
-    return fn;
-}
-
 template <int D>
 int launch_fwd(const void* packed, void* o_lo, void* o_hi, float* lse, long long BH, int N, float scale,
                cudaStream_t stream, std::string* err) {
     using C = FwdCfg<D>;
-    auto enc = get_encode_fwd(err);
-    if (!enc) return PSA_ERR_CUDA;
     // two maps over packed [BH*4, N, D]: 128-row boxes (Q) and 64-row boxes (K, V)
     CUtensorMap tm, tm_kv;
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)(BH * 4)};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    const CUtensorMapSwizzle sw = D == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
-                                  : D == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                            : CU_TENSOR_MAP_SWIZZLE_32B;
-    for (int which = 0; which < 2; ++which) {
-        const cuuint32_t box[3] = {(cuuint32_t)D, which == 0 ? (cuuint32_t)C::BQ : (cuuint32_t)C::BK, 1u};
-        const CUresult r = enc(which == 0 ? &tm : &tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                               const_cast<void*>(packed), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                               sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) {
-            *err = "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")";
-            return PSA_ERR_CUDA;
-        }
-    }
+    if (!encode_bf16_rows(&tm, packed, D, N, BH * 4, C::BQ, D, err) ||
+        !encode_bf16_rows(&tm_kv, packed, D, N, BH * 4, C::BK, D, err))
+        return PSA_ERR_CUDA;
     static std::once_flag attr_once;
     static cudaError_t attr_st = cudaSuccess;
     std::call_once(attr_once, [] {

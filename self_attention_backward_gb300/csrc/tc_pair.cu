@@ -58,6 +58,7 @@
 #include "psa_internal.h"
 #include "tc_ptx.cuh"
 #include "tc_sync.cuh"
+#include "tc_tmap.h"
 
 namespace psa {
 namespace {
@@ -666,43 +667,6 @@ bwd_q_pair_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_cons
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encoder(std::string* err) {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    static cudaError_t st = cudaSuccess;
-    std::call_once(once, [] {
-        cudaDriverEntryPointQueryResult q;
-        void* p = nullptr;
-        st = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
-        if (st == cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    if (!fn) *err = std::string("cuTensorMapEncodeTiled unavailable: ") + cudaGetErrorString(st);
-    return fn;
-}
-
-// 3-D map over a [Z, N, D] bf16 tensor with box [1, rows, cols]; the swizzle
-// span matches the box's row bytes (cols * 2: 128, 64 or 32).
-bool map3d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* base, int D, int N, long long Z,
-           int rows, int cols, std::string* err) {
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)Z};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)cols, (cuuint32_t)rows, 1u};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    const int rowb = cols * 2;
-    const CUtensorMapSwizzle sw = rowb == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
-                                  : rowb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                               : CU_TENSOR_MAP_SWIZZLE_32B;
-    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        *err = "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")";
-        return false;
-    }
-    return true;
-}
-
 template <typename K>
 int set_smem(K kernel, int bytes, std::string* err) {
     const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -715,18 +679,17 @@ int set_smem(K kernel, int bytes, std::string* err) {
 
 template <int D>
 int launch_pair(const BwdArgs& a, std::string* err) {
-    auto enc = encoder(err);
-    if (!enc) return PSA_ERR_CUDA;
     const long long Z = a.BH * 4;
     CUtensorMap p128, p32, ph, lo32, hi32, lo64, hi64, lo128, hi128;
-    if (!map3d(enc, &p128, a.packed, D, a.N, Z, 128, D, err) || !map3d(enc, &p32, a.packed, D, a.N, Z, 32, D, err) ||
-        !map3d(enc, &ph, a.packed, D, a.N, Z, 64, D / 2, err) ||
-        !map3d(enc, &lo32, a.do_lo, D, a.N, a.BH, 32, D, err) ||
-        !map3d(enc, &hi32, a.do_hi, D, a.N, a.BH, 32, D, err) ||
-        !map3d(enc, &lo64, a.do_lo, D, a.N, a.BH, 64, D, err) ||
-        !map3d(enc, &hi64, a.do_hi, D, a.N, a.BH, 64, D, err) ||
-        !map3d(enc, &lo128, a.do_lo, D, a.N, a.BH, 128, D, err) ||
-        !map3d(enc, &hi128, a.do_hi, D, a.N, a.BH, 128, D, err))
+    if (!encode_bf16_rows(&p128, a.packed, D, a.N, Z, 128, D, err) ||
+        !encode_bf16_rows(&p32, a.packed, D, a.N, Z, 32, D, err) ||
+        !encode_bf16_rows(&ph, a.packed, D, a.N, Z, 64, D / 2, err) ||
+        !encode_bf16_rows(&lo32, a.do_lo, D, a.N, a.BH, 32, D, err) ||
+        !encode_bf16_rows(&hi32, a.do_hi, D, a.N, a.BH, 32, D, err) ||
+        !encode_bf16_rows(&lo64, a.do_lo, D, a.N, a.BH, 64, D, err) ||
+        !encode_bf16_rows(&hi64, a.do_hi, D, a.N, a.BH, 64, D, err) ||
+        !encode_bf16_rows(&lo128, a.do_lo, D, a.N, a.BH, 128, D, err) ||
+        !encode_bf16_rows(&hi128, a.do_hi, D, a.N, a.BH, 128, D, err))
         return PSA_ERR_CUDA;
     static std::once_flag once;
     static int attr_rc = PSA_OK;

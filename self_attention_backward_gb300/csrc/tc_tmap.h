@@ -1,0 +1,19 @@
+// tc_tmap.h -- host-side TMA tensor-map encoding shared by the tensor-core
+// translation units.
+#pragma once
+
+#include <cuda.h>
+
+#include <string>
+
+namespace psa {
+
+// 3-D tiled map over a bf16 tensor laid out as Z slices of [N, D] rows (row
+// stride D elements, slice stride N*D), copied in boxes of `rows` rows by
+// `cols` columns (cols <= D, cols*2 bytes a multiple of 16); the shared-memory
+// swizzle span equals the box's row bytes (128, 64 or 32).  Rows past N are
+// out of bounds and read as zeros.  Returns false and sets *err on failure.
+bool encode_bf16_rows(CUtensorMap* map, const void* base, int D, int N, long long Z, int rows, int cols,
+                      std::string* err);
+
+}  // namespace psa

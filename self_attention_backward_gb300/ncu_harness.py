@@ -159,12 +159,45 @@ def measured_hbm_gbs() -> float:
         return 6800.0   # the profiling recipe's fallback
 
 
+# the library's profiling slot (bench.py's kernels_ms_per_step keys) of each kernel
+SLOT_OF = {"bwd_main_kernel": "bwd_main", "bwd_kv_pair_kernel": "bwd_main", "bwd_dkdv_kernel": "bwd_main",
+           "dkdv_kernel": "bwd_main", "bwd_q_pair_kernel": "bwd_dq", "dq_kernel": "bwd_dq",
+           "dq_finalize_kernel": "bwd_dq", "pre_kernel": "bwd_pre"}
+
+
+def record_traffic(items, workload: str, algo: str, path=None) -> dict:
+    """Writes each captured backward kernel's DRAM bytes per launch into
+    profiles/traffic.json under (workload, algo, slot), with the hash of the
+    sources the kernel family is built from (bench.py nulls a record whose
+    sources changed since)."""
+    sys.path.insert(0, ROOT)
+    import bench  # noqa: E402  (the benchmark owns the source lists and the hash)
+    path = path or os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        rec = {}
+    fam = rec.setdefault(workload, {}).setdefault(algo, {})
+    for it in items:
+        slot = SLOT_OF.get(it["kernel"].split("<", 1)[0])
+        if slot is None:
+            continue
+        fam[slot] = {"dram_bytes_per_launch": it["dram_read"] + it["dram_write"],
+                     "source_hash": bench.source_hash(algo), "sources": ", ".join(bench.TRAFFIC_SOURCES[algo]),
+                     "ncu": f"dram__bytes_read.sum + dram__bytes_write.sum of {it['kernel']}, one launch "
+                            "(ncu_harness run), cache control all"}
+    with open(path, "w") as f:
+        json.dump(rec, f, indent=1)
+    return rec
+
+
 def _run(cmd, log_path: str) -> int:
     with open(log_path, "w") as log:
         return subprocess.call(cmd, cwd=ROOT, stdout=log, stderr=subprocess.STDOUT)
 
 
-def run(out_dir: str, algo: str, workload: str | None) -> int:
+def run(out_dir: str, algo: str, workload: str | None, record: bool = False) -> int:
     os.makedirs(out_dir, exist_ok=True)
     bench = [sys.executable, "bench.py", "--steps", "2", "--warmup", "3", "--no-cpu", "--no-secondary",
              "--algo", algo]
@@ -195,6 +228,10 @@ def run(out_dir: str, algo: str, workload: str | None) -> int:
     with open(os.path.join(out_dir, "summary.md"), "w") as f:
         f.write(text)
     print(text)
+    if record and algo in ("tc", "tc2", "simt"):
+        sys.path.insert(0, ROOT)
+        import bench  # noqa: E402
+        record_traffic(items, workload or bench.HEADLINE, algo, os.path.join(out_dir, "traffic.json"))
     return 0
 
 
@@ -205,6 +242,8 @@ def main(argv=None) -> int:
     r.add_argument("--out", required=True)
     r.add_argument("--algo", default="auto", choices=["auto", "tc", "tc2", "simt"])
     r.add_argument("--workload", default=None)
+    r.add_argument("--record-traffic", action="store_true",
+                   help="also write the DRAM bytes per launch to OUT/traffic.json (profiles/traffic.json format)")
     la = sub.add_parser("launches")
     la.add_argument("csv")
     ke = sub.add_parser("kernels")
@@ -212,7 +251,7 @@ def main(argv=None) -> int:
     ke.add_argument("--hbm-gbs", type=float, default=None)
     a = ap.parse_args(argv)
     if a.cmd == "run":
-        return run(a.out, a.algo, a.workload)
+        return run(a.out, a.algo, a.workload, a.record_traffic)
     if a.cmd == "launches":
         table, total = summarize_launches(read_metric_rows(a.csv))
         print(launches_markdown(table, total))

@@ -84,6 +84,20 @@ def test_bwd_rejects(lib, kw, code):
     assert _bwd(**kw) == code
 
 
+@pytest.mark.parametrize("algo", [B.PSA_ALGO_AUTO, B.PSA_ALGO_SIMT, B.PSA_ALGO_TC, B.PSA_ALGO_TC_2PASS])
+@pytest.mark.parametrize("dtype", [B.PSA_F32, B.PSA_BF16])
+def test_bwd_empty_is_ok(lib, algo, dtype):
+    """An empty problem (N = 0 or B*heads = 0) returns PSA_OK without looking
+    at any pointer or launching anything, for every kernel family that
+    supports the dtype; the workspace it needs is 0 bytes."""
+    tc = algo in (B.PSA_ALGO_TC, B.PSA_ALGO_TC_2PASS)
+    want = B.PSA_ERR_UNSUPPORTED if (tc and dtype == B.PSA_F32) else B.PSA_OK
+    none = dict(packed=None, o_lo=None, o_hi=None, lse=None, do_lo=None, do_hi=None, d_packed=None, workspace=None)
+    assert _bwd(N=0, dtype=dtype, head_dim=32, algo=algo, **none) == want
+    assert _bwd(B=0, dtype=dtype, head_dim=32, algo=algo, **none) == want
+    assert B.psa_attn_bwd_workspace_bytes(1, 2, 0, 32, dtype, algo) == 0
+
+
 def test_bwd_bad_algo(lib):
     assert _bwd(algo=9, workspace_bytes=1 << 20) == B.PSA_ERR_ARG
 

@@ -67,3 +67,20 @@ def test_kernel_bandwidth_and_tensor_pipe(tmp_path):
 
 def test_measured_peak_is_read():
     assert H.measured_hbm_gbs() > 1000.0
+
+
+def test_record_traffic(tmp_path):
+    import json
+    items = [{"kernel": "bwd_main_kernel<32>", "dram_read": 5e7, "dram_write": 1e6},
+             {"kernel": "pre_kernel<32>", "dram_read": 2e7, "dram_write": 0.0},
+             {"kernel": "vectorized_elementwise_kernel<4>", "dram_read": 1.0, "dram_write": 1.0}]
+    path = str(tmp_path / "traffic.json")
+    H.record_traffic(items, "wl", "tc", path)
+    rec = json.load(open(path))["wl"]["tc"]
+    assert set(rec) == {"bwd_main", "bwd_pre"}
+    assert rec["bwd_main"]["dram_bytes_per_launch"] == 5.1e7
+    import importlib.util, os
+    spec = importlib.util.spec_from_file_location("bench", os.path.join(H.ROOT, "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    assert rec["bwd_main"]["source_hash"] == b.source_hash("tc")
