@@ -212,3 +212,25 @@ def test_host_buffers_pipelined_match_device_path(chunks):
     np.testing.assert_array_equal(got, dev["d_packed"])
     ref = oracle_fwd_bwd(inp)["d_packed"]
     assert rel_err(got, ref) < TOL["bf16"]
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("algo", [B.PSA_ALGO_TC, B.PSA_ALGO_TC_2PASS])
+def test_tensor_core_many_subtiles_repeated(d, algo):
+    """Every tensor-core mode on inputs with many key and query tiles (N = 1000
+    and 1537: 16 and 25 sub-tiles of 64 queries, ragged), three seeds, three
+    runs each, all against the oracle: a scheduling-dependent hazard between
+    pipeline stages would show up as a run or a sub-tile out of tolerance."""
+    from gpu_helpers import TOL
+    for N, seed in ((1000, 301), (1537, 302), (1000, 303)):
+        inp = make_custom(BH=2, N=N, d=d, dtype="bf16", seed=seed + d)
+        ref = oracle_fwd_bwd(inp)
+        for _ in range(3):
+            g = gpu_fwd_bwd(inp, algo)["d_packed"]
+            for sec in range(4):
+                err = rel_err(g[:, sec], ref["d_packed"][:, sec])
+                assert err < TOL["bf16"], (N, seed, sec, err)
+                # and per 64-query block of dQ (a single bad sub-tile stands out)
+            for q0 in range(0, N, 64):
+                blk = slice(q0, min(N, q0 + 64))
+                assert rel_err(g[:, 0, blk], ref["d_packed"][:, 0, blk]) < 3 * TOL["bf16"], (N, seed, q0)
