@@ -228,11 +228,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CU
             for (int c = 0; c < C::BK / 32; ++c)
                 tmem_ld_32x32b_x32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
             tmem_wait_ld();
-            float mt = -INFINITY;
+            // scaled scores (any sign of scale) and their max, in four partial
+            // maxima to keep the dependent chains short
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int e = 0; e < C::BK; ++e)
-                if (e < nvalid) mt = fmaxf(mt, __uint_as_float(sr[e]));
-            mt *= scale_log2;
+            for (int e = 0; e < C::BK; ++e) {
+                const float x = __uint_as_float(sr[e]) * scale_log2;
+                sr[e] = __float_as_uint(x);
+                if (e < nvalid) m4[e & 3] = fmaxf(m4[e & 3], x);
+            }
+            const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             const bool move = mt > m + kRescaleLog2;
             const float m_new = move ? mt : m;
             const float alpha = move ? ex2_approx(m - m_new) : 1.f;   // 0 on the first tile
@@ -256,22 +261,24 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CU
                 tmem_wait_st();
             }
             m = m_new;
+            float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < C::BK / 32; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     const int k = 32 * c + e;
-                    float p0 = ex2_approx(fmaf(__uint_as_float(sr[k]), scale_log2, -m));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(sr[k + 1]), scale_log2, -m));
+                    float p0 = ex2_approx(__uint_as_float(sr[k]) - m);
+                    float p1 = ex2_approx(__uint_as_float(sr[k + 1]) - m);
                     if (k >= nvalid) p0 = 0.f;
                     if (k + 1 >= nvalid) p1 = 0.f;
-                    l += p0 + p1;
+                    l4[(e >> 1) & 3] += p0 + p1;
                     pk[e / 2] = pack_bf16x2(p0, p1);
                 }
                 // P over the S columns (all of S is in registers)
                 tmem_st_32x32b_x16(tS + 16 * c, pk);
             }
+            l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
             tmem_wait_st();
             tc_fence_before();
             // stand-in waits for the issuer: V_j and K_{j+2} are in shared memory

@@ -293,6 +293,9 @@ bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_const
         }
         const CUtensorMap* tm_g = r ? &tm_hi64 : &tm_lo64;
         const float inv_scale = 1.f / scale;
+        // a padded query's shift: -29952 (bf16) times the sign of the scale, so
+        // that (S + shift) * scale * log2(e) is hugely negative and P = 0
+        const uint32_t pad_shift = scale > 0.f ? 0x0000C6EAu : 0x000046EAu;
         bool ok = true;
         int s = 0, ph = 0;
         for (int u = 0; u < nsub; ++u) {
@@ -314,10 +317,10 @@ bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_const
             {
                 // statistics columns of this CTA's 32 queries (one per lane): -LSE/scale
                 // and -D as bf16 (high, remainder) pairs; a padded query gets a large
-                // negative shift (P = 0) and D = 0
+                // shift against the scale's sign (P = 0) and D = 0
                 const int i = u * 64 + 32 * r + lane;
                 const bool v = i < N;
-                const uint32_t lx = v ? split_bf16x2(-lse[(size_t)bh * N + i] * inv_scale) : 0x0000C6EAu;
+                const uint32_t lx = v ? split_bf16x2(-lse[(size_t)bh * N + i] * inv_scale) : pad_shift;
                 const uint32_t dx = v ? split_bf16x2(-Drow[(size_t)bh * N + i]) : 0u;
                 const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE;
                 asm volatile("st.shared.b32 [%0], %1;" ::"r"(st + C::S_LX + sw32_offset(lane, 0)), "r"(lx) : "memory");

@@ -234,3 +234,16 @@ def test_tensor_core_many_subtiles_repeated(d, algo):
             for q0 in range(0, N, 64):
                 blk = slice(q0, min(N, q0 + 64))
                 assert rel_err(g[:, 0, blk], ref["d_packed"][:, 0, blk]) < 3 * TOL["bf16"], (N, seed, q0)
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 16), ("bf16", 32), ("bf16", 64), ("f32", 32)])
+def test_negative_scale(dtype, d):
+    """The scale is any finite number: with a negative one the softmax favours
+    the smallest q.k.  Forward and every backward family against the oracle."""
+    import dataclasses
+    inp = make_custom(BH=2, N=300, d=d, dtype=dtype, seed=400 + d)
+    inp = dataclasses.replace(inp, scale=-inp.scale)
+    ref = oracle_fwd_bwd(inp)
+    for algo in algos_for(dtype, d):
+        errs = compare(gpu_fwd_bwd(inp, algo), ref, dtype)
+        assert_within(errs, dtype)
