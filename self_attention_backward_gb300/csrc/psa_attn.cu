@@ -250,8 +250,8 @@ int psa_attn_bwd_algo(const void* packed, const void* o_lo, const void* o_hi, co
         std::string err;
         if (algo == PSA_ALGO_TC)
             rc = psa::tc_bwd_launch(a, &err);
-        else if (psa::tc_pair_supported(dtype, head_dim))
-            rc = psa::tc_pair_launch(a, &err);
+        else if (psa::tc_pair_supported(dtype, head_dim) && std::fabs(scale) >= 1e-30f)
+            rc = psa::tc_pair_launch(a, &err);   // folds -LSE/scale into its MMAs: needs scale != 0
         else
             rc = psa::tc_two_pass_launch(a, &err);
         if (rc) return fail(rc, "%s", err.c_str());

@@ -247,3 +247,22 @@ def test_negative_scale(dtype, d):
     for algo in algos_for(dtype, d):
         errs = compare(gpu_fwd_bwd(inp, algo), ref, dtype)
         assert_within(errs, dtype)
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 32), ("bf16", 64), ("f32", 16)])
+def test_zero_scale_is_uniform_attention(dtype, d):
+    """scale = 0: P is uniform (1/N per key), so dQ = dK = 0, every dV_h row is
+    the mean of dO_h over the queries, O_h rows are the mean of V_h and
+    LSE = log N.  Every kernel family that supports the case."""
+    import dataclasses
+    from gpu_helpers import TOL
+    inp = dataclasses.replace(make_custom(BH=2, N=193, d=d, dtype=dtype, seed=500 + d), scale=0.0)
+    tol = TOL[dtype]
+    for algo in algos_for(dtype, d):
+        g = gpu_fwd_bwd(inp, algo)
+        assert np.allclose(g["lse"], np.log(193.0), rtol=1e-5)
+        dp = g["d_packed"]
+        assert np.max(np.abs(dp[:, 0:2])) == 0.0, algo
+        for h, do in ((2, inp.do_lo), (3, inp.do_hi)):
+            mean = do.astype(np.float64).mean(axis=1, keepdims=True)      # [BH, 1, d]
+            assert rel_err(dp[:, h], np.broadcast_to(mean, dp[:, h].shape)) < tol, (algo, h)
