@@ -266,3 +266,15 @@ def test_zero_scale_is_uniform_attention(dtype, d):
         for h, do in ((2, inp.do_lo), (3, inp.do_hi)):
             mean = do.astype(np.float64).mean(axis=1, keepdims=True)      # [BH, 1, d]
             assert rel_err(dp[:, h], np.broadcast_to(mean, dp[:, h].shape)) < tol, (algo, h)
+
+
+def test_many_slices_large_grid():
+    """B*heads = 70001 with N = 16: one-dimensional grids of more than 65535
+    CTAs on every kernel family; sampled slices (first, middle, last) against
+    the oracle."""
+    inp = make_custom(BH=70001, N=16, d=32, dtype="bf16", seed=600)
+    slices = [0, 35000, 70000]
+    ref = oracle_fwd_bwd(inp, slices)
+    for algo in algos_for("bf16", 32):
+        errs = compare(gpu_fwd_bwd(inp, algo), ref, "bf16", slices)
+        assert_within(errs, "bf16")
