@@ -21,18 +21,19 @@
 // into an fp32 accumulator in the workspace; a last kernel scales and casts it
 // into d_packed.
 //
-// Pipelining.  S^T/dP^T are double-buffered in TMEM (buffer u & 1) and two
+// Pipelining.  S^T/dP^T live in NB TMEM buffers (buffer u % NB; NB = 3 for
+// d <= 32, 2 for d = 64, where the accumulators take the rest of TMEM), and two
 // softmax-gradient warpgroups take alternate sub-tiles, so the tensor core
-// works on one sub-tile while a warpgroup turns the previous S/dP into P and
-// dS.  dS^T lives in a 4-block shared ring (u & 3), so a pair's dS stays intact
-// until its dQ MMA has read it.  For d <= 32, P^T goes to a 4-slot TMEM ring
-// (bf16 pairs, the A operand of the dV MMA) and S/dP of sub-tile u+2 is issued
-// before dV/dK of u; for d = 64 the accumulators fill TMEM, so P^T goes to a
-// 2-block shared ring and S/dP(u+2) is issued after dV/dK/dQ(u).
+// works on later sub-tiles while a warpgroup turns S/dP(u) into P and dS.  P^T
+// is written over the first 32 columns of its S^T buffer as bf16 pairs (the A
+// operand of the dV MMA); S/dP(u+NB) reuse u's buffer and are issued after
+// dV/dK(u), the pipe keeping issue order.  dS^T lives in a 4-block shared ring
+// (u & 3), so a pair's dS stays intact until its dQ MMA has read it.
 //
 // Cost model that shaped it (measured on GB300): a tcgen05.mma with M = 128,
 // K = 16 costs about max(46, N/2) cycles, so the MMA count, not the flop
-// count, bounds small head dims; the single issuing thread precomputes every
+// count, bounds small head dims; a barrier wait of the issuing thread first
+// waits for its own MMAs in flight.  The issuing thread precomputes every
 // descriptor so that issuing an MMA is one add per operand.
 //
 // Warp roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer (one
@@ -72,14 +73,13 @@ constexpr int kThreads = 448;
 
 template <int D>
 struct Cfg {
-    static constexpr bool kPT = D <= 32;           // P^T in TMEM (else shared memory)
     static constexpr int BM = 128;                 // keys per CTA (MMA M)
     static constexpr int BS = 64;                  // queries per sub-tile
     static constexpr int ROWB = D * 2;             // bytes per [*, D] bf16 row
     static constexpr int KTILE = BM * ROWB;        // [128, D] tile
     static constexpr int QTILE = BS * ROWB;        // [64, D] tile
-    static constexpr int NB = kPT ? 3 : 2;         // S^T/dP^T buffers in TMEM
-    static constexpr int NST = kPT ? 6 : 3;        // Q/dO stages
+    static constexpr int NB = D == 64 ? 2 : 3;     // S^T/dP^T buffers in TMEM
+    static constexpr int NST = D == 64 ? 3 : 6;    // Q/dO stages
     static constexpr uint32_t SW = D == 64 ? 2u : D == 32 ? 4u : 6u;  // swizzle code of [*, D] tiles
     static constexpr int OFF_K = 0;
     static constexpr int OFF_VL = KTILE;
@@ -87,8 +87,7 @@ struct Cfg {
     static constexpr int OFF_STAGE = 3 * KTILE;    // stage s: Q, dO_lo, dO_hi at +s*STAGE
     static constexpr int STAGE = 3 * QTILE;
     static constexpr int OFF_DS = OFF_STAGE + NST * STAGE;  // dS^T ring: 4 x [128 keys][64 queries] bf16
-    static constexpr int OFF_P = OFF_DS + 4 * 16384;        // P^T ring (shared-memory variant): 2 blocks
-    static constexpr int OFF_L2 = OFF_P + (kPT ? 0 : 2 * 16384);  // NST x 64 fp32: LSE * log2(e)
+    static constexpr int OFF_L2 = OFF_DS + 4 * 16384;       // NST x 64 fp32: LSE * log2(e)
     static constexpr int OFF_DD = OFF_L2 + NST * 256;      // NST x 64 fp32: D
     static constexpr int OFF_BAR = OFF_DD + NST * 256;     // mbarriers
     static constexpr int OFF_MISC = OFF_BAR + 256;
@@ -97,8 +96,8 @@ struct Cfg {
     // an SM (its TMEM allocation is all 512 columns)
     static constexpr int SMEM = (USED + 1024) > 118784 ? (USED + 1024) : 118784;
     // TMEM columns (fp32): buffer b = [128b, 128b+128): S^T (64), dP^T (64)
-    // (for d <= 32, P^T is written over the first 32 columns of its S^T as bf16
-    // pairs); then dV_lo|dV_hi, dK, dQ
+    // (P^T is written over the first 32 columns of its S^T as bf16 pairs); then
+    // dV_lo|dV_hi, dK, dQ
     static constexpr uint32_t C_DV = 128 * NB;
     static constexpr uint32_t C_DK = C_DV + 2 * D, C_DQ = C_DV + 3 * D;
     static constexpr uint32_t TMEM_COLS = 512;
@@ -255,7 +254,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             const uint64_t dStage0mn = smem_desc(sb + C::OFF_STAGE + C::QTILE, C::QTILE, SBO, C::SW);
             const uint64_t dDS0 = smem_desc(sb + C::OFF_DS, 16, 1024, 2);
             const uint64_t dDS0mn = smem_desc(sb + C::OFF_DS, 16384, 1024, 2);
-            const uint64_t dP0 = smem_desc(sb + C::OFF_P, 16, 1024, 2);
             constexpr uint32_t STAGE_U = C::STAGE >> 4, QTILE_U = C::QTILE >> 4, BLK_U = 16384 >> 4;
 
             // S^T(u), dP^T(u) into TMEM buffer u & 1.  Its Q/dO stage is known to be
@@ -284,11 +282,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
 #pragma unroll
                 for (int kk = 0; kk < C::BS / 16; ++kk) {
                     const uint32_t acc = (u > 0 || kk > 0) ? 1u : 0u;
-                    if constexpr (C::kPT)
-                        mma_bf16_ts(tmem + C::C_DV, tmem + 128u * (u % C::NB) + 8 * kk, dGmn + KSTEP * kk, ID_DV,
-                                    acc);
-                    else
-                        mma_bf16_ss(tmem + C::C_DV, dP0 + BLK_U * (u & 1) + 2 * kk, dGmn + KSTEP * kk, ID_DV, acc);
+                    mma_bf16_ts(tmem + C::C_DV, tmem + 128u * (u % C::NB) + 8 * kk, dGmn + KSTEP * kk, ID_DV, acc);
                     mma_bf16_ss(tmem + C::C_DK, dDS + 2 * kk, dQmn + KSTEP * kk, ID_DK, acc);
                 }
                 mma_commit(sy.bar(B_QE + s));
@@ -319,19 +313,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 if (!ok) break;
                 tc_fence_after();
                 const bool pair_done = b == 1 || u == nsub - 1;
-                if constexpr (C::kPT) {
-                    // P(u) lives in S/dP buffer u % 3: dV(u) reads it before S/dP(u+3)
-                    // reuses the buffer; the other two buffers keep the softmax fed
-                    issue_dv_dk(u);
-                    if (pair_done) issue_dq(u >> 1);
-                    if (u + C::NB < nsub) issue_s_dp(u + C::NB);
-                } else {
-                    // P^T's 2-block shared ring: dV/dK(u) must read P(u) before S/dP(u+2)
-                    // lets the next softmax of this warpgroup overwrite it
-                    issue_dv_dk(u);
-                    if (pair_done) issue_dq(u >> 1);
-                    if (u + 2 < nsub) issue_s_dp(u + 2);
-                }
+                // P(u) lives in S/dP buffer u % NB: dV(u) reads it before S/dP(u+NB)
+                // reuses the buffer (the pipe keeps issue order); the other buffers
+                // keep the softmax fed
+                issue_dv_dk(u);
+                if (pair_done) issue_dq(u >> 1);
+                if (u + C::NB < nsub) issue_s_dp(u + C::NB);
             }
             // all MMAs done (also on abort, before TMEM is freed)
             mma_commit(sy.bar(B_ACC));
@@ -357,7 +344,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             const float* L2s = reinterpret_cast<const float*>(smem + C::OFF_L2) + s * 64;
             const float* Ds = reinterpret_cast<const float*>(smem + C::OFF_DD) + s * 64;
             const uint32_t ds_row = sb + C::OFF_DS + 16384 * (u & 3) + jl * 128;
-            const uint32_t p_row = sb + C::OFF_P + 16384 * grp + jl * 128;
             const uint32_t tS = trow + 128u * buf, tDP = tS + 64;
 #pragma unroll 1
             for (int c = 0; c < 2; ++c) {
@@ -371,16 +357,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 else
                     softmax_vals<true>(sr, pr, L2s + 32 * c, Ds + 32 * c, scale_log2, kvalid, pk, dk);
                 // P over the S^T columns already read (chunk c's S is in registers)
-                if constexpr (C::kPT) tmem_st_32x32b_x16(tS + 16 * c, pk);
+                tmem_st_32x32b_x16(tS + 16 * c, pk);
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     const uint32_t ch = (uint32_t)((c * 4 + v) ^ (jl & 7)) << 4;
                     st_shared_v4(ds_row + ch, dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
-                    if constexpr (!C::kPT)
-                        st_shared_v4(p_row + ch, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
                 }
             }
-            if constexpr (C::kPT) tmem_wait_st();
+            tmem_wait_st();
             tc_fence_before();
             fence_proxy_async_smem();
             // stand-in waits for the MMA issuer (see its loop): the stage of u+2 is
