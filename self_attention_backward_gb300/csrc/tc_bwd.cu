@@ -36,9 +36,10 @@
 // waits for its own MMAs in flight.  The issuing thread precomputes every
 // descriptor so that issuing an MMA is one add per operand.
 //
-// Warp roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer (one
-// thread) and TMEM owner, warps 2-5 / 6-9 softmax-gradient warpgroups 0 / 1
-// (one key row per thread), warps 10-13 dQ drain (one query row per thread).
+// Warp roles: warp 0 TMA producer, warp 1 MMA issuer (one thread) and TMEM
+// owner, warps 2-5 / 6-9 softmax-gradient warpgroups 0 / 1 (one key row per
+// thread), warps 10-13 dQ drain (one query row per thread); for d <= 32 a
+// warp 14 whose one thread issues the dQ MMAs (480 threads, else 448).
 //
 // Every mbarrier wait is bounded (kTimeoutNs); on timeout the CTA sets a device
 // error word (read by psa_attn_sync_status), skips the rest of its work, waits
@@ -69,7 +70,6 @@ using bf16 = __nv_bfloat16;
 
 __device__ int g_tc_error = 0;  // 0 = fine; else (1 + role) << 24 | tile
 
-constexpr int kThreads = 448;
 
 template <int D>
 struct Cfg {
@@ -80,6 +80,11 @@ struct Cfg {
     static constexpr int QTILE = BS * ROWB;        // [64, D] tile
     static constexpr int NB = D == 64 ? 2 : 3;     // S^T/dP^T buffers in TMEM
     static constexpr int NST = D == 64 ? 3 : 6;    // Q/dO stages
+    // d <= 32: the dQ MMAs have their own issuing thread (warp 14), which takes
+    // a quarter of the MMAs off the main issuer, the bottleneck at small d; at
+    // d = 64 the main issuer keeps them (measured faster there)
+    static constexpr bool SPLIT_DQ = D != 64;
+    static constexpr int THREADS = SPLIT_DQ ? 480 : 448;
     static constexpr uint32_t SW = D == 64 ? 2u : D == 32 ? 4u : 6u;  // swizzle code of [*, D] tiles
     static constexpr int OFF_K = 0;
     static constexpr int OFF_VL = KTILE;
@@ -111,9 +116,12 @@ struct Cfg {
 // with NB <= 3 no warp runs 4 sub-tiles ahead of a slower one and a PF barrier
 // never gets arrivals for two of its phases at once (a ring of 2 would allow a
 // warp two sub-tiles ahead to complete a slower warp's phase).
-enum { B_KV = 0, B_SF = 1, B_PF = 4, B_DQF = 8, B_DQE = 9, B_ACC = 10, B_QF = 11, B_QE = 17 };
+// DQF: the dQ product of 128-query group g is done, at DQF + (g & 1), so that a
+// waiter on group g can never see group g+1's phase (see the dQ issuer);
+// DQE: the drain has read the dQ accumulator; DQA: the dQ issuer's final commit.
+enum { B_KV = 0, B_SF = 1, B_PF = 4, B_DQE = 8, B_ACC = 9, B_DQA = 10, B_QF = 11, B_QE = 17, B_DQF = 23 };
 constexpr int kPfRing = 4;
-static_assert(B_QE + 6 <= 32, "barrier area holds 32 barriers");
+static_assert(B_DQF + 2 <= 32, "barrier area holds 32 barriers");
 
 // P and dS of one 32-query chunk of this thread's key row, packed to bf16
 // pairs: P = exp2(S * scale*log2e - L), dS = P (dP - D).
@@ -140,7 +148,7 @@ __device__ __forceinline__ void softmax_vals(const uint32_t (&sr)[32], const uin
 
 // ---------------------------------------------------------------- main kernel
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_do_lo, const __grid_constant__ CUtensorMap tm_do_hi,
                 const float* __restrict__ lse, const float* __restrict__ Drow, float* __restrict__ dq_acc,
@@ -163,8 +171,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         for (int b = 0; b < C::NB; ++b) mbar_init(sy.bar(B_SF + b), 1);
         for (int x = 0; x < kPfRing; ++x) mbar_init(sy.bar(B_PF + x), 128);
         mbar_init(sy.bar(B_DQF), 1);
+        mbar_init(sy.bar(B_DQF + 1), 1);
         mbar_init(sy.bar(B_DQE), 128);
         mbar_init(sy.bar(B_ACC), 1);
+        mbar_init(sy.bar(B_DQA), 1);
         for (int s = 0; s < C::NST; ++s) {
             mbar_init(sy.bar(B_QF + s), 32);
             mbar_init(sy.bar(B_QE + s), 1);
@@ -178,7 +188,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
     }
     // the dS ring starts zeroed: a last, half-filled 128-query group reads a
     // block no sub-tile wrote (rows of queries >= N, discarded, but finite)
-    for (int x = threadIdx.x; x < 4 * 16384 / 16; x += kThreads)
+    for (int x = threadIdx.x; x < 4 * 16384 / 16; x += C::THREADS)
         st_shared_v4(sb + C::OFF_DS + 16 * x, 0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     if (warp == 1) {
@@ -287,16 +297,16 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 }
                 mma_commit(sy.bar(B_QE + s));
             };
-            // dQ of the 128-query group g: A = dS (queries x keys) read MN-major from the
-            // pair's two dS^T blocks (16 KB apart); B = K_j rows (MN-major)
+            // dQ of the 128-query group g (when this thread issues it): A = dS
+            // (queries x keys) read MN-major from the pair's two dS^T blocks (16 KB
+            // apart); B = K_j rows (MN-major)
             auto issue_dq = [&](int g) {
                 const uint64_t dA = dDS0mn + BLK_U * ((2 * g) & 3);
 #pragma unroll
                 for (int kk = 0; kk < C::BM / 16; ++kk)
                     mma_bf16_ss(tmem + C::C_DQ, dA + 128 * kk, dK + KSTEP * kk, ID_DQ, kk);
-                mma_commit(sy.bar(B_DQF));
+                mma_commit(sy.bar(B_DQF + (g & 1)));
             };
-
             bool ok = wait_bounded(sy, sy.bar(B_KV), 0, 1, -1);
             for (int u = 0; u < C::NB && u < nsub && ok; ++u)
                 ok = wait_bounded(sy, sy.bar(B_QF + u), 0, 1, u);
@@ -305,19 +315,18 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 for (int u = 0; u < C::NB && u < nsub; ++u) issue_s_dp(u);
             }
             // One barrier per sub-tile: PF(u) also certifies that the Q/dO stage of
-            // u+NB is loaded and, when u closes a 128-query group, that the dQ drain
-            // has emptied the dQ accumulator (the softmax warpgroup waited for both).
+            // u+NB is loaded and, when this thread issues the dQ products and u
+            // closes a 128-query group, that the drain has emptied the dQ
+            // accumulator (the softmax warpgroup waited for both).
             for (int u = 0; u < nsub && ok; ++u) {
-                const int b = u & 1;
                 ok = wait_bounded(sy, sy.bar(B_PF + u % kPfRing), (u / kPfRing) & 1, 1, u);
                 if (!ok) break;
                 tc_fence_after();
-                const bool pair_done = b == 1 || u == nsub - 1;
                 // P(u) lives in S/dP buffer u % NB: dV(u) reads it before S/dP(u+NB)
                 // reuses the buffer (the pipe keeps issue order); the other buffers
                 // keep the softmax fed
                 issue_dv_dk(u);
-                if (pair_done) issue_dq(u >> 1);
+                if (!C::SPLIT_DQ && ((u & 1) == 1 || u == nsub - 1)) issue_dq(u >> 1);
                 if (u + C::NB < nsub) issue_s_dp(u + C::NB);
             }
             // all MMAs done (also on abort, before TMEM is freed)
@@ -358,20 +367,33 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                     softmax_vals<true>(sr, pr, L2s + 32 * c, Ds + 32 * c, scale_log2, kvalid, pk, dk);
                 // P over the S^T columns already read (chunk c's S is in registers)
                 tmem_st_32x32b_x16(tS + 16 * c, pk);
+                // dS block u & 3 last held sub-tile u-4, whose 128-query group h's dQ
+                // product (issued by warp 14) must have read it.  Group h-2 was waited
+                // for at sub-tile u-4 by this warpgroup, and group h+2 needs PF(u),
+                // so the parity test on DQF + (h & 1) is exact.
+                if (C::SPLIT_DQ && c == 0 && u >= 4) {
+                    const int h = (u - 4) >> 1;
+                    ok = warp_wait(sy, sy.bar(B_DQF + (h & 1)), (h >> 1) & 1, 2, u);
+                    tc_fence_after();
+                }
+                if (ok) {
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const uint32_t ch = (uint32_t)((c * 4 + v) ^ (jl & 7)) << 4;
-                    st_shared_v4(ds_row + ch, dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
+                    for (int v = 0; v < 4; ++v) {
+                        const uint32_t ch = (uint32_t)((c * 4 + v) ^ (jl & 7)) << 4;
+                        st_shared_v4(ds_row + ch, dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
+                    }
                 }
             }
             tmem_wait_st();
             tc_fence_before();
             fence_proxy_async_smem();
-            // stand-in waits for the MMA issuer (see its loop): the stage of u+2 is
-            // loaded, and the dQ accumulator is free before this group's dQ MMA
-            if (u + C::NB < nsub)
+            // stand-in waits for the MMA issuer (see its loop): the stage of u+NB is
+            // loaded and, when it issues this group's dQ product, the dQ accumulator
+            // is free (then the dQ MMA that last read dS block u & 3 was issued
+            // before S/dP(u), and the pipe keeps issue order)
+            if (ok && u + C::NB < nsub)
                 ok = warp_wait(sy, sy.bar(B_QF + (u + C::NB) % C::NST), ((u + C::NB) / C::NST) & 1, 2, u);
-            if (ok && ((u & 1) == 1 || u == nsub - 1) && u >= 2)
+            if (!C::SPLIT_DQ && ok && ((u & 1) == 1 || u == nsub - 1) && u >= 2)
                 ok = warp_wait(sy, sy.bar(B_DQE), ((u >> 1) - 1) & 1, 2, u);
             mbar_arrive(sy.bar(B_PF + u % kPfRing));
             if (!ok) break;
@@ -405,13 +427,13 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 }
             }
         }
-    } else {
+    } else if (warp < 14) {
         // ------------------------------------------------------------ dQ drain
         const int q4 = warp & 3;
         const int il = q4 * 32 + lane;           // query row within the 128-query group
         const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
         for (int g = 0; g < ngrp; ++g) {
-            if (!warp_wait(sy, sy.bar(B_DQF), g & 1, 3, g)) break;
+            if (!warp_wait(sy, sy.bar(B_DQF + (g & 1)), (g >> 1) & 1, 3, g)) break;
             tc_fence_after();
             uint32_t v[D];
             tmem_ld_row<D>(trow + C::C_DQ, v);
@@ -427,6 +449,39 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                                                        __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])));
             }
         }
+    } else if (C::SPLIT_DQ) {
+        // ------------------------------------------------------------ dQ issuer
+        // dQ of the 128-query group g = sub-tiles 2g, 2g+1: A = dS (queries x keys)
+        // read MN-major from the pair's two dS^T blocks (16 KB apart), B = K_j rows
+        // (MN-major).  It waits for both sub-tiles' softmax (PF) and for the drain
+        // to have read group g-1 (DQE).  PF(u+4) cannot complete before this
+        // thread has seen PF(u): the softmax of u+4 first waits for this group's
+        // DQF, so the PF ring never runs a phase ahead of it.
+        if (lane == 0) {
+            constexpr uint32_t ID_DQ = idesc_bf16(128, D, 1, 1);
+            constexpr uint32_t KSTEP = (16 * C::ROWB) >> 4;
+            constexpr uint32_t BLK_U = 16384 >> 4;
+            const uint64_t dK = smem_desc(sb + C::OFF_K, 16, 8 * C::ROWB, C::SW);
+            const uint64_t dDS0mn = smem_desc(sb + C::OFF_DS, 16384, 1024, 2);
+            bool ok = wait_bounded(sy, sy.bar(B_KV), 0, 5, -1);
+            for (int g = 0; g < ngrp && ok; ++g) {
+                const int u0 = 2 * g, u1 = 2 * g + 1;
+                ok = wait_bounded(sy, sy.bar(B_PF + u0 % kPfRing), (u0 / kPfRing) & 1, 5, u0);
+                if (ok && u1 < nsub) ok = wait_bounded(sy, sy.bar(B_PF + u1 % kPfRing), (u1 / kPfRing) & 1, 5, u1);
+                if (ok && g > 0) ok = wait_bounded(sy, sy.bar(B_DQE), (g - 1) & 1, 5, g);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t dA = dDS0mn + BLK_U * (u0 & 3);
+#pragma unroll
+                for (int kk = 0; kk < C::BM / 16; ++kk)
+                    mma_bf16_ss(tmem + C::C_DQ, dA + 128 * kk, dK + KSTEP * kk, ID_DQ, kk);
+                mma_commit(sy.bar(B_DQF + (g & 1)));
+            }
+            // this thread's MMAs are done before TMEM is freed (also on abort)
+            mma_commit(sy.bar(B_DQA));
+            wait_drain(sy.bar(B_DQA), 0);
+        }
+        __syncwarp();
     }
 
     // ---------------------------------------------------------------- teardown
@@ -809,7 +864,7 @@ int launch(const BwdArgs& a, std::string* err) {
     }
     {
         ProfScope prof(kSlotMain, a.stream);
-        bwd_main_kernel<D><<<(unsigned)grid, kThreads, M::SMEM, a.stream>>>(
+        bwd_main_kernel<D><<<(unsigned)grid, M::THREADS, M::SMEM, a.stream>>>(
             tm_kv, tm_q, tm_lo, tm_hi, a.lse, Drow, dq_acc, dp, a.N, nkt, a.scale, a.scale * kLog2e);
     }
     {
@@ -947,9 +1002,9 @@ int tc_take_device_error(std::string* err) {
     if (e != cudaSuccess || v == 0) return 0;
     const int zero = 0;
     cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(int));
-    static const char* roles[] = {"?", "producer", "mma", "softmax", "dq", "self-test"};
+    static const char* roles[] = {"?", "producer", "mma", "softmax", "dq", "self-test", "dq-mma"};
     const int role = (v >> 24) & 0xff;
-    *err = std::string("tensor-core backward: a bounded wait gave up (") + roles[role < 6 ? role : 0] +
+    *err = std::string("tensor-core backward: a bounded wait gave up (") + roles[role < 7 ? role : 0] +
            " warp, query tile " + std::to_string(v & 0xFFFFFF) + ")";
     return 1;
 }
