@@ -39,7 +39,7 @@
 // Warp roles: warp 0 TMA producer, warp 1 MMA issuer (one thread) and TMEM
 // owner, warps 2-5 / 6-9 softmax-gradient warpgroups 0 / 1 (one key row per
 // thread), warps 10-13 dQ drain (one query row per thread); for d <= 32 a
-// warp 14 whose one thread issues the dQ MMAs (480 threads, else 448).
+// warp 14 whose one thread issues the dK and dQ MMAs (480 threads, else 448).
 //
 // Every mbarrier wait is bounded (kTimeoutNs); on timeout the CTA sets a device
 // error word (read by psa_attn_sync_status), skips the rest of its work, waits
@@ -80,11 +80,11 @@ struct Cfg {
     static constexpr int QTILE = BS * ROWB;        // [64, D] tile
     static constexpr int NB = D == 64 ? 2 : 3;     // S^T/dP^T buffers in TMEM
     static constexpr int NST = D == 64 ? 3 : 6;    // Q/dO stages
-    // d <= 32: the dQ MMAs have their own issuing thread (warp 14), which takes
-    // a quarter of the MMAs off the main issuer, the bottleneck at small d; at
-    // d = 64 the main issuer keeps them (measured faster there)
-    static constexpr bool SPLIT_DQ = D != 64;
-    static constexpr int THREADS = SPLIT_DQ ? 480 : 448;
+    // d <= 32: the dK and dQ MMAs have their own issuing thread (warp 14), which
+    // takes them off the main issuer, the bottleneck at small d; at d = 64 the
+    // main issuer keeps them (measured faster there)
+    static constexpr bool SPLIT_MMA = D != 64;
+    static constexpr int THREADS = SPLIT_MMA ? 480 : 448;
     static constexpr uint32_t SW = D == 64 ? 2u : D == 32 ? 4u : 6u;  // swizzle code of [*, D] tiles
     static constexpr int OFF_K = 0;
     static constexpr int OFF_VL = KTILE;
@@ -177,7 +177,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         mbar_init(sy.bar(B_DQA), 1);
         for (int s = 0; s < C::NST; ++s) {
             mbar_init(sy.bar(B_QF + s), 32);
-            mbar_init(sy.bar(B_QE + s), 1);
+            mbar_init(sy.bar(B_QE + s), C::SPLIT_MMA ? 2 : 1);  // a commit from each issuer
         }
         *sy.abort = 0;
         fence_mbar_init();
@@ -293,7 +293,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 for (int kk = 0; kk < C::BS / 16; ++kk) {
                     const uint32_t acc = (u > 0 || kk > 0) ? 1u : 0u;
                     mma_bf16_ts(tmem + C::C_DV, tmem + 128u * (u % C::NB) + 8 * kk, dGmn + KSTEP * kk, ID_DV, acc);
-                    mma_bf16_ss(tmem + C::C_DK, dDS + 2 * kk, dQmn + KSTEP * kk, ID_DK, acc);
+                    if (!C::SPLIT_MMA) mma_bf16_ss(tmem + C::C_DK, dDS + 2 * kk, dQmn + KSTEP * kk, ID_DK, acc);
                 }
                 mma_commit(sy.bar(B_QE + s));
             };
@@ -326,7 +326,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 // reuses the buffer (the pipe keeps issue order); the other buffers
                 // keep the softmax fed
                 issue_dv_dk(u);
-                if (!C::SPLIT_DQ && ((u & 1) == 1 || u == nsub - 1)) issue_dq(u >> 1);
+                if (!C::SPLIT_MMA && ((u & 1) == 1 || u == nsub - 1)) issue_dq(u >> 1);
                 if (u + C::NB < nsub) issue_s_dp(u + C::NB);
             }
             // all MMAs done (also on abort, before TMEM is freed)
@@ -371,7 +371,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 // product (issued by warp 14) must have read it.  Group h-2 was waited
                 // for at sub-tile u-4 by this warpgroup, and group h+2 needs PF(u),
                 // so the parity test on DQF + (h & 1) is exact.
-                if (C::SPLIT_DQ && c == 0 && u >= 4) {
+                if (C::SPLIT_MMA && c == 0 && u >= 4) {
                     const int h = (u - 4) >> 1;
                     ok = warp_wait(sy, sy.bar(B_DQF + (h & 1)), (h >> 1) & 1, 2, u);
                     tc_fence_after();
@@ -393,7 +393,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             // before S/dP(u), and the pipe keeps issue order)
             if (ok && u + C::NB < nsub)
                 ok = warp_wait(sy, sy.bar(B_QF + (u + C::NB) % C::NST), ((u + C::NB) / C::NST) & 1, 2, u);
-            if (!C::SPLIT_DQ && ok && ((u & 1) == 1 || u == nsub - 1) && u >= 2)
+            if (!C::SPLIT_MMA && ok && ((u & 1) == 1 || u == nsub - 1) && u >= 2)
                 ok = warp_wait(sy, sy.bar(B_DQE), ((u >> 1) - 1) & 1, 2, u);
             mbar_arrive(sy.bar(B_PF + u % kPfRing));
             if (!ok) break;
@@ -401,6 +401,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         // epilogue (warpgroup 0): dK, dV_lo, dV_hi rows of this thread's key
         if (grp == 0) {
             if (ok) ok = warp_wait(sy, sy.bar(B_ACC), 0, 2, nsub);
+            if (C::SPLIT_MMA && ok) ok = warp_wait(sy, sy.bar(B_DQA), 0, 2, nsub);
             if (ok) {
                 tc_fence_after();
                 uint32_t v[D];
@@ -449,32 +450,46 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                                                        __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])));
             }
         }
-    } else if (C::SPLIT_DQ) {
-        // ------------------------------------------------------------ dQ issuer
-        // dQ of the 128-query group g = sub-tiles 2g, 2g+1: A = dS (queries x keys)
-        // read MN-major from the pair's two dS^T blocks (16 KB apart), B = K_j rows
-        // (MN-major).  It waits for both sub-tiles' softmax (PF) and for the drain
-        // to have read group g-1 (DQE).  PF(u+4) cannot complete before this
-        // thread has seen PF(u): the softmax of u+4 first waits for this group's
-        // DQF, so the PF ring never runs a phase ahead of it.
+    } else if (C::SPLIT_MMA) {
+        // ------------------------------------------------------------ dK / dQ issuer
+        // Per sub-tile u, after its softmax (PF): dK += dS^T(u) Q_u.  Per 128-query
+        // group g = sub-tiles 2g, 2g+1, once the drain has read group g-1 (DQE):
+        // dQ_g = dS_g K_j, A = dS read MN-major from the pair's two dS^T blocks
+        // (16 KB apart), B = K_j rows (MN-major).  PF(u+4) cannot complete before
+        // this thread has seen PF(u): the softmax of u+4 first waits for the DQF
+        // of u's group, so the PF ring never runs a phase ahead of it.
         if (lane == 0) {
+            constexpr uint32_t ID_DK = idesc_bf16(128, D, 0, 1);
             constexpr uint32_t ID_DQ = idesc_bf16(128, D, 1, 1);
             constexpr uint32_t KSTEP = (16 * C::ROWB) >> 4;
-            constexpr uint32_t BLK_U = 16384 >> 4;
+            constexpr uint32_t BLK_U = 16384 >> 4, STAGE_U = C::STAGE >> 4;
             const uint64_t dK = smem_desc(sb + C::OFF_K, 16, 8 * C::ROWB, C::SW);
+            const uint64_t dStage0 = smem_desc(sb + C::OFF_STAGE, 16, 8 * C::ROWB, C::SW);
+            const uint64_t dDS0 = smem_desc(sb + C::OFF_DS, 16, 1024, 2);
             const uint64_t dDS0mn = smem_desc(sb + C::OFF_DS, 16384, 1024, 2);
             bool ok = wait_bounded(sy, sy.bar(B_KV), 0, 5, -1);
-            for (int g = 0; g < ngrp && ok; ++g) {
-                const int u0 = 2 * g, u1 = 2 * g + 1;
-                ok = wait_bounded(sy, sy.bar(B_PF + u0 % kPfRing), (u0 / kPfRing) & 1, 5, u0);
-                if (ok && u1 < nsub) ok = wait_bounded(sy, sy.bar(B_PF + u1 % kPfRing), (u1 / kPfRing) & 1, 5, u1);
-                if (ok && g > 0) ok = wait_bounded(sy, sy.bar(B_DQE), (g - 1) & 1, 5, g);
+            for (int u = 0; u < nsub && ok; ++u) {
+                ok = wait_bounded(sy, sy.bar(B_PF + u % kPfRing), (u / kPfRing) & 1, 5, u);
                 if (!ok) break;
                 tc_fence_after();
-                const uint64_t dA = dDS0mn + BLK_U * (u0 & 3);
+                // dK += dS^T(u) Q_u; with the main issuer's commit after dV(u) this
+                // releases the Q/dO stage
+                const int s = u % C::NST;
+                const uint64_t dQmn = dStage0 + STAGE_U * s;
+                const uint64_t dDS = dDS0 + BLK_U * (u & 3);
+#pragma unroll
+                for (int kk = 0; kk < C::BS / 16; ++kk)
+                    mma_bf16_ss(tmem + C::C_DK, dDS + 2 * kk, dQmn + KSTEP * kk, ID_DK, (u > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(sy.bar(B_QE + s));
+                if ((u & 1) == 0 && u < nsub - 1) continue;
+                const int g = u >> 1;
+                if (g > 0 && !wait_bounded(sy, sy.bar(B_DQE), (g - 1) & 1, 5, g)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t dA = dDS0mn + BLK_U * ((2 * g) & 3);
 #pragma unroll
                 for (int kk = 0; kk < C::BM / 16; ++kk)
                     mma_bf16_ss(tmem + C::C_DQ, dA + 128 * kk, dK + KSTEP * kk, ID_DQ, kk);
+                // also covers dK of both sub-tiles (a commit tracks all earlier MMAs)
                 mma_commit(sy.bar(B_DQF + (g & 1)));
             }
             // this thread's MMAs are done before TMEM is freed (also on abort)
