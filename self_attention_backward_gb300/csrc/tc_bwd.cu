@@ -152,7 +152,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_do_lo, const __grid_constant__ CUtensorMap tm_do_hi,
                 const float* __restrict__ lse, const float* __restrict__ Drow, float* __restrict__ dq_acc,
-                bf16* __restrict__ d_packed, int N, int nkt, float scale, float scale_log2) {
+                bf16* __restrict__ d_packed, int N, int nkt, float scale, float scale_log2, int nfull,
+                int tail_f, float* __restrict__ dkv_part) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -161,9 +162,23 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 16);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x / nkt, kt = blockIdx.x % nkt;
+    // Work unit = (batch*head, key tile).  The units of the last, partial wave
+    // (blocks >= nfull) are each split into tail_f query ranges of whole
+    // 128-query groups; such a piece writes fp32 dK/dV partials to dkv_part,
+    // summed by the finalize kernel.  Sub-tile indices below are local to the
+    // CTA's range, which starts at sub-tile ubase.
+    const int nsub_all = (N + C::BS - 1) / C::BS;
+    int unit = (int)blockIdx.x, ubase = 0, nsub = nsub_all, piece = -1;
+    if (unit >= nfull) {
+        piece = unit - nfull;
+        unit = nfull + piece / tail_f;
+        const int p = piece % tail_f, ng = (nsub_all + 1) / 2;
+        const int gb = p * ng / tail_f, ge = (p + 1) * ng / tail_f;
+        ubase = 2 * gb;
+        nsub = min(2 * ge, nsub_all) - ubase;
+    }
+    const int bh = unit / nkt, kt = unit % nkt;
     const int k0 = kt * C::BM;
-    const int nsub = (N + C::BS - 1) / C::BS;     // 64-query sub-tiles
     const int ngrp = (nsub + 1) / 2;              // 128-query groups (dQ granularity)
 
     if (threadIdx.x == 0) {
@@ -219,9 +234,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             if (lane == 0) {
                 const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE;
                 mbar_expect_tx(sy.bar(B_QF + s), 3 * C::QTILE);
-                tma_load_3d(st, &tm_q, 0, u * C::BS, bh * 4 + 0, sy.bar(B_QF + s));
-                tma_load_3d(st + C::QTILE, &tm_do_lo, 0, u * C::BS, bh, sy.bar(B_QF + s));
-                tma_load_3d(st + 2 * C::QTILE, &tm_do_hi, 0, u * C::BS, bh, sy.bar(B_QF + s));
+                const int q0 = (ubase + u) * C::BS;
+                tma_load_3d(st, &tm_q, 0, q0, bh * 4 + 0, sy.bar(B_QF + s));
+                tma_load_3d(st + C::QTILE, &tm_do_lo, 0, q0, bh, sy.bar(B_QF + s));
+                tma_load_3d(st + 2 * C::QTILE, &tm_do_hi, 0, q0, bh, sy.bar(B_QF + s));
             }
 #pragma unroll
             for (int x = 0; x < C::NST; ++x)
@@ -231,7 +247,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int q = lane * 2 + e;
-                const int i = u * C::BS + q;
+                const int i = (ubase + u) * C::BS + q;
                 const bool v = i < N;
                 L2s[s * 64 + q] = v ? lse[(size_t)bh * N + i] * kLog2e : INFINITY;
                 Ds[s * 64 + q] = v ? Drow[(size_t)bh * N + i] : 0.f;
@@ -413,7 +429,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                     const float mul = which == 0 ? scale : 1.f;
                     tmem_ld_row<D>(trow + col, v);
                     tmem_wait_ld();
-                    if (kvalid) {
+                    if (piece >= 0) {
+                        // a piece's partial: [piece][key row][dK | dV_lo | dV_hi] fp32
+                        float4* o = reinterpret_cast<float4*>(dkv_part + ((size_t)piece * C::BM + jl) * 3 * D + which * D);
+#pragma unroll
+                        for (int e = 0; e < D; e += 4)
+                            o[e / 4] = make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                                                   __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+                    } else if (kvalid) {
                         bf16* o = out + (size_t)(1 + which) * sec;
 #pragma unroll
                         for (int e = 0; e < D; e += 8) {
@@ -441,7 +464,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(sy.bar(B_DQE));
-            const int i = g * 128 + il;
+            const int i = (ubase / 2 + g) * 128 + il;
             if (i < N) {
                 float4* dst = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * N + i) * D);
 #pragma unroll
@@ -817,10 +840,37 @@ pre_kernel(const bf16* __restrict__ o_lo, const bf16* __restrict__ o_hi, const b
 template <int D>
 __global__ void __launch_bounds__(256)
 dq_finalize_kernel(const float* __restrict__ dq_acc, bf16* __restrict__ d_packed, long long rows, int N,
-                   float scale) {
+                   float scale, const float* __restrict__ dkv_part, int nfull, int ntail, int tail_f, int nkt) {
     constexpr int PPR = D / 8;  // 8-element parts per row
     const long long idx = (long long)blockIdx.x * 256 + threadIdx.x;
-    if (idx >= rows * PPR) return;
+    if (idx >= rows * PPR) {
+        // dK, dV_lo, dV_hi of the split units: the sum of their pieces'
+        // partials, in piece order
+        const long long t = idx - rows * PPR;
+        if (t >= (long long)ntail * 128 * 3 * PPR) return;
+        const int part = (int)(t % PPR);
+        const int which = (int)(t / PPR % 3);
+        const int jl = (int)(t / (3 * PPR) % 128);
+        const int r = (int)(t / (3 * PPR * 128));
+        const int unit = nfull + r, bh = unit / nkt, key = (unit % nkt) * 128 + jl;
+        if (key >= N) return;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int p = 0; p < tail_f; ++p) {
+            const float4* src = reinterpret_cast<const float4*>(
+                dkv_part + ((size_t)(r * tail_f + p) * 128 + jl) * 3 * D + which * D + part * 8);
+            const float4 a = src[0], b = src[1];
+            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+        }
+        const float mul = which == 0 ? scale : 1.f;
+        uint4 u;
+        u.x = pack_bf16x2(acc[0] * mul, acc[1] * mul);
+        u.y = pack_bf16x2(acc[2] * mul, acc[3] * mul);
+        u.z = pack_bf16x2(acc[4] * mul, acc[5] * mul);
+        u.w = pack_bf16x2(acc[6] * mul, acc[7] * mul);
+        *reinterpret_cast<uint4*>(d_packed + (((size_t)bh * 4 + 1 + which) * N + key) * D + part * 8) = u;
+        return;
+    }
     const long long row = idx / PPR;
     const int part = (int)(idx % PPR);
     const long long bh = row / N, i = row % N;
@@ -836,6 +886,35 @@ dq_finalize_kernel(const float* __restrict__ dq_acc, bf16* __restrict__ d_packed
 
 // ---------------------------------------------------------------- host side
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// The fused kernel's units (one per batch*head and 128-key tile) all take the
+// same time, so with U units on S SMs the last wave holds U mod S of them and
+// leaves the other SMs idle.  Those ntail units are split into f query ranges
+// (f pieces of whole 128-query groups each, ntail*f <= min(S, kMaxPieces)).
+constexpr int kMaxPieces = 256;
+struct TailSplit {
+    int ntail = 0, f = 1;
+};
+TailSplit tail_split(long long units, int N, int sms) {
+    TailSplit t;
+    if (sms <= 0 || units <= 0) return t;
+    const int cap = sms < kMaxPieces ? sms : kMaxPieces;
+    const long long rem = units % sms;
+    const int ngrp = (N + 127) / 128;
+    if (rem == 0 || rem > cap / 2 || ngrp < 2) return t;
+    t.ntail = (int)rem;
+    t.f = cap / t.ntail < ngrp ? cap / t.ntail : ngrp;
+    if (t.f < 2) t = TailSplit{};
+    return t;
+}
+// Bytes of partials the split can need, whatever the SM count (kMaxPieces bounds it)
+size_t tail_part_bytes(long long BH, int N, int d) {
+    const long long units = BH * ((N + 127) / 128);
+    const int ngrp = (N + 127) / 128;
+    if (ngrp < 2) return 0;
+    const long long pieces = units * ngrp < kMaxPieces ? units * ngrp : kMaxPieces;
+    return (size_t)pieces * 128 * 3 * (size_t)d * 4;
+}
 
 template <int D>
 int launch(const BwdArgs& a, std::string* err) {
@@ -860,10 +939,19 @@ int launch(const BwdArgs& a, std::string* err) {
     const long long rows = a.BH * a.N;
     float* Drow = static_cast<float*>(a.workspace);
     float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + align256((size_t)rows * 4));
+    float* dkv_part = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + align256((size_t)rows * 4) +
+                                               align256((size_t)rows * D * 4));
     const int nkt = (a.N + M::BM - 1) / M::BM;
-    const long long grid = a.BH * nkt;
+    const long long units = a.BH * nkt;
+    // split the last wave's units along the query axis so that it fills the SMs
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 0;
+    const TailSplit ts = tail_split(units, a.N, sms);
+    const long long nfull = units - ts.ntail;
+    const long long grid = nfull + (long long)ts.ntail * ts.f;
     const long long pre_grid = (rows + 256 / (D / 8) - 1) / (256 / (D / 8));
-    const long long fin_grid = (rows * (D / 8) + 255) / 256;
+    const long long fin_grid = (rows * (D / 8) + (long long)ts.ntail * 128 * 3 * (D / 8) + 255) / 256;
     if (grid > 0x7fffffffll || pre_grid > 0x7fffffffll || fin_grid > 0x7fffffffll) {
         *err = "grid too large";
         return PSA_ERR_UNSUPPORTED;
@@ -880,11 +968,13 @@ int launch(const BwdArgs& a, std::string* err) {
     {
         ProfScope prof(kSlotMain, a.stream);
         bwd_main_kernel<D><<<(unsigned)grid, M::THREADS, M::SMEM, a.stream>>>(
-            tm_kv, tm_q, tm_lo, tm_hi, a.lse, Drow, dq_acc, dp, a.N, nkt, a.scale, a.scale * kLog2e);
+            tm_kv, tm_q, tm_lo, tm_hi, a.lse, Drow, dq_acc, dp, a.N, nkt, a.scale, a.scale * kLog2e, (int)nfull, ts.f,
+            dkv_part);
     }
     {
         ProfScope prof(kSlotDq, a.stream);
-        dq_finalize_kernel<D><<<(unsigned)fin_grid, 256, 0, a.stream>>>(dq_acc, dp, rows, a.N, a.scale);
+        dq_finalize_kernel<D><<<(unsigned)fin_grid, 256, 0, a.stream>>>(dq_acc, dp, rows, a.N, a.scale, dkv_part,
+                                                                        (int)nfull, ts.ntail, ts.f, nkt);
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -949,7 +1039,7 @@ bool tc_supported(int dtype, int d) { return dtype == PSA_BF16 && (d == 16 || d 
 
 size_t tc_workspace_bytes(long long BH, int N, int d) {
     const size_t rows = (size_t)BH * (size_t)N;
-    return align256(rows * 4) + rows * (size_t)d * 4;
+    return align256(rows * 4) + align256(rows * (size_t)d * 4) + tail_part_bytes(BH, N, d);
 }
 
 size_t tc_two_pass_workspace_bytes(long long BH, int N) { return align256((size_t)BH * (size_t)N * 4); }

@@ -278,3 +278,30 @@ def test_many_slices_large_grid():
     for algo in algos_for("bf16", 32):
         errs = compare(gpu_fwd_bwd(inp, algo), ref, "bf16", slices)
         assert_within(errs, "bf16")
+
+
+@pytest.mark.parametrize("BH,N,d,slices", [
+    (1, 900, 32, None),      # 8 units, each split into 8 one-group pieces; last piece one sub-tile
+    (3, 700, 64, None),      # 18 units, 6 pieces each
+    (2, 1537, 16, None),     # 26 units, 5 pieces of 2-3 groups
+    (20, 1000, 32, [0, 19]),  # 160 units on 152 SMs: 152 whole units, the last 8 split
+])
+def test_fused_query_split_of_last_wave(BH, N, d, slices):
+    """The fused tensor-core mode splits the units (batch*head, 128-key tile)
+    of its last, partial wave along the query axis and sums the pieces' dK/dV
+    partials afterwards.  Shapes whose unit counts make it split (on a
+    152-SM GPU) into 1-group pieces, ragged pieces and a mix of whole and split
+    units; every section per 128-key block against the oracle."""
+    from gpu_helpers import TOL
+    inp = make_custom(BH=BH, N=N, d=d, dtype="bf16", seed=700 + d + BH)
+    ref = oracle_fwd_bwd(inp, slices)
+    g = gpu_fwd_bwd(inp, B.PSA_ALGO_TC)["d_packed"]
+    rows = slices if slices is not None else list(range(BH))
+    for k, bh in enumerate(rows):
+        r = ref["d_packed"][k] if slices is not None else ref["d_packed"][bh]
+        for sec in range(4):
+            assert rel_err(g[bh, sec], r[sec]) < TOL["bf16"], (bh, sec)
+        for k0 in range(0, N, 128):
+            blk = slice(k0, min(N, k0 + 128))
+            for sec in (1, 2, 3):
+                assert rel_err(g[bh, sec, blk], r[sec, blk]) < 3 * TOL["bf16"], (bh, sec, k0)
