@@ -164,6 +164,50 @@ long long psa_attn_bwd_noalloc_max_rows(void);
 size_t psa_attn_bwd_workspace_bytes_algo(int B, int heads, int N, int head_dim, int dtype, int algo);
 
 /*
+ * psa_attn_bwd_host -- the backward on HOST buffers: copies the inputs to the
+ * device, runs psa_attn_bwd_algo and copies d_packed back, all enqueued on
+ * `stream`.  (The pages have no counterpart; it is this library's end-to-end
+ * entry point.)  The (batch*head) slices are independent, so they are split
+ * into `chunks` groups whose copy in, backward and copy back are pipelined:
+ * the copies run on two streams this library creates once per device, and the
+ * kernels on `stream`.
+ *   packed ... d_packed  HOST pointers, layouts as in psa_attn_bwd (d_packed is
+ *                written).  Page-locked memory (cudaHostAlloc or
+ *                cudaHostRegister) makes the copies asynchronous; with pageable
+ *                memory the call still works, but the copies block the host.
+ *   dev_buf      DEVICE scratch, 256-byte aligned, at least
+ *                psa_attn_bwd_host_buffer_bytes(...) bytes: the device copies of
+ *                every input and of d_packed, then the backward workspace.
+ *                Contents on entry are ignored; on exit unspecified.
+ *   algo         as psa_attn_bwd_algo.
+ *   chunks       0 = chosen by the library from the sizes and the GPU
+ *                (psa_attn_bwd_host_chunks); else 1..64, capped at B*heads.
+ *                With N % 4 != 0 the call runs as one chunk (every chunk's lse
+ *                must start on a 16-byte boundary).
+ *   stream       the call starts after earlier work on `stream`; work enqueued
+ *                on `stream` after the call starts after d_packed has landed in
+ *                host memory.  Asynchronous: synchronise `stream` before reading
+ *                d_packed.
+ * Returns as psa_attn_bwd (PSA_ERR_WORKSPACE: dev_buf missing or too small;
+ * PSA_ERR_ALIGN: dev_buf not 256-byte aligned).  An empty problem returns 0
+ * and touches nothing.  Calls that share dev_buf must not overlap on the GPU;
+ * calls from several host threads are serialised while they enqueue.
+ */
+int psa_attn_bwd_host(const void* packed, const void* o_lo, const void* o_hi, const float* lse,
+                      const void* do_lo, const void* do_hi, void* d_packed,
+                      void* dev_buf, size_t dev_buf_bytes,
+                      int B, int heads, int N, int head_dim, float scale,
+                      int dtype, int algo, int chunks, void* stream);
+
+/* Device buffer bytes psa_attn_bwd_host needs (0 for an empty or invalid
+ * problem); they do not depend on the chunk count. */
+size_t psa_attn_bwd_host_buffer_bytes(int B, int heads, int N, int head_dim, int dtype, int algo);
+
+/* The chunk count psa_attn_bwd_host uses for chunks = 0 on the current device
+ * (1 when no device is available). */
+int psa_attn_bwd_host_chunks(int B, int heads, int N, int head_dim, int dtype, int algo);
+
+/*
  * Synchronises `stream`, then reports whether any kernel of this library gave
  * up on a bounded device-side wait since the last check (PSA_ERR_TIMEOUT, and
  * the flag is cleared), or whether the stream has a CUDA error (PSA_ERR_CUDA).

@@ -31,6 +31,9 @@ _SIGS = {
     "psa_attn_bwd_algo": ([_vp] * 8 + [_sz, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
     "psa_attn_bwd_noalloc": ([_vp] * 7 + [_i, _i, _i, _i, _f, _i, _vp], _i),
     "psa_attn_bwd_noalloc_max_rows": ([], ctypes.c_longlong),
+    "psa_attn_bwd_host": ([_vp] * 8 + [_sz, _i, _i, _i, _i, _f, _i, _i, _i, _vp], _i),
+    "psa_attn_bwd_host_buffer_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
+    "psa_attn_bwd_host_chunks": ([_i, _i, _i, _i, _i, _i], _i),
     "psa_attn_sync_status": ([_vp], _i),
     "psa_attn_selftest_wait_timeout": ([_vp], _i),
     "psa_attn_profile_enable": ([_i], _i),
@@ -151,6 +154,26 @@ def psa_attn_bwd_noalloc_max_rows() -> int:
     return int(lib().psa_attn_bwd_noalloc_max_rows())
 
 
+def psa_attn_bwd_host(packed, o_lo, o_hi, lse, do_lo, do_hi, d_packed, dev_buf, dev_buf_bytes,
+                      B, heads, N, head_dim, scale, dtype=None, algo=PSA_ALGO_AUTO, chunks=0, stream=None,
+                      check=True) -> int:
+    """Backward on HOST tensors (ideally pinned), `dev_buf` a device scratch of
+    psa_attn_bwd_host_buffer_bytes(...) bytes (see include/psa_attn.h)."""
+    dtype = _dtype_code(packed) if dtype is None else dtype
+    rc = lib().psa_attn_bwd_host(_ptr(packed), _ptr(o_lo), _ptr(o_hi), _ptr(lse), _ptr(do_lo), _ptr(do_hi),
+                                 _ptr(d_packed), _ptr(dev_buf), int(dev_buf_bytes), B, heads, N, head_dim,
+                                 float(scale), dtype, algo, int(chunks), _stream(stream))
+    return _check(rc) if check else rc
+
+
+def psa_attn_bwd_host_buffer_bytes(B, heads, N, head_dim, dtype, algo=PSA_ALGO_AUTO) -> int:
+    return int(lib().psa_attn_bwd_host_buffer_bytes(B, heads, N, head_dim, dtype, algo))
+
+
+def psa_attn_bwd_host_chunks(B, heads, N, head_dim, dtype, algo=PSA_ALGO_AUTO) -> int:
+    return int(lib().psa_attn_bwd_host_chunks(B, heads, N, head_dim, dtype, algo))
+
+
 def psa_attn_sync_status(stream=None, check=True) -> int:
     rc = lib().psa_attn_sync_status(_stream(stream))
     return _check(rc) if check else rc
@@ -233,73 +256,32 @@ def attn_bwd(packed, o_lo, o_hi, lse, do_lo, do_hi, scale: float, d_packed=None,
 
 
 class HostBwd:
-    """psa_attn_bwd on HOST tensors: copies the inputs host->device, runs the
-    backward, copies d_packed device->host.  Host tensors should be pinned for
-    asynchronous copies.  Device staging buffers and the workspace are
-    allocated once, for one shape.
-
-    The (batch*head) slices are independent, so the work is split into
-    `chunks` groups of slices and pipelined over three streams: the copy of
-    group c+1 to the device and the copy of group c-1 back to the host run
-    while the backward of group c runs on the caller's stream.  The call
-    returns with the caller's stream ordered after the last copy back."""
+    """psa_attn_bwd_host for one shape: the device buffer it needs (the
+    device copies of the inputs and of d_packed, and the workspace) is
+    allocated once here, by torch; each call passes the host tensors (pinned
+    for asynchronous copies) to the native entry point, which pipelines the
+    copies in, the backward and the copy back over `chunks` groups of
+    (batch*head) slices (None = the library's choice)."""
 
     def __init__(self, BH: int, N: int, d: int, dtype: int, device="cuda", algo=PSA_ALGO_AUTO, chunks=None):
         import torch
-        tdt = _torch_dtype(dtype)
         self.shape = (BH, N, d)
         self.dtype, self.algo = dtype, algo
-        self.packed = torch.empty((BH, 4, N, d), dtype=tdt, device=device)
-        self.o_lo = torch.empty((BH, N, d), dtype=tdt, device=device)
-        self.o_hi = torch.empty_like(self.o_lo)
-        self.do_lo = torch.empty_like(self.o_lo)
-        self.do_hi = torch.empty_like(self.o_lo)
-        self.lse = torch.empty((BH, N), dtype=torch.float32, device=device)
-        self.d_packed = torch.empty_like(self.packed)
-        if chunks is None:
-            # two groups: more would shrink each launch's grid below a few waves
-            chunks = 2 if BH >= 4 else 1
-        if N % 4:
-            chunks = 1  # every slice of `lse` must start on a 16-byte boundary
-        chunks = max(1, min(int(chunks), BH))
-        self.bounds = [(BH * c // chunks, BH * (c + 1) // chunks) for c in range(chunks)]
-        self.ws_bytes = max(psa_attn_bwd_workspace_bytes(b1 - b0, 1, N, d, dtype, algo) for b0, b1 in self.bounds)
-        self.ws = BwdWorkspace(device).get(self.ws_bytes)
-        self.s_in = torch.cuda.Stream(device=device)
-        self.s_out = torch.cuda.Stream(device=device)
-        self.ev_in = [torch.cuda.Event() for _ in self.bounds]
-        self.ev_k = [torch.cuda.Event() for _ in self.bounds]
-        self.ev_done = torch.cuda.Event()
+        self.chunks = 0 if chunks is None else int(chunks)
+        self.buf_bytes = psa_attn_bwd_host_buffer_bytes(BH, 1, N, d, dtype, algo)
+        self.buf = torch.empty(max(self.buf_bytes, 1), dtype=torch.uint8, device=device)
+        es = 2 if dtype == PSA_BF16 else 4
+        self._in_bytes = BH * N * (8 * d * es + 4)
+        self._out_bytes = BH * N * 4 * d * es
 
     def h2d_bytes(self) -> int:
-        ts = (self.packed, self.o_lo, self.o_hi, self.lse, self.do_lo, self.do_hi)
-        return sum(t.numel() * t.element_size() for t in ts)
+        return self._in_bytes
 
     def d2h_bytes(self) -> int:
-        return self.d_packed.numel() * self.d_packed.element_size()
+        return self._out_bytes
 
     def __call__(self, packed, o_lo, o_hi, lse, do_lo, do_hi, scale: float, out, stream=None):
-        import torch
-        _, N, d = self.shape
-        main = stream if stream is not None else torch.cuda.current_stream()
-        # the staging buffers and d_packed are free once the caller's stream got here
-        self.s_in.wait_stream(main)
-        self.s_out.wait_stream(main)
-        pairs = ((self.packed, packed), (self.o_lo, o_lo), (self.o_hi, o_hi), (self.lse, lse),
-                 (self.do_lo, do_lo), (self.do_hi, do_hi))
-        for c, (b0, b1) in enumerate(self.bounds):
-            with torch.cuda.stream(self.s_in):
-                for dst, src in pairs:
-                    dst[b0:b1].copy_(src[b0:b1], non_blocking=True)
-                self.ev_in[c].record(self.s_in)
-            main.wait_event(self.ev_in[c])
-            psa_attn_bwd(self.packed[b0:b1], self.o_lo[b0:b1], self.o_hi[b0:b1], self.lse[b0:b1],
-                         self.do_lo[b0:b1], self.do_hi[b0:b1], self.d_packed[b0:b1], self.ws, self.ws_bytes,
-                         b1 - b0, 1, N, d, scale, dtype=self.dtype, stream=main, algo=self.algo)
-            self.ev_k[c].record(main)
-            self.s_out.wait_event(self.ev_k[c])
-            with torch.cuda.stream(self.s_out):
-                out[b0:b1].copy_(self.d_packed[b0:b1], non_blocking=True)
-        self.ev_done.record(self.s_out)
-        main.wait_event(self.ev_done)
+        BH, N, d = self.shape
+        psa_attn_bwd_host(packed, o_lo, o_hi, lse, do_lo, do_hi, out, self.buf, self.buf_bytes, BH, 1, N, d,
+                          scale, dtype=self.dtype, algo=self.algo, chunks=self.chunks, stream=stream)
         return out

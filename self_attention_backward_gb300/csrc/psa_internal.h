@@ -51,6 +51,9 @@ int tc_fwd_take_device_error(std::string* err);
 // Tensor-core (tcgen05) backward: tc_bwd.cu.
 bool tc_supported(int dtype, int d);
 size_t tc_workspace_bytes(long long BH, int N, int d);
+// Waves of the fused backward kernel for `units` (batch*head, 128-key tile)
+// units on `sms` SMs, its last-wave split included (a fraction for a split wave).
+double tc_bwd_waves(long long units, int N, int sms);
 // Returns 0 or a psa_status; `err` receives a message on failure.
 int tc_bwd_launch(const BwdArgs& a, std::string* err);
 // Two-pass tensor-core backward (no atomics, reproducible bit for bit): D,

@@ -1037,6 +1037,15 @@ int launch_two_pass(const BwdArgs& a, std::string* err) {
 
 bool tc_supported(int dtype, int d) { return dtype == PSA_BF16 && (d == 16 || d == 32 || d == 64); }
 
+double tc_bwd_waves(long long units, int N, int sms) {
+    if (units <= 0) return 0.0;
+    if (sms <= 0) return (double)units;
+    const TailSplit t = tail_split(units, N, sms);
+    if (t.ntail == 0) return (double)((units + sms - 1) / sms);
+    const int ngrp = (N + 127) / 128;
+    return (double)((units - t.ntail) / sms) + (double)((ngrp + t.f - 1) / t.f) / ngrp;
+}
+
 size_t tc_workspace_bytes(long long BH, int N, int d) {
     const size_t rows = (size_t)BH * (size_t)N;
     return align256(rows * 4) + align256(rows * (size_t)d * 4) + tail_part_bytes(BH, N, d);

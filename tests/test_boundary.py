@@ -136,3 +136,53 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(B, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         B.lib()
+
+
+def _bwd_host(**kw):
+    a = dict(packed=FAKE, o_lo=FAKE, o_hi=FAKE, lse=FAKE, do_lo=FAKE, do_hi=FAKE, d_packed=FAKE,
+             dev_buf=FAKE * 16, dev_buf_bytes=0, B=1, heads=2, N=16, head_dim=16, scale=0.25,
+             dtype=B.PSA_F32, algo=B.PSA_ALGO_AUTO, chunks=0, stream=0, check=False)
+    a.update(kw)
+    return B.psa_attn_bwd_host(**a)
+
+
+def test_bwd_host_buffer_layout(lib):
+    """The host entry point's device buffer: packed, o_lo, o_hi, do_lo, do_hi,
+    lse, d_packed, then the workspace, each start 256-byte aligned."""
+    a = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    for (BH, N, d, dt, algo) in [(1, 100, 32, B.PSA_BF16, B.PSA_ALGO_TC), (3, 17, 16, B.PSA_F32, B.PSA_ALGO_AUTO),
+                                 (2, 130, 64, B.PSA_BF16, B.PSA_ALGO_TC_2PASS)]:
+        es = 2 if dt == B.PSA_BF16 else 4
+        sec = BH * N * d * es
+        ws = B.psa_attn_bwd_workspace_bytes(BH, 1, N, d, dt, algo)
+        want = a(4 * sec) + 4 * a(sec) + a(BH * N * 4) + a(4 * sec) + a(ws)
+        assert B.psa_attn_bwd_host_buffer_bytes(BH, 1, N, d, dt, algo) == want
+    assert B.psa_attn_bwd_host_buffer_bytes(1, 1, 0, 32, B.PSA_BF16, B.PSA_ALGO_TC) == 0
+    assert B.psa_attn_bwd_host_buffer_bytes(1, 1, 64, 48, B.PSA_BF16, B.PSA_ALGO_TC) == 0
+    assert B.psa_attn_bwd_host_buffer_bytes(1, 1, 64, 32, B.PSA_F32, B.PSA_ALGO_TC) == 0
+    assert B.psa_attn_bwd_host_buffer_bytes(1, 1, 64, 32, B.PSA_F32, 9) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dev_buf_bytes=1), B.PSA_ERR_WORKSPACE),
+    (dict(dev_buf=None, dev_buf_bytes=1 << 30), B.PSA_ERR_WORKSPACE),
+    (dict(dev_buf=FAKE * 16 + 16, dev_buf_bytes=1 << 30), B.PSA_ERR_ALIGN),
+    (dict(chunks=-1, dev_buf_bytes=1 << 30), B.PSA_ERR_ARG),
+    (dict(chunks=65, dev_buf_bytes=1 << 30), B.PSA_ERR_ARG),
+    (dict(packed=None, dev_buf_bytes=1 << 30), B.PSA_ERR_ARG),
+    (dict(d_packed=None, dev_buf_bytes=1 << 30), B.PSA_ERR_ARG),
+    (dict(scale=float("nan"), dev_buf_bytes=1 << 30), B.PSA_ERR_ARG),
+    (dict(head_dim=48, dev_buf_bytes=1 << 30), B.PSA_ERR_UNSUPPORTED),
+    (dict(N=-1), B.PSA_ERR_ARG),
+    (dict(dtype=7), B.PSA_ERR_ARG),
+    (dict(algo=9, dev_buf_bytes=1 << 30), B.PSA_ERR_ARG),
+    (dict(algo=B.PSA_ALGO_TC, dev_buf_bytes=1 << 30), B.PSA_ERR_UNSUPPORTED),
+    (dict(N=0, packed=None, dev_buf=None), B.PSA_OK),
+    (dict(B=0, d_packed=None, dev_buf=None), B.PSA_OK),
+])
+def test_bwd_host_rejects_before_any_copy(lib, kw, code):
+    """psa_attn_bwd_host checks sizes, dtype, algo, chunks, host pointers and
+    its device buffer before it enqueues a copy (no GPU is touched here)."""
+    assert _bwd_host(**kw) == code
+    if code != B.PSA_OK:
+        assert B.psa_attn_last_error()

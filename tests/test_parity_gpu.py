@@ -188,11 +188,12 @@ def test_tensor_core_forward_full_size_sampled():
     assert rel_err(lse[3].double().cpu().numpy(), ref["lse"][0]) <= TOL_LSE
 
 
-@pytest.mark.parametrize("chunks", [1, 3])
+@pytest.mark.parametrize("chunks", [None, 1, 3, 6])
 def test_host_buffers_pipelined_match_device_path(chunks):
-    """HostBwd (host tensors in, host d_packed out, slices pipelined over
-    streams in `chunks` groups) gives the device path's result: bit for bit in
-    the two-pass mode, and within tolerance of the oracle."""
+    """psa_attn_bwd_host through HostBwd (host tensors in, host d_packed out,
+    slices pipelined over streams in `chunks` groups, None = the library's
+    choice) gives the device path's result: bit for bit in the two-pass mode,
+    and within tolerance of the oracle."""
     import torch
     from gpu_helpers import to_device, TOL
     inp = make_custom(BH=6, N=132, d=32, dtype="bf16", seed=95)
@@ -203,7 +204,6 @@ def test_host_buffers_pipelined_match_device_path(chunks):
     o_lo, o_hi, lse = o_lo.cpu().pin_memory(), o_hi.cpu().pin_memory(), lse.cpu().pin_memory()
     out = torch.empty(packed.shape, dtype=torch.bfloat16).pin_memory()
     runner = B.HostBwd(6, 132, 32, B.PSA_BF16, algo=B.PSA_ALGO_TC_2PASS, chunks=chunks)
-    assert len(runner.bounds) == chunks
     for _ in range(2):  # the second call reuses the staging buffers
         runner(packed, o_lo, o_hi, lse, do_lo, do_hi, inp.scale, out)
     torch.cuda.synchronize()
@@ -305,3 +305,30 @@ def test_fused_query_split_of_last_wave(BH, N, d, slices):
             blk = slice(k0, min(N, k0 + 128))
             for sec in (1, 2, 3):
                 assert rel_err(g[bh, sec, blk], r[sec, blk]) < 3 * TOL["bf16"], (bh, sec, k0)
+
+
+@pytest.mark.parametrize("N,chunks", [(130, 3), (6400, None)])
+def test_host_entry_fused_mode(N, chunks):
+    """psa_attn_bwd_host in the fused tensor-core mode: N = 130 (N % 4 != 0,
+    so one chunk whatever is asked) and the N = 6400, d = 32 shape with four
+    slices and the library's chunk choice; against the oracle (sampled slices
+    at N = 6400)."""
+    import torch
+    from gpu_helpers import TOL
+    BH = 4
+    inp = make_custom(BH=BH, N=N, d=32, dtype="bf16", seed=97 + N)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).pin_memory()  # noqa: E731
+    packed, do_lo, do_hi = pin(inp.packed), pin(inp.do_lo), pin(inp.do_hi)
+    o_lo, o_hi, lse = B.attn_fwd(packed.cuda(), inp.scale)
+    o_lo, o_hi, lse = o_lo.cpu().pin_memory(), o_hi.cpu().pin_memory(), lse.cpu().pin_memory()
+    out = torch.full(packed.shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+    runner = B.HostBwd(BH, N, 32, B.PSA_BF16, algo=B.PSA_ALGO_TC, chunks=chunks)
+    runner(packed, o_lo, o_hi, lse, do_lo, do_hi, inp.scale, out)
+    torch.cuda.synchronize()
+    B.psa_attn_sync_status()
+    slices = [0, BH - 1] if N > 1000 else None
+    ref = oracle_fwd_bwd(inp, slices)["d_packed"]
+    got = out.double().numpy()
+    got = got[slices] if slices else got
+    assert np.isfinite(got).all()
+    assert rel_err(got, ref) < TOL["bf16"]
