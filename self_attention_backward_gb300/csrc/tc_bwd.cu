@@ -80,9 +80,9 @@ struct Cfg {
     static constexpr int QTILE = BS * ROWB;        // [64, D] tile
     static constexpr int NB = D == 64 ? 2 : 3;     // S^T/dP^T buffers in TMEM
     static constexpr int NST = D == 64 ? 3 : 6;    // Q/dO stages
-    // d <= 32: the dK and dQ MMAs have their own issuing thread (warp 14), which
-    // takes them off the main issuer, the bottleneck at small d; at d = 64 the
-    // main issuer keeps them (measured faster there)
+    // d <= 32: the dQ MMAs have their own issuing thread (warp 14), which takes
+    // them off the main issuer; at d = 64 the main issuer keeps them (measured
+    // faster there)
     static constexpr bool SPLIT_MMA = D != 64;
     static constexpr int THREADS = SPLIT_MMA ? 480 : 448;
     static constexpr uint32_t SW = D == 64 ? 2u : D == 32 ? 4u : 6u;  // swizzle code of [*, D] tiles
@@ -192,7 +192,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         mbar_init(sy.bar(B_DQA), 1);
         for (int s = 0; s < C::NST; ++s) {
             mbar_init(sy.bar(B_QF + s), 32);
-            mbar_init(sy.bar(B_QE + s), C::SPLIT_MMA ? 2 : 1);  // a commit from each issuer
+            mbar_init(sy.bar(B_QE + s), 1);
         }
         *sy.abort = 0;
         fence_mbar_init();
@@ -278,7 +278,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             const uint64_t dVH = smem_desc(sb + C::OFF_VH, 16, SBO, C::SW);
             const uint64_t dStage0 = smem_desc(sb + C::OFF_STAGE, 16, SBO, C::SW);
             const uint64_t dStage0mn = smem_desc(sb + C::OFF_STAGE + C::QTILE, C::QTILE, SBO, C::SW);
-            const uint64_t dDS0 = smem_desc(sb + C::OFF_DS, 16, 1024, 2);
             const uint64_t dDS0mn = smem_desc(sb + C::OFF_DS, 16384, 1024, 2);
             constexpr uint32_t STAGE_U = C::STAGE >> 4, QTILE_U = C::QTILE >> 4, BLK_U = 16384 >> 4;
 
@@ -304,12 +303,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 const int s = u % C::NST;
                 const uint64_t dGmn = dStage0mn + STAGE_U * s;      // [dO_lo | dO_hi], MN-major
                 const uint64_t dQmn = dStage0 + STAGE_U * s;        // Q rows, MN-major
-                const uint64_t dDS = dDS0 + BLK_U * (u & 3);
 #pragma unroll
                 for (int kk = 0; kk < C::BS / 16; ++kk) {
                     const uint32_t acc = (u > 0 || kk > 0) ? 1u : 0u;
                     mma_bf16_ts(tmem + C::C_DV, tmem + 128u * (u % C::NB) + 8 * kk, dGmn + KSTEP * kk, ID_DV, acc);
-                    if (!C::SPLIT_MMA) mma_bf16_ss(tmem + C::C_DK, dDS + 2 * kk, dQmn + KSTEP * kk, ID_DK, acc);
+                    mma_bf16_ts(tmem + C::C_DK, tmem + 128u * (u % C::NB) + 64 + 8 * kk, dQmn + KSTEP * kk, ID_DK, acc);
                 }
                 mma_commit(sy.bar(B_QE + s));
             };
@@ -381,8 +379,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                     softmax_vals<false>(sr, pr, L2s + 32 * c, Ds + 32 * c, scale_log2, kvalid, pk, dk);
                 else
                     softmax_vals<true>(sr, pr, L2s + 32 * c, Ds + 32 * c, scale_log2, kvalid, pk, dk);
-                // P over the S^T columns already read (chunk c's S is in registers)
+                // P over the S^T columns, dS over the dP^T columns already read (chunk
+                // c's values are in registers); dS also goes to shared memory for dQ
                 tmem_st_32x32b_x16(tS + 16 * c, pk);
+                tmem_st_32x32b_x16(tDP + 16 * c, dk);
                 // dS block u & 3 last held sub-tile u-4, whose 128-query group h's dQ
                 // product (issued by warp 14) must have read it.  Group h-2 was waited
                 // for at sub-tile u-4 by this warpgroup, and group h+2 needs PF(u),
@@ -417,7 +417,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         // epilogue (warpgroup 0): dK, dV_lo, dV_hi rows of this thread's key
         if (grp == 0) {
             if (ok) ok = warp_wait(sy, sy.bar(B_ACC), 0, 2, nsub);
-            if (C::SPLIT_MMA && ok) ok = warp_wait(sy, sy.bar(B_DQA), 0, 2, nsub);
             if (ok) {
                 tc_fence_after();
                 uint32_t v[D];
@@ -474,45 +473,31 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             }
         }
     } else if (C::SPLIT_MMA) {
-        // ------------------------------------------------------------ dK / dQ issuer
-        // Per sub-tile u, after its softmax (PF): dK += dS^T(u) Q_u.  Per 128-query
-        // group g = sub-tiles 2g, 2g+1, once the drain has read group g-1 (DQE):
-        // dQ_g = dS_g K_j, A = dS read MN-major from the pair's two dS^T blocks
-        // (16 KB apart), B = K_j rows (MN-major).  PF(u+4) cannot complete before
-        // this thread has seen PF(u): the softmax of u+4 first waits for the DQF
-        // of u's group, so the PF ring never runs a phase ahead of it.
+        // ------------------------------------------------------------ dQ issuer
+        // dQ of the 128-query group g = sub-tiles 2g, 2g+1: A = dS (queries x keys)
+        // read MN-major from the pair's two dS^T blocks (16 KB apart), B = K_j rows
+        // (MN-major).  It waits for both sub-tiles' softmax (PF) and for the drain
+        // to have read group g-1 (DQE).  PF(u+4) cannot complete before this
+        // thread has seen PF(u): the softmax of u+4 first waits for this group's
+        // DQF, so the PF ring never runs a phase ahead of it.
         if (lane == 0) {
-            constexpr uint32_t ID_DK = idesc_bf16(128, D, 0, 1);
             constexpr uint32_t ID_DQ = idesc_bf16(128, D, 1, 1);
             constexpr uint32_t KSTEP = (16 * C::ROWB) >> 4;
-            constexpr uint32_t BLK_U = 16384 >> 4, STAGE_U = C::STAGE >> 4;
+            constexpr uint32_t BLK_U = 16384 >> 4;
             const uint64_t dK = smem_desc(sb + C::OFF_K, 16, 8 * C::ROWB, C::SW);
-            const uint64_t dStage0 = smem_desc(sb + C::OFF_STAGE, 16, 8 * C::ROWB, C::SW);
-            const uint64_t dDS0 = smem_desc(sb + C::OFF_DS, 16, 1024, 2);
             const uint64_t dDS0mn = smem_desc(sb + C::OFF_DS, 16384, 1024, 2);
             bool ok = wait_bounded(sy, sy.bar(B_KV), 0, 5, -1);
-            for (int u = 0; u < nsub && ok; ++u) {
-                ok = wait_bounded(sy, sy.bar(B_PF + u % kPfRing), (u / kPfRing) & 1, 5, u);
+            for (int g = 0; g < ngrp && ok; ++g) {
+                const int u0 = 2 * g, u1 = 2 * g + 1;
+                ok = wait_bounded(sy, sy.bar(B_PF + u0 % kPfRing), (u0 / kPfRing) & 1, 5, u0);
+                if (ok && u1 < nsub) ok = wait_bounded(sy, sy.bar(B_PF + u1 % kPfRing), (u1 / kPfRing) & 1, 5, u1);
+                if (ok && g > 0) ok = wait_bounded(sy, sy.bar(B_DQE), (g - 1) & 1, 5, g);
                 if (!ok) break;
                 tc_fence_after();
-                // dK += dS^T(u) Q_u; with the main issuer's commit after dV(u) this
-                // releases the Q/dO stage
-                const int s = u % C::NST;
-                const uint64_t dQmn = dStage0 + STAGE_U * s;
-                const uint64_t dDS = dDS0 + BLK_U * (u & 3);
-#pragma unroll
-                for (int kk = 0; kk < C::BS / 16; ++kk)
-                    mma_bf16_ss(tmem + C::C_DK, dDS + 2 * kk, dQmn + KSTEP * kk, ID_DK, (u > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(sy.bar(B_QE + s));
-                if ((u & 1) == 0 && u < nsub - 1) continue;
-                const int g = u >> 1;
-                if (g > 0 && !wait_bounded(sy, sy.bar(B_DQE), (g - 1) & 1, 5, g)) { ok = false; break; }
-                tc_fence_after();
-                const uint64_t dA = dDS0mn + BLK_U * ((2 * g) & 3);
+                const uint64_t dA = dDS0mn + BLK_U * (u0 & 3);
 #pragma unroll
                 for (int kk = 0; kk < C::BM / 16; ++kk)
                     mma_bf16_ss(tmem + C::C_DQ, dA + 128 * kk, dK + KSTEP * kk, ID_DQ, kk);
-                // also covers dK of both sub-tiles (a commit tracks all earlier MMAs)
                 mma_commit(sy.bar(B_DQF + (g & 1)));
             }
             // this thread's MMAs are done before TMEM is freed (also on abort)
