@@ -79,7 +79,7 @@ struct Cfg {
     static constexpr int KTILE = BM * ROWB;        // [128, D] tile
     static constexpr int QTILE = BS * ROWB;        // [64, D] tile
     static constexpr int NB = D == 64 ? 2 : 3;     // S^T/dP^T buffers in TMEM
-    static constexpr int NST = D == 64 ? 3 : 6;    // Q/dO stages
+    static constexpr int NST = D == 64 ? 4 : 6;    // Q/dO stages
     // d <= 32: the dQ MMAs have their own issuing thread (warp 14), which takes
     // them off the main issuer; at d = 64 the main issuer keeps them (measured
     // faster there)
@@ -368,7 +368,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             const float* Ds = reinterpret_cast<const float*>(smem + C::OFF_DD) + s * 64;
             const uint32_t ds_row = sb + C::OFF_DS + 16384 * (u & 3) + jl * 128;
             const uint32_t tS = trow + 128u * buf, tDP = tS + 64;
-#pragma unroll 1
+// both chunks unrolled: chunk 1's TMEM loads can overlap chunk 0's arithmetic
+#pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t sr[32], pr[32];
                 tmem_ld_32x32b_x32(tS + 32 * c, sr);
