@@ -362,6 +362,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             const int buf = u % C::NB;
             ok = warp_wait(sy, sy.bar(B_SF + buf), (u / C::NB) & 1, 2, u) &&
                  warp_wait(sy, sy.bar(B_QF + s), (u / C::NST) & 1, 2, u);
+            // dS block u & 3 last held sub-tile u-4, whose 128-query group h's dQ
+            // product (the dQ issuer's) must have read it before this sub-tile
+            // writes it.  The parity test on DQF + (h & 1) is exact: group h-2 was
+            // waited for at sub-tile u-4 by this warpgroup, and group h+2 needs
+            // PF(u).  (Waiting here rather than just before the stores leaves the
+            // compiler free to interleave the two chunks; the product is almost
+            // always complete by now.)
+            if (ok && C::SPLIT_MMA && u >= 4) {
+                const int h = (u - 4) >> 1;
+                ok = warp_wait(sy, sy.bar(B_DQF + (h & 1)), (h >> 1) & 1, 2, u);
+            }
             if (!ok) break;
             tc_fence_after();
             const float* L2s = reinterpret_cast<const float*>(smem + C::OFF_L2) + s * 64;
@@ -384,21 +395,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 // c's values are in registers); dS also goes to shared memory for dQ
                 tmem_st_32x32b_x16(tS + 16 * c, pk);
                 tmem_st_32x32b_x16(tDP + 16 * c, dk);
-                // dS block u & 3 last held sub-tile u-4, whose 128-query group h's dQ
-                // product (issued by warp 14) must have read it.  Group h-2 was waited
-                // for at sub-tile u-4 by this warpgroup, and group h+2 needs PF(u),
-                // so the parity test on DQF + (h & 1) is exact.
-                if (C::SPLIT_MMA && c == 0 && u >= 4) {
-                    const int h = (u - 4) >> 1;
-                    ok = warp_wait(sy, sy.bar(B_DQF + (h & 1)), (h >> 1) & 1, 2, u);
-                    tc_fence_after();
-                }
-                if (ok) {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const uint32_t ch = (uint32_t)((c * 4 + v) ^ (jl & 7)) << 4;
-                        st_shared_v4(ds_row + ch, dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
-                    }
+                for (int v = 0; v < 4; ++v) {
+                    const uint32_t ch = (uint32_t)((c * 4 + v) ^ (jl & 7)) << 4;
+                    st_shared_v4(ds_row + ch, dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
                 }
             }
             tmem_wait_st();

@@ -437,7 +437,8 @@ bwd_kv_pair_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_const
             if (!ok) break;
             tc_fence_after();
             const uint32_t tS = trow + 128u * buf, tDP = tS + 64;
-#pragma unroll 1
+// both chunks unrolled: the second chunk's work can overlap the first's
+#pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t sr[32], pr[32];
                 tmem_ld_32x32b_x32(tS + 32 * c, sr);
@@ -631,7 +632,8 @@ bwd_q_pair_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_cons
             tc_fence_after();
             const uint32_t tS = trow + 128u * buf, tDP = tS + 64;
             const int nvalid = N - v * 64;   // keys of this sub-tile that exist
-#pragma unroll 1
+// both chunks unrolled: the second chunk's work can overlap the first's
+#pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t sr[32], pr[32];
                 tmem_ld_32x32b_x32(tS + 32 * c, sr);
