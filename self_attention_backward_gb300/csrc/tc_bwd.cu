@@ -27,8 +27,10 @@
 // works on later sub-tiles while a warpgroup turns S/dP(u) into P and dS.  P^T
 // is written over the first 32 columns of its S^T buffer as bf16 pairs (the A
 // operand of the dV MMA); S/dP(u+NB) reuse u's buffer and are issued after
-// dV/dK(u), the pipe keeping issue order.  dS^T lives in a 4-block shared ring
-// (u & 3), so a pair's dS stays intact until its dQ MMA has read it.
+// dV/dK(u), the pipe keeping issue order.  dS^T goes over the first 32 columns
+// of its dP^T buffer (the A operand of the dK MMA) and into a 4-block shared
+// ring (u & 3) for the dQ MMA, which needs it with queries as rows; a pair's
+// dS stays in the ring until its dQ MMA has read it.
 //
 // Cost model that shaped it (measured on GB300): a tcgen05.mma with M = 128,
 // K = 16 costs about max(46, N/2) cycles, so the MMA count, not the flop
@@ -39,7 +41,7 @@
 // Warp roles: warp 0 TMA producer, warp 1 MMA issuer (one thread) and TMEM
 // owner, warps 2-5 / 6-9 softmax-gradient warpgroups 0 / 1 (one key row per
 // thread), warps 10-13 dQ drain (one query row per thread); for d <= 32 a
-// warp 14 whose one thread issues the dK and dQ MMAs (480 threads, else 448).
+// warp 14 whose one thread issues the dQ MMAs (480 threads, else 448).
 //
 // Every mbarrier wait is bounded (kTimeoutNs); on timeout the CTA sets a device
 // error word (read by psa_attn_sync_status), skips the rest of its work, waits
@@ -281,9 +283,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             const uint64_t dDS0mn = smem_desc(sb + C::OFF_DS, 16384, 1024, 2);
             constexpr uint32_t STAGE_U = C::STAGE >> 4, QTILE_U = C::QTILE >> 4, BLK_U = 16384 >> 4;
 
-            // S^T(u), dP^T(u) into TMEM buffer u & 1.  Its Q/dO stage is known to be
+            // S^T(u), dP^T(u) into TMEM buffer u % NB.  Its Q/dO stage is known to be
             // loaded: the prologue waits for it, later the softmax warpgroup that
-            // arrives PF(u-2) has waited for it first.
+            // arrives PF(u-NB) has waited for it first.
             auto issue_s_dp = [&](int u) {
                 const int s = u % C::NST;
                 const uint64_t dQs = dStage0 + STAGE_U * s;
