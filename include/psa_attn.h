@@ -59,7 +59,9 @@ typedef enum {
  * exists for the (dtype, head_dim) and the CUDA-core (SIMT) path elsewhere.
  *   PSA_ALGO_TC        one key-outer pass; dQ partial sums are added to an
  *                      fp32 accumulator with atomics, so the rounding of dQ
- *                      can differ from run to run.
+ *                      can differ from run to run.  (The units of its last,
+ *                      partial wave are split along the queries; their dK/dV
+ *                      partials are summed in a fixed order.)
  *   PSA_ALGO_TC_2PASS  a key-outer dK/dV pass and a query-outer dQ pass
  *                      ("Struct PsaFa2Backward" description: dQ by iterating
  *                      over keys, dK/dV by iterating over queries); no atomics,
@@ -90,8 +92,9 @@ int psa_attn_fwd_algo(const void* packed, void* o_lo, void* o_hi, float* lse,
 
 /*
  * Bytes of device workspace psa_attn_bwd needs for these sizes and the kernel
- * AUTO would pick (fp32 row statistics D and, on the tensor-core path, an fp32
- * dQ accumulator).  Returns 0 for an empty or invalid problem.
+ * AUTO would pick (fp32 row statistics D and, on the fused tensor-core path, an
+ * fp32 dQ accumulator and room for the fp32 dK/dV partials of split units; the
+ * size does not depend on the GPU).  Returns 0 for an empty or invalid problem.
  */
 size_t psa_attn_bwd_workspace_bytes(int B, int heads, int N, int head_dim, int dtype);
 
