@@ -198,9 +198,10 @@ int psa_attn_bwd_host(const void* packed, const void* o_lo, const void* o_hi, co
     };
 
     // the staging buffers are free once the caller's stream got here
-    if ((ce = cudaEventRecord(p->ev_start, main)) != cudaSuccess) return cuda_fail("cudaEventRecord", ce);
-    cudaStreamWaitEvent(p->s_in, p->ev_start, 0);
-    cudaStreamWaitEvent(p->s_out, p->ev_start, 0);
+    ce = cudaEventRecord(p->ev_start, main);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(p->s_in, p->ev_start, 0);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(p->s_out, p->ev_start, 0);
+    if (ce != cudaSuccess) return cuda_fail("ordering the copy streams after the caller's stream", ce);
 
     int rc = PSA_OK;
     for (int c = 0; c < chunks; ++c) {
@@ -233,12 +234,12 @@ int psa_attn_bwd_host(const void* packed, const void* o_lo, const void* o_hi, co
     // the caller's stream continues after every copy this call enqueued (also
     // after an error, so that a later call may reuse the buffers)
     const std::string keep = rc ? std::string(psa_attn_last_error()) : std::string();
-    cudaEventRecord(p->ev_in_end, p->s_in);
-    cudaStreamWaitEvent(main, p->ev_in_end, 0);
-    cudaEventRecord(p->ev_done, p->s_out);
-    ce = cudaStreamWaitEvent(main, p->ev_done, 0);
+    ce = cudaEventRecord(p->ev_in_end, p->s_in);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(main, p->ev_in_end, 0);
+    if (ce == cudaSuccess) ce = cudaEventRecord(p->ev_done, p->s_out);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(main, p->ev_done, 0);
     if (rc) return psa::set_last_error(rc, keep);
-    if (ce != cudaSuccess) return cuda_fail("cudaStreamWaitEvent", ce);
+    if (ce != cudaSuccess) return cuda_fail("ordering the caller's stream after the copies", ce);
     return psa::set_last_error(PSA_OK, "");
 }
 
