@@ -118,12 +118,15 @@ struct Cfg {
 // with NB <= 3 no warp runs 4 sub-tiles ahead of a slower one and a PF barrier
 // never gets arrivals for two of its phases at once (a ring of 2 would allow a
 // warp two sub-tiles ahead to complete a slower warp's phase).
-// DQF: the dQ product of 128-query group g is done, at DQF + (g & 1), so that a
-// waiter on group g can never see group g+1's phase (see the dQ issuer);
-// DQE: the drain has read the dQ accumulator; DQA: the dQ issuer's final commit.
-enum { B_KV = 0, B_SF = 1, B_PF = 4, B_DQE = 8, B_ACC = 9, B_DQA = 10, B_QF = 11, B_QE = 17, B_DQF = 23 };
+// DQF: the dQ product of 128-query group g is done, at DQF + (g & 1); DQE: the
+// drain has read group g from the dQ accumulator, at DQE + (g & 1).  Each pair
+// alternates by group so that a waiter on group g finds the barrier at most one
+// phase on: the barrier's previous phase (group g-2) is known complete when the
+// wait starts, and its next one (group g+2) cannot complete before the waiter
+// has acted (see each wait).  DQA: the dQ issuer's final commit.
+enum { B_KV = 0, B_SF = 1, B_PF = 4, B_ACC = 9, B_DQA = 10, B_QF = 11, B_QE = 17, B_DQF = 23, B_DQE = 25 };
 constexpr int kPfRing = 4;
-static_assert(B_DQF + 2 <= 32, "barrier area holds 32 barriers");
+static_assert(B_DQE + 2 <= 32, "barrier area holds 32 barriers");
 
 // P and dS of one 32-query chunk of this thread's key row, packed to bf16
 // pairs: P = exp2(S * scale*log2e - L), dS = P (dP - D).
@@ -190,6 +193,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         mbar_init(sy.bar(B_DQF), 1);
         mbar_init(sy.bar(B_DQF + 1), 1);
         mbar_init(sy.bar(B_DQE), 128);
+        mbar_init(sy.bar(B_DQE + 1), 128);
         mbar_init(sy.bar(B_ACC), 1);
         mbar_init(sy.bar(B_DQA), 1);
         for (int s = 0; s < C::NST; ++s) {
@@ -412,8 +416,13 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             // before S/dP(u), and the pipe keeps issue order)
             if (ok && u + C::NB < nsub)
                 ok = warp_wait(sy, sy.bar(B_QF + (u + C::NB) % C::NST), ((u + C::NB) / C::NST) & 1, 2, u);
-            if (!C::SPLIT_MMA && ok && ((u & 1) == 1 || u == nsub - 1) && u >= 2)
-                ok = warp_wait(sy, sy.bar(B_DQE), ((u >> 1) - 1) & 1, 2, u);
+            // (the drain of group gp = u/2 - 1: group gp-2's drain was complete
+            // before S/dP(u) was issued, as the softmax of the sub-tile closing
+            // group gp-1 waited for it, and group gp+2's drain needs PF(u))
+            if (!C::SPLIT_MMA && ok && ((u & 1) == 1 || u == nsub - 1) && u >= 2) {
+                const int gp = (u >> 1) - 1;
+                ok = warp_wait(sy, sy.bar(B_DQE + (gp & 1)), (gp >> 1) & 1, 2, u);
+            }
             mbar_arrive(sy.bar(B_PF + u % kPfRing));
             if (!ok) break;
         }
@@ -465,7 +474,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             tmem_ld_row<D>(trow + C::C_DQ, v);
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(sy.bar(B_DQE));
+            mbar_arrive(sy.bar(B_DQE + (g & 1)));
             const int i = (ubase / 2 + g) * 128 + il;
             if (i < N) {
                 float4* dst = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * N + i) * D);
@@ -494,7 +503,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 const int u0 = 2 * g, u1 = 2 * g + 1;
                 ok = wait_bounded(sy, sy.bar(B_PF + u0 % kPfRing), (u0 / kPfRing) & 1, 5, u0);
                 if (ok && u1 < nsub) ok = wait_bounded(sy, sy.bar(B_PF + u1 % kPfRing), (u1 / kPfRing) & 1, 5, u1);
-                if (ok && g > 0) ok = wait_bounded(sy, sy.bar(B_DQE), (g - 1) & 1, 5, g);
+                // the drain of group g-1 (this thread waited for g-2's before
+                // issuing dQ(g-1); group g+1's drain needs dQ(g+1))
+                if (ok && g > 0) ok = wait_bounded(sy, sy.bar(B_DQE + ((g - 1) & 1)), ((g - 1) >> 1) & 1, 5, g);
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t dA = dDS0mn + BLK_U * (u0 & 3);

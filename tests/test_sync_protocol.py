@@ -1,0 +1,288 @@
+"""A model of the fused tensor-core backward's barrier protocol (bwd_main_kernel
+in self_attention_backward_gb300/csrc/tc_bwd.cu), run under random
+interleavings on the CPU.
+
+Every role of one CTA is a coroutine that makes the same waits, arrivals, MMA
+issues and commits, in the same order and with the same phase parities, as the
+kernel: the TMA producer, the MMA issuer, the softmax warps (two warpgroups of
+four warps), the four dQ drain warps and, for head_dim <= 32, the dQ issuer.
+Each issuing thread's MMAs and commits go through its own FIFO and complete in
+issue order; the two FIFOs interleave freely (the kernel relies on no order
+between issuers).  mbarriers keep a completed-phase count and answer a parity
+wait as the hardware does.
+
+For many sub-tile counts and random schedules the model checks:
+- every wait that passes sees exactly the phase it means (a ring or a parity
+  test that could alias would pass a phase early or late);
+- no arrival lands on a phase other than the barrier's current one;
+- no data hazard: an MMA or a softmax warp reads a TMEM buffer, a Q/dO stage,
+  a dS block or the dQ accumulator only when it holds the sub-tile (or group)
+  the reader means, and nothing is overwritten before its last reader ran;
+- no deadlock: every role finishes.
+"""
+import random
+
+import pytest
+
+
+class Bar:
+    def __init__(self, name, count):
+        self.name, self.count, self.done, self.arrived = name, count, 0, 0
+
+    def passes(self, k):
+        # try_wait.parity(k & 1): true once the phase with that parity completed
+        return (self.done & 1) != (k & 1)
+
+    def arrive(self, k):
+        assert k == self.done, f"{self.name}: arrival for phase {k} while phase {self.done} is open"
+        self.arrived += 1
+        if self.arrived == self.count:
+            self.arrived = 0
+            self.done += 1
+
+
+def run(nsub, split, NB, NST, seed, dqe_pair=True):
+    """One random schedule of one CTA with nsub sub-tiles.  split: the dQ MMAs
+    have an issuing thread of their own (head_dim <= 32).  dqe_pair: the
+    drain's "accumulator read" barrier alternates between two barriers by
+    group parity, as the kernel does (False models a single barrier)."""
+    rnd = random.Random(seed)
+    ngrp = (nsub + 1) // 2
+    bars = {}
+
+    def bar(name, count=1):
+        if name not in bars:
+            bars[name] = Bar(name, count)
+        return bars[name]
+
+    for b in range(NB):
+        bar(("SF", b))
+    for x in range(4):
+        bar(("PF", x), 4)           # four warps of one warpgroup
+    for s in range(NST):
+        bar(("QF", s))
+        bar(("QE", s))
+    for x in range(2 if dqe_pair else 1):
+        bar(("DQE", x), 4)          # four drain warps
+
+    def dqe(g):
+        """The barrier and phase index on which group g's drain arrives."""
+        return (bar(("DQE", g & 1)), g >> 1) if dqe_pair else (bar(("DQE", 0)), g)
+    for x in range(2):
+        bar(("DQF", x))
+
+    # data state
+    tmem = {b: ("free", None) for b in range(NB)}               # whole buffer, MMA side
+    tq = {(b, q): None for b in range(NB) for q in range(4)}     # per lane quarter: ("S"|"P", u)
+    stage = {s: None for s in range(NST)}                         # sub-tile loaded in stage s
+    stage_readers = {s: set() for s in range(NST)}
+    stage_soft = {s: 0 for s in range(NST)}                       # softmax warps done with the stage
+    ds = {(blk, q): ("zero", None, True) for blk in range(4) for q in range(4)}  # (kind, u, read by dQ)
+    acc = {q: ("idle", -1) for q in range(4)}                     # dQ accumulator per quarter
+    fifo = {"main": [], "dq": []}
+
+    def mma_sdp(u):
+        b, s = u % NB, u % NST
+        assert tmem[b][0] == "free", f"S/dP({u}) overwrites buffer {b} holding {tmem[b]}"
+        assert stage[s] == u, f"S/dP({u}) reads stage {s} holding {stage[s]}"
+        stage_readers[s].add("sdp")
+        tmem[b] = ("S", u)
+        for q in range(4):
+            tq[(b, q)] = ("S", u)
+
+    def mma_dvdk(u):
+        b, s = u % NB, u % NST
+        for q in range(4):
+            assert tq[(b, q)] == ("P", u), f"dV/dK({u}) reads {tq[(b, q)]}"
+        assert stage[s] == u and "sdp" in stage_readers[s]
+        stage_readers[s].add("dvdk")
+        tmem[b] = ("free", None)
+
+    def mma_dq(g):
+        for j in (2 * g, 2 * g + 1):
+            if j >= nsub:
+                continue
+            for q in range(4):
+                kind, uu, _ = ds[(j & 3, q)]
+                assert (kind, uu) == ("dS", j), f"dQ({g}) reads dS block {j & 3} holding {(kind, uu)}"
+                ds[(j & 3, q)] = ("dS", j, True)
+        for q in range(4):
+            assert acc[q] in (("idle", -1), ("read", g - 1)), f"dQ({g}) overwrites accumulator {acc[q]}"
+            acc[q] = ("dq", g)
+
+    def issue(who, item):
+        fifo[who].append(item)
+
+    # ---------------------------------------------------------------- roles
+    def producer():
+        for u in range(nsub):
+            s = u % NST
+            k = u // NST - 1
+            yield ("wait", bar(("QE", s)), k)
+            if stage[s] is not None:
+                assert stage_readers[s] >= {"sdp", "dvdk"} and stage_soft[s] == 4, \
+                    f"stage {s} reused early: {stage_readers[s]}, {stage_soft[s]} softmax warps done"
+            stage[s] = u
+            stage_readers[s] = set()
+            stage_soft[s] = 0
+            yield ("arrive", bar(("QF", s)), u // NST)
+
+    def main_issuer():
+        for u in range(min(NB, nsub)):
+            yield ("wait", bar(("QF", u)), 0)
+        for u in range(min(NB, nsub)):
+            issue("main", ("mma", mma_sdp, u))
+            issue("main", ("commit", bar(("SF", u % NB)), u // NB))
+        for u in range(nsub):
+            yield ("wait", bar(("PF", u % 4)), u // 4)
+            issue("main", ("mma", mma_dvdk, u))
+            issue("main", ("commit", bar(("QE", u % NST)), u // NST))
+            if not split and (u % 2 == 1 or u == nsub - 1):
+                g = u // 2
+                issue("main", ("mma", mma_dq, g))
+                issue("main", ("commit", bar(("DQF", g & 1)), g >> 1))
+            if u + NB < nsub:
+                v = u + NB
+                issue("main", ("mma", mma_sdp, v))
+                issue("main", ("commit", bar(("SF", v % NB)), v // NB))
+
+    def softmax(grp, q):
+        for u in range(grp, nsub, 2):
+            b, s = u % NB, u % NST
+            yield ("wait", bar(("SF", b)), u // NB)
+            yield ("wait", bar(("QF", s)), u // NST)
+            if split and u >= 4:
+                h = (u - 4) >> 1
+                yield ("wait", bar(("DQF", h & 1)), h >> 1)
+            # the warp's work: TMEM S/dP(u) -> P/dS(u); dS into the ring
+            assert tq[(b, q)] == ("S", u), f"softmax({u}) reads {tq[(b, q)]}"
+            assert stage[s] == u
+            kind, uu, read = ds[(u & 3, q)]
+            assert read, f"softmax({u}) overwrites dS of sub-tile {uu} before its dQ product read it"
+            ds[(u & 3, q)] = ("dS", u, False)
+            tq[(b, q)] = ("P", u)
+            stage_soft[s] += 1
+            if u + NB < nsub:
+                v = u + NB
+                yield ("wait", bar(("QF", v % NST)), v // NST)
+            if not split and (u % 2 == 1 or u == nsub - 1) and u >= 2:
+                yield ("wait",) + dqe((u >> 1) - 1)
+            yield ("arrive", bar(("PF", u % 4)), u // 4)
+
+    def dq_issuer():
+        for g in range(ngrp):
+            for u in (2 * g, 2 * g + 1):
+                if u < nsub:
+                    yield ("wait", bar(("PF", u % 4)), u // 4)
+            if g > 0:
+                yield ("wait",) + dqe(g - 1)
+            issue("dq", ("mma", mma_dq, g))
+            issue("dq", ("commit", bar(("DQF", g & 1)), g >> 1))
+
+    def drain(q):
+        for g in range(ngrp):
+            yield ("wait", bar(("DQF", g & 1)), g >> 1)
+            assert acc[q] == ("dq", g), f"drain({g}) reads {acc[q]}"
+            acc[q] = ("read", g)
+            yield ("arrive",) + dqe(g)
+
+    roles = [producer(), main_issuer()]
+    roles += [softmax(g, q) for g in range(2) for q in range(4)]
+    roles += [drain(q) for q in range(4)]
+    if split:
+        roles.append(dq_issuer())
+    pending = {i: None for i in range(len(roles))}   # the request each role is blocked on
+
+    def advance(i):
+        try:
+            pending[i] = roles[i].send(None)
+        except StopIteration:
+            pending[i] = "done"
+
+    for i in range(len(roles)):
+        advance(i)
+    steps = 0
+    while True:
+        steps += 1
+        assert steps < 200000
+        enabled = []
+        for i, req in pending.items():
+            if req == "done":
+                continue
+            kind = req[0]
+            if kind == "wait":
+                _, br, k = req
+                # a later phase completed before this waiter saw its own: on the
+                # GPU the parity test could then block forever or pass a phase late
+                assert br.done <= k + 1, f"{br.name}: phase {k + 1} completed before a waiter for phase {k} passed"
+                if br.passes(k):
+                    enabled.append(("role", i))
+            else:
+                enabled.append(("role", i))
+        for who in ("main", "dq"):
+            if fifo[who]:
+                enabled.append(("pipe", who))
+        if not enabled:
+            blocked = {i: (r[1].name, r[2], r[1].done) for i, r in pending.items() if r != "done"}
+            assert not blocked, f"deadlock: {blocked}"
+            assert not fifo["main"] and not fifo["dq"]
+            return
+        kind, x = rnd.choice(enabled)
+        if kind == "pipe":
+            item = fifo[x].pop(0)
+            if item[0] == "mma":
+                item[1](item[2])
+            else:
+                item[1].arrive(item[2])
+            continue
+        req = pending[x]
+        if req[0] == "wait":
+            _, br, k = req
+            assert br.done == k + 1, f"{br.name}: wait for phase {k} passed at {br.done} completed phases"
+        elif req[0] == "arrive":
+            req[1].arrive(req[2])
+        advance(x)
+
+
+@pytest.mark.parametrize("nsub", list(range(1, 14)) + [20, 33])
+@pytest.mark.parametrize("split,NB,NST", [(True, 3, 6), (False, 2, 4)])
+def test_fused_protocol_random_schedules(nsub, split, NB, NST):
+    """head_dim <= 32 (dQ issuer of its own, 3 S/dP buffers, 6 Q/dO stages) and
+    head_dim 64 (dQ on the MMA issuer, 2 buffers, 4 stages), odd and even
+    sub-tile counts, 40 random schedules each."""
+    for seed in range(40):
+        run(nsub, split, NB, NST, seed * 1000 + nsub)
+
+
+def test_single_drain_barrier_aliases():
+    """Why the drain barrier alternates: with a single barrier, at head_dim 64
+    with an odd sub-tile count the softmax of the last (even) sub-tile waits for
+    the drain of group g-1 while the drain of group g-2 may still be open, so
+    its parity test can pass a phase early (and the dQ product of group g could
+    overwrite group g-1's accumulator before it was read)."""
+    failures = 0
+    for seed in range(200):
+        try:
+            run(5, False, 2, 4, seed, dqe_pair=False)
+        except AssertionError:
+            failures += 1
+    assert failures > 0
+
+
+def test_model_catches_a_broken_protocol():
+    """The model is not vacuous: without the softmax's wait for the dQ product
+    (head_dim <= 32), some schedule overwrites a dS block that dQ has not read."""
+    import inspect
+    src = inspect.getsource(run)
+    broken = src.replace("if split and u >= 4:", "if False:")
+    assert broken != src
+    ns = {}
+    exec(compile("import random\n" + broken.replace("def run(", "def run_broken(", 1), "<broken>", "exec"),
+         {"Bar": Bar, "random": random}, ns)
+    failures = 0
+    for seed in range(200):
+        try:
+            ns["run_broken"](12, True, 3, 6, seed)
+        except AssertionError:
+            failures += 1
+    assert failures > 0
