@@ -1,6 +1,8 @@
-"""A model of the fused tensor-core backward's barrier protocol (bwd_main_kernel
-in self_attention_backward_gb300/csrc/tc_bwd.cu), run under random
-interleavings on the CPU.
+"""Models of the tensor-core backward kernels' barrier protocols, run under
+random interleavings on the CPU: the fused kernel (bwd_main_kernel in
+self_attention_backward_gb300/csrc/tc_bwd.cu) and the two passes of the
+two-pass mode on CTA pairs (bwd_kv_pair_kernel, bwd_q_pair_kernel in
+self_attention_backward_gb300/csrc/tc_pair.cu).
 
 Every role of one CTA is a coroutine that makes the same waits, arrivals, MMA
 issues and commits, in the same order and with the same phase parities, as the
@@ -242,6 +244,200 @@ def run(nsub, split, NB, NST, seed, dqe_pair=True):
         elif req[0] == "arrive":
             req[1].arrive(req[2])
         advance(x)
+
+
+def run_pair(nsub, NB, NST, seed, soft_waits_full, ordered=True):
+    """One random schedule of a CTA pair in either pass of the two-pass mode.
+
+    Per CTA r: a producer (stage s of sub-tile u, FULL_r(s) / EMPTY_r(s)) and
+    two softmax warpgroups of four warps; in CTA 0 the two issuing threads:
+    warp 10 issues S/dP(u) once the pair is ready (RDY, both producers) and,
+    from u = NB on, once EMPTY(u-NB) shows the buffer's previous sub-tile
+    consumed; warp 1 issues the PF(u)-gated product (dV/dK in pass 1, dQ in
+    pass 2) and commits EMPTY(u).  Commits go to both CTAs' barriers (a
+    multicast) and the softmax warps arrive on CTA 0's PF barrier (a remote
+    arrive); both are modelled as deliveries that may land later.  Deliveries
+    from one source (an issuing thread's commits, one warp's arrives) to one
+    CTA land in the order they were made (a later commit tracks the earlier
+    one's MMAs too); deliveries on different such channels interleave freely.
+    soft_waits_full: pass 1's softmax also waits for its own stage.  ordered:
+    False lets every delivery land in any order (see the test below)."""
+    rnd = random.Random(seed)
+    serial = [0]
+
+    def channel(ch):
+        serial[0] += 1
+        return ch if ordered else (ch, serial[0])
+    bars = {}
+
+    def bar(name, count=1):
+        if name not in bars:
+            bars[name] = Bar(name, count)
+        return bars[name]
+
+    for r in range(2):
+        for b in range(NB):
+            bar(("SF", r, b))
+        for st in range(NST):
+            bar(("FULL", r, st))
+            bar(("EMPTY", r, st))
+    for x in range(4):
+        bar(("PF", x), 8)            # four warps of one warpgroup, in each CTA
+    bar("RDY", 2)                    # both producers
+    nready = min(nsub, NB)
+
+    stage = {(r, st): None for r in range(2) for st in range(NST)}
+    stage_use = {(r, st): set() for r in range(2) for st in range(NST)}
+    tmem = {b: "free" for b in range(NB)}                        # the pair's buffer b, MMA side
+    tq = {(r, b, q): None for r in range(2) for b in range(NB) for q in range(4)}
+    fifo = {"w10": [], "w1": []}
+    later = {}                                                    # (source, CTA) -> deliveries in flight
+
+    def mma_sdp(u):
+        b = u % NB
+        assert tmem[b] == "free", f"S/dP({u}) overwrites buffer {b}"
+        for r in range(2):
+            assert stage[(r, u % NST)] == u, f"S/dP({u}) reads CTA {r}'s stage holding {stage[(r, u % NST)]}"
+            stage_use[(r, u % NST)].add("sdp")
+            for q in range(4):
+                tq[(r, b, q)] = ("S", u)
+        tmem[b] = ("S", u)
+
+    def mma_second(u):
+        b = u % NB
+        for r in range(2):
+            assert stage[(r, u % NST)] == u and "sdp" in stage_use[(r, u % NST)]
+            stage_use[(r, u % NST)].add("second")
+            for q in range(4):
+                assert tq[(r, b, q)] == ("P", u), f"product({u}) reads {tq[(r, b, q)]}"
+        tmem[b] = "free"
+
+    def producer(r):
+        for u in range(nsub):
+            st = u % NST
+            yield ("wait", bar(("EMPTY", r, st)), u // NST - 1)
+            if stage[(r, st)] is not None:
+                assert stage_use[(r, st)] >= {"sdp", "second"}, f"CTA {r} stage {st} reused early"
+            stage[(r, st)] = u
+            stage_use[(r, st)] = set()
+            yield ("arrive", bar(("FULL", r, st)), u // NST)
+            if u == nready - 1:
+                for x in range(nready):
+                    yield ("wait", bar(("FULL", r, x)), 0)
+                yield ("arrive", bar("RDY"), 0)
+
+    def warp10():
+        yield ("wait", bar("RDY"), 0)
+        for u in range(nsub):
+            if u >= NB:
+                w = u - NB
+                yield ("wait", bar(("EMPTY", 0, w % NST)), w // NST)
+            fifo["w10"].append(("mma", mma_sdp, u))
+            fifo["w10"].append(("commit", [(("w10", r), bar(("SF", r, u % NB)), u // NB) for r in range(2)]))
+
+    def warp1():
+        for u in range(nsub):
+            yield ("wait", bar(("PF", u % 4)), u // 4)
+            fifo["w1"].append(("mma", mma_second, u))
+            fifo["w1"].append(("commit", [(("w1", r), bar(("EMPTY", r, u % NST)), u // NST) for r in range(2)]))
+
+    def softmax(r, grp, q):
+        for u in range(grp, nsub, 2):
+            b = u % NB
+            yield ("wait", bar(("SF", r, b)), u // NB)
+            if soft_waits_full:
+                yield ("wait", bar(("FULL", r, u % NST)), u // NST)
+            assert tq[(r, b, q)] == ("S", u), f"softmax({u}) reads {tq[(r, b, q)]}"
+            tq[(r, b, q)] = ("P", u)
+            if u + NB < nsub:
+                v = u + NB
+                yield ("wait", bar(("FULL", r, v % NST)), v // NST)
+            yield ("remote", ("soft", r, grp, q), bar(("PF", u % 4)), u // 4)
+
+    roles = [producer(0), producer(1), warp10(), warp1()]
+    roles += [softmax(r, g, q) for r in range(2) for g in range(2) for q in range(4)]
+    pending = {}
+
+    def advance(i):
+        try:
+            pending[i] = roles[i].send(None)
+        except StopIteration:
+            pending[i] = "done"
+
+    for i in range(len(roles)):
+        advance(i)
+    steps = 0
+    while True:
+        steps += 1
+        assert steps < 400000
+        enabled = []
+        for i, req in pending.items():
+            if req == "done":
+                continue
+            if req[0] == "wait":
+                _, br, k = req
+                assert br.done <= k + 1, f"{br.name}: phase {k + 1} completed before a waiter for phase {k} passed"
+                if br.passes(k):
+                    enabled.append(("role", i))
+            else:
+                enabled.append(("role", i))
+        for who in fifo:
+            if fifo[who]:
+                enabled.append(("pipe", who))
+        for ch, queue in later.items():
+            if queue:
+                enabled.append(("later", ch))
+        if not enabled:
+            blocked = {i: (r[1].name, r[2], r[1].done) for i, r in pending.items() if r != "done"}
+            assert not blocked, f"deadlock: {blocked}"
+            return
+        kind, x = rnd.choice(enabled)
+        if kind == "pipe":
+            item = fifo[x].pop(0)
+            if item[0] == "mma":
+                item[1](item[2])
+            else:
+                for ch, br, k in item[1]:
+                    later.setdefault(channel(ch), []).append((br, k))
+            continue
+        if kind == "later":
+            br, k = later[x].pop(0)
+            br.arrive(k)
+            continue
+        req = pending[x]
+        if req[0] == "wait":
+            _, br, k = req
+            assert br.done == k + 1, f"{br.name}: wait for phase {k} passed at {br.done} completed phases"
+        elif req[0] == "arrive":
+            req[1].arrive(req[2])
+        elif req[0] == "remote":
+            later.setdefault(channel(req[1]), []).append((req[2], req[3]))
+        advance(x)
+
+
+@pytest.mark.parametrize("nsub", list(range(1, 12)) + [17, 26])
+@pytest.mark.parametrize("NB,NST,soft_waits_full", [
+    (3, 6, True), (2, 4, True),      # pass 1 (dK/dV), head_dim 32 and 64
+    (3, 6, False), (2, 6, False),    # pass 2 (dQ), head_dim 32 and 64
+])
+def test_pair_protocol_random_schedules(nsub, NB, NST, soft_waits_full):
+    """Both passes of the two-pass mode with their buffer and stage counts,
+    25 random schedules each."""
+    for seed in range(25):
+        run_pair(nsub, NB, NST, seed * 7 + nsub, soft_waits_full)
+
+
+def test_pair_protocol_relies_on_ordered_commits():
+    """The pair kernels rely on one issuing thread's commits reaching a CTA in
+    issue order: with every delivery free to land in any order, a softmax warp
+    can find S/dP's barrier a phase behind and pass its parity test early."""
+    failures = 0
+    for seed in range(100):
+        try:
+            run_pair(7, 3, 6, seed, True, ordered=False)
+        except AssertionError:
+            failures += 1
+    assert failures > 0
 
 
 @pytest.mark.parametrize("nsub", list(range(1, 14)) + [20, 33])
