@@ -1,8 +1,9 @@
-"""Models of the tensor-core backward kernels' barrier protocols, run under
-random interleavings on the CPU: the fused kernel (bwd_main_kernel in
-self_attention_backward_gb300/csrc/tc_bwd.cu) and the two passes of the
-two-pass mode on CTA pairs (bwd_kv_pair_kernel, bwd_q_pair_kernel in
-self_attention_backward_gb300/csrc/tc_pair.cu).
+"""Models of the tensor-core kernels' barrier protocols, run under random
+interleavings on the CPU: the fused backward (bwd_main_kernel in
+self_attention_backward_gb300/csrc/tc_bwd.cu), the two passes of the two-pass
+mode on CTA pairs (bwd_kv_pair_kernel, bwd_q_pair_kernel in
+self_attention_backward_gb300/csrc/tc_pair.cu) and the forward (fwd_kernel in
+self_attention_backward_gb300/csrc/tc_fwd.cu).
 
 Every role of one CTA is a coroutine that makes the same waits, arrivals, MMA
 issues and commits, in the same order and with the same phase parities, as the
@@ -425,6 +426,172 @@ def test_pair_protocol_random_schedules(nsub, NB, NST, soft_waits_full):
     25 random schedules each."""
     for seed in range(25):
         run_pair(nsub, NB, NST, seed * 7 + nsub, soft_waits_full)
+
+
+def run_fwd(nk, seed, p_move):
+    """One random schedule of one forward CTA over nk key tiles: the producer
+    (Q once; K tile j into stage j % 2 after KE, [V_lo | V_hi] tile j into
+    stage j % 2 after VE; each copy lands on its own, in any order), the MMA
+    issuer (S(0), S(1) after Q, K_0, K_1; then per tile: wait PF(j), P(j) V_j,
+    commits VE and OD, S(j+2)) and four softmax warps (per tile: wait SF(j);
+    with probability p_move the warp's row max moves, and for j > 0 it waits
+    OD(j-1) and rescales its O rows; it writes P(j), waits for V_j and K_{j+2},
+    arrives PF(j))."""
+    rnd = random.Random(seed)
+    bars = {}
+
+    def bar(name, count=1):
+        if name not in bars:
+            bars[name] = Bar(name, count)
+        return bars[name]
+
+    for x in range(2):
+        for nm in ("SF", "KF", "KE", "VF", "VE"):
+            bar((nm, x))
+        bar(("PF", x), 4)
+    bar("OD")
+    kst = {0: None, 1: None}
+    kuse = {0: set(), 1: set()}
+    vst = {0: None, 1: None}
+    vuse = {0: set(), 1: set()}
+    sbuf = {0: "free", 1: "free"}
+    tq = {(b, q): None for b in range(2) for q in range(4)}
+    o_last = {q: -1 for q in range(4)}        # last P V product applied to this warp's O rows
+    o_pv = [-1]                               # last P V product executed
+    fifo = []
+    landing = []                              # copies in flight: (barrier, phase, effect)
+
+    def mma_s(j):
+        b = j & 1
+        assert sbuf[b] == "free", f"S({j}) overwrites buffer {b}"
+        assert kst[j % 2] == j, f"S({j}) reads K stage holding {kst[j % 2]}"
+        kuse[j % 2].add("s")
+        sbuf[b] = ("S", j)
+        for q in range(4):
+            tq[(b, q)] = ("S", j)
+
+    def mma_pv(j):
+        b = j & 1
+        for q in range(4):
+            assert tq[(b, q)] == ("P", j), f"PV({j}) reads {tq[(b, q)]}"
+            assert o_last[q] == j - 1, f"PV({j}) accumulates onto O rows holding PV({o_last[q]})"
+            o_last[q] = j
+        assert vst[j % 2] == j
+        vuse[j % 2].add("pv")
+        o_pv[0] = j
+        sbuf[b] = "free"
+
+    def producer():
+        for j in range(nk):
+            sk = j % 2
+            yield ("wait", bar(("KE", sk)), j // 2 - 1)
+            if kst[sk] is not None:
+                assert "s" in kuse[sk], f"K stage {sk} reused before S({kst[sk]}) read it"
+            landing.append((bar(("KF", sk)), j // 2, ("k", sk, j)))
+            yield ("wait", bar(("VE", sk)), j // 2 - 1)
+            if vst[sk] is not None:
+                assert "pv" in vuse[sk], f"V stage {sk} reused before PV({vst[sk]}) read it"
+            landing.append((bar(("VF", sk)), j // 2, ("v", sk, j)))
+
+    def issuer():
+        for j in range(min(2, nk)):
+            yield ("wait", bar(("KF", j)), 0)
+        for j in range(min(2, nk)):
+            fifo.append(("mma", mma_s, j))
+            fifo.append(("commit", bar(("SF", j & 1)), j >> 1))
+            fifo.append(("commit", bar(("KE", j % 2)), j // 2))
+        for j in range(nk):
+            yield ("wait", bar(("PF", j & 1)), j >> 1)
+            fifo.append(("mma", mma_pv, j))
+            fifo.append(("commit", bar(("VE", j % 2)), j // 2))
+            fifo.append(("commit", bar("OD"), j))
+            if j + 2 < nk:
+                v = j + 2
+                fifo.append(("mma", mma_s, v))
+                fifo.append(("commit", bar(("SF", v & 1)), v >> 1))
+                fifo.append(("commit", bar(("KE", v % 2)), v // 2))
+
+    def softmax(q):
+        for j in range(nk):
+            b = j & 1
+            yield ("wait", bar(("SF", b)), j >> 1)
+            assert tq[(b, q)] == ("S", j), f"softmax({j}) reads {tq[(b, q)]}"
+            if j > 0 and rnd.random() < p_move:
+                yield ("wait", bar("OD"), j - 1)
+                assert o_last[q] == j - 1, f"rescale at tile {j} sees O rows at PV({o_last[q]})"
+            tq[(b, q)] = ("P", j)
+            yield ("wait", bar(("VF", j % 2)), j // 2)
+            if j + 2 < nk:
+                yield ("wait", bar(("KF", (j + 2) % 2)), (j + 2) // 2)
+            yield ("arrive", bar(("PF", j & 1)), j >> 1)
+
+    roles = [producer(), issuer()] + [softmax(q) for q in range(4)]
+    pending = {}
+
+    def advance(i):
+        try:
+            pending[i] = roles[i].send(None)
+        except StopIteration:
+            pending[i] = "done"
+
+    for i in range(len(roles)):
+        advance(i)
+    steps = 0
+    while True:
+        steps += 1
+        assert steps < 200000
+        enabled = []
+        for i, req in pending.items():
+            if req == "done":
+                continue
+            if req[0] == "wait":
+                _, br, k = req
+                assert br.done <= k + 1, f"{br.name}: phase {k + 1} completed before a waiter for phase {k} passed"
+                if br.passes(k):
+                    enabled.append(("role", i))
+            else:
+                enabled.append(("role", i))
+        if fifo:
+            enabled.append(("pipe", None))
+        for x in range(len(landing)):
+            enabled.append(("land", x))
+        if not enabled:
+            blocked = {i: (r[1].name, r[2], r[1].done) for i, r in pending.items() if r != "done"}
+            assert not blocked, f"deadlock: {blocked}"
+            return
+        kind, x = rnd.choice(enabled)
+        if kind == "pipe":
+            item = fifo.pop(0)
+            if item[0] == "mma":
+                item[1](item[2])
+            else:
+                item[1].arrive(item[2])
+            continue
+        if kind == "land":
+            br, k, (what, st, j) = landing.pop(x)
+            if what == "k":
+                kst[st], kuse[st] = j, set()
+            else:
+                vst[st], vuse[st] = j, set()
+            br.arrive(k)
+            continue
+        req = pending[x]
+        if req[0] == "wait":
+            _, br, k = req
+            assert br.done == k + 1, f"{br.name}: wait for phase {k} passed at {br.done} completed phases"
+        elif req[0] == "arrive":
+            req[1].arrive(req[2])
+        advance(x)
+
+
+@pytest.mark.parametrize("nk", list(range(1, 12)) + [25])
+@pytest.mark.parametrize("p_move", [0.0, 0.3, 1.0])
+def test_forward_protocol_random_schedules(nk, p_move):
+    """The forward with row maxima that never move after the first tile, move
+    sometimes, or move on every tile (each move waits for the previous P V
+    product and rescales O); 30 random schedules each."""
+    for seed in range(30):
+        run_fwd(nk, seed * 31 + nk, p_move)
 
 
 def test_pair_protocol_relies_on_ordered_commits():
