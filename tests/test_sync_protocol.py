@@ -44,11 +44,13 @@ class Bar:
             self.done += 1
 
 
-def run(nsub, split, NB, NST, seed, dqe_pair=True):
+def run(nsub, split, NB, NST, seed, dqe_pair=True, with_dq=True):
     """One random schedule of one CTA with nsub sub-tiles.  split: the dQ MMAs
     have an issuing thread of their own (head_dim <= 32).  dqe_pair: the
     drain's "accumulator read" barrier alternates between two barriers by
-    group parity, as the kernel does (False models a single barrier)."""
+    group parity, as the kernel does (False models a single barrier).
+    with_dq=False models the two-pass mode's single-CTA dK/dV pass
+    (bwd_dkdv_kernel): the same roles without dQ, its drain and the dS ring."""
     rnd = random.Random(seed)
     ngrp = (nsub + 1) // 2
     bars = {}
@@ -140,7 +142,7 @@ def run(nsub, split, NB, NST, seed, dqe_pair=True):
             yield ("wait", bar(("PF", u % 4)), u // 4)
             issue("main", ("mma", mma_dvdk, u))
             issue("main", ("commit", bar(("QE", u % NST)), u // NST))
-            if not split and (u % 2 == 1 or u == nsub - 1):
+            if with_dq and not split and (u % 2 == 1 or u == nsub - 1):
                 g = u // 2
                 issue("main", ("mma", mma_dq, g))
                 issue("main", ("commit", bar(("DQF", g & 1)), g >> 1))
@@ -154,21 +156,22 @@ def run(nsub, split, NB, NST, seed, dqe_pair=True):
             b, s = u % NB, u % NST
             yield ("wait", bar(("SF", b)), u // NB)
             yield ("wait", bar(("QF", s)), u // NST)
-            if split and u >= 4:
+            if with_dq and split and u >= 4:
                 h = (u - 4) >> 1
                 yield ("wait", bar(("DQF", h & 1)), h >> 1)
             # the warp's work: TMEM S/dP(u) -> P/dS(u); dS into the ring
             assert tq[(b, q)] == ("S", u), f"softmax({u}) reads {tq[(b, q)]}"
             assert stage[s] == u
-            kind, uu, read = ds[(u & 3, q)]
-            assert read, f"softmax({u}) overwrites dS of sub-tile {uu} before its dQ product read it"
-            ds[(u & 3, q)] = ("dS", u, False)
+            if with_dq:
+                kind, uu, read = ds[(u & 3, q)]
+                assert read, f"softmax({u}) overwrites dS of sub-tile {uu} before its dQ product read it"
+                ds[(u & 3, q)] = ("dS", u, False)
             tq[(b, q)] = ("P", u)
             stage_soft[s] += 1
             if u + NB < nsub:
                 v = u + NB
                 yield ("wait", bar(("QF", v % NST)), v // NST)
-            if not split and (u % 2 == 1 or u == nsub - 1) and u >= 2:
+            if with_dq and not split and (u % 2 == 1 or u == nsub - 1) and u >= 2:
                 yield ("wait",) + dqe((u >> 1) - 1)
             yield ("arrive", bar(("PF", u % 4)), u // 4)
 
@@ -191,9 +194,10 @@ def run(nsub, split, NB, NST, seed, dqe_pair=True):
 
     roles = [producer(), main_issuer()]
     roles += [softmax(g, q) for g in range(2) for q in range(4)]
-    roles += [drain(q) for q in range(4)]
-    if split:
-        roles.append(dq_issuer())
+    if with_dq:
+        roles += [drain(q) for q in range(4)]
+        if split:
+            roles.append(dq_issuer())
     pending = {i: None for i in range(len(roles))}   # the request each role is blocked on
 
     def advance(i):
@@ -607,6 +611,143 @@ def test_pair_protocol_relies_on_ordered_commits():
     assert failures > 0
 
 
+@pytest.mark.parametrize("nsub", list(range(1, 12)) + [20])
+def test_single_cta_dkdv_protocol_random_schedules(nsub):
+    """The two-pass mode's single-CTA dK/dV pass (head_dim 16: 3 buffers, 6
+    stages), 30 random schedules each."""
+    for seed in range(30):
+        run(nsub, False, 3, 6, seed * 13 + nsub, with_dq=False)
+
+
+def run_dq_single(nsub, seed, NB=3, NST=4):
+    """One random schedule of the two-pass mode's single-CTA dQ pass
+    (tc_dq.cu): a producer (K/V stage s of key sub-tile v after EMPTY(s)), an
+    MMA issuer (S/dP of the first NB sub-tiles after Q and their stages; per
+    sub-tile: wait SD(v % NB), dQ += dS(v) K_v, commit EMPTY, S/dP(v+NB)) and
+    four softmax warps that take every sub-tile (wait SF(v % NB), write dS over
+    S, wait for the stage of v+NB, arrive SD(v % NB))."""
+    rnd = random.Random(seed)
+    bars = {}
+
+    def bar(name, count=1):
+        if name not in bars:
+            bars[name] = Bar(name, count)
+        return bars[name]
+
+    for b in range(NB):
+        bar(("SF", b))
+        bar(("SD", b), 4)
+    stage = {st: None for st in range(NST)}
+    suse = {st: set() for st in range(NST)}
+    tq = {(b, q): None for b in range(NB) for q in range(4)}
+    tbuf = {b: "free" for b in range(NB)}
+    fifo = []
+
+    def mma_sdp(v):
+        b = v % NB
+        assert tbuf[b] == "free", f"S/dP({v}) overwrites buffer {b}"
+        assert stage[v % NST] == v
+        suse[v % NST].add("sdp")
+        tbuf[b] = ("S", v)
+        for q in range(4):
+            tq[(b, q)] = ("S", v)
+
+    def mma_dq(v):
+        b = v % NB
+        for q in range(4):
+            assert tq[(b, q)] == ("dS", v), f"dQ({v}) reads {tq[(b, q)]}"
+        assert stage[v % NST] == v and "sdp" in suse[v % NST]
+        suse[v % NST].add("dq")
+        tbuf[b] = "free"
+
+    def producer():
+        for v in range(nsub):
+            st = v % NST
+            yield ("wait", bar(("EMPTY", st)), v // NST - 1)
+            if stage[st] is not None:
+                assert suse[st] >= {"sdp", "dq"}, f"stage {st} reused early"
+            stage[st], suse[st] = v, set()
+            yield ("arrive", bar(("FULL", st)), v // NST)
+
+    def issuer():
+        for v in range(min(NB, nsub)):
+            yield ("wait", bar(("FULL", v)), 0)
+        for v in range(min(NB, nsub)):
+            fifo.append(("mma", mma_sdp, v))
+            fifo.append(("commit", bar(("SF", v % NB)), v // NB))
+        for v in range(nsub):
+            yield ("wait", bar(("SD", v % NB)), v // NB)
+            fifo.append(("mma", mma_dq, v))
+            fifo.append(("commit", bar(("EMPTY", v % NST)), v // NST))
+            if v + NB < nsub:
+                w = v + NB
+                fifo.append(("mma", mma_sdp, w))
+                fifo.append(("commit", bar(("SF", w % NB)), w // NB))
+
+    def softmax(q):
+        for v in range(nsub):
+            b = v % NB
+            yield ("wait", bar(("SF", b)), v // NB)
+            assert tq[(b, q)] == ("S", v), f"softmax({v}) reads {tq[(b, q)]}"
+            tq[(b, q)] = ("dS", v)
+            if v + NB < nsub:
+                w = v + NB
+                yield ("wait", bar(("FULL", w % NST)), w // NST)
+            yield ("arrive", bar(("SD", b)), v // NB)
+
+    roles = [producer(), issuer()] + [softmax(q) for q in range(4)]
+    pending = {}
+
+    def advance(i):
+        try:
+            pending[i] = roles[i].send(None)
+        except StopIteration:
+            pending[i] = "done"
+
+    for i in range(len(roles)):
+        advance(i)
+    while True:
+        enabled = []
+        for i, req in pending.items():
+            if req == "done":
+                continue
+            if req[0] == "wait":
+                _, br, k = req
+                assert br.done <= k + 1, f"{br.name}: phase {k + 1} completed before a waiter for phase {k} passed"
+                if br.passes(k):
+                    enabled.append(i)
+            else:
+                enabled.append(i)
+        if fifo:
+            enabled.append("pipe")
+        if not enabled:
+            blocked = {i: (r[1].name, r[2], r[1].done) for i, r in pending.items() if r != "done"}
+            assert not blocked, f"deadlock: {blocked}"
+            return
+        x = rnd.choice(enabled)
+        if x == "pipe":
+            item = fifo.pop(0)
+            if item[0] == "mma":
+                item[1](item[2])
+            else:
+                item[1].arrive(item[2])
+            continue
+        req = pending[x]
+        if req[0] == "wait":
+            assert req[1].done == req[2] + 1, f"{req[1].name}: wait for phase {req[2]} passed at {req[1].done}"
+        elif req[0] == "arrive":
+            req[1].arrive(req[2])
+        advance(x)
+
+
+@pytest.mark.parametrize("nsub", list(range(1, 12)) + [20])
+def test_single_cta_dq_protocol_random_schedules(nsub):
+    """The two-pass mode's single-CTA dQ pass (head_dim 16), 30 random
+    schedules each."""
+    for seed in range(30):
+        run_dq_single(nsub, seed * 17 + nsub)
+
+
 @pytest.mark.parametrize("nsub", list(range(1, 14)) + [20, 33])
 @pytest.mark.parametrize("split,NB,NST", [(True, 3, 6), (False, 2, 4)])
 def test_fused_protocol_random_schedules(nsub, split, NB, NST):
@@ -637,7 +778,7 @@ def test_model_catches_a_broken_protocol():
     (head_dim <= 32), some schedule overwrites a dS block that dQ has not read."""
     import inspect
     src = inspect.getsource(run)
-    broken = src.replace("if split and u >= 4:", "if False:")
+    broken = src.replace("if with_dq and split and u >= 4:", "if False:")
     assert broken != src
     ns = {}
     exec(compile("import random\n" + broken.replace("def run(", "def run_broken(", 1), "<broken>", "exec"),
