@@ -1,7 +1,6 @@
 """The C-ABI library: it loads, exports every function include/psa_attn.h
 declares, and rejects bad arguments before launching anything (no GPU needed:
 every call below fails argument checks, so no CUDA call is made)."""
-import ctypes
 
 import pytest
 
