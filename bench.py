@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 METRIC = "PSA attn-bwd TFLOP/s (1 GB300, N=400/1600/6400) and % of roofline"
 UNIT = "TFLOP/s"
 HEADLINE = "psa_bf16_b8_h2_n6400_d32"
-SECONDARY = ["psa_bf16_b32_h8_n400_d64", "psa_bf16_b16_h4_n1600_d64"]
+SECONDARY = ["psa_bf16_b32_h8_n400_d64", "psa_bf16_b16_h4_n1600_d64", "psa_f32_b8_h4_n400_d64"]
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -374,12 +374,17 @@ def run_ours(args, w):
         for name in SECONDARY:
             from self_attention_backward_gb300.inputs import WORKLOADS
             w2 = WORKLOADS[name]
+            # a kernel family the workload's storage type lacks falls back to AUTO
+            dt2 = 1 if w2.dtype == "bf16" else 0
+            algo2 = algo if B.psa_attn_bwd_workspace_bytes(1, 1, 16, w2.d, dt2, algo) > 0 else B.PSA_ALGO_AUTO
             b2 = device_inputs(w2, device)
-            time_steps(w2, b2, 3, flush, device, algo)
-            t2 = statistics.mean(time_steps(w2, b2, max(5, args.steps // 2), flush, device, algo))
+            time_steps(w2, b2, 3, flush, device, algo2)
+            t2 = statistics.mean(time_steps(w2, b2, max(5, args.steps // 2), flush, device, algo2))
             tr, bd = roofline_time_s(w2, peaks)
             sec[name] = {"tflops": metric_flops(w2) / (t2 * 1e-3) / 1e12, "ms": t2, "bound": bd,
-                         "roofline_frac": tr / (t2 * 1e-3)}
+                         "roofline_frac": tr / (t2 * 1e-3), "storage": w2.dtype,
+                         "algo": resolved_algo(B, {B.PSA_ALGO_AUTO: "auto", B.PSA_ALGO_SIMT: "simt",
+                                                   B.PSA_ALGO_TC: "tc", B.PSA_ALGO_TC_2PASS: "tc2"}[algo2], w2)}
             del b2
         line["other_workloads"] = sec
 

@@ -63,8 +63,9 @@ typedef enum {
  *                      partial wave are split along the queries; their dK/dV
  *                      partials are summed in a fixed order.)
  *   PSA_ALGO_TC_2PASS  a key-outer dK/dV pass and a query-outer dQ pass
- *                      ("Struct PsaFa2Backward" description: dQ by iterating
- *                      over keys, dK/dV by iterating over queries); no atomics,
+ *                      (the split of "Struct PsaFa2Backward", description:
+ *                      query gradients from a sweep over keys, key gradients
+ *                      from a sweep over queries); no atomics,
  *                      bit-for-bit reproducible.  Backward only (the forward
  *                      entry points reject it). */
 typedef enum { PSA_ALGO_AUTO = 0, PSA_ALGO_SIMT = 1, PSA_ALGO_TC = 2, PSA_ALGO_TC_2PASS = 3 } psa_algo;
@@ -100,8 +101,9 @@ size_t psa_attn_bwd_workspace_bytes(int B, int heads, int N, int head_dim, int d
 
 /*
  * psa_attn_bwd -- PSA backward (the lo/hi pair of FA2 backward calls).
- * "Struct PsaFa2Backward": description (recompute P from Q, K and the row
- * statistics; dQ by iterating over keys, dK/dV by iterating over queries),
+ * "Struct PsaFa2Backward": description (P is recomputed from Q, K and the row
+ * statistics; query gradients need a sweep over keys, key gradients a sweep
+ * over queries),
  * "Atomicity" (dQ, dK summed over lo and hi; each call owns its dV section).
  *   packed       [BH,4,N,d] dtype, read (Q, K, V_lo, V_hi)
  *   o_lo, o_hi   [BH,N,d] dtype, read (forward outputs)

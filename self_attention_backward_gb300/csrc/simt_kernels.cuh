@@ -8,9 +8,10 @@
 //   pre      : D_i = <dO_lo[i], O_lo[i]> + <dO_hi[i], O_hi[i]>
 //   dK / dV  : one CTA per 64-key tile iterates over all queries
 //   dQ       : one CTA per 64-query tile iterates over all keys
-// "Struct PsaFa2Backward" (description): dQ_n by iterating over all K rows and
-// dK_n / dV_n by iterating over all Q rows; the two iterations are split into
-// two kernels here, so no atomics are needed and the result is deterministic.
+// "Struct PsaFa2Backward" (description): a query row's gradient is a sweep over
+// the keys, a key row's gradients a sweep over the queries.  Here the two
+// sweeps are separate kernels, so nothing is added atomically and the result
+// is deterministic.
 //
 // Thread layout: 4 threads per row; thread `sub` owns the 4-float chunks
 // g = sub + 4c (c < D/16) of a d-row, so the 4 threads of a row read 64

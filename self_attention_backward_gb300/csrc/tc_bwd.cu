@@ -10,8 +10,9 @@
 //
 // Decomposition: one CTA per (batch*head, 128-key tile j).  The CTA keeps K_j,
 // V_lo,j, V_hi,j in shared memory and its dV_lo|dV_hi and dK accumulators in
-// TMEM, and walks over all queries (the page's "dK_n / dV_n by iterating over
-// all Q rows") in 64-query sub-tiles u:
+// TMEM, and sweeps over every query of its slice ("Struct PsaFa2Backward",
+// description: key-row gradients come from such a sweep) in 64-query
+// sub-tiles u:
 //   S^T  = K_j Q_u^T                 (M = 128 keys, N = 64 queries, K = d)
 //   dP^T = V_lo,j dO_lo,u^T + V_hi,j dO_hi,u^T          (K = 2d)
 //   P^T  = exp2(S^T * scale*log2e - LSE*log2e),  dS^T = P^T o (dP^T - D)
@@ -94,9 +95,10 @@ struct Cfg {
     static constexpr int OFF_STAGE = 3 * KTILE;    // stage s: Q, dO_lo, dO_hi at +s*STAGE
     static constexpr int STAGE = 3 * QTILE;
     static constexpr int OFF_DS = OFF_STAGE + NST * STAGE;  // dS^T ring: 4 x [128 keys][64 queries] bf16
-    static constexpr int OFF_L2 = OFF_DS + 4 * 16384;       // NST x 64 fp32: LSE * log2(e)
-    static constexpr int OFF_DD = OFF_L2 + NST * 256;      // NST x 64 fp32: D
-    static constexpr int OFF_BAR = OFF_DD + NST * 256;     // mbarriers
+    // NST x 32 float4, one per query pair c of the stage's 64 queries:
+    // {-LSE_2c log2(e), -LSE_2c+1 log2(e), D_2c, D_2c+1}
+    static constexpr int OFF_ST = OFF_DS + 4 * 16384;
+    static constexpr int OFF_BAR = OFF_ST + NST * 512;     // mbarriers
     static constexpr int OFF_MISC = OFF_BAR + 256;
     static constexpr int USED = OFF_MISC + 64;
     // + 1 KB to align the base to 1024; at least 116 KB so that one CTA owns
@@ -232,8 +234,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             tma_load_3d(sb + C::OFF_VL, &tm_kv, 0, k0, bh * 4 + 2, sy.bar(B_KV));
             tma_load_3d(sb + C::OFF_VH, &tm_kv, 0, k0, bh * 4 + 3, sy.bar(B_KV));
         }
-        float* L2s = reinterpret_cast<float*>(smem + C::OFF_L2);
-        float* Ds = reinterpret_cast<float*>(smem + C::OFF_DD);
+        float4* St = reinterpret_cast<float4*>(smem + C::OFF_ST);
         int s = 0, ph = 0;
         for (int u = 0; u < nsub; ++u) {
             if (!warp_wait(sy, sy.bar(B_QE + s), ph ^ 1, 0, u)) break;
@@ -248,15 +249,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
 #pragma unroll
             for (int x = 0; x < C::NST; ++x)
                 if (x == s) last_issued[x] = u;
-            // row statistics of the 64 queries, 2 per lane; padded rows get
-            // LSE = +inf (so P = 0) and D = 0
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int q = lane * 2 + e;
-                const int i = (ubase + u) * C::BS + q;
-                const bool v = i < N;
-                L2s[s * 64 + q] = v ? lse[(size_t)bh * N + i] * kLog2e : INFINITY;
-                Ds[s * 64 + q] = v ? Drow[(size_t)bh * N + i] : 0.f;
+            // row statistics of the query pair `lane` (queries 2 lane, 2 lane + 1);
+            // padded rows get -LSE log2(e) = -inf (so P = 0) and D = 0
+            {
+                const int i0 = (ubase + u) * C::BS + 2 * lane;
+                const bool v0 = i0 < N, v1 = i0 + 1 < N;
+                const float* l = lse + (size_t)bh * N + i0;
+                const float* dd = Drow + (size_t)bh * N + i0;
+                St[s * 32 + lane] = make_float4(v0 ? -l[0] * kLog2e : -INFINITY, v1 ? -l[1] * kLog2e : -INFINITY,
+                                                v0 ? dd[0] : 0.f, v1 ? dd[1] : 0.f);
             }
             mbar_arrive(sy.bar(B_QF + s));
             if (++s == C::NST) { s = 0; ph ^= 1; }
@@ -356,24 +357,36 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         __syncwarp();
     } else if (warp < 10) {
         // ------------------------------------------------------------ softmax-gradient warpgroups
+        // TMEM fragments of the 16x256b shape: in each 16-lane half hb of the
+        // warp's lane quarter, thread t holds key rows 16 hb + t/4 and 16 hb + 8 + t/4
+        // and, of the sub-tile's 64 queries, the pairs 8k + 2(t%4), +1 (k < 8).  So
+        // a thread needs the statistics of 16 queries (8 pairs), which it loads once
+        // per sub-tile into registers, instead of all 64.
         const int grp = (warp - 2) >> 2;         // 0: even sub-tiles, 1: odd
         const int q4 = warp & 3;                 // TMEM lane quarter of this warp
-        const int jl = q4 * 32 + lane;           // key row within the tile
-        const bool kvalid = k0 + jl < N;
+        const int tq = lane & 3, tr = lane >> 2;
         const bool full = k0 + C::BM <= N;       // uniform: no padded keys in this tile
-        const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+        const uint64_t cs2 = f2_pack(scale_log2, scale_log2);
         bool ok = true;
         for (int u = grp; u < nsub; u += 2) {
             const int s = u % C::NST;
             const int buf = u % C::NB;
-            ok = warp_wait(sy, sy.bar(B_SF + buf), (u / C::NB) & 1, 2, u) &&
-                 warp_wait(sy, sy.bar(B_QF + s), (u / C::NST) & 1, 2, u);
+            ok = warp_wait(sy, sy.bar(B_QF + s), (u / C::NST) & 1, 2, u);
+            // this thread's 8 query pairs: {-LSE log2(e) x2, D x2} (the stage's
+            // statistics are written before its QF arrive)
+            float4 stat[8];
+            if (ok) {
+                const float4* St = reinterpret_cast<const float4*>(smem + C::OFF_ST) + s * 32 + tq;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) stat[k] = St[4 * k];
+            }
+            ok = ok && warp_wait(sy, sy.bar(B_SF + buf), (u / C::NB) & 1, 2, u);
             // dS block u & 3 last held sub-tile u-4, whose 128-query group h's dQ
             // product (the dQ issuer's) must have read it before this sub-tile
             // writes it.  The parity test on DQF + (h & 1) is exact: group h-2 was
             // waited for at sub-tile u-4 by this warpgroup, and group h+2 needs
             // PF(u).  (Waiting here rather than just before the stores leaves the
-            // compiler free to interleave the two chunks; the product is almost
+            // compiler free to interleave the halves; the product is almost
             // always complete by now.)
             if (ok && C::SPLIT_MMA && u >= 4) {
                 const int h = (u - 4) >> 1;
@@ -381,30 +394,55 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             }
             if (!ok) break;
             tc_fence_after();
-            const float* L2s = reinterpret_cast<const float*>(smem + C::OFF_L2) + s * 64;
-            const float* Ds = reinterpret_cast<const float*>(smem + C::OFF_DD) + s * 64;
-            const uint32_t ds_row = sb + C::OFF_DS + 16384 * (u & 3) + jl * 128;
-            const uint32_t tS = trow + 128u * buf, tDP = tS + 64;
-// both chunks unrolled: chunk 1's TMEM loads can overlap chunk 0's arithmetic
+            const uint32_t ds_blk = sb + C::OFF_DS + 16384 * (u & 3);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t sr[32], pr[32];
-                tmem_ld_32x32b_x32(tS + 32 * c, sr);
-                tmem_ld_32x32b_x32(tDP + 32 * c, pr);
-                tmem_wait_ld();
-                uint32_t pk[16], dk[16];
-                if (full)
-                    softmax_vals<false>(sr, pr, L2s + 32 * c, Ds + 32 * c, scale_log2, kvalid, pk, dk);
-                else
-                    softmax_vals<true>(sr, pr, L2s + 32 * c, Ds + 32 * c, scale_log2, kvalid, pk, dk);
-                // P over the S^T columns, dS over the dP^T columns already read (chunk
-                // c's values are in registers); dS also goes to shared memory for dQ
-                tmem_st_32x32b_x16(tS + 16 * c, pk);
-                tmem_st_32x32b_x16(tDP + 16 * c, dk);
+            for (int hb = 0; hb < 2; ++hb) {
+                const int r0 = q4 * 32 + 16 * hb + tr;          // key rows r0, r0 + 8 of the tile
+                const bool kv0 = full || k0 + r0 < N, kv1 = full || k0 + r0 + 8 < N;
+                const uint32_t tS = tmem + ((uint32_t)(q4 * 32 + 16 * hb) << 16) + 128u * buf, tDP = tS + 64;
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const uint32_t ch = (uint32_t)((c * 4 + v) ^ (jl & 7)) << 4;
-                    st_shared_v4(ds_row + ch, dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t sr[16], pr[16];
+                    tmem_ld_16x256b_x4(tS + 32 * c, sr);
+                    tmem_ld_16x256b_x4(tDP + 32 * c, pr);
+                    tmem_wait_ld();
+                    uint32_t pk[8], dk[8];
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const float4 st = stat[4 * c + kk];
+                        const uint64_t nl = f2_pack(st.x, st.y), dd = f2_pack(st.z, st.w);
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[4 * kk + 2 * e]),
+                                                              __uint_as_float(sr[4 * kk + 2 * e + 1])),
+                                                      cs2, nl);
+                            float x0, x1;
+                            f2_unpack(x, x0, x1);
+                            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                            if (!(e ? kv1 : kv0)) p0 = p1 = 0.f;
+                            pk[2 * kk + e] = pack_bf16x2(p0, p1);
+                            const uint64_t t = f2_sub(f2_pack(__uint_as_float(pr[4 * kk + 2 * e]),
+                                                              __uint_as_float(pr[4 * kk + 2 * e + 1])),
+                                                      dd);
+                            float d0, d1;
+                            f2_unpack(f2_mul(f2_pack(p0, p1), t), d0, d1);
+                            dk[2 * kk + e] = pack_bf16x2(d0, d1);
+                        }
+                    }
+                    // P over the S^T columns, dS over the dP^T columns already read
+                    // (this chunk's values are in registers): packed pair 4k + t%4
+                    tmem_st_16x128b_x4(tS + 16 * c, pk);
+                    tmem_st_16x128b_x4(tDP + 16 * c, dk);
+                    // dS also to the 128B-swizzled ring block (row = key, 16-byte
+                    // chunk = query / 8 xor row % 8) for the dQ product: one 4-byte
+                    // word per (row, pair), bank-conflict free across the warp
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            st_shared_b32(ds_blk + (uint32_t)(r0 + 8 * e) * 128u +
+                                              ((uint32_t)((4 * c + kk) ^ tr) << 4) + 4u * tq,
+                                          dk[2 * kk + e]);
                 }
             }
             tmem_wait_st();
@@ -426,6 +464,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             mbar_arrive(sy.bar(B_PF + u % kPfRing));
             if (!ok) break;
         }
+        const int jl = q4 * 32 + lane;           // epilogue: one key row per thread
+        const bool kvalid = k0 + jl < N;
+        const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
         // epilogue (warpgroup 0): dK, dV_lo, dV_hi rows of this thread's key
         if (grp == 0) {
             if (ok) ok = warp_wait(sy, sy.bar(B_ACC), 0, 2, nsub);
@@ -926,15 +967,7 @@ int launch(const BwdArgs& a, std::string* err) {
         !encode_bf16_rows(&tm_lo, a.do_lo, D, a.N, a.BH, M::BS, D, err) ||
         !encode_bf16_rows(&tm_hi, a.do_hi, D, a.N, a.BH, M::BS, D, err))
         return PSA_ERR_CUDA;
-    static std::once_flag attr_once;
-    static cudaError_t attr_st = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_st = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, M::SMEM);
-    });
-    if (attr_st != cudaSuccess) {
-        *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(attr_st);
-        return PSA_ERR_CUDA;
-    }
+    if (!set_max_dynamic_smem((const void*)bwd_main_kernel<D>, M::SMEM, err)) return PSA_ERR_CUDA;
     const long long rows = a.BH * a.N;
     float* Drow = static_cast<float*>(a.workspace);
     float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + align256((size_t)rows * 4));
@@ -994,15 +1027,7 @@ int launch_two_pass(const BwdArgs& a, std::string* err) {
         !encode_bf16_rows(&tm_lo, a.do_lo, D, a.N, a.BH, M::BS, D, err) ||
         !encode_bf16_rows(&tm_hi, a.do_hi, D, a.N, a.BH, M::BS, D, err))
         return PSA_ERR_CUDA;
-    static std::once_flag attr_once;
-    static cudaError_t attr_st = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_st = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, M::SMEM);
-    });
-    if (attr_st != cudaSuccess) {
-        *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(attr_st);
-        return PSA_ERR_CUDA;
-    }
+    if (!set_max_dynamic_smem((const void*)bwd_dkdv_kernel<D>, M::SMEM, err)) return PSA_ERR_CUDA;
     const long long rows = a.BH * a.N;
     float* Drow = static_cast<float*>(a.workspace);
     const int nkt = (a.N + M::BM - 1) / M::BM;

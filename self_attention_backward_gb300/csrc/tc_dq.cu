@@ -1,8 +1,8 @@
 // tc_dq.cu -- tensor-core dQ pass of the PSA backward (bf16), query-outer.
 //
-// "Struct PsaFa2Backward" (description): dQ_n is obtained by iterating over
-// all K rows.  Here one CTA owns a 128-query tile of one (batch, head) and
-// walks over the keys in 64-key sub-tiles v:
+// "Struct PsaFa2Backward" (description): the gradient of a query row needs a
+// sweep over every key of its slice.  Here one CTA owns a 128-query tile of one
+// (batch, head) and makes that sweep in 64-key sub-tiles v:
 //   S    = Q K_v^T                    (M = 128 queries, N = 64 keys, K = d)
 //   dP   = dO_lo V_lo,v^T + dO_hi V_hi,v^T             (K = 2d)
 //   P    = exp2(S * scale*log2e - LSE*log2e),  dS = P o (dP - D)
@@ -275,15 +275,7 @@ int launch_dq(const BwdArgs& a, const float* Drow, std::string* err) {
         !encode_bf16_rows(&tlo, a.do_lo, D, a.N, a.BH, C::BQ, D, err) ||
         !encode_bf16_rows(&thi, a.do_hi, D, a.N, a.BH, C::BQ, D, err))
         return PSA_ERR_CUDA;
-    static std::once_flag attr_once;
-    static cudaError_t attr_st = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_st = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    });
-    if (attr_st != cudaSuccess) {
-        *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(attr_st);
-        return PSA_ERR_CUDA;
-    }
+    if (!set_max_dynamic_smem((const void*)dq_kernel<D>, C::SMEM, err)) return PSA_ERR_CUDA;
     const int nqt = (a.N + C::BQ - 1) / C::BQ;
     const long long grid = a.BH * nqt;
     if (grid > 0x7fffffffll) {

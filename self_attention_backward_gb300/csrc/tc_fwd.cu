@@ -334,15 +334,7 @@ int launch_fwd(const void* packed, void* o_lo, void* o_hi, float* lse, long long
     if (!encode_bf16_rows(&tm, packed, D, N, BH * 4, C::BQ, D, err) ||
         !encode_bf16_rows(&tm_kv, packed, D, N, BH * 4, C::BK, D, err))
         return PSA_ERR_CUDA;
-    static std::once_flag attr_once;
-    static cudaError_t attr_st = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_st = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    });
-    if (attr_st != cudaSuccess) {
-        *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(attr_st);
-        return PSA_ERR_CUDA;
-    }
+    if (!set_max_dynamic_smem((const void*)fwd_kernel<D>, C::SMEM, err)) return PSA_ERR_CUDA;
     const int nqt = (N + C::BQ - 1) / C::BQ;
     const long long grid = BH * nqt;
     if (grid > 0x7fffffffll) {

@@ -1,8 +1,9 @@
 // tc_pair.cu -- two-pass tensor-core backward of PSA attention on SM pairs
 // (bf16, head_dim 32 or 64).
 //
-// "Struct PsaFa2Backward" (description): dK/dV are obtained by iterating over
-// the query rows and dQ by iterating over the key rows.  Both passes here run
+// "Struct PsaFa2Backward" (description): key-row gradients come from a sweep
+// over the queries, query-row gradients from a sweep over the keys.  Both
+// sweeps here run
 // on clusters of two CTAs whose tcgen05.mma instructions span the pair
 // (cta_group::2, M = 256).  Each SM still does its own 128 rows of every
 // instruction at the single-SM rate; what the pair halves is the number of
@@ -672,16 +673,6 @@ bwd_q_pair_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_cons
 }
 
 // ---------------------------------------------------------------- host side
-template <typename K>
-int set_smem(K kernel, int bytes, std::string* err) {
-    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) {
-        *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
-        return PSA_ERR_CUDA;
-    }
-    return PSA_OK;
-}
-
 template <int D>
 int launch_pair(const BwdArgs& a, std::string* err) {
     const long long Z = a.BH * 4;
@@ -696,17 +687,9 @@ int launch_pair(const BwdArgs& a, std::string* err) {
         !encode_bf16_rows(&lo128, a.do_lo, D, a.N, a.BH, 128, D, err) ||
         !encode_bf16_rows(&hi128, a.do_hi, D, a.N, a.BH, 128, D, err))
         return PSA_ERR_CUDA;
-    static std::once_flag once;
-    static int attr_rc = PSA_OK;
-    static std::string attr_err;
-    std::call_once(once, [] {
-        attr_rc = set_smem(bwd_kv_pair_kernel<D>, KvCfg<D>::SMEM, &attr_err);
-        if (attr_rc == PSA_OK) attr_rc = set_smem(bwd_q_pair_kernel<D>, QCfg<D>::SMEM, &attr_err);
-    });
-    if (attr_rc != PSA_OK) {
-        *err = attr_err;
-        return attr_rc;
-    }
+    if (!set_max_dynamic_smem((const void*)bwd_kv_pair_kernel<D>, KvCfg<D>::SMEM, err) ||
+        !set_max_dynamic_smem((const void*)bwd_q_pair_kernel<D>, QCfg<D>::SMEM, err))
+        return PSA_ERR_CUDA;
     float* Drow = static_cast<float*>(a.workspace);
     int rc = tc_pre_d_launch(a, Drow, err);
     if (rc != PSA_OK) return rc;

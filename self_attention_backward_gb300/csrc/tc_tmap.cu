@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <set>
+#include <utility>
 
 namespace psa {
 
@@ -46,6 +48,26 @@ bool encode_bf16_rows(CUtensorMap* map, const void* base, int D, int N, long lon
         *err = "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")";
         return false;
     }
+    return true;
+}
+
+bool set_max_dynamic_smem(const void* kernel, int bytes, std::string* err) {
+    static std::mutex mu;
+    static std::set<std::pair<int, const void*>> done;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        *err = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+        return false;
+    }
+    std::lock_guard<std::mutex> g(mu);
+    if (done.count({dev, kernel})) return true;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) {
+        *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+        return false;
+    }
+    done.insert({dev, kernel});
     return true;
 }
 

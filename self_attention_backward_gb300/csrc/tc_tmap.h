@@ -16,4 +16,10 @@ namespace psa {
 bool encode_bf16_rows(CUtensorMap* map, const void* base, int D, int N, long long Z, int rows, int cols,
                       std::string* err);
 
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device) pair for the life of the process (a
+// function attribute is per device, so a second GPU needs its own call).
+// Returns false and sets *err on failure.
+bool set_max_dynamic_smem(const void* kernel, int bytes, std::string* err);
+
 }  // namespace psa

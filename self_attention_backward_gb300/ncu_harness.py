@@ -1,12 +1,14 @@
 """ncu evidence harness for the backward kernels.
 
-On a machine with the GPU it runs the benchmark once plainly, then twice under
+On a machine with the GPU it runs the benchmark once plainly, then under
 Nsight Compute (`--clock-control none` always):
 
 1. the launch list (`gpu__time_duration.sum` only, one pass per launch) of the
    whole benchmark command;
-2. one backward step's kernels with DRAM bytes, duration and tensor-pipe
-   utilisation (a handful of passes per launch, a few launches);
+2. for each backward kernel of the family, its own capture of ONE launch (the
+   first timed step's) with DRAM bytes, duration and tensor-pipe utilisation
+   (a handful of passes for that launch only; every other launch runs
+   unprofiled);
 
 and writes Markdown summaries: per kernel its launches, total time and share,
 and per captured launch its DRAM traffic, achieved DRAM bandwidth against the
@@ -34,7 +36,13 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 KERNEL_METRICS = ["gpu__time_duration.sum", "dram__bytes_read.sum", "dram__bytes_write.sum",
                   "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active"]
-BACKWARD_KERNELS = "regex:bwd_main_kernel|pair_kernel|dkdv_kernel|dq_kernel|pre_kernel|dq_finalize"
+# the backward kernels of each family, by function name, in launch order
+FAMILY_KERNELS = {
+    "tc": ["pre_kernel", "bwd_main_kernel", "dq_finalize_kernel"],
+    "tc2": ["pre_kernel", "bwd_kv_pair_kernel", "bwd_q_pair_kernel", "bwd_dkdv_kernel", "dq_kernel"],
+    "simt": ["pre_kernel", "dkdv_kernel", "dq_kernel"],
+}
+WARMUP_STEPS = 3
 
 _TIME_SCALE_US = {"ns": 1e-3, "nsecond": 1e-3, "us": 1.0, "usecond": 1.0, "ms": 1e3, "msecond": 1e3,
                   "s": 1e6, "second": 1e6}
@@ -197,10 +205,19 @@ def _run(cmd, log_path: str) -> int:
         return subprocess.call(cmd, cwd=ROOT, stdout=log, stderr=subprocess.STDOUT)
 
 
+def kernel_capture_cmd(name: str, csv_path: str, bench_cmd) -> list:
+    """ncu command line that profiles ONE launch of kernel `name`: the first
+    launch after the warm-up steps (`-s` counts only launches that match the
+    name filter), with the DRAM, duration and tensor-pipe metrics."""
+    return ["ncu", "--metrics", ",".join(KERNEL_METRICS), "--clock-control", "none",
+            "-k", f"regex:^{name}$|^{name}<", "-s", str(WARMUP_STEPS), "-c", "1", "--csv",
+            "--log-file", csv_path] + list(bench_cmd)
+
+
 def run(out_dir: str, algo: str, workload: str | None, record: bool = False) -> int:
     os.makedirs(out_dir, exist_ok=True)
-    bench = [sys.executable, "bench.py", "--steps", "2", "--warmup", "3", "--no-cpu", "--no-secondary",
-             "--algo", algo]
+    bench = [sys.executable, "bench.py", "--steps", "2", "--warmup", str(WARMUP_STEPS), "--no-cpu",
+             "--no-secondary", "--algo", algo]
     if workload:
         bench += ["--workload", workload]
     # the same command must exit 0 without ncu before ncu runs it
@@ -212,19 +229,25 @@ def run(out_dir: str, algo: str, workload: str | None, record: bool = False) -> 
                "--log-file", launches] + bench, os.path.join(out_dir, "ncu_launches.log"))
     if rc != 0:
         return rc
-    # one backward step's kernels: skip the warm-up steps' launches (at most 3
-    # backward kernels per step; 3 warm-up steps)
-    kernels = os.path.join(out_dir, "kernels.csv")
-    rc = _run(["ncu", "--metrics", ",".join(KERNEL_METRICS), "--clock-control", "none", "-k", BACKWARD_KERNELS,
-               "-s", "9", "-c", "3", "--csv", "--log-file", kernels] + bench,
-              os.path.join(out_dir, "ncu_kernels.log"))
-    if rc != 0:
-        return rc
+    # one capture per backward kernel that the launch list shows, one launch each
+    family = algo if algo in FAMILY_KERNELS else "tc"
+    seen = {short_name(k).split("<", 1)[0] for _, k, _, _, _ in read_metric_rows(launches)}
+    rows = []
+    for name in FAMILY_KERNELS[family]:
+        if name not in seen:
+            continue
+        csv_path = os.path.join(out_dir, f"kernel_{name}.csv")
+        rc = _run(kernel_capture_cmd(name, csv_path, bench), os.path.join(out_dir, f"ncu_{name}.log"))
+        if rc != 0:
+            return rc
+        # launch ids restart in every capture: key them by the kernel name too
+        rows += [(f"{name}:{lid}", k, m, u, v) for lid, k, m, u, v in read_metric_rows(csv_path)]
     hbm = measured_hbm_gbs()
     table, total = summarize_launches(read_metric_rows(launches))
-    items = summarize_kernels(read_metric_rows(kernels), hbm)
+    items = summarize_kernels(rows, hbm)
     text = ("# ncu evidence: " + " ".join(bench[1:]) + "\n\n## Launch list (cold-cache, serialised)\n\n" +
-            launches_markdown(table, total) + "\n\n## One backward step\n\n" + kernels_markdown(items, hbm) + "\n")
+            launches_markdown(table, total) + "\n\n## One launch of each backward kernel (separate captures)\n\n" +
+            kernels_markdown(items, hbm) + "\n")
     with open(os.path.join(out_dir, "summary.md"), "w") as f:
         f.write(text)
     print(text)

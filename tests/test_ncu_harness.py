@@ -84,3 +84,17 @@ def test_record_traffic(tmp_path):
     b = importlib.util.module_from_spec(spec)
     spec.loader.exec_module(b)
     assert rec["bwd_main"]["source_hash"] == b.source_hash("tc")
+
+
+def test_kernel_capture_is_one_kernel_one_launch():
+    """Every capture that collects more than the duration names one kernel and
+    takes one launch, after the warm-up steps, with the clocks left alone."""
+    cmd = H.kernel_capture_cmd("bwd_main_kernel", "/tmp/x.csv", ["python", "bench.py"])
+    assert cmd[cmd.index("-c") + 1] == "1"
+    assert cmd[cmd.index("-s") + 1] == str(H.WARMUP_STEPS)
+    assert cmd[cmd.index("--clock-control") + 1] == "none"
+    k = cmd[cmd.index("-k") + 1]
+    assert k.startswith("regex:") and "|" in k and all(p.lstrip("^").startswith("bwd_main_kernel")
+                                                       for p in k[len("regex:"):].split("|"))
+    for fam in H.FAMILY_KERNELS.values():
+        assert len(set(fam)) == len(fam)

@@ -154,8 +154,10 @@ def run(nsub, split, NB, NST, seed, dqe_pair=True, with_dq=True):
     def softmax(grp, q):
         for u in range(grp, nsub, 2):
             b, s = u % NB, u % NST
-            yield ("wait", bar(("SF", b)), u // NB)
             yield ("wait", bar(("QF", s)), u // NST)
+            # the row statistics of the stage are read here, before the S/dP wait
+            assert stage[s] == u, f"softmax({u}) reads the statistics of stage {s} holding {stage[s]}"
+            yield ("wait", bar(("SF", b)), u // NB)
             if with_dq and split and u >= 4:
                 h = (u - 4) >> 1
                 yield ("wait", bar(("DQF", h & 1)), h >> 1)

@@ -40,7 +40,7 @@ def test_noalloc_matches_workspace_entry_point_two_calls():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     _lib()
-    from gpu_helpers import TOL, rel_err, to_device
+    from gpu_helpers import TOL, oracle_fwd_bwd, rel_err, to_device
 
     # two calls in a row: a larger problem, then a smaller one that reuses the
     # same static scratch (stale rows from the first call must not leak in)
@@ -57,5 +57,8 @@ def test_noalloc_matches_workspace_entry_point_two_calls():
         B.psa_attn_sync_status()
         g, r = got.double().cpu().numpy(), ref.double().cpu().numpy()
         assert np.isfinite(g).all()
+        oracle = oracle_fwd_bwd(inp)["d_packed"]
         for s in range(4):
             assert rel_err(g[:, s], r[:, s]) <= TOL[inp.dtype], (inp.dtype, s)
+            # and against the fp64 oracle itself, not only the other entry point
+            assert rel_err(g[:, s], oracle[:, s]) <= TOL[inp.dtype], (inp.dtype, s, "oracle")
