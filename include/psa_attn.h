@@ -93,9 +93,11 @@ int psa_attn_fwd_algo(const void* packed, void* o_lo, void* o_hi, float* lse,
 
 /*
  * Bytes of device workspace psa_attn_bwd needs for these sizes and the kernel
- * AUTO would pick (fp32 row statistics D and, on the fused tensor-core path, an
- * fp32 dQ accumulator and room for the fp32 dK/dV partials of split units; the
- * size does not depend on the GPU).  Returns 0 for an empty or invalid problem.
+ * AUTO would pick: the fp32 row statistics D (the CUDA-core and two-pass
+ * paths), or on the fused tensor-core path 8 bytes of row statistics per query
+ * (LSE and D, padded to whole 64-query tiles), an fp32 dQ accumulator and room
+ * for the fp32 dK/dV partials of split units.  The size does not depend on the
+ * GPU.  Returns 0 for an empty or invalid problem.
  */
 size_t psa_attn_bwd_workspace_bytes(int B, int heads, int N, int head_dim, int dtype);
 

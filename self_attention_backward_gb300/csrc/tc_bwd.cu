@@ -83,11 +83,12 @@ struct Cfg {
     static constexpr int QTILE = BS * ROWB;        // [64, D] tile
     static constexpr int NB = D == 64 ? 2 : 3;     // S^T/dP^T buffers in TMEM
     static constexpr int NST = D == 64 ? 4 : 6;    // Q/dO stages
-    // d <= 32: the dQ MMAs have their own issuing thread (warp 14), which takes
-    // them off the main issuer; at d = 64 the main issuer keeps them (measured
-    // faster there)
-    static constexpr bool SPLIT_MMA = D != 64;
-    static constexpr int THREADS = SPLIT_MMA ? 480 : 448;
+    // warps: 0 producer, 1 the main MMA issuer (with TWO_ISSUERS: of the even
+    // sub-tiles, and warp 15 of the odd ones), 2-9 softmax, 10-13 dQ drain, 14
+    // the dQ MMA issuer.  Two main issuers gave 1% at head_dim 32 (N = 6400) and
+    // cost 5% at head_dim 64 (N = 1600), measured.
+    static constexpr bool TWO_ISSUERS = D != 64;
+    static constexpr int THREADS = TWO_ISSUERS ? 512 : 480;
     static constexpr uint32_t SW = D == 64 ? 2u : D == 32 ? 4u : 6u;  // swizzle code of [*, D] tiles
     static constexpr int OFF_K = 0;
     static constexpr int OFF_VL = KTILE;
@@ -98,8 +99,8 @@ struct Cfg {
     // NST x 32 float4, one per query pair c of the stage's 64 queries:
     // {-LSE_2c log2(e), -LSE_2c+1 log2(e), D_2c, D_2c+1}
     static constexpr int OFF_ST = OFF_DS + 4 * 16384;
-    static constexpr int OFF_BAR = OFF_ST + NST * 512;     // mbarriers
-    static constexpr int OFF_MISC = OFF_BAR + 256;
+    static constexpr int OFF_BAR = OFF_ST + NST * 512;     // mbarriers (48)
+    static constexpr int OFF_MISC = OFF_BAR + 384;
     static constexpr int USED = OFF_MISC + 64;
     // + 1 KB to align the base to 1024; at least 116 KB so that one CTA owns
     // an SM (its TMEM allocation is all 512 columns)
@@ -130,6 +131,26 @@ enum { B_KV = 0, B_SF = 1, B_PF = 4, B_ACC = 9, B_DQA = 10, B_QF = 11, B_QE = 17
 constexpr int kPfRing = 4;
 static_assert(B_DQE + 2 <= 32, "barrier area holds 32 barriers");
 
+// The fused kernel's barriers.  Two threads issue its main MMAs: the one for
+// sub-tiles of parity p issues dV/dK(u) for its u and then S/dP(u + NB) (so
+// buffer reuse stays in one thread's issue order), each waiting only for its
+// own sub-tiles' PF.  PF is a ring of 8: PF(u + 8) needs S/dP(u + 8), which the
+// thread of u + 5 issues after PF(u + 5), whose S/dP(u + 5) the thread of u + 2
+// -- the same parity as u -- issued after it had seen PF(u + 2), hence PF(u);
+// so no PF phase completes before each of its waiters (the issuer of its parity
+// and the dQ issuer) has seen the previous one.  ACC / ACCB: each main issuer's
+// final commit.  SF is a ring of 2 NB over the sub-tiles (u % 2NB): with NB odd
+// the sub-tiles of one buffer alternate between the issuers, and two issuers
+// give no order between their commits, so each SF barrier has one committing
+// thread (the issuer of the parity opposite to u's) and one waiting warpgroup
+// (u's), which saw its previous phase (u - 2NB) before this one.  DQF, DQE, DQA
+// as above.
+enum {
+    F_KV = 0, F_SF = 1, F_PF = 7, F_ACC = 15, F_ACCB = 16, F_DQA = 17, F_QF = 18, F_QE = 24, F_DQF = 30, F_DQE = 32
+};
+constexpr int kPfRingF = 8;
+static_assert(F_DQE + 2 <= 48, "barrier area holds 48 barriers");
+
 // P and dS of one 32-query chunk of this thread's key row, packed to bf16
 // pairs: P = exp2(S * scale*log2e - L), dS = P (dP - D).
 template <bool MASK>
@@ -158,9 +179,8 @@ template <int D>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_do_lo, const __grid_constant__ CUtensorMap tm_do_hi,
-                const float* __restrict__ lse, const float* __restrict__ Drow, float* __restrict__ dq_acc,
-                bf16* __restrict__ d_packed, int N, int nkt, float scale, float scale_log2, int nfull,
-                int tail_f, float* __restrict__ dkv_part) {
+                const float4* __restrict__ stats, float* __restrict__ dq_acc, bf16* __restrict__ d_packed, int N,
+                int nkt, float scale, float scale_log2, int nfull, int tail_f, float* __restrict__ dkv_part) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -189,18 +209,19 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
     const int ngrp = (nsub + 1) / 2;              // 128-query groups (dQ granularity)
 
     if (threadIdx.x == 0) {
-        mbar_init(sy.bar(B_KV), 1);
-        for (int b = 0; b < C::NB; ++b) mbar_init(sy.bar(B_SF + b), 1);
-        for (int x = 0; x < kPfRing; ++x) mbar_init(sy.bar(B_PF + x), 128);
-        mbar_init(sy.bar(B_DQF), 1);
-        mbar_init(sy.bar(B_DQF + 1), 1);
-        mbar_init(sy.bar(B_DQE), 128);
-        mbar_init(sy.bar(B_DQE + 1), 128);
-        mbar_init(sy.bar(B_ACC), 1);
-        mbar_init(sy.bar(B_DQA), 1);
+        mbar_init(sy.bar(F_KV), 1);
+        for (int b = 0; b < 2 * C::NB; ++b) mbar_init(sy.bar(F_SF + b), 1);
+        for (int x = 0; x < kPfRingF; ++x) mbar_init(sy.bar(F_PF + x), 128);
+        mbar_init(sy.bar(F_DQF), 1);
+        mbar_init(sy.bar(F_DQF + 1), 1);
+        mbar_init(sy.bar(F_DQE), 128);
+        mbar_init(sy.bar(F_DQE + 1), 128);
+        mbar_init(sy.bar(F_ACC), 1);
+        mbar_init(sy.bar(F_ACCB), 1);
+        mbar_init(sy.bar(F_DQA), 1);
         for (int s = 0; s < C::NST; ++s) {
-            mbar_init(sy.bar(B_QF + s), 32);
-            mbar_init(sy.bar(B_QE + s), 1);
+            mbar_init(sy.bar(F_QF + s), 1);
+            mbar_init(sy.bar(F_QE + s), 1);
         }
         *sy.abort = 0;
         fence_mbar_init();
@@ -229,54 +250,53 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
 #pragma unroll
         for (int s = 0; s < C::NST; ++s) last_issued[s] = -1;
         if (lane == 0) {
-            mbar_arrive_expect_tx(sy.bar(B_KV), 3 * C::KTILE);
-            tma_load_3d(sb + C::OFF_K, &tm_kv, 0, k0, bh * 4 + 1, sy.bar(B_KV));
-            tma_load_3d(sb + C::OFF_VL, &tm_kv, 0, k0, bh * 4 + 2, sy.bar(B_KV));
-            tma_load_3d(sb + C::OFF_VH, &tm_kv, 0, k0, bh * 4 + 3, sy.bar(B_KV));
+            mbar_arrive_expect_tx(sy.bar(F_KV), 3 * C::KTILE);
+            tma_load_3d(sb + C::OFF_K, &tm_kv, 0, k0, bh * 4 + 1, sy.bar(F_KV));
+            tma_load_3d(sb + C::OFF_VL, &tm_kv, 0, k0, bh * 4 + 2, sy.bar(F_KV));
+            tma_load_3d(sb + C::OFF_VH, &tm_kv, 0, k0, bh * 4 + 3, sy.bar(F_KV));
         }
-        float4* St = reinterpret_cast<float4*>(smem + C::OFF_ST);
+        // the slice's statistics, 32 float4 per 64-query sub-tile (padded rows
+        // hold -inf and 0), written by the preprocess kernel
+        const float4* st_slice = stats + (size_t)bh * nsub_all * 32;
         int s = 0, ph = 0;
         for (int u = 0; u < nsub; ++u) {
-            if (!warp_wait(sy, sy.bar(B_QE + s), ph ^ 1, 0, u)) break;
+            if (!warp_wait(sy, sy.bar(F_QE + s), ph ^ 1, 0, u)) break;
             if (lane == 0) {
                 const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE;
-                mbar_expect_tx(sy.bar(B_QF + s), 3 * C::QTILE);
+                mbar_arrive_expect_tx(sy.bar(F_QF + s), 3 * C::QTILE + 512);
                 const int q0 = (ubase + u) * C::BS;
-                tma_load_3d(st, &tm_q, 0, q0, bh * 4 + 0, sy.bar(B_QF + s));
-                tma_load_3d(st + C::QTILE, &tm_do_lo, 0, q0, bh, sy.bar(B_QF + s));
-                tma_load_3d(st + 2 * C::QTILE, &tm_do_hi, 0, q0, bh, sy.bar(B_QF + s));
+                tma_load_3d(st, &tm_q, 0, q0, bh * 4 + 0, sy.bar(F_QF + s));
+                tma_load_3d(st + C::QTILE, &tm_do_lo, 0, q0, bh, sy.bar(F_QF + s));
+                tma_load_3d(st + 2 * C::QTILE, &tm_do_hi, 0, q0, bh, sy.bar(F_QF + s));
+                bulk_load(sb + C::OFF_ST + s * 512, st_slice + (size_t)(ubase + u) * 32, 512, sy.bar(F_QF + s));
             }
 #pragma unroll
             for (int x = 0; x < C::NST; ++x)
                 if (x == s) last_issued[x] = u;
-            // row statistics of the query pair `lane` (queries 2 lane, 2 lane + 1);
-            // padded rows get -LSE log2(e) = -inf (so P = 0) and D = 0
-            {
-                const int i0 = (ubase + u) * C::BS + 2 * lane;
-                const bool v0 = i0 < N, v1 = i0 + 1 < N;
-                const float* l = lse + (size_t)bh * N + i0;
-                const float* dd = Drow + (size_t)bh * N + i0;
-                St[s * 32 + lane] = make_float4(v0 ? -l[0] * kLog2e : -INFINITY, v1 ? -l[1] * kLog2e : -INFINITY,
-                                                v0 ? dd[0] : 0.f, v1 ? dd[1] : 0.f);
-            }
-            mbar_arrive(sy.bar(B_QF + s));
             if (++s == C::NST) { s = 0; ph ^= 1; }
         }
         __syncwarp();
         if (*sy.abort && lane == 0) {
             // let this CTA's own copies land before its shared memory is released
-            wait_drain(sy.bar(B_KV), 0);
+            wait_drain(sy.bar(F_KV), 0);
 #pragma unroll
             for (int x = 0; x < C::NST; ++x)
-                if (last_issued[x] >= 0) wait_drain(sy.bar(B_QF + x), (last_issued[x] / C::NST) & 1);
+                if (last_issued[x] >= 0) wait_drain(sy.bar(F_QF + x), (last_issued[x] / C::NST) & 1);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 15) {
+        // ------------------------------------------------------------ main MMA issuers
+        // warp 1 takes the even sub-tiles, warp 15 the odd ones.  Each issues, per
+        // sub-tile u of its parity, dV/dK(u) once PF(u) shows P/dS(u) ready, then
+        // S/dP(u + NB) into the buffer dV/dK(u) just read: one thread's MMAs run in
+        // issue order, so the buffer is reused only after its last reader.  While
+        // one thread waits for its next PF (such a wait first lets its own MMAs in
+        // flight finish), the other's keep the tensor core fed.
+        const int par = warp == 1 ? 0 : 1;
+        constexpr int USTEP = C::TWO_ISSUERS ? 2 : 1;
         if (lane == 0) {
             constexpr uint32_t ID_S = idesc_bf16(128, 64, 0, 0);     // S^T, dP^T: 64 queries
             constexpr uint32_t ID_DV = idesc_bf16(128, 2 * D, 0, 1); // dV_lo | dV_hi: B MN-major
             constexpr uint32_t ID_DK = idesc_bf16(128, D, 0, 1);     // dK: A K-major, B MN-major
-            constexpr uint32_t ID_DQ = idesc_bf16(128, D, 1, 1);     // dQ: A, B MN-major
             constexpr uint32_t SBO = 8 * C::ROWB;
             constexpr uint32_t KSTEP = (16 * C::ROWB) >> 4;          // 16 rows, in descriptor address units
             // every descriptor is built once; an MMA adds its k-step offset to the address field
@@ -285,8 +305,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             const uint64_t dVH = smem_desc(sb + C::OFF_VH, 16, SBO, C::SW);
             const uint64_t dStage0 = smem_desc(sb + C::OFF_STAGE, 16, SBO, C::SW);
             const uint64_t dStage0mn = smem_desc(sb + C::OFF_STAGE + C::QTILE, C::QTILE, SBO, C::SW);
-            const uint64_t dDS0mn = smem_desc(sb + C::OFF_DS, 16384, 1024, 2);
-            constexpr uint32_t STAGE_U = C::STAGE >> 4, QTILE_U = C::QTILE >> 4, BLK_U = 16384 >> 4;
+            constexpr uint32_t STAGE_U = C::STAGE >> 4, QTILE_U = C::QTILE >> 4;
 
             // S^T(u), dP^T(u) into TMEM buffer u % NB.  Its Q/dO stage is known to be
             // loaded: the prologue waits for it, later the softmax warpgroup that
@@ -303,7 +322,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_bf16_ss(tDP, dVH + 2 * kk, dQs + 2 * QTILE_U + 2 * kk, ID_S, 1);
-                mma_commit(sy.bar(B_SF + u % C::NB));
+                mma_commit(sy.bar(F_SF + u % (2 * C::NB)));
             };
             // dV, dK of sub-tile u (A = P^T, dS^T over 64 queries = 4 k-steps)
             auto issue_dv_dk = [&](int u) {
@@ -316,43 +335,34 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                     mma_bf16_ts(tmem + C::C_DV, tmem + 128u * (u % C::NB) + 8 * kk, dGmn + KSTEP * kk, ID_DV, acc);
                     mma_bf16_ts(tmem + C::C_DK, tmem + 128u * (u % C::NB) + 64 + 8 * kk, dQmn + KSTEP * kk, ID_DK, acc);
                 }
-                mma_commit(sy.bar(B_QE + s));
+                mma_commit(sy.bar(F_QE + s));
             };
-            // dQ of the 128-query group g (when this thread issues it): A = dS
-            // (queries x keys) read MN-major from the pair's two dS^T blocks (16 KB
-            // apart); B = K_j rows (MN-major)
-            auto issue_dq = [&](int g) {
-                const uint64_t dA = dDS0mn + BLK_U * ((2 * g) & 3);
-#pragma unroll
-                for (int kk = 0; kk < C::BM / 16; ++kk)
-                    mma_bf16_ss(tmem + C::C_DQ, dA + 128 * kk, dK + KSTEP * kk, ID_DQ, kk);
-                mma_commit(sy.bar(B_DQF + (g & 1)));
-            };
-            bool ok = wait_bounded(sy, sy.bar(B_KV), 0, 1, -1);
-            for (int u = 0; u < C::NB && u < nsub && ok; ++u)
-                ok = wait_bounded(sy, sy.bar(B_QF + u), 0, 1, u);
-            if (ok) {
-                tc_fence_after();
-                for (int u = 0; u < C::NB && u < nsub; ++u) issue_s_dp(u);
+            bool ok = wait_bounded(sy, sy.bar(F_KV), 0, 1, -1);
+            if (par == 0) {
+                for (int u = 0; u < C::NB && u < nsub && ok; ++u)
+                    ok = wait_bounded(sy, sy.bar(F_QF + u), 0, 1, u);
+                if (ok) {
+                    tc_fence_after();
+                    for (int u = 0; u < C::NB && u < nsub; ++u) issue_s_dp(u);
+                }
+            } else if (nsub > 1 && ok && C::TWO_ISSUERS) {
+                // dV/dK(0), whose first MMAs overwrite the accumulators, must be done
+                // before this thread adds to them: its commit is QE(0)'s first phase
+                ok = wait_bounded(sy, sy.bar(F_QE + 0), 0, 1, 0);
             }
-            // One barrier per sub-tile: PF(u) also certifies that the Q/dO stage of
-            // u+NB is loaded and, when this thread issues the dQ products and u
-            // closes a 128-query group, that the drain has emptied the dQ
-            // accumulator (the softmax warpgroup waited for both).
-            for (int u = 0; u < nsub && ok; ++u) {
-                ok = wait_bounded(sy, sy.bar(B_PF + u % kPfRing), (u / kPfRing) & 1, 1, u);
+            // PF(u) also certifies that the Q/dO stage of u+NB is loaded (the
+            // softmax warpgroup waited for it)
+            for (int u = par; u < nsub && ok; u += USTEP) {
+                ok = wait_bounded(sy, sy.bar(F_PF + u % kPfRingF), (u / kPfRingF) & 1, 1, u);
                 if (!ok) break;
                 tc_fence_after();
-                // P(u) lives in S/dP buffer u % NB: dV(u) reads it before S/dP(u+NB)
-                // reuses the buffer (the pipe keeps issue order); the other buffers
-                // keep the softmax fed
                 issue_dv_dk(u);
-                if (!C::SPLIT_MMA && ((u & 1) == 1 || u == nsub - 1)) issue_dq(u >> 1);
                 if (u + C::NB < nsub) issue_s_dp(u + C::NB);
             }
-            // all MMAs done (also on abort, before TMEM is freed)
-            mma_commit(sy.bar(B_ACC));
-            if (!ok) wait_drain(sy.bar(B_ACC), 0);
+            // all of this thread's MMAs done (also on abort, before TMEM is freed)
+            const uint32_t acc_bar = sy.bar(par == 0 ? F_ACC : F_ACCB);
+            mma_commit(acc_bar);
+            if (!ok) wait_drain(acc_bar, 0);
         }
         __syncwarp();
     } else if (warp < 10) {
@@ -367,31 +377,36 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         const int tq = lane & 3, tr = lane >> 2;
         const bool full = k0 + C::BM <= N;       // uniform: no padded keys in this tile
         const uint64_t cs2 = f2_pack(scale_log2, scale_log2);
-        bool ok = true;
-        for (int u = grp; u < nsub; u += 2) {
-            const int s = u % C::NST;
-            const int buf = u % C::NB;
-            ok = warp_wait(sy, sy.bar(B_QF + s), (u / C::NST) & 1, 2, u);
-            // this thread's 8 query pairs: {-LSE log2(e) x2, D x2} (the stage's
-            // statistics are written before its QF arrive)
-            float4 stat[8];
-            if (ok) {
-                const float4* St = reinterpret_cast<const float4*>(smem + C::OFF_ST) + s * 32 + tq;
+        // this thread's 8 query pairs of a stage: {-LSE log2(e) x2, D x2} (the
+        // producer writes a stage's statistics before its QF arrive, and the stage
+        // is not refilled before this warpgroup's PF arrive for that sub-tile)
+        float4 stat[8];
+        auto load_stats = [&](int u) {
+            const float4* St = reinterpret_cast<const float4*>(smem + C::OFF_ST) + (u % C::NST) * 32 + tq;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) stat[k] = St[4 * k];
-            }
-            ok = ok && warp_wait(sy, sy.bar(B_SF + buf), (u / C::NB) & 1, 2, u);
-            // dS block u & 3 last held sub-tile u-4, whose 128-query group h's dQ
-            // product (the dQ issuer's) must have read it before this sub-tile
-            // writes it.  The parity test on DQF + (h & 1) is exact: group h-2 was
-            // waited for at sub-tile u-4 by this warpgroup, and group h+2 needs
-            // PF(u).  (Waiting here rather than just before the stores leaves the
-            // compiler free to interleave the halves; the product is almost
-            // always complete by now.)
-            if (ok && C::SPLIT_MMA && u >= 4) {
+            for (int k = 0; k < 8; ++k) stat[k] = St[4 * k];
+        };
+        bool ok = true;
+        if (grp < nsub) {
+            ok = warp_wait(sy, sy.bar(F_QF + grp % C::NST), (grp / C::NST) & 1, 2, grp);
+            if (ok) load_stats(grp);
+        }
+        for (int u = grp; u < nsub && ok; u += 2) {
+            const int buf = u % C::NB;
+            // One round trip for S/dP(u) and, with the split issuer, the dQ product
+            // that last read dS block u & 3: it held sub-tile u-4, of 128-query
+            // group h, whose product must have read it before this sub-tile writes
+            // it.  The parity test on DQF + (h & 1) is exact: group h-2 was waited
+            // for at sub-tile u-4 by this warpgroup, and group h+2 needs PF(u).
+            // (The product is almost always complete by now.)
+            const uint32_t bsf = sy.bar(F_SF + u % (2 * C::NB)), psf = (u / (2 * C::NB)) & 1;
+            uint32_t bdq = bsf, pdq = psf;
+            if (u >= 4) {
                 const int h = (u - 4) >> 1;
-                ok = warp_wait(sy, sy.bar(B_DQF + (h & 1)), (h >> 1) & 1, 2, u);
+                bdq = sy.bar(F_DQF + (h & 1));
+                pdq = (h >> 1) & 1;
             }
+            ok = warp_wait_all(sy, bsf, psf, bdq, pdq, bsf, psf, bsf, psf, 2, u);
             if (!ok) break;
             tc_fence_after();
             const uint32_t ds_blk = sb + C::OFF_DS + 16384 * (u & 3);
@@ -448,20 +463,22 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             tmem_wait_st();
             tc_fence_before();
             fence_proxy_async_smem();
-            // stand-in waits for the MMA issuer (see its loop): the stage of u+NB is
-            // loaded and, when it issues this group's dQ product, the dQ accumulator
-            // is free (then the dQ MMA that last read dS block u & 3 was issued
-            // before S/dP(u), and the pipe keeps issue order)
-            if (ok && u + C::NB < nsub)
-                ok = warp_wait(sy, sy.bar(B_QF + (u + C::NB) % C::NST), ((u + C::NB) / C::NST) & 1, 2, u);
-            // (the drain of group gp = u/2 - 1: group gp-2's drain was complete
-            // before S/dP(u) was issued, as the softmax of the sub-tile closing
-            // group gp-1 waited for it, and group gp+2's drain needs PF(u))
-            if (!C::SPLIT_MMA && ok && ((u & 1) == 1 || u == nsub - 1) && u >= 2) {
-                const int gp = (u >> 1) - 1;
-                ok = warp_wait(sy, sy.bar(B_DQE + (gp & 1)), (gp >> 1) & 1, 2, u);
+            // One round trip for: (a) a stand-in wait for the MMA issuer of u (see
+            // its loop): the stage of u+NB is loaded; (b) the stage of u+2, this
+            // warpgroup's next sub-tile, whose statistics it loads now.
+            {
+                const bool v0 = u + C::NB < nsub, v1 = C::NB != 2 && u + 2 < nsub;
+                uint32_t b0 = sy.bar(F_QF + (u + C::NB) % C::NST), p0 = ((u + C::NB) / C::NST) & 1;
+                uint32_t b1 = sy.bar(F_QF + (u + 2) % C::NST), p1 = ((u + 2) / C::NST) & 1;
+                if (v0 || v1) {
+                    // a phase that is not needed is replaced by one that is
+                    if (!v0) { b0 = b1; p0 = p1; }
+                    if (!v1) { b1 = b0; p1 = p0; }
+                    ok = warp_wait_all(sy, b0, p0, b1, p1, b0, p0, b0, p0, 2, u);
+                }
             }
-            mbar_arrive(sy.bar(B_PF + u % kPfRing));
+            if (ok && u + 2 < nsub) load_stats(u + 2);
+            mbar_arrive(sy.bar(F_PF + u % kPfRingF));
             if (!ok) break;
         }
         const int jl = q4 * 32 + lane;           // epilogue: one key row per thread
@@ -469,7 +486,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
         // epilogue (warpgroup 0): dK, dV_lo, dV_hi rows of this thread's key
         if (grp == 0) {
-            if (ok) ok = warp_wait(sy, sy.bar(B_ACC), 0, 2, nsub);
+            if (ok) ok = warp_wait(sy, sy.bar(F_ACC), 0, 2, nsub) &&
+                         (!C::TWO_ISSUERS || warp_wait(sy, sy.bar(F_ACCB), 0, 2, nsub));
             if (ok) {
                 tc_fence_after();
                 uint32_t v[D];
@@ -509,13 +527,13 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         const int il = q4 * 32 + lane;           // query row within the 128-query group
         const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
         for (int g = 0; g < ngrp; ++g) {
-            if (!warp_wait(sy, sy.bar(B_DQF + (g & 1)), (g >> 1) & 1, 3, g)) break;
+            if (!warp_wait(sy, sy.bar(F_DQF + (g & 1)), (g >> 1) & 1, 3, g)) break;
             tc_fence_after();
             uint32_t v[D];
             tmem_ld_row<D>(trow + C::C_DQ, v);
             tmem_wait_ld();
             tc_fence_before();
-            mbar_arrive(sy.bar(B_DQE + (g & 1)));
+            mbar_arrive(sy.bar(F_DQE + (g & 1)));
             const int i = (ubase / 2 + g) * 128 + il;
             if (i < N) {
                 float4* dst = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * N + i) * D);
@@ -525,7 +543,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                                                        __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])));
             }
         }
-    } else if (C::SPLIT_MMA) {
+    } else if (warp == 14) {
         // ------------------------------------------------------------ dQ issuer
         // dQ of the 128-query group g = sub-tiles 2g, 2g+1: A = dS (queries x keys)
         // read MN-major from the pair's two dS^T blocks (16 KB apart), B = K_j rows
@@ -539,25 +557,25 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             constexpr uint32_t BLK_U = 16384 >> 4;
             const uint64_t dK = smem_desc(sb + C::OFF_K, 16, 8 * C::ROWB, C::SW);
             const uint64_t dDS0mn = smem_desc(sb + C::OFF_DS, 16384, 1024, 2);
-            bool ok = wait_bounded(sy, sy.bar(B_KV), 0, 5, -1);
+            bool ok = wait_bounded(sy, sy.bar(F_KV), 0, 5, -1);
             for (int g = 0; g < ngrp && ok; ++g) {
                 const int u0 = 2 * g, u1 = 2 * g + 1;
-                ok = wait_bounded(sy, sy.bar(B_PF + u0 % kPfRing), (u0 / kPfRing) & 1, 5, u0);
-                if (ok && u1 < nsub) ok = wait_bounded(sy, sy.bar(B_PF + u1 % kPfRing), (u1 / kPfRing) & 1, 5, u1);
+                ok = wait_bounded(sy, sy.bar(F_PF + u0 % kPfRingF), (u0 / kPfRingF) & 1, 5, u0);
+                if (ok && u1 < nsub) ok = wait_bounded(sy, sy.bar(F_PF + u1 % kPfRingF), (u1 / kPfRingF) & 1, 5, u1);
                 // the drain of group g-1 (this thread waited for g-2's before
                 // issuing dQ(g-1); group g+1's drain needs dQ(g+1))
-                if (ok && g > 0) ok = wait_bounded(sy, sy.bar(B_DQE + ((g - 1) & 1)), ((g - 1) >> 1) & 1, 5, g);
+                if (ok && g > 0) ok = wait_bounded(sy, sy.bar(F_DQE + ((g - 1) & 1)), ((g - 1) >> 1) & 1, 5, g);
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t dA = dDS0mn + BLK_U * (u0 & 3);
 #pragma unroll
                 for (int kk = 0; kk < C::BM / 16; ++kk)
                     mma_bf16_ss(tmem + C::C_DQ, dA + 128 * kk, dK + KSTEP * kk, ID_DQ, kk);
-                mma_commit(sy.bar(B_DQF + (g & 1)));
+                mma_commit(sy.bar(F_DQF + (g & 1)));
             }
             // this thread's MMAs are done before TMEM is freed (also on abort)
-            mma_commit(sy.bar(B_DQA));
-            wait_drain(sy.bar(B_DQA), 0);
+            mma_commit(sy.bar(F_DQA));
+            wait_drain(sy.bar(F_DQA), 0);
         }
         __syncwarp();
     }
@@ -876,6 +894,58 @@ pre_kernel(const bf16* __restrict__ o_lo, const bf16* __restrict__ o_hi, const b
     if (row < rows && part == 0) Drow[row] = acc;
 }
 
+// ---------------------------------------------------------------- statistics for the fused kernel
+// Per (batch*head) slice, its queries padded to whole 64-query sub-tiles
+// (npad = 64 * ceil(N / 64)): for each query pair c one float4
+//   {-LSE_2c log2(e), -LSE_2c+1 log2(e), D_2c, D_2c+1},  D_i = <dO_lo, O_lo> + <dO_hi, O_hi>
+// with -inf and 0 for padded queries (so P = 0 there), the layout the fused
+// kernel copies into shared memory per sub-tile; also zeroes the dQ accumulator.
+template <int D>
+__global__ void __launch_bounds__(256)
+pre_stats_kernel(const bf16* __restrict__ o_lo, const bf16* __restrict__ o_hi, const bf16* __restrict__ do_lo,
+                 const bf16* __restrict__ do_hi, const float* __restrict__ lse, float4* __restrict__ stats,
+                 float* __restrict__ dq_acc, long long rows_pad, int N, int npad) {
+    constexpr int TPR = D / 8;                // threads per row, 8 bf16 (16 B) each
+    constexpr int RPB = 256 / TPR;
+    const long long row = (long long)blockIdx.x * RPB + threadIdx.x / TPR;
+    const int part = threadIdx.x % TPR;
+    const long long bh = row / npad;
+    const int i = (int)(row % npad);
+    const bool valid = row < rows_pad && i < N;
+    float acc = 0.f;
+    if (valid) {
+        const size_t off = ((size_t)bh * N + i) * D + part * 8;
+        const uint4 a = *reinterpret_cast<const uint4*>(o_lo + off);
+        const uint4 b = *reinterpret_cast<const uint4*>(do_lo + off);
+        const uint4 c = *reinterpret_cast<const uint4*>(o_hi + off);
+        const uint4 d = *reinterpret_cast<const uint4*>(do_hi + off);
+        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+        const __nv_bfloat162* pc = reinterpret_cast<const __nv_bfloat162*>(&c);
+        const __nv_bfloat162* pd = reinterpret_cast<const __nv_bfloat162*>(&d);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 fa = __bfloat1622float2(pa[k]), fb = __bfloat1622float2(pb[k]);
+            const float2 fc = __bfloat1622float2(pc[k]), fd = __bfloat1622float2(pd[k]);
+            acc = fmaf(fa.x, fb.x, acc);
+            acc = fmaf(fa.y, fb.y, acc);
+            acc = fmaf(fc.x, fd.x, acc);
+            acc = fmaf(fc.y, fd.y, acc);
+        }
+        float4* z = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * N + i) * D);
+#pragma unroll
+        for (int k = part; k < D / 4; k += TPR) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int o = TPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, TPR);
+    const float nl = valid ? -lse[(size_t)bh * N + i] * kLog2e : -INFINITY;
+    // the odd row of the pair is the next TPR lanes of the same warp (npad and
+    // the rows of a block are even)
+    const float nl1 = __shfl_down_sync(0xffffffffu, nl, TPR);
+    const float d1 = __shfl_down_sync(0xffffffffu, acc, TPR);
+    if (row < rows_pad && part == 0 && (i & 1) == 0) stats[row >> 1] = make_float4(nl, nl1, acc, d1);
+}
+
 // ---------------------------------------------------------------- dQ = scale * acc -> bf16
 template <int D>
 __global__ void __launch_bounds__(256)
@@ -969,10 +1039,12 @@ int launch(const BwdArgs& a, std::string* err) {
         return PSA_ERR_CUDA;
     if (!set_max_dynamic_smem((const void*)bwd_main_kernel<D>, M::SMEM, err)) return PSA_ERR_CUDA;
     const long long rows = a.BH * a.N;
-    float* Drow = static_cast<float*>(a.workspace);
-    float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + align256((size_t)rows * 4));
-    float* dkv_part = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + align256((size_t)rows * 4) +
-                                               align256((size_t)rows * D * 4));
+    const int npad = (a.N + M::BS - 1) / M::BS * M::BS;
+    const long long rows_pad = a.BH * npad;
+    float4* stats = static_cast<float4*>(a.workspace);
+    char* ws = static_cast<char*>(a.workspace) + align256((size_t)rows_pad * 8);
+    float* dq_acc = reinterpret_cast<float*>(ws);
+    float* dkv_part = reinterpret_cast<float*>(ws + align256((size_t)rows * D * 4));
     const int nkt = (a.N + M::BM - 1) / M::BM;
     const long long units = a.BH * nkt;
     // split the last wave's units along the query axis so that it fills the SMs
@@ -982,7 +1054,7 @@ int launch(const BwdArgs& a, std::string* err) {
     const TailSplit ts = tail_split(units, a.N, sms);
     const long long nfull = units - ts.ntail;
     const long long grid = nfull + (long long)ts.ntail * ts.f;
-    const long long pre_grid = (rows + 256 / (D / 8) - 1) / (256 / (D / 8));
+    const long long pre_grid = (rows_pad + 256 / (D / 8) - 1) / (256 / (D / 8));
     const long long fin_grid = (rows * (D / 8) + (long long)ts.ntail * 128 * 3 * (D / 8) + 255) / 256;
     if (grid > 0x7fffffffll || pre_grid > 0x7fffffffll || fin_grid > 0x7fffffffll) {
         *err = "grid too large";
@@ -995,12 +1067,13 @@ int launch(const BwdArgs& a, std::string* err) {
     bf16* dp = static_cast<bf16*>(a.d_packed);
     {
         ProfScope prof(kSlotPre, a.stream);
-        pre_kernel<D><<<(unsigned)pre_grid, 256, 0, a.stream>>>(o_lo, o_hi, do_lo, do_hi, Drow, dq_acc, rows);
+        pre_stats_kernel<D><<<(unsigned)pre_grid, 256, 0, a.stream>>>(o_lo, o_hi, do_lo, do_hi, a.lse, stats, dq_acc,
+                                                                      rows_pad, a.N, npad);
     }
     {
         ProfScope prof(kSlotMain, a.stream);
         bwd_main_kernel<D><<<(unsigned)grid, M::THREADS, M::SMEM, a.stream>>>(
-            tm_kv, tm_q, tm_lo, tm_hi, a.lse, Drow, dq_acc, dp, a.N, nkt, a.scale, a.scale * kLog2e, (int)nfull, ts.f,
+            tm_kv, tm_q, tm_lo, tm_hi, stats, dq_acc, dp, a.N, nkt, a.scale, a.scale * kLog2e, (int)nfull, ts.f,
             dkv_part);
     }
     {
@@ -1071,8 +1144,11 @@ double tc_bwd_waves(long long units, int N, int sms) {
 }
 
 size_t tc_workspace_bytes(long long BH, int N, int d) {
+    // statistics (8 bytes per query, padded to whole 64-query sub-tiles), the
+    // fp32 dQ accumulator, the dK/dV partials of split units
     const size_t rows = (size_t)BH * (size_t)N;
-    return align256(rows * 4) + align256(rows * (size_t)d * 4) + tail_part_bytes(BH, N, d);
+    const size_t rows_pad = (size_t)BH * (size_t)((N + 63) / 64 * 64);
+    return align256(rows_pad * 8) + align256(rows * (size_t)d * 4) + tail_part_bytes(BH, N, d);
 }
 
 size_t tc_two_pass_workspace_bytes(long long BH, int N) { return align256((size_t)BH * (size_t)N * 4); }

@@ -76,10 +76,40 @@ __device__ __forceinline__ bool wait_bounded_cluster(const Sync& s, uint32_t bar
     return wait_slow_cluster(s, bar, parity, role, tile);
 }
 
+// Four barrier phases tested in one round trip: the try_waits issue back to
+// back and only their combined result is waited for.  (Pass a phase twice to
+// test fewer.)  The fast path of warp_wait_all.
+__device__ __forceinline__ bool mbar_try_wait4(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1, uint32_t b2,
+                                               uint32_t p2, uint32_t b3, uint32_t p3) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred q0, q1, q2, q3;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q3, [%7], %8;\n\t"
+        "and.pred q0, q0, q1;\n\tand.pred q2, q2, q3;\n\tand.pred q0, q0, q2;\n\t"
+        "selp.u32 %0, 1, 0, q0;\n\t}"
+        : "=r"(ok)
+        : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2), "r"(b3), "r"(p3)
+        : "memory");
+    return ok != 0;
+}
+
 // Whole-warp wait: every lane waits, the warp agrees on the outcome.
 __device__ __forceinline__ bool warp_wait(const Sync& s, uint32_t bar, uint32_t parity, int role, int tile) {
     const bool ok = wait_bounded(s, bar, parity, role, tile);
     return __all_sync(0xffffffffu, ok);
+}
+
+// Whole-warp wait on four barrier phases (b_i, p_i): one round trip when all
+// are complete already, else each in turn with the bounded wait.
+__device__ __forceinline__ bool warp_wait_all(const Sync& s, uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1,
+                                              uint32_t b2, uint32_t p2, uint32_t b3, uint32_t p3, int role,
+                                              int tile) {
+    if (__all_sync(0xffffffffu, mbar_try_wait4(b0, p0, b1, p1, b2, p2, b3, p3))) return true;
+    return warp_wait(s, b0, p0, role, tile) && warp_wait(s, b1, p1, role, tile) && warp_wait(s, b2, p2, role, tile) &&
+           warp_wait(s, b3, p3, role, tile);
 }
 
 // Wait without the abort short-cut (used only to drain work after an abort).

@@ -112,8 +112,9 @@ def test_two_pass_workspace_and_forward_rejects_it(lib):
     assert B.psa_attn_bwd_workspace_bytes(2, 3, 100, 32, B.PSA_BF16, B.PSA_ALGO_TC_2PASS) == 2560
     assert B.psa_attn_bwd_workspace_bytes(1, 1, 100, 32, B.PSA_BF16, B.PSA_ALGO_TC_2PASS) == 512
     assert B.psa_attn_bwd_workspace_bytes(1, 1, 100, 32, B.PSA_F32, B.PSA_ALGO_TC_2PASS) == 0
-    # the fused mode also holds an fp32 dQ accumulator
-    assert B.psa_attn_bwd_workspace_bytes(1, 1, 100, 32, B.PSA_BF16, B.PSA_ALGO_TC) == 512 + 100 * 32 * 4
+    # the fused mode holds 8 bytes of statistics per query, padded to whole
+    # 64-query sub-tiles, and an fp32 dQ accumulator
+    assert B.psa_attn_bwd_workspace_bytes(1, 1, 100, 32, B.PSA_BF16, B.PSA_ALGO_TC) == 128 * 8 + 100 * 32 * 4
     rc = B.lib().psa_attn_fwd_algo(FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 16, 1.0, B.PSA_BF16, B.PSA_ALGO_TC_2PASS, None)
     assert rc == B.PSA_ERR_ARG
 

@@ -44,13 +44,18 @@ class Bar:
             self.done += 1
 
 
-def run(nsub, split, NB, NST, seed, dqe_pair=True, with_dq=True):
+def run(nsub, split, NB, NST, seed, dqe_pair=True, with_dq=True, two_issuers=False, pf_ring=4, slow_role=None,
+        sf_ring=None):
     """One random schedule of one CTA with nsub sub-tiles.  split: the dQ MMAs
-    have an issuing thread of their own (head_dim <= 32).  dqe_pair: the
-    drain's "accumulator read" barrier alternates between two barriers by
-    group parity, as the kernel does (False models a single barrier).
+    have an issuing thread of their own.  dqe_pair: the drain's "accumulator
+    read" barrier alternates between two barriers by group parity, as the
+    kernel does (False models a single barrier).  two_issuers: the fused
+    kernel's two main issuing threads, one per sub-tile parity (each issues
+    dV/dK(u) and then S/dP(u+NB) for its u, and the odd one first waits for
+    dV/dK(0) to be done); pf_ring: the number of PF barriers.  slow_role: the
+    index of a role the scheduler picks only rarely while others can run.
     with_dq=False models the two-pass mode's single-CTA dK/dV pass
-    (bwd_dkdv_kernel): the same roles without dQ, its drain and the dS ring."""
+    (bwd_dkdv_kernel): one issuer, no dQ, no drain, no dS ring."""
     rnd = random.Random(seed)
     ngrp = (nsub + 1) // 2
     bars = {}
@@ -60,9 +65,10 @@ def run(nsub, split, NB, NST, seed, dqe_pair=True, with_dq=True):
             bars[name] = Bar(name, count)
         return bars[name]
 
-    for b in range(NB):
+    nsf = sf_ring or NB                     # SF barriers: a ring over the sub-tiles
+    for b in range(nsf):
         bar(("SF", b))
-    for x in range(4):
+    for x in range(pf_ring):
         bar(("PF", x), 4)           # four warps of one warpgroup
     for s in range(NST):
         bar(("QF", s))
@@ -84,7 +90,8 @@ def run(nsub, split, NB, NST, seed, dqe_pair=True, with_dq=True):
     stage_soft = {s: 0 for s in range(NST)}                       # softmax warps done with the stage
     ds = {(blk, q): ("zero", None, True) for blk in range(4) for q in range(4)}  # (kind, u, read by dQ)
     acc = {q: ("idle", -1) for q in range(4)}                     # dQ accumulator per quarter
-    fifo = {"main": [], "dq": []}
+    fifo = {"main": [], "main1": [], "dq": []}
+    dvdk_done = set()
 
     def mma_sdp(u):
         b, s = u % NB, u % NST
@@ -97,6 +104,9 @@ def run(nsub, split, NB, NST, seed, dqe_pair=True, with_dq=True):
 
     def mma_dvdk(u):
         b, s = u % NB, u % NST
+        # the first dV/dK product overwrites the accumulators; every later one adds
+        assert u == 0 or 0 in dvdk_done, f"dV/dK({u}) adds to accumulators dV/dK(0) has not yet zeroed"
+        dvdk_done.add(u)
         for q in range(4):
             assert tq[(b, q)] == ("P", u), f"dV/dK({u}) reads {tq[(b, q)]}"
         assert stage[s] == u and "sdp" in stage_readers[s]
@@ -132,32 +142,37 @@ def run(nsub, split, NB, NST, seed, dqe_pair=True, with_dq=True):
             stage_soft[s] = 0
             yield ("arrive", bar(("QF", s)), u // NST)
 
-    def main_issuer():
-        for u in range(min(NB, nsub)):
-            yield ("wait", bar(("QF", u)), 0)
-        for u in range(min(NB, nsub)):
-            issue("main", ("mma", mma_sdp, u))
-            issue("main", ("commit", bar(("SF", u % NB)), u // NB))
-        for u in range(nsub):
-            yield ("wait", bar(("PF", u % 4)), u // 4)
-            issue("main", ("mma", mma_dvdk, u))
-            issue("main", ("commit", bar(("QE", u % NST)), u // NST))
+    def main_issuer(par=0, step=1):
+        me = "main" if par == 0 else "main1"
+        if par == 0:
+            for u in range(min(NB, nsub)):
+                yield ("wait", bar(("QF", u)), 0)
+            for u in range(min(NB, nsub)):
+                issue(me, ("mma", mma_sdp, u))
+                issue(me, ("commit", bar(("SF", u % nsf)), u // nsf))
+        elif nsub > 1:
+            yield ("wait", bar(("QE", 0)), 0)
+        for u in range(par, nsub, step):
+            yield ("wait", bar(("PF", u % pf_ring)), u // pf_ring)
+            issue(me, ("mma", mma_dvdk, u))
+            issue(me, ("commit", bar(("QE", u % NST)), u // NST))
             if with_dq and not split and (u % 2 == 1 or u == nsub - 1):
                 g = u // 2
-                issue("main", ("mma", mma_dq, g))
-                issue("main", ("commit", bar(("DQF", g & 1)), g >> 1))
+                issue(me, ("mma", mma_dq, g))
+                issue(me, ("commit", bar(("DQF", g & 1)), g >> 1))
             if u + NB < nsub:
                 v = u + NB
-                issue("main", ("mma", mma_sdp, v))
-                issue("main", ("commit", bar(("SF", v % NB)), v // NB))
+                issue(me, ("mma", mma_sdp, v))
+                issue(me, ("commit", bar(("SF", v % nsf)), v // nsf))
 
     def softmax(grp, q):
+        if grp < nsub:
+            yield ("wait", bar(("QF", grp % NST)), grp // NST)
+            assert stage[grp % NST] == grp, f"softmax reads the statistics of stage {grp % NST} too early"
         for u in range(grp, nsub, 2):
             b, s = u % NB, u % NST
-            yield ("wait", bar(("QF", s)), u // NST)
-            # the row statistics of the stage are read here, before the S/dP wait
-            assert stage[s] == u, f"softmax({u}) reads the statistics of stage {s} holding {stage[s]}"
-            yield ("wait", bar(("SF", b)), u // NB)
+            # the statistics of u were read at the end of u-2 (or before the loop)
+            yield ("wait", bar(("SF", u % nsf)), u // nsf)
             if with_dq and split and u >= 4:
                 h = (u - 4) >> 1
                 yield ("wait", bar(("DQF", h & 1)), h >> 1)
@@ -173,15 +188,20 @@ def run(nsub, split, NB, NST, seed, dqe_pair=True, with_dq=True):
             if u + NB < nsub:
                 v = u + NB
                 yield ("wait", bar(("QF", v % NST)), v // NST)
+            if u + 2 < nsub:
+                yield ("wait", bar(("QF", (u + 2) % NST)), (u + 2) // NST)
             if with_dq and not split and (u % 2 == 1 or u == nsub - 1) and u >= 2:
                 yield ("wait",) + dqe((u >> 1) - 1)
-            yield ("arrive", bar(("PF", u % 4)), u // 4)
+            if u + 2 < nsub:
+                # the next sub-tile's statistics are read before PF(u)
+                assert stage[(u + 2) % NST] == u + 2, f"softmax({u}) reads stage {(u + 2) % NST} too early"
+            yield ("arrive", bar(("PF", u % pf_ring)), u // pf_ring)
 
     def dq_issuer():
         for g in range(ngrp):
             for u in (2 * g, 2 * g + 1):
                 if u < nsub:
-                    yield ("wait", bar(("PF", u % 4)), u // 4)
+                    yield ("wait", bar(("PF", u % pf_ring)), u // pf_ring)
             if g > 0:
                 yield ("wait",) + dqe(g - 1)
             issue("dq", ("mma", mma_dq, g))
@@ -194,7 +214,8 @@ def run(nsub, split, NB, NST, seed, dqe_pair=True, with_dq=True):
             acc[q] = ("read", g)
             yield ("arrive",) + dqe(g)
 
-    roles = [producer(), main_issuer()]
+    roles = [producer()]
+    roles += [main_issuer(0, 2), main_issuer(1, 2)] if two_issuers else [main_issuer()]
     roles += [softmax(g, q) for g in range(2) for q in range(4)]
     if with_dq:
         roles += [drain(q) for q in range(4)]
@@ -228,14 +249,16 @@ def run(nsub, split, NB, NST, seed, dqe_pair=True, with_dq=True):
                     enabled.append(("role", i))
             else:
                 enabled.append(("role", i))
-        for who in ("main", "dq"):
+        for who in ("main", "main1", "dq"):
             if fifo[who]:
                 enabled.append(("pipe", who))
         if not enabled:
             blocked = {i: (r[1].name, r[2], r[1].done) for i, r in pending.items() if r != "done"}
             assert not blocked, f"deadlock: {blocked}"
-            assert not fifo["main"] and not fifo["dq"]
+            assert not any(fifo.values())
             return
+        if slow_role is not None and len(enabled) > 1 and rnd.random() > 0.02:
+            enabled = [e for e in enabled if e != ("role", slow_role)] or enabled
         kind, x = rnd.choice(enabled)
         if kind == "pipe":
             item = fifo[x].pop(0)
@@ -750,14 +773,35 @@ def test_single_cta_dq_protocol_random_schedules(nsub):
         run_dq_single(nsub, seed * 17 + nsub)
 
 
+FUSED = [(3, 6, True), (2, 4, False)]   # (S/dP buffers, Q/dO stages, two main issuers): head_dim <= 32, 64
+
+
 @pytest.mark.parametrize("nsub", list(range(1, 14)) + [20, 33])
-@pytest.mark.parametrize("split,NB,NST", [(True, 3, 6), (False, 2, 4)])
-def test_fused_protocol_random_schedules(nsub, split, NB, NST):
-    """head_dim <= 32 (dQ issuer of its own, 3 S/dP buffers, 6 Q/dO stages) and
-    head_dim 64 (dQ on the MMA issuer, 2 buffers, 4 stages), odd and even
+@pytest.mark.parametrize("NB,NST,two", FUSED)
+def test_fused_protocol_random_schedules(nsub, NB, NST, two):
+    """The fused kernel: a dQ issuer, PF and SF rings of 8 and 2 NB; head_dim <=
+    32 (two main issuers, one per sub-tile parity, 3 S/dP buffers, 6 Q/dO
+    stages) and head_dim 64 (one main issuer, 2 buffers, 4 stages), odd and even
     sub-tile counts, 40 random schedules each."""
     for seed in range(40):
-        run(nsub, split, NB, NST, seed * 1000 + nsub)
+        run(nsub, True, NB, NST, seed * 1000 + nsub, two_issuers=two, pf_ring=8, sf_ring=2 * NB)
+
+
+@pytest.mark.parametrize("slow", [1, 2])
+def test_fused_two_issuers_need_the_longer_ring(slow):
+    """With two main issuers a PF ring of 4 is not enough: the issuer of one
+    parity can fall behind until a later phase of its PF barrier completes
+    before it saw the earlier one.  The model finds such schedules when that
+    issuer (role 1 or 2) runs slowly; with the kernel's ring of 8 it finds none."""
+    failures = 0
+    for seed in range(200):
+        try:
+            run(20, True, 3, 6, seed, two_issuers=True, pf_ring=4, slow_role=slow, sf_ring=6)
+        except AssertionError:
+            failures += 1
+    assert failures > 0
+    for seed in range(200):
+        run(20, True, 3, 6, seed, two_issuers=True, pf_ring=8, slow_role=slow, sf_ring=6)
 
 
 def test_single_drain_barrier_aliases():
@@ -792,3 +836,14 @@ def test_model_catches_a_broken_protocol():
         except AssertionError:
             failures += 1
     assert failures > 0
+
+
+@pytest.mark.parametrize("NB,NST,two", FUSED)
+def test_fused_protocol_with_one_slow_role(NB, NST, two):
+    """The fused kernel's protocol with each role in turn running slowly (the
+    producer, either main issuer, a softmax warp, a drain warp, the dQ issuer):
+    skewed schedules reach interleavings that uniform ones rarely do."""
+    nroles = 1 + (2 if two else 1) + 8 + 4 + 1
+    for slow in range(nroles):
+        for seed in range(12):
+            run(17, True, NB, NST, seed * 31 + slow, two_issuers=two, pf_ring=8, slow_role=slow, sf_ring=2 * NB)
