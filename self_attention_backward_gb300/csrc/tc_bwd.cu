@@ -101,7 +101,14 @@ struct Cfg {
     static constexpr int OFF_ST = OFF_DS + 4 * 16384;
     static constexpr int OFF_BAR = OFF_ST + NST * 512;     // mbarriers (48)
     static constexpr int OFF_MISC = OFF_BAR + 384;
-    static constexpr int USED = OFF_MISC + 64;
+    // d <= 32: the dQ drain stages each 128-query partial here (two buffers of
+    // [128][D] fp32, 128B / 64B-swizzled rows) and adds it to the fp32
+    // accumulator with one TMA bulk reduce; at d = 64 (no room) it adds with
+    // vector atomics
+    static constexpr bool DQ_BULK = D <= 32;
+    static constexpr int DQS_BYTES = 128 * D * 4;
+    static constexpr int OFF_DQS = (OFF_MISC + 64 + 1023) / 1024 * 1024;
+    static constexpr int USED = DQ_BULK ? OFF_DQS + 2 * DQS_BYTES : OFF_MISC + 64;
     // + 1 KB to align the base to 1024; at least 116 KB so that one CTA owns
     // an SM (its TMEM allocation is all 512 columns)
     static constexpr int SMEM = (USED + 1024) > 118784 ? (USED + 1024) : 118784;
@@ -179,7 +186,7 @@ template <int D>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_do_lo, const __grid_constant__ CUtensorMap tm_do_hi,
-                const float4* __restrict__ stats, float* __restrict__ dq_acc, bf16* __restrict__ d_packed, int N,
+                const __grid_constant__ CUtensorMap tm_dq, const float4* __restrict__ stats, float* __restrict__ dq_acc, bf16* __restrict__ d_packed, int N,
                 int nkt, float scale, float scale_log2, int nfull, int tail_f, float* __restrict__ dkv_part) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -526,23 +533,51 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         const int q4 = warp & 3;
         const int il = q4 * 32 + lane;           // query row within the 128-query group
         const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+        const bool elected = warp == 10 && lane == 0;
         for (int g = 0; g < ngrp; ++g) {
-            if (!warp_wait(sy, sy.bar(F_DQF + (g & 1)), (g >> 1) & 1, 3, g)) break;
+            bool okw = warp_wait(sy, sy.bar(F_DQF + (g & 1)), (g >> 1) & 1, 3, g);
+            // the four drain warps decide together (they meet at named barriers below)
+            if (C::DQ_BULK) okw = named_bar_and(2, 128, okw);
+            if (!okw) break;
             tc_fence_after();
             uint32_t v[D];
             tmem_ld_row<D>(trow + C::C_DQ, v);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(sy.bar(F_DQE + (g & 1)));
-            const int i = (ubase / 2 + g) * 128 + il;
-            if (i < N) {
-                float4* dst = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * N + i) * D);
+            if constexpr (C::DQ_BULK) {
+                // staging buffer g & 1: its previous reduce (group g-2) must have read it
+                const uint32_t buf = sb + C::OFF_DQS + (g & 1) * C::DQS_BYTES;
+                if (elected) bulk_wait_group_read<1>();
+                named_bar_sync(1, 128);
+                // row il, swizzled as the tensor map expects (16-byte chunk c of a
+                // row at c xor (row bits above the 128-byte line))
+                constexpr uint32_t M = D == 32 ? 7u : D == 16 ? 3u : 1u;
 #pragma unroll
-                for (int e = 0; e < D; e += 4)
-                    atomicAdd(dst + e / 4, make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                                                       __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])));
+                for (int c = 0; c < D / 4; ++c) {
+                    const uint32_t a = (uint32_t)il * (D * 4) + 16u * c;
+                    st_shared_v4(buf + (a ^ (((a >> 7) & M) << 4)), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(1, 128);
+                // rows past N lie outside the tensor and are skipped
+                if (elected) {
+                    tma_reduce_add_3d(&tm_dq, buf, 0, (ubase / 2 + g) * 128, bh);
+                    bulk_commit_group();
+                }
+            } else {
+                const int i = (ubase / 2 + g) * 128 + il;
+                if (i < N) {
+                    float4* dst = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * N + i) * D);
+#pragma unroll
+                    for (int e = 0; e < D; e += 4)
+                        atomicAdd(dst + e / 4, make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                                                           __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])));
+                }
             }
         }
+        // every reduce has written global memory and read its staging buffer
+        if (C::DQ_BULK && elected) bulk_wait_group<0>();
     } else if (warp == 14) {
         // ------------------------------------------------------------ dQ issuer
         // dQ of the 128-query group g = sub-tiles 2g, 2g+1: A = dS (queries x keys)
@@ -1031,19 +1066,21 @@ int launch(const BwdArgs& a, std::string* err) {
     using M = Cfg<D>;
     // K/V tiles: 128 rows; Q/dO sub-tiles: 64 rows (the byte counts the
     // kernel's barriers expect)
-    CUtensorMap tm_kv, tm_q, tm_lo, tm_hi;
-    if (!encode_bf16_rows(&tm_kv, a.packed, D, a.N, a.BH * 4, M::BM, D, err) ||
-        !encode_bf16_rows(&tm_q, a.packed, D, a.N, a.BH * 4, M::BS, D, err) ||
-        !encode_bf16_rows(&tm_lo, a.do_lo, D, a.N, a.BH, M::BS, D, err) ||
-        !encode_bf16_rows(&tm_hi, a.do_hi, D, a.N, a.BH, M::BS, D, err))
-        return PSA_ERR_CUDA;
-    if (!set_max_dynamic_smem((const void*)bwd_main_kernel<D>, M::SMEM, err)) return PSA_ERR_CUDA;
     const long long rows = a.BH * a.N;
     const int npad = (a.N + M::BS - 1) / M::BS * M::BS;
     const long long rows_pad = a.BH * npad;
     float4* stats = static_cast<float4*>(a.workspace);
     char* ws = static_cast<char*>(a.workspace) + align256((size_t)rows_pad * 8);
     float* dq_acc = reinterpret_cast<float*>(ws);
+    // dq_acc in 128-query boxes of min(D, 32) columns (the reduce path uses it at D <= 32)
+    CUtensorMap tm_kv, tm_q, tm_lo, tm_hi, tm_dq;
+    if (!encode_bf16_rows(&tm_kv, a.packed, D, a.N, a.BH * 4, M::BM, D, err) ||
+        !encode_bf16_rows(&tm_q, a.packed, D, a.N, a.BH * 4, M::BS, D, err) ||
+        !encode_bf16_rows(&tm_lo, a.do_lo, D, a.N, a.BH, M::BS, D, err) ||
+        !encode_bf16_rows(&tm_hi, a.do_hi, D, a.N, a.BH, M::BS, D, err) ||
+        !encode_f32_rows(&tm_dq, dq_acc, D, a.N, a.BH, 128, D < 32 ? D : 32, err))
+        return PSA_ERR_CUDA;
+    if (!set_max_dynamic_smem((const void*)bwd_main_kernel<D>, M::SMEM, err)) return PSA_ERR_CUDA;
     float* dkv_part = reinterpret_cast<float*>(ws + align256((size_t)rows * D * 4));
     const int nkt = (a.N + M::BM - 1) / M::BM;
     const long long units = a.BH * nkt;
@@ -1073,8 +1110,8 @@ int launch(const BwdArgs& a, std::string* err) {
     {
         ProfScope prof(kSlotMain, a.stream);
         bwd_main_kernel<D><<<(unsigned)grid, M::THREADS, M::SMEM, a.stream>>>(
-            tm_kv, tm_q, tm_lo, tm_hi, stats, dq_acc, dp, a.N, nkt, a.scale, a.scale * kLog2e, (int)nfull, ts.f,
-            dkv_part);
+            tm_kv, tm_q, tm_lo, tm_hi, tm_dq, stats, dq_acc, dp, a.N, nkt, a.scale, a.scale * kLog2e, (int)nfull,
+            ts.f, dkv_part);
     }
     {
         ProfScope prof(kSlotDq, a.stream);

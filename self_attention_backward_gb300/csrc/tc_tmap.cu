@@ -29,19 +29,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder(std::string* err) {
 
 }  // namespace
 
-bool encode_bf16_rows(CUtensorMap* map, const void* base, int D, int N, long long Z, int rows, int cols,
-                      std::string* err) {
+static bool encode_rows(CUtensorMap* map, CUtensorMapDataType type, int esize, const void* base, int D, int N, long long Z,
+                 int rows, int cols, std::string* err) {
     auto enc = encoder(err);
     if (!enc) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)Z};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * esize, (cuuint64_t)N * D * esize};
     const cuuint32_t box[3] = {(cuuint32_t)cols, (cuuint32_t)rows, 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
-    const int rowb = cols * 2;
+    const int rowb = cols * esize;
     const CUtensorMapSwizzle sw = rowb == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : rowb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                : CU_TENSOR_MAP_SWIZZLE_32B;
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+    const CUresult r = enc(map, type, 3, const_cast<void*>(base), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -49,6 +49,16 @@ bool encode_bf16_rows(CUtensorMap* map, const void* base, int D, int N, long lon
         return false;
     }
     return true;
+}
+
+bool encode_bf16_rows(CUtensorMap* map, const void* base, int D, int N, long long Z, int rows, int cols,
+                      std::string* err) {
+    return encode_rows(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, D, N, Z, rows, cols, err);
+}
+
+bool encode_f32_rows(CUtensorMap* map, const void* base, int D, int N, long long Z, int rows, int cols,
+                     std::string* err) {
+    return encode_rows(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, D, N, Z, rows, cols, err);
 }
 
 bool set_max_dynamic_smem(const void* kernel, int bytes, std::string* err) {

@@ -16,6 +16,12 @@ namespace psa {
 bool encode_bf16_rows(CUtensorMap* map, const void* base, int D, int N, long long Z, int rows, int cols,
                       std::string* err);
 
+// The same over an fp32 tensor of Z slices of [N, D] rows, boxes of `rows` x
+// `cols` (cols * 4 bytes a multiple of 16, at most 128; the swizzle span is the
+// box's row bytes: 128, 64 or 32).
+bool encode_f32_rows(CUtensorMap* map, const void* base, int D, int N, long long Z, int rows, int cols,
+                     std::string* err);
+
 // Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
 // device, once per (kernel, device) pair for the life of the process (a
 // function attribute is per device, so a second GPU needs its own call).
