@@ -102,13 +102,16 @@ struct Cfg {
     static constexpr int OFF_BAR = OFF_ST + NST * 512;     // mbarriers (48)
     static constexpr int OFF_MISC = OFF_BAR + 384;
     // d <= 32: the dQ drain stages each 128-query partial here (two buffers of
-    // [128][D] fp32, 128B / 64B-swizzled rows) and adds it to the fp32
-    // accumulator with one TMA bulk reduce; at d = 64 (no room) it adds with
-    // vector atomics
+    // [128][D] fp32 as boxes of at most 32 columns, 128B / 64B-swizzled rows) and
+    // adds it to the fp32 accumulator with TMA bulk reduces.  At d = 64 it adds
+    // with vector atomics: the MMA issuer bounds that kernel, and one staging
+    // buffer with three Q/dO stages (what shared memory leaves room for) was no
+    // faster (N = 400 1% faster, N = 1600 2% slower, measured).
     static constexpr bool DQ_BULK = D <= 32;
+    static constexpr int NDQS = 2;
     static constexpr int DQS_BYTES = 128 * D * 4;
     static constexpr int OFF_DQS = (OFF_MISC + 64 + 1023) / 1024 * 1024;
-    static constexpr int USED = DQ_BULK ? OFF_DQS + 2 * DQS_BYTES : OFF_MISC + 64;
+    static constexpr int USED = DQ_BULK ? OFF_DQS + NDQS * DQS_BYTES : OFF_MISC + 64;
     // + 1 KB to align the base to 1024; at least 116 KB so that one CTA owns
     // an SM (its TMEM allocation is all 512 columns)
     static constexpr int SMEM = (USED + 1024) > 118784 ? (USED + 1024) : 118784;
@@ -120,6 +123,7 @@ struct Cfg {
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(C_DQ + D <= TMEM_COLS, "TMEM budget");
     static_assert(USED + 1024 <= 232448, "shared memory budget");
+    static_assert(NST > NB, "the softmax's wait for the stage of u+NB would wait on its own release");
 };
 
 // barrier indices (SF: one per S/dP buffer; PF: softmax done, a ring of 4 over
@@ -546,23 +550,30 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             tc_fence_before();
             mbar_arrive(sy.bar(F_DQE + (g & 1)));
             if constexpr (C::DQ_BULK) {
-                // staging buffer g & 1: its previous reduce (group g-2) must have read it
-                const uint32_t buf = sb + C::OFF_DQS + (g & 1) * C::DQS_BYTES;
-                if (elected) bulk_wait_group_read<1>();
+                // staging buffer g % NDQS: the reduces that last read it (group
+                // g - NDQS) must be done reading
+                const uint32_t buf = sb + C::OFF_DQS + (g % C::NDQS) * C::DQS_BYTES;
+                if (elected) bulk_wait_group_read<C::NDQS - 1>();
                 named_bar_sync(1, 128);
-                // row il, swizzled as the tensor map expects (16-byte chunk c of a
-                // row at c xor (row bits above the 128-byte line))
-                constexpr uint32_t M = D == 32 ? 7u : D == 16 ? 3u : 1u;
+                // row il of each box of BOXC columns, swizzled as the tensor map
+                // expects (16-byte chunk c of a row at c xor the row bits above the
+                // 128-byte line)
+                constexpr int BOXC = D < 32 ? D : 32;
+                constexpr uint32_t RB = BOXC * 4, M = RB == 128 ? 7u : RB == 64 ? 3u : 1u;
 #pragma unroll
                 for (int c = 0; c < D / 4; ++c) {
-                    const uint32_t a = (uint32_t)il * (D * 4) + 16u * c;
-                    st_shared_v4(buf + (a ^ (((a >> 7) & M) << 4)), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                    const uint32_t half = (uint32_t)c / (RB / 16), cc = (uint32_t)c % (RB / 16);
+                    const uint32_t a = (uint32_t)il * RB + 16u * cc;
+                    st_shared_v4(buf + half * 128u * RB + (a ^ (((a >> 7) & M) << 4)), v[4 * c], v[4 * c + 1],
+                                 v[4 * c + 2], v[4 * c + 3]);
                 }
                 fence_proxy_async_smem();
                 named_bar_sync(1, 128);
                 // rows past N lie outside the tensor and are skipped
                 if (elected) {
-                    tma_reduce_add_3d(&tm_dq, buf, 0, (ubase / 2 + g) * 128, bh);
+#pragma unroll
+                    for (int h = 0; h < D / BOXC; ++h)
+                        tma_reduce_add_3d(&tm_dq, buf + h * 128u * RB, h * BOXC, (ubase / 2 + g) * 128, bh);
                     bulk_commit_group();
                 }
             } else {
