@@ -150,14 +150,15 @@ static_assert(B_DQE + 2 <= 32, "barrier area holds 32 barriers");
 // -- the same parity as u -- issued after it had seen PF(u + 2), hence PF(u);
 // so no PF phase completes before each of its waiters (the issuer of its parity
 // and the dQ issuer) has seen the previous one.  ACC / ACCB: each main issuer's
-// final commit.  SF is a ring of 2 NB over the sub-tiles (u % 2NB): with NB odd
-// the sub-tiles of one buffer alternate between the issuers, and two issuers
-// give no order between their commits, so each SF barrier has one committing
-// thread (the issuer of the parity opposite to u's) and one waiting warpgroup
-// (u's), which saw its previous phase (u - 2NB) before this one.  DQF, DQE, DQA
-// as above.
+// final commit.  S^T(u) and dP^T(u) signal separately, SFS and SFD: rings of
+// 2 NB over the sub-tiles (u % 2NB).  With NB odd the sub-tiles of one buffer
+// alternate between the issuers, and two issuers give no order between their
+// commits; with the ring each barrier has one committing thread (the issuer of
+// u - NB) and one waiting warpgroup (u's), which saw its previous phase
+// (u - 2NB) before this one.  DQF, DQE, DQA as above.
 enum {
-    F_KV = 0, F_SF = 1, F_PF = 7, F_ACC = 15, F_ACCB = 16, F_DQA = 17, F_QF = 18, F_QE = 24, F_DQF = 30, F_DQE = 32
+    F_KV = 0, F_SFS = 1, F_SFD = 7, F_PF = 13, F_ACC = 21, F_ACCB = 22, F_DQA = 23, F_QF = 24, F_QE = 30, F_DQF = 36,
+    F_DQE = 38
 };
 constexpr int kPfRingF = 8;
 static_assert(F_DQE + 2 <= 48, "barrier area holds 48 barriers");
@@ -221,7 +222,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
 
     if (threadIdx.x == 0) {
         mbar_init(sy.bar(F_KV), 1);
-        for (int b = 0; b < 2 * C::NB; ++b) mbar_init(sy.bar(F_SF + b), 1);
+        for (int b = 0; b < 2 * C::NB; ++b) {
+            mbar_init(sy.bar(F_SFS + b), 1);
+            mbar_init(sy.bar(F_SFD + b), 1);
+        }
         for (int x = 0; x < kPfRingF; ++x) mbar_init(sy.bar(F_PF + x), 128);
         mbar_init(sy.bar(F_DQF), 1);
         mbar_init(sy.bar(F_DQF + 1), 1);
@@ -318,35 +322,44 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             const uint64_t dStage0mn = smem_desc(sb + C::OFF_STAGE + C::QTILE, C::QTILE, SBO, C::SW);
             constexpr uint32_t STAGE_U = C::STAGE >> 4, QTILE_U = C::QTILE >> 4;
 
-            // S^T(u), dP^T(u) into TMEM buffer u % NB.  Its Q/dO stage is known to be
-            // loaded: the prologue waits for it, later the softmax warpgroup that
-            // arrives PF(u-NB) has waited for it first.
-            auto issue_s_dp = [&](int u) {
-                const int s = u % C::NST;
-                const uint64_t dQs = dStage0 + STAGE_U * s;
-                const uint32_t tS = tmem + 128u * (u % C::NB), tDP = tS + 64;
+            // S^T(u) and dP^T(u) into the two halves of TMEM buffer u % NB, each with
+            // its own barrier.  Their Q/dO stage is known to be loaded: the prologue
+            // waits for it, later the softmax warpgroup that arrives PF(u-NB) has
+            // waited for it first.
+            auto issue_s = [&](int u) {
+                const uint64_t dQs = dStage0 + STAGE_U * (u % C::NST);
+                const uint32_t tS = tmem + 128u * (u % C::NB);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) mma_bf16_ss(tS, dK + 2 * kk, dQs + 2 * kk, ID_S, kk);
+                mma_commit(sy.bar(F_SFS + u % (2 * C::NB)));
+            };
+            auto issue_dp = [&](int u) {
+                const uint64_t dQs = dStage0 + STAGE_U * (u % C::NST);
+                const uint32_t tDP = tmem + 128u * (u % C::NB) + 64;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_bf16_ss(tDP, dVL + 2 * kk, dQs + QTILE_U + 2 * kk, ID_S, kk);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_bf16_ss(tDP, dVH + 2 * kk, dQs + 2 * QTILE_U + 2 * kk, ID_S, 1);
-                mma_commit(sy.bar(F_SF + u % (2 * C::NB)));
+                mma_commit(sy.bar(F_SFD + u % (2 * C::NB)));
             };
-            // dV, dK of sub-tile u (A = P^T, dS^T over 64 queries = 4 k-steps)
-            auto issue_dv_dk = [&](int u) {
-                const int s = u % C::NST;
-                const uint64_t dGmn = dStage0mn + STAGE_U * s;      // [dO_lo | dO_hi], MN-major
-                const uint64_t dQmn = dStage0 + STAGE_U * s;        // Q rows, MN-major
+            // dV of sub-tile u (A = P^T from the S half, 64 queries = 4 k-steps)
+            auto issue_dv = [&](int u) {
+                const uint64_t dGmn = dStage0mn + STAGE_U * (u % C::NST);   // [dO_lo | dO_hi], MN-major
 #pragma unroll
-                for (int kk = 0; kk < C::BS / 16; ++kk) {
-                    const uint32_t acc = (u > 0 || kk > 0) ? 1u : 0u;
-                    mma_bf16_ts(tmem + C::C_DV, tmem + 128u * (u % C::NB) + 8 * kk, dGmn + KSTEP * kk, ID_DV, acc);
-                    mma_bf16_ts(tmem + C::C_DK, tmem + 128u * (u % C::NB) + 64 + 8 * kk, dQmn + KSTEP * kk, ID_DK, acc);
-                }
-                mma_commit(sy.bar(F_QE + s));
+                for (int kk = 0; kk < C::BS / 16; ++kk)
+                    mma_bf16_ts(tmem + C::C_DV, tmem + 128u * (u % C::NB) + 8 * kk, dGmn + KSTEP * kk, ID_DV,
+                                (u > 0 || kk > 0) ? 1u : 0u);
+            };
+            // dK of sub-tile u (A = dS^T from the dP half); then the stage is free
+            auto issue_dk = [&](int u) {
+                const uint64_t dQmn = dStage0 + STAGE_U * (u % C::NST);     // Q rows, MN-major
+#pragma unroll
+                for (int kk = 0; kk < C::BS / 16; ++kk)
+                    mma_bf16_ts(tmem + C::C_DK, tmem + 128u * (u % C::NB) + 64 + 8 * kk, dQmn + KSTEP * kk, ID_DK,
+                                (u > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(sy.bar(F_QE + u % C::NST));
             };
             bool ok = wait_bounded(sy, sy.bar(F_KV), 0, 1, -1);
             if (par == 0) {
@@ -354,7 +367,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                     ok = wait_bounded(sy, sy.bar(F_QF + u), 0, 1, u);
                 if (ok) {
                     tc_fence_after();
-                    for (int u = 0; u < C::NB && u < nsub; ++u) issue_s_dp(u);
+                    for (int u = 0; u < C::NB && u < nsub; ++u) {
+                        issue_s(u);
+                        issue_dp(u);
+                    }
                 }
             } else if (nsub > 1 && ok && C::TWO_ISSUERS) {
                 // dV/dK(0), whose first MMAs overwrite the accumulators, must be done
@@ -362,13 +378,19 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 ok = wait_bounded(sy, sy.bar(F_QE + 0), 0, 1, 0);
             }
             // PF(u) also certifies that the Q/dO stage of u+NB is loaded (the
-            // softmax warpgroup waited for it)
+            // softmax warpgroup waited for it).  The tensor core runs one thread's
+            // MMAs in issue order: S^T(u+NB) follows dV(u), the last reader of the
+            // S half, and dP^T(u+NB) follows dK(u), the last reader of the dP half;
+            // the softmax of u+NB starts on S^T while dK(u) and dP^T(u+NB) run.
             for (int u = par; u < nsub && ok; u += USTEP) {
                 ok = wait_bounded(sy, sy.bar(F_PF + u % kPfRingF), (u / kPfRingF) & 1, 1, u);
                 if (!ok) break;
                 tc_fence_after();
-                issue_dv_dk(u);
-                if (u + C::NB < nsub) issue_s_dp(u + C::NB);
+                const int v = u + C::NB;
+                issue_dv(u);
+                if (v < nsub) issue_s(v);
+                issue_dk(u);
+                if (v < nsub) issue_dp(v);
             }
             // all of this thread's MMAs done (also on abort, before TMEM is freed)
             const uint32_t acc_bar = sy.bar(par == 0 ? F_ACC : F_ACCB);
@@ -404,13 +426,13 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         }
         for (int u = grp; u < nsub && ok; u += 2) {
             const int buf = u % C::NB;
-            // One round trip for S/dP(u) and, with the split issuer, the dQ product
-            // that last read dS block u & 3: it held sub-tile u-4, of 128-query
-            // group h, whose product must have read it before this sub-tile writes
-            // it.  The parity test on DQF + (h & 1) is exact: group h-2 was waited
-            // for at sub-tile u-4 by this warpgroup, and group h+2 needs PF(u).
-            // (The product is almost always complete by now.)
-            const uint32_t bsf = sy.bar(F_SF + u % (2 * C::NB)), psf = (u / (2 * C::NB)) & 1;
+            // One round trip for S^T(u) and the dQ product that last read dS block
+            // u & 3: it held sub-tile u-4, of 128-query group h, whose product must
+            // have read it before this sub-tile writes it.  The parity test on
+            // DQF + (h & 1) is exact: group h-2 was waited for at sub-tile u-4 by
+            // this warpgroup, and group h+2 needs PF(u).  (The product is almost
+            // always complete by now.)
+            const uint32_t bsf = sy.bar(F_SFS + u % (2 * C::NB)), psf = (u / (2 * C::NB)) & 1;
             uint32_t bdq = bsf, pdq = psf;
             if (u >= 4) {
                 const int h = (u - 4) >> 1;
@@ -421,22 +443,23 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             if (!ok) break;
             tc_fence_after();
             const uint32_t ds_blk = sb + C::OFF_DS + 16384 * (u & 3);
+            // phase 1: P = exp2(S scale log2(e) - LSE log2(e)) as bf16 pairs, over
+            // the S^T columns already read (the dP^T products may still run)
+            uint32_t pk[2][2][8];
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
                 const int r0 = q4 * 32 + 16 * hb + tr;          // key rows r0, r0 + 8 of the tile
                 const bool kv0 = full || k0 + r0 < N, kv1 = full || k0 + r0 + 8 < N;
-                const uint32_t tS = tmem + ((uint32_t)(q4 * 32 + 16 * hb) << 16) + 128u * buf, tDP = tS + 64;
+                const uint32_t tS = tmem + ((uint32_t)(q4 * 32 + 16 * hb) << 16) + 128u * buf;
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
-                    uint32_t sr[16], pr[16];
+                    uint32_t sr[16];
                     tmem_ld_16x256b_x4(tS + 32 * c, sr);
-                    tmem_ld_16x256b_x4(tDP + 32 * c, pr);
                     tmem_wait_ld();
-                    uint32_t pk[8], dk[8];
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const float4 st = stat[4 * c + kk];
-                        const uint64_t nl = f2_pack(st.x, st.y), dd = f2_pack(st.z, st.w);
+                        const uint64_t nl = f2_pack(st.x, st.y);
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const uint64_t x = f2_fma(f2_pack(__uint_as_float(sr[4 * kk + 2 * e]),
@@ -446,18 +469,47 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                             f2_unpack(x, x0, x1);
                             float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                             if (!(e ? kv1 : kv0)) p0 = p1 = 0.f;
-                            pk[2 * kk + e] = pack_bf16x2(p0, p1);
+                            pk[hb][c][2 * kk + e] = pack_bf16x2(p0, p1);
+                        }
+                    }
+                    // packed pair 4k + t%4 over the S^T columns
+                    tmem_st_16x128b_x4(tS + 16 * c, pk[hb][c]);
+                }
+            }
+            // phase 2: dS = P (dP - D), with P as rounded for the dV product
+            ok = warp_wait(sy, sy.bar(F_SFD + u % (2 * C::NB)), (u / (2 * C::NB)) & 1, 2, u);
+            if (!ok) {
+                mbar_arrive(sy.bar(F_PF + u % kPfRingF));
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+                const int r0 = q4 * 32 + 16 * hb + tr;
+                const uint32_t tDP = tmem + ((uint32_t)(q4 * 32 + 16 * hb) << 16) + 128u * buf + 64;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t pr[16];
+                    tmem_ld_16x256b_x4(tDP + 32 * c, pr);
+                    tmem_wait_ld();
+                    uint32_t dk[8];
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const float4 st = stat[4 * c + kk];
+                        const uint64_t dd = f2_pack(st.z, st.w);
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const uint32_t pp = pk[hb][c][2 * kk + e];
                             const uint64_t t = f2_sub(f2_pack(__uint_as_float(pr[4 * kk + 2 * e]),
                                                               __uint_as_float(pr[4 * kk + 2 * e + 1])),
                                                       dd);
                             float d0, d1;
-                            f2_unpack(f2_mul(f2_pack(p0, p1), t), d0, d1);
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u)), t),
+                                      d0, d1);
                             dk[2 * kk + e] = pack_bf16x2(d0, d1);
                         }
                     }
-                    // P over the S^T columns, dS over the dP^T columns already read
-                    // (this chunk's values are in registers): packed pair 4k + t%4
-                    tmem_st_16x128b_x4(tS + 16 * c, pk);
+                    // dS over the dP^T columns already read
                     tmem_st_16x128b_x4(tDP + 16 * c, dk);
                     // dS also to the 128B-swizzled ring block (row = key, 16-byte
                     // chunk = query / 8 xor row % 8) for the dQ product: one 4-byte

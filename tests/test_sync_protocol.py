@@ -258,6 +258,256 @@ def run(nsub, split, NB, NST, seed, dqe_pair=True, with_dq=True, two_issuers=Fal
             assert not any(fifo.values())
             return
         if slow_role is not None and len(enabled) > 1 and rnd.random() > 0.02:
+            # a role index, or the name of an issuing thread's MMA pipe
+            slow = ("pipe", slow_role) if isinstance(slow_role, str) else ("role", slow_role)
+            enabled = [e for e in enabled if e != slow] or enabled
+        kind, x = rnd.choice(enabled)
+        if kind == "pipe":
+            item = fifo[x].pop(0)
+            if item[0] == "mma":
+                item[1](item[2])
+            else:
+                item[1].arrive(item[2])
+            continue
+        req = pending[x]
+        if req[0] == "wait":
+            _, br, k = req
+            assert br.done == k + 1, f"{br.name}: wait for phase {k} passed at {br.done} completed phases"
+        elif req[0] == "arrive":
+            req[1].arrive(req[2])
+        advance(x)
+
+
+def run_fused(nsub, NB, NST, seed, two_issuers, pf_ring=8, sf_ring=None, slow_role=None, s_first=True,
+              plant=None):
+    """One random schedule of one CTA of the fused backward kernel (bwd_main_kernel).
+
+    Roles: the TMA producer (stage s of sub-tile u after QE(s)); one or two main
+    issuers (two: one per sub-tile parity); four softmax warps in each of two
+    warpgroups (even / odd sub-tiles); the dQ issuer; four drain warps.  Buffer
+    b = u % NB has an S^T region and a dP^T region.  After PF(u) the issuer of
+    u issues, in this order, dV(u) (reads P(u) from the S region), S^T(u+NB)
+    (overwrites the S region) and commits SFs(u+NB), dK(u) (reads dS(u) from
+    the dP region), commits QE, dP^T(u+NB) (overwrites the dP region) and
+    commits SFd(u+NB).  The softmax of u waits SFs(u) (and the dQ product that
+    last read its dS ring block), turns S into P, waits SFd(u), turns dP into
+    dS (region and ring), waits for the stages of u+NB and u+2, reads the
+    statistics of u+2 and arrives PF(u).  s_first=False issues dV/dK(u) before
+    both halves of S/dP(u+NB).  plant
+    names a mistake to put into the protocol: "no_dqf_wait" drops the softmax's
+    wait for the dQ product, "s_before_dv" issues S^T(u+NB) before dV(u)."""
+    rnd = random.Random(seed)
+    ngrp = (nsub + 1) // 2
+    nsf = sf_ring or 2 * NB
+    bars = {}
+
+    def bar(name, count=1):
+        if name not in bars:
+            bars[name] = Bar(name, count)
+        return bars[name]
+
+    for b in range(nsf):
+        bar(("SFs", b))
+        bar(("SFd", b))
+    for x in range(pf_ring):
+        bar(("PF", x), 4)
+    for st in range(NST):
+        bar(("QF", st))
+        bar(("QE", st))
+    for x in range(2):
+        bar(("DQE", x), 4)
+        bar(("DQF", x))
+
+    sreg = {(b, q): ("free", None) for b in range(NB) for q in range(4)}
+    dreg = {(b, q): ("free", None) for b in range(NB) for q in range(4)}
+    stage = {st: None for st in range(NST)}
+    readers = {st: set() for st in range(NST)}
+    stage_soft = {st: 0 for st in range(NST)}
+    ds = {(blk, q): ("zero", None, True) for blk in range(4) for q in range(4)}
+    acc = {q: ("idle", -1) for q in range(4)}
+    fifo = {"main": [], "main1": [], "dq": []}
+    dv_done = set()
+
+    def check_stage(u, what):
+        st = u % NST
+        assert stage[st] == u, f"{what}({u}) reads stage {st} holding {stage[st]}"
+        readers[st].add(what)
+
+    def mma_s(u):
+        b = u % NB
+        for q in range(4):
+            assert sreg[(b, q)][0] == "free", f"S({u}) overwrites {sreg[(b, q)]}"
+            sreg[(b, q)] = ("S", u)
+        check_stage(u, "s")
+
+    def mma_dp(u):
+        b = u % NB
+        for q in range(4):
+            assert dreg[(b, q)][0] == "free", f"dP({u}) overwrites {dreg[(b, q)]}"
+            dreg[(b, q)] = ("dP", u)
+        check_stage(u, "dp")
+
+    def mma_dv(u):
+        b = u % NB
+        assert u == 0 or 0 in dv_done, f"dV({u}) adds to accumulators dV(0) has not yet zeroed"
+        dv_done.add(u)
+        for q in range(4):
+            assert sreg[(b, q)] == ("P", u), f"dV({u}) reads {sreg[(b, q)]}"
+            sreg[(b, q)] = ("free", None)
+        check_stage(u, "dv")
+
+    def mma_dk(u):
+        b = u % NB
+        for q in range(4):
+            assert dreg[(b, q)] == ("dS", u), f"dK({u}) reads {dreg[(b, q)]}"
+            dreg[(b, q)] = ("free", None)
+        check_stage(u, "dk")
+
+    def mma_dq(g):
+        for j in (2 * g, 2 * g + 1):
+            if j >= nsub:
+                continue
+            for q in range(4):
+                kind, uu, _ = ds[(j & 3, q)]
+                assert (kind, uu) == ("dS", j), f"dQ({g}) reads dS block {j & 3} holding {(kind, uu)}"
+                ds[(j & 3, q)] = ("dS", j, True)
+        for q in range(4):
+            assert acc[q] in (("idle", -1), ("read", g - 1)), f"dQ({g}) overwrites accumulator {acc[q]}"
+            acc[q] = ("dq", g)
+
+    def producer():
+        for u in range(nsub):
+            st = u % NST
+            yield ("wait", bar(("QE", st)), u // NST - 1)
+            if stage[st] is not None:
+                assert readers[st] >= {"s", "dp", "dv", "dk"} and stage_soft[st] == 4, \
+                    f"stage {st} reused early: {readers[st]}, {stage_soft[st]} softmax warps done"
+            stage[st] = u
+            readers[st] = set()
+            stage_soft[st] = 0
+            yield ("arrive", bar(("QF", st)), u // NST)
+
+    def issue_sdp(me, v, split):
+        fifo[me].append(("mma", mma_s, v))
+        fifo[me].append(("commit", bar(("SFs", v % nsf)), v // nsf))
+        if not split:
+            fifo[me].append(("mma", mma_dp, v))
+            fifo[me].append(("commit", bar(("SFd", v % nsf)), v // nsf))
+
+    def main_issuer(par, step):
+        me = "main" if par == 0 else "main1"
+        if par == 0:
+            for u in range(min(NB, nsub)):
+                yield ("wait", bar(("QF", u)), 0)
+            for u in range(min(NB, nsub)):
+                issue_sdp(me, u, False)
+        elif nsub > 1:
+            yield ("wait", bar(("QE", 0)), 0)
+        for u in range(par, nsub, step):
+            yield ("wait", bar(("PF", u % pf_ring)), u // pf_ring)
+            v = u + NB
+            if plant != "s_before_dv":
+                fifo[me].append(("mma", mma_dv, u))
+            if s_first and v < nsub:
+                fifo[me].append(("mma", mma_s, v))
+                fifo[me].append(("commit", bar(("SFs", v % nsf)), v // nsf))
+            if plant == "s_before_dv":
+                fifo[me].append(("mma", mma_dv, u))
+            fifo[me].append(("mma", mma_dk, u))
+            fifo[me].append(("commit", bar(("QE", u % NST)), u // NST))
+            if v < nsub:
+                if not s_first:
+                    fifo[me].append(("mma", mma_s, v))
+                    fifo[me].append(("commit", bar(("SFs", v % nsf)), v // nsf))
+                fifo[me].append(("mma", mma_dp, v))
+                fifo[me].append(("commit", bar(("SFd", v % nsf)), v // nsf))
+
+    def softmax(grp, q):
+        if grp < nsub:
+            yield ("wait", bar(("QF", grp % NST)), grp // NST)
+            assert stage[grp % NST] == grp
+        for u in range(grp, nsub, 2):
+            b, st = u % NB, u % NST
+            yield ("wait", bar(("SFs", u % nsf)), u // nsf)
+            if u >= 4 and plant != "no_dqf_wait":
+                h = (u - 4) >> 1
+                yield ("wait", bar(("DQF", h & 1)), h >> 1)
+            assert sreg[(b, q)] == ("S", u), f"softmax({u}) reads S region {sreg[(b, q)]}"
+            sreg[(b, q)] = ("P", u)
+            yield ("wait", bar(("SFd", u % nsf)), u // nsf)
+            assert dreg[(b, q)] == ("dP", u), f"softmax({u}) reads dP region {dreg[(b, q)]}"
+            dreg[(b, q)] = ("dS", u)
+            kind, uu, read = ds[(u & 3, q)]
+            assert read, f"softmax({u}) overwrites dS of sub-tile {uu} before its dQ product read it"
+            ds[(u & 3, q)] = ("dS", u, False)
+            stage_soft[st] += 1
+            if u + NB < nsub:
+                v = u + NB
+                yield ("wait", bar(("QF", v % NST)), v // NST)
+            if u + 2 < nsub:
+                yield ("wait", bar(("QF", (u + 2) % NST)), (u + 2) // NST)
+                assert stage[(u + 2) % NST] == u + 2
+            yield ("arrive", bar(("PF", u % pf_ring)), u // pf_ring)
+
+    def dq_issuer():
+        for g in range(ngrp):
+            for u in (2 * g, 2 * g + 1):
+                if u < nsub:
+                    yield ("wait", bar(("PF", u % pf_ring)), u // pf_ring)
+            if g > 0:
+                yield ("wait", bar(("DQE", (g - 1) & 1)), (g - 1) >> 1)
+            fifo["dq"].append(("mma", mma_dq, g))
+            fifo["dq"].append(("commit", bar(("DQF", g & 1)), g >> 1))
+
+    def drain(q):
+        for g in range(ngrp):
+            yield ("wait", bar(("DQF", g & 1)), g >> 1)
+            assert acc[q] == ("dq", g), f"drain({g}) reads {acc[q]}"
+            acc[q] = ("read", g)
+            yield ("arrive", bar(("DQE", g & 1)), g >> 1)
+
+    roles = [producer()]
+    roles += [main_issuer(0, 2), main_issuer(1, 2)] if two_issuers else [main_issuer(0, 1)]
+    roles += [softmax(g, q) for g in range(2) for q in range(4)]
+    roles += [drain(q) for q in range(4)] + [dq_issuer()]
+    schedule(roles, fifo, rnd, slow_role)
+
+
+def schedule(roles, fifo, rnd, slow_role=None):
+    """Runs coroutine roles and MMA FIFOs under a random schedule (see run)."""
+    pending = {i: None for i in range(len(roles))}
+
+    def advance(i):
+        try:
+            pending[i] = roles[i].send(None)
+        except StopIteration:
+            pending[i] = "done"
+
+    for i in range(len(roles)):
+        advance(i)
+    steps = 0
+    while True:
+        steps += 1
+        assert steps < 400000
+        enabled = []
+        for i, req in pending.items():
+            if req == "done":
+                continue
+            if req[0] == "wait":
+                _, br, k = req
+                assert br.done <= k + 1, f"{br.name}: phase {k + 1} completed before a waiter for phase {k} passed"
+                if br.passes(k):
+                    enabled.append(("role", i))
+            else:
+                enabled.append(("role", i))
+        for who, f in fifo.items():
+            if f:
+                enabled.append(("pipe", who))
+        if not enabled:
+            blocked = {i: (r[1].name, r[2], r[1].done) for i, r in pending.items() if r != "done"}
+            assert not blocked, f"deadlock: {blocked}"
+            return
+        if slow_role is not None and len(enabled) > 1 and rnd.random() > 0.02:
             enabled = [e for e in enabled if e != ("role", slow_role)] or enabled
         kind, x = rnd.choice(enabled)
         if kind == "pipe":
@@ -784,7 +1034,7 @@ def test_fused_protocol_random_schedules(nsub, NB, NST, two):
     stages) and head_dim 64 (one main issuer, 2 buffers, 4 stages), odd and even
     sub-tile counts, 40 random schedules each."""
     for seed in range(40):
-        run(nsub, True, NB, NST, seed * 1000 + nsub, two_issuers=two, pf_ring=8, sf_ring=2 * NB)
+        run_fused(nsub, NB, NST, seed * 1000 + nsub, two)
 
 
 @pytest.mark.parametrize("slow", [1, 2])
@@ -796,12 +1046,12 @@ def test_fused_two_issuers_need_the_longer_ring(slow):
     failures = 0
     for seed in range(200):
         try:
-            run(20, True, 3, 6, seed, two_issuers=True, pf_ring=4, slow_role=slow, sf_ring=6)
+            run_fused(20, 3, 6, seed, True, pf_ring=4, slow_role=slow)
         except AssertionError:
             failures += 1
     assert failures > 0
     for seed in range(200):
-        run(20, True, 3, 6, seed, two_issuers=True, pf_ring=8, slow_role=slow, sf_ring=6)
+        run_fused(20, 3, 6, seed, True, slow_role=slow)
 
 
 def test_single_drain_barrier_aliases():
@@ -820,22 +1070,19 @@ def test_single_drain_barrier_aliases():
 
 
 def test_model_catches_a_broken_protocol():
-    """The model is not vacuous: without the softmax's wait for the dQ product
-    (head_dim <= 32), some schedule overwrites a dS block that dQ has not read."""
-    import inspect
-    src = inspect.getsource(run)
-    broken = src.replace("if with_dq and split and u >= 4:", "if False:")
-    assert broken != src
-    ns = {}
-    exec(compile("import random\n" + broken.replace("def run(", "def run_broken(", 1), "<broken>", "exec"),
-         {"Bar": Bar, "random": random}, ns)
-    failures = 0
-    for seed in range(200):
-        try:
-            ns["run_broken"](12, True, 3, 6, seed)
-        except AssertionError:
-            failures += 1
-    assert failures > 0
+    """The fused model is not vacuous: without the softmax's wait for the dQ
+    product, some schedule overwrites a dS block that dQ has not read; with the
+    S^T product issued before dV (which reads the same half), some schedule
+    overwrites P before dV read it."""
+    for plant, msg in (("no_dqf_wait", "before its dQ product read it"), ("s_before_dv", "overwrites")):
+        failures = 0
+        for seed in range(200):
+            try:
+                run_fused(12, 3, 6, seed, True, plant=plant)
+            except AssertionError as e:
+                assert msg in str(e), (plant, str(e))
+                failures += 1
+        assert failures > 0, plant
 
 
 @pytest.mark.parametrize("NB,NST,two", FUSED)
@@ -844,6 +1091,9 @@ def test_fused_protocol_with_one_slow_role(NB, NST, two):
     producer, either main issuer, a softmax warp, a drain warp, the dQ issuer):
     skewed schedules reach interleavings that uniform ones rarely do."""
     nroles = 1 + (2 if two else 1) + 8 + 4 + 1
-    for slow in range(nroles):
+    slows = list(range(nroles)) + ["main", "dq"] + (["main1"] if two else [])
+    for slow in slows:
         for seed in range(12):
-            run(17, True, NB, NST, seed * 31 + slow, two_issuers=two, pf_ring=8, slow_role=slow, sf_ring=2 * NB)
+            run_fused(17, NB, NST, seed * 31 + len(str(slow)), two, slow_role=slow)
+
+
