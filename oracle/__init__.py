@@ -49,6 +49,10 @@ def _load():
             lib.psa_oracle_fwd.restype = ctypes.c_int
             lib.psa_oracle_bwd.argtypes = [ctypes.c_int] * 4 + [ctypes.c_double] + [_dp] * 10
             lib.psa_oracle_bwd.restype = ctypes.c_int
+            lib.psa_oracle_merge_fwd.argtypes = [ctypes.c_int] * 4 + [_dp] * 3
+            lib.psa_oracle_merge_fwd.restype = ctypes.c_int
+            lib.psa_oracle_merge_bwd.argtypes = [ctypes.c_int] * 4 + [_dp] * 3
+            lib.psa_oracle_merge_bwd.restype = ctypes.c_int
             lib.psa_oracle_threads.argtypes = []
             lib.psa_oracle_threads.restype = ctypes.c_int
             lib.psa_oracle_set_threads.argtypes = [ctypes.c_int]
@@ -136,3 +140,30 @@ def psa_bwd(packed, do_lo, do_hi, scale: float):
     dos = np.stack([_f64(do_lo), _f64(do_hi)])
     dq, dk, dvs = attn_bwd(packed[:, 0], packed[:, 1], vs, dos, scale)
     return np.stack([dq, dk, dvs[0], dvs[1]], axis=1)
+
+
+def merge_fwd(o_lo, o_hi, B: int, heads: int):
+    """PSA attention merge ("Struct PsaMergeAttnRuntimeOp"): O_lo, O_hi
+    [B*heads, N, d] -> merged [B, 2*heads*d, N], lo in the low half of the
+    channels and hi in the high half, head-major in each (the reading stated in
+    psa_oracle.c)."""
+    o_lo, o_hi = _f64(o_lo), _f64(o_hi)
+    BH, N, d = o_lo.shape
+    assert BH == B * heads and o_hi.shape == o_lo.shape
+    out = np.empty((B, 2 * heads * d, N))
+    if _load().psa_oracle_merge_fwd(B, heads, N, d, _ptr(o_lo), _ptr(o_hi), _ptr(out)):
+        raise RuntimeError("psa_oracle_merge_fwd failed")
+    return out
+
+
+def merge_bwd(d_merged, heads: int, d: int):
+    """The merge's backward: d_merged [B, 2*heads*d, N] -> (dO_lo, dO_hi), each
+    [B*heads, N, d]."""
+    g = _f64(d_merged)
+    B, c, N = g.shape
+    assert c == 2 * heads * d
+    d_lo = np.empty((B * heads, N, d))
+    d_hi = np.empty((B * heads, N, d))
+    if _load().psa_oracle_merge_bwd(B, heads, N, d, _ptr(g), _ptr(d_lo), _ptr(d_hi)):
+        raise RuntimeError("psa_oracle_merge_bwd failed")
+    return d_lo, d_hi

@@ -211,3 +211,49 @@ done:
     if (!D_out) free(D);
     return err;
 }
+
+/*
+ * PSA attention merge ("Struct PsaMergeAttnRuntimeOp": the op after the lo/hi
+ * pair; its backward takes d_merged, d_lo, d_hi, c, H, W and the head count,
+ * one thread block per (batch*head, position)).  The pages do not spell the
+ * channel order out; the reading taken here: the merged tensor is [B, c, H, W]
+ * with c = 2 * heads * d channels, the lo outputs of every head in the low
+ * half of the channels and the hi outputs in the high half, head-major inside
+ * each half, positions n = y * W + x:
+ *   merged[b, s*heads*d + h*d + j, n] = O_s[b*heads + h, n, j],   s = 0 (lo), 1 (hi)
+ * The merge is a permutation of elements, so its backward is the inverse
+ * gather:
+ *   dO_s[b*heads + h, n, j] = d_merged[b, s*heads*d + h*d + j, n]
+ * Layouts: o_lo, o_hi, d_lo, d_hi [B*heads, N, d]; merged [B, c, N]; fp64.
+ */
+int psa_oracle_merge_fwd(int B, int heads, int N, int d, const double* o_lo, const double* o_hi,
+                         double* merged) {
+    if (B < 0 || heads <= 0 || N < 0 || d <= 0) return -1;
+    const long c = 2L * heads * d;
+    for (int b = 0; b < B; ++b)
+        for (int s = 0; s < 2; ++s)
+            for (int h = 0; h < heads; ++h)
+                for (int j = 0; j < d; ++j)
+                    for (int n = 0; n < N; ++n) {
+                        const double* o = s == 0 ? o_lo : o_hi;
+                        merged[((size_t)b * c + (size_t)s * heads * d + (size_t)h * d + j) * N + n] =
+                            o[(((size_t)b * heads + h) * N + n) * d + j];
+                    }
+    return 0;
+}
+
+int psa_oracle_merge_bwd(int B, int heads, int N, int d, const double* d_merged, double* d_lo,
+                         double* d_hi) {
+    if (B < 0 || heads <= 0 || N < 0 || d <= 0) return -1;
+    const long c = 2L * heads * d;
+    for (int b = 0; b < B; ++b)
+        for (int s = 0; s < 2; ++s)
+            for (int h = 0; h < heads; ++h)
+                for (int n = 0; n < N; ++n)
+                    for (int j = 0; j < d; ++j) {
+                        double* g = s == 0 ? d_lo : d_hi;
+                        g[(((size_t)b * heads + h) * N + n) * d + j] =
+                            d_merged[((size_t)b * c + (size_t)s * heads * d + (size_t)h * d + j) * N + n];
+                    }
+    return 0;
+}

@@ -257,3 +257,67 @@ def test_thread_count_independent(oracle_mod):
         oracle_mod.set_threads(n0)
     for x, y in zip(a, b):
         np.testing.assert_array_equal(x, y)
+
+
+# ---------------------------------------------------------------- the merge op
+def test_merge_bwd_index_map(oracle_mod):
+    """The merge's backward against the reading written as a closed form of the
+    indices: with d_merged[b, ch, n] = 1000 b + 10 ch + n, dO_lo[b*heads + h, n, j]
+    must be 1000 b + 10 (h d + j) + n and dO_hi the same with ch shifted by heads d
+    (lo channels first, head-major within each half)."""
+    B, heads, d, N = 2, 3, 2, 5
+    b, ch, n = np.meshgrid(np.arange(B), np.arange(2 * heads * d), np.arange(N), indexing="ij")
+    g = 1000.0 * b + 10.0 * ch + n
+    d_lo, d_hi = oracle_mod.merge_bwd(g, heads, d)
+    for bb in range(B):
+        for h in range(heads):
+            for nn in range(N):
+                for j in range(d):
+                    assert d_lo[bb * heads + h, nn, j] == 1000 * bb + 10 * (h * d + j) + nn
+                    assert d_hi[bb * heads + h, nn, j] == 1000 * bb + 10 * (heads * d + h * d + j) + nn
+
+
+def test_merge_backward_is_the_adjoint_and_inverse(oracle_mod):
+    """The merge is a permutation of elements: its backward is the adjoint of the
+    forward (<M x, g> = <x, M^T g>) and inverts it."""
+    rng = np.random.default_rng(7)
+    B, heads, N, d = 2, 3, 7, 4
+    o_lo, o_hi = rng.normal(size=(2, B * heads, N, d))
+    g = rng.normal(size=(B, 2 * heads * d, N))
+    m = oracle_mod.merge_fwd(o_lo, o_hi, B, heads)
+    g_lo, g_hi = oracle_mod.merge_bwd(g, heads, d)
+    assert abs(np.sum(m * g) - (np.sum(o_lo * g_lo) + np.sum(o_hi * g_hi))) < 1e-10
+    r_lo, r_hi = oracle_mod.merge_bwd(m, heads, d)
+    np.testing.assert_array_equal(r_lo, o_lo)
+    np.testing.assert_array_equal(r_hi, o_hi)
+    assert sorted(m.ravel()) == sorted(np.concatenate([o_lo.ravel(), o_hi.ravel()]))
+
+
+def test_merged_backward_against_finite_differences(oracle_mod):
+    """The attention backward fed by the merge's backward is the gradient of
+    L = <merge(O_lo, O_hi), G> with respect to Q, K and V (central differences
+    over every input element of a tiny case)."""
+    rng = np.random.default_rng(11)
+    B, heads, N, d = 1, 2, 3, 2
+    q, k = rng.normal(size=(2, B * heads, N, d))
+    vs = rng.normal(size=(2, B * heads, N, d))
+    G = rng.normal(size=(B, 2 * heads * d, N))
+    scale = 0.7
+
+    def loss():
+        o, _ = oracle_mod.attn_fwd(q, k, vs, scale)
+        return float(np.sum(oracle_mod.merge_fwd(o[0], o[1], B, heads) * G))
+
+    dos = np.stack(oracle_mod.merge_bwd(G, heads, d))
+    dq, dk, dvs = oracle_mod.attn_bwd(q, k, vs, dos, scale)
+    h = 1e-5
+    for arr, grad in ((q, dq), (k, dk), (vs, dvs)):
+        flat, gflat = arr.reshape(-1), grad.reshape(-1)
+        for idx in range(flat.size):
+            old = flat[idx]
+            flat[idx] = old + h
+            lp = loss()
+            flat[idx] = old - h
+            lm = loss()
+            flat[idx] = old
+            assert abs((lp - lm) / (2 * h) - gflat[idx]) < 1e-7 * max(1.0, abs(gflat[idx]))
