@@ -391,6 +391,7 @@ def run_ours(args, w):
     if rank == 0:
         line["e2e"] = run_e2e(w, args, device, algo)
         line["forward"] = time_forward(w, bufs, flush, args.steps)
+        line["merge"] = time_merge(w, bufs, flush, args.steps, algo)
     if rank == 0 and world == 1 and not args.no_cpu:
         v, n, t = oracle_sample(w, args.cpu_budget)
         import oracle
@@ -423,6 +424,48 @@ def time_forward(w, bufs, flush, steps):
     torch.cuda.synchronize()
     ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     return {"ms": ms, "tflops": 6.0 * w.BH * w.N * w.N * w.d / (ms * 1e-3) / 1e12, "flops_per_bh": "6 N^2 d"}
+
+
+def time_merge(w, bufs, flush, steps, algo):
+    """The merge op's backward with the attention backward on the same
+    workload, dO_lo / dO_hi given as one merged [B, 2*heads*d, H, W] gradient
+    (synthetic, drawn like dO): fused (psa_merge_attn_bwd reads dO out of it)
+    against separate (psa_merge_bwd into contiguous dO, then psa_attn_bwd).
+    CUDA events per call, L2 flushed before each."""
+    import torch
+    from self_attention_backward_gb300 import binding as B
+    packed, o_lo, o_hi, lse = bufs[0], bufs[1], bufs[2], bufs[3]
+    H, Wd = (int(x) for x in w.fmap.split("x"))
+    g = torch.randn((w.B, 2 * w.heads * w.d, H, Wd), generator=torch.Generator().manual_seed(w.seed + 100))
+    gm = g.to(packed.device).to(packed.dtype)
+    d_packed = torch.empty_like(packed)
+    ws = B.BwdWorkspace(packed.device)
+    d_lo = torch.empty_like(o_lo)
+    d_hi = torch.empty_like(o_lo)
+
+    def fused():
+        B.merge_attn_bwd(packed, o_lo, o_hi, lse, gm, w.heads, w.scale, d_packed=d_packed, workspace=ws, algo=algo)
+
+    def separate():
+        B.psa_merge_bwd(gm, d_lo, d_hi, w.B, w.heads, H, Wd, w.d, 1 if w.dtype == "bf16" else 0)
+        B.attn_bwd(packed, o_lo, o_hi, lse, d_lo, d_hi, w.scale, d_packed=d_packed, workspace=ws, algo=algo)
+
+    st = torch.cuda.current_stream()
+    out = {}
+    for name, fn in (("fused", fused), ("separate", separate)):
+        for _ in range(3):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(st)
+            fn()
+            b.record(st)
+        torch.cuda.synchronize()
+        out[name + "_ms"] = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    B.psa_attn_sync_status()
+    out["d_merged"] = list(gm.shape)
+    return out
 
 
 def run_e2e(w, args, device, algo):

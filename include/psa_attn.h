@@ -134,6 +134,87 @@ int psa_attn_bwd_algo(const void* packed, const void* o_lo, const void* o_hi, co
                       int dtype, int algo, void* stream);
 
 /*
+ * psa_attn_view -- a strided view of a [B, heads, N, d] tensor: element
+ * (b, h, n, j) (batch, head, position, feature) is at
+ *   base + b*batch_stride + h*head_stride + n*pos_stride + j*feat_stride
+ * with strides in elements.  Row-major rows ([N, d] per slice, as
+ * psa_attn_bwd takes dO): feat_stride = 1, pos_stride >= d (a padded row when
+ * larger).  Channel-major ([d, N] per slice, as a [B, c, H, W] feature map
+ * holds it): pos_stride = 1, feat_stride >= N.
+ */
+typedef struct {
+    const void* base;
+    long long batch_stride, head_stride, pos_stride, feat_stride;
+} psa_attn_view;
+
+/*
+ * psa_attn_bwd_ex -- psa_attn_bwd on strided layouts.  "Struct
+ * PsaMergeAttnRuntimeOp" (forward_output_row_stride,
+ * backward_grad_output_row_stride: a buffer's row stride may be rounded up
+ * past the row length so that every row starts on a 16-byte boundary, as TMA
+ * copies need) and the channel-major feature maps of the model around the op.
+ *   packed          [BH, 4, N, qkv_row_stride] dtype, read: rows of d used
+ *                   (section stride N*qkv_row_stride, slice stride 4*N*qkv_row_stride)
+ *   qkv_row_stride  >= head_dim; also the row stride of d_packed
+ *   o_lo, o_hi      [BH, N, o_row_stride] dtype, read; o_row_stride >= head_dim
+ *   lse             [BH, N] fp32, read
+ *   do_lo, do_hi    views (above) of the upstream gradients, read
+ *   d_packed        [BH, 4, N, qkv_row_stride] dtype: the first head_dim
+ *                   elements of every row are OVERWRITTEN, the padding is not
+ *                   touched
+ *   workspace       at least psa_attn_bwd_ex_workspace_bytes(...) bytes
+ *   algo            PSA_ALGO_AUTO, PSA_ALGO_TC (fused tensor-core kernel, bf16)
+ *                   or PSA_ALGO_SIMT; the two-pass mode takes contiguous
+ *                   tensors only (psa_attn_bwd_algo)
+ * Alignment: every pointer 16-byte aligned.  The tensor-core path also needs
+ * every stride other than a unit one to be a multiple of 16 bytes (TMA); the
+ * CUDA-core path needs qkv_row_stride = o_row_stride = head_dim (it gathers
+ * strided dO views into the workspace first).  Violations return
+ * PSA_ERR_ALIGN or PSA_ERR_UNSUPPORTED before anything is launched.
+ * Other arguments, results and errors as psa_attn_bwd_algo.
+ */
+int psa_attn_bwd_ex(const void* packed, long long qkv_row_stride,
+                    const void* o_lo, const void* o_hi, long long o_row_stride,
+                    const float* lse, const psa_attn_view* do_lo, const psa_attn_view* do_hi,
+                    void* d_packed, void* workspace, size_t workspace_bytes,
+                    int B, int heads, int N, int head_dim, float scale,
+                    int dtype, int algo, void* stream);
+
+/* Workspace bytes psa_attn_bwd_ex needs (0 for an empty or invalid problem). */
+size_t psa_attn_bwd_ex_workspace_bytes(const psa_attn_view* do_lo, const psa_attn_view* do_hi,
+                                       int B, int heads, int N, int head_dim, int dtype, int algo);
+
+/*
+ * psa_merge_bwd -- the backward of the PSA attention merge alone
+ * ("Struct PsaMergeAttnRuntimeOp", pack_backward_args: d_merged, d_lo, d_hi,
+ * c, H, W, num_heads; backward_grid: one block per (batch*head, position)).
+ * The merged tensor is [B, c, H, W], c = 2 * heads * head_dim, N = H * W;
+ * its channels hold the lo outputs of every head in the low half and the hi
+ * outputs in the high half, head-major in each half (a reading: the pages
+ * name the arguments, not the order):
+ *   d_lo[b*heads + h, n, j] = d_merged[b, h*head_dim + j, n]
+ *   d_hi[b*heads + h, n, j] = d_merged[b, heads*head_dim + h*head_dim + j, n]
+ *   d_merged  [B, c, H, W] dtype, read;  d_lo, d_hi  [B*heads, N, d] dtype, written
+ */
+int psa_merge_bwd(const void* d_merged, void* d_lo, void* d_hi, int B, int heads, int H, int W,
+                  int head_dim, int dtype, void* stream);
+
+/*
+ * psa_merge_attn_bwd -- the merge's backward fused into the attention
+ * backward: the kernels read dO_lo and dO_hi straight out of d_merged (the
+ * views of psa_merge_bwd's mapping), so d_lo / d_hi are never written.
+ * Arguments as psa_attn_bwd, with d_merged [B, 2*heads*head_dim, H, W] in
+ * place of do_lo / do_hi and N = H * W; the workspace is
+ * psa_merge_attn_bwd_workspace_bytes(...) bytes.  The tensor-core path needs
+ * H * W a multiple of 8 (rows of d_merged 16-byte aligned).
+ */
+int psa_merge_attn_bwd(const void* packed, const void* o_lo, const void* o_hi, const float* lse,
+                       const void* d_merged, void* d_packed, void* workspace, size_t workspace_bytes,
+                       int B, int heads, int H, int W, int head_dim, float scale,
+                       int dtype, int algo, void* stream);
+size_t psa_merge_attn_bwd_workspace_bytes(int B, int heads, int H, int W, int head_dim, int dtype, int algo);
+
+/*
  * psa_attn_bwd_noalloc -- the backward for callers that cannot allocate device
  * memory.  (The pages have no counterpart of this entry point; it is a
  * convenience of this library.)

@@ -22,6 +22,17 @@ PSA_ERR_WORKSPACE, PSA_ERR_CUDA, PSA_ERR_TIMEOUT = -4, -5, -6
 PSA_ALGO_AUTO, PSA_ALGO_SIMT, PSA_ALGO_TC, PSA_ALGO_TC_2PASS = 0, 1, 2, 3
 
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_ll = ctypes.c_longlong
+
+
+class psa_attn_view(ctypes.Structure):
+    """A strided view of a [B, heads, N, d] tensor (strides in elements), as in
+    include/psa_attn.h."""
+    _fields_ = [("base", ctypes.c_void_p), ("batch_stride", ctypes.c_longlong), ("head_stride", ctypes.c_longlong),
+                ("pos_stride", ctypes.c_longlong), ("feat_stride", ctypes.c_longlong)]
+
+
+_vw = ctypes.POINTER(psa_attn_view)
 _SIGS = {
     "psa_attn_fwd": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp], _i),
     "psa_attn_fwd_algo": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
@@ -41,6 +52,11 @@ _SIGS = {
     "psa_attn_profile_slot_name": ([_i], ctypes.c_char_p),
     "psa_attn_last_error": ([], ctypes.c_char_p),
     "psa_attn_version": ([], _i),
+    "psa_attn_bwd_ex": ([_vp, _ll, _vp, _vp, _ll, _vp, _vw, _vw, _vp, _vp, _sz, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
+    "psa_attn_bwd_ex_workspace_bytes": ([_vw, _vw, _i, _i, _i, _i, _i, _i], _sz),
+    "psa_merge_bwd": ([_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp], _i),
+    "psa_merge_attn_bwd": ([_vp] * 6 + [_vp, _sz, _i, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
+    "psa_merge_attn_bwd_workspace_bytes": ([_i] * 7, _sz),
 }
 
 _lock = threading.Lock()
@@ -75,7 +91,7 @@ def header_functions() -> list[str]:
     with open(HEADER) as f:
         text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(psa_attn_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(psa_\w+)\s*\(", text)))
 
 
 def _ptr(x) -> int | None:
@@ -285,3 +301,92 @@ class HostBwd:
         psa_attn_bwd_host(packed, o_lo, o_hi, lse, do_lo, do_hi, out, self.buf, self.buf_bytes, BH, 1, N, d,
                           scale, dtype=self.dtype, algo=self.algo, chunks=self.chunks, stream=stream)
         return out
+
+
+# ----------------------------------------------------------------- strided layouts and the merge
+def view_of(t) -> psa_attn_view:
+    """psa_attn_view of a 4-D torch tensor [B, heads, N, d] with any strides."""
+    assert t.dim() == 4
+    sb, sh, sn, sj = t.stride()
+    return psa_attn_view(t.data_ptr(), sb, sh, sn, sj)
+
+
+def psa_attn_bwd_ex(packed, qkv_row_stride, o_lo, o_hi, o_row_stride, lse, do_lo: psa_attn_view,
+                    do_hi: psa_attn_view, d_packed, workspace, workspace_bytes, B, heads, N, head_dim, scale,
+                    dtype, algo=PSA_ALGO_AUTO, stream=None, check=True) -> int:
+    rc = lib().psa_attn_bwd_ex(_ptr(packed), int(qkv_row_stride), _ptr(o_lo), _ptr(o_hi), int(o_row_stride),
+                               _ptr(lse), ctypes.byref(do_lo), ctypes.byref(do_hi), _ptr(d_packed), _ptr(workspace),
+                               int(workspace_bytes), B, heads, N, head_dim, float(scale), dtype, algo,
+                               _stream(stream))
+    return _check(rc) if check else rc
+
+
+def psa_attn_bwd_ex_workspace_bytes(do_lo: psa_attn_view, do_hi: psa_attn_view, B, heads, N, head_dim, dtype,
+                                    algo=PSA_ALGO_AUTO) -> int:
+    return int(lib().psa_attn_bwd_ex_workspace_bytes(ctypes.byref(do_lo), ctypes.byref(do_hi), B, heads, N,
+                                                     head_dim, dtype, algo))
+
+
+def psa_merge_bwd(d_merged, d_lo, d_hi, B, heads, H, W, head_dim, dtype, stream=None, check=True) -> int:
+    rc = lib().psa_merge_bwd(_ptr(d_merged), _ptr(d_lo), _ptr(d_hi), B, heads, H, W, head_dim, dtype,
+                             _stream(stream))
+    return _check(rc) if check else rc
+
+
+def psa_merge_attn_bwd(packed, o_lo, o_hi, lse, d_merged, d_packed, workspace, workspace_bytes, B, heads, H, W,
+                       head_dim, scale, dtype, algo=PSA_ALGO_AUTO, stream=None, check=True) -> int:
+    rc = lib().psa_merge_attn_bwd(_ptr(packed), _ptr(o_lo), _ptr(o_hi), _ptr(lse), _ptr(d_merged), _ptr(d_packed),
+                                  _ptr(workspace), int(workspace_bytes), B, heads, H, W, head_dim, float(scale),
+                                  dtype, algo, _stream(stream))
+    return _check(rc) if check else rc
+
+
+def psa_merge_attn_bwd_workspace_bytes(B, heads, H, W, head_dim, dtype, algo=PSA_ALGO_AUTO) -> int:
+    return int(lib().psa_merge_attn_bwd_workspace_bytes(B, heads, H, W, head_dim, dtype, algo))
+
+
+def attn_bwd_ex(packed, d, o_lo, o_hi, lse, do_lo4, do_hi4, scale: float, heads: int, d_packed=None,
+                workspace=None, algo=PSA_ALGO_AUTO, stream=None):
+    """psa_attn_bwd_ex on torch tensors: packed [BH, 4, N, ld] (rows of d used),
+    o_lo / o_hi [BH, N, ld_o], do_lo4 / do_hi4 any 4-D [B, heads, N, d] views
+    (their torch strides are passed through).  Returns d_packed, shaped like
+    packed (only the first d elements of each row are written)."""
+    import torch
+    BH, _, N, ld = packed.shape
+    B = BH // heads
+    dt = _dtype_code(packed)
+    if d_packed is None:
+        d_packed = torch.zeros_like(packed)
+    vlo, vhi = view_of(do_lo4), view_of(do_hi4)
+    nbytes = psa_attn_bwd_ex_workspace_bytes(vlo, vhi, B, heads, N, d, dt, algo)
+    ws = (workspace or BwdWorkspace(packed.device)).get(nbytes)
+    psa_attn_bwd_ex(packed, ld, o_lo, o_hi, o_lo.shape[-1], lse, vlo, vhi, d_packed, ws, nbytes, B, heads, N, d,
+                    scale, dt, algo=algo, stream=stream)
+    return d_packed
+
+
+def merge_bwd(d_merged, heads: int, d: int, stream=None):
+    """psa_merge_bwd: d_merged [B, 2*heads*d, H, W] -> (dO_lo, dO_hi) [B*heads, H*W, d]."""
+    import torch
+    B, c, H, W = d_merged.shape
+    d_lo = torch.empty((B * heads, H * W, d), dtype=d_merged.dtype, device=d_merged.device)
+    d_hi = torch.empty_like(d_lo)
+    psa_merge_bwd(d_merged, d_lo, d_hi, B, heads, H, W, d, _dtype_code(d_merged), stream=stream)
+    return d_lo, d_hi
+
+
+def merge_attn_bwd(packed, o_lo, o_hi, lse, d_merged, heads: int, scale: float, d_packed=None, workspace=None,
+                   algo=PSA_ALGO_AUTO, stream=None):
+    """psa_merge_attn_bwd: the merge's backward fused into the attention
+    backward; d_merged [B, 2*heads*d, H, W].  Returns d_packed."""
+    import torch
+    BH, _, N, d = packed.shape
+    B, c, H, W = d_merged.shape
+    dt = _dtype_code(packed)
+    if d_packed is None:
+        d_packed = torch.empty_like(packed)
+    nbytes = psa_merge_attn_bwd_workspace_bytes(B, heads, H, W, d, dt, algo)
+    ws = (workspace or BwdWorkspace(packed.device)).get(nbytes)
+    psa_merge_attn_bwd(packed, o_lo, o_hi, lse, d_merged, d_packed, ws, nbytes, B, heads, H, W, d, scale, dt,
+                       algo=algo, stream=stream)
+    return d_packed

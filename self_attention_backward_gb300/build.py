@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "_psa_attn.so")
 BUILD_DIR = os.path.join(PKG, "_build")
-SOURCES = ["psa_attn.cu", "tc_bwd.cu", "tc_fwd.cu", "noalloc.cu", "tc_dq.cu", "tc_pair.cu", "tc_tmap.cu", "host_pipe.cu"]
+SOURCES = ["psa_attn.cu", "tc_bwd.cu", "tc_fwd.cu", "noalloc.cu", "tc_dq.cu", "tc_pair.cu", "tc_tmap.cu", "host_pipe.cu",
+           "merge.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

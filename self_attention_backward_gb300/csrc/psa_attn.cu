@@ -170,6 +170,116 @@ size_t workspace_for(const Shape& s, int dtype, int algo) {
     return 0;
 }
 
+bool view_contiguous(const psa::View& v, int heads, int N, int d) {
+    return v.sJ == 1 && v.sN == d && v.sH == (long long)N * d && v.sB == (long long)heads * N * d;
+}
+
+// Checks a dO view: aligned base, row-major (sJ = 1, sN >= d) or channel-major
+// (sN = 1, sJ >= N), non-negative strides; with `tma`, every non-unit stride a
+// multiple of 16 bytes.
+int check_view(const char* name, const psa_attn_view* v, int N, int d, int esize, bool tma) {
+    if (!v || !v->base) return fail(PSA_ERR_ARG, "%s view is NULL", name);
+    if (!aligned16(v->base)) return fail(PSA_ERR_ALIGN, "%s view base is not 16-byte aligned", name);
+    if (v->batch_stride < 0 || v->head_stride < 0 || v->pos_stride < 0 || v->feat_stride < 0)
+        return fail(PSA_ERR_ARG, "%s view has a negative stride", name);
+    const bool rows = v->feat_stride == 1 && v->pos_stride >= d;
+    const bool chans = v->pos_stride == 1 && v->feat_stride >= N && !rows;
+    if (!rows && !chans)
+        return fail(PSA_ERR_UNSUPPORTED, "%s view is neither row-major (feat_stride 1, pos_stride >= d) nor "
+                    "channel-major (pos_stride 1, feat_stride >= N)", name);
+    if (tma) {
+        const long long outer = rows ? v->pos_stride : v->feat_stride;
+        for (long long st : {outer, v->head_stride, v->batch_stride})
+            if ((st * esize) % 16 != 0)
+                return fail(PSA_ERR_ALIGN, "%s view: strides must be multiples of 16 bytes on the tensor-core path",
+                            name);
+    }
+    return PSA_OK;
+}
+
+psa::View to_view(const psa_attn_view* v) {
+    return psa::View{v->base, v->batch_stride, v->head_stride, v->pos_stride, v->feat_stride};
+}
+
+// Workspace of psa_attn_bwd_ex: the kernel family's own, then (CUDA-core path
+// with non-contiguous dO) room for the gathered dO_lo and dO_hi.
+size_t ex_workspace(const Shape& s, int heads, int dtype, int algo, bool gather) {
+    if (s.empty) return 0;
+    algo = resolve_algo(dtype, s.d, algo);
+    size_t w = (workspace_for(s, dtype, algo) + 255) & ~size_t(255);
+    if (algo == PSA_ALGO_SIMT && gather)
+        w += 2 * (((size_t)s.BH * s.N * s.d * (dtype == PSA_F32 ? 4 : 2) + 255) & ~size_t(255));
+    (void)heads;
+    return w;
+}
+
+// psa_attn_bwd_ex with views already built (also behind psa_merge_attn_bwd).
+int bwd_ex(const void* packed, long long ldq, const void* o_lo, const void* o_hi, long long ldo, const float* lse,
+           const psa_attn_view* do_lo, const psa_attn_view* do_hi, void* d_packed, void* workspace,
+           size_t workspace_bytes, int B, int heads, int N, int head_dim, float scale, int dtype, int algo,
+           void* stream) {
+    Shape s;
+    int rc = check_shape(B, heads, N, head_dim, scale, dtype, &s);
+    if (rc) return rc;
+    if (!is_bwd_algo(algo)) return fail(PSA_ERR_ARG, "algo %d is not a psa_algo", algo);
+    algo = resolve_algo(dtype, head_dim, algo);
+    if (algo == PSA_ALGO_TC_2PASS)
+        return fail(PSA_ERR_UNSUPPORTED, "the two-pass mode takes contiguous tensors (psa_attn_bwd_algo)");
+    if (algo == PSA_ALGO_TC && !psa::tc_supported(dtype, head_dim))
+        return fail(PSA_ERR_UNSUPPORTED, "no tensor-core backward for dtype %d, head_dim %d", dtype, head_dim);
+    const bool tc = algo == PSA_ALGO_TC;
+    const int esize = dtype == PSA_F32 ? 4 : 2;
+    if (ldq < head_dim || ldo < head_dim)
+        return fail(PSA_ERR_ARG, "row strides must be >= head_dim (qkv %lld, o %lld)", ldq, ldo);
+    if (tc && ((ldq * esize) % 16 || (ldo * esize) % 16))
+        return fail(PSA_ERR_ALIGN, "row strides must be multiples of 16 bytes on the tensor-core path");
+    if (!tc && (ldq != head_dim || ldo != head_dim))
+        return fail(PSA_ERR_UNSUPPORTED, "the CUDA-core path takes packed and O rows of head_dim elements");
+    if (s.empty) return ok();
+    rc = check_view("do_lo", do_lo, N, head_dim, esize, tc);
+    if (!rc) rc = check_view("do_hi", do_hi, N, head_dim, esize, tc);
+    if (rc) return rc;
+    if ((do_lo->pos_stride == 1) != (do_hi->pos_stride == 1))
+        return fail(PSA_ERR_UNSUPPORTED, "do_lo and do_hi must both be row-major or both channel-major");
+    rc = check_ptrs({{"packed", packed}, {"o_lo", o_lo}, {"o_hi", o_hi}, {"lse", lse}, {"d_packed", d_packed}});
+    if (rc) return rc;
+    const psa::View vlo = to_view(do_lo), vhi = to_view(do_hi);
+    const bool gather = !view_contiguous(vlo, heads, N, head_dim) || !view_contiguous(vhi, heads, N, head_dim);
+    const size_t need = ex_workspace(s, heads, dtype, algo, gather);
+    if (workspace_bytes < need) return fail(PSA_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+    if (need > 0) {
+        rc = check_ptrs({{"workspace", workspace}});
+        if (rc) return rc == PSA_ERR_ARG ? fail(PSA_ERR_WORKSPACE, "workspace is NULL") : rc;
+    }
+    psa::BwdArgs a{packed, o_lo, o_hi, lse, vlo.base, vhi.base, d_packed, workspace, workspace_bytes,
+                   s.BH, N, head_dim, scale, dtype, (cudaStream_t)stream};
+    a.heads = heads;
+    a.ld_qkv = ldq;
+    a.ld_o = ldo;
+    a.views = true;
+    a.vlo = vlo;
+    a.vhi = vhi;
+    std::string err;
+    if (tc) {
+        rc = psa::tc_bwd_launch(a, &err);
+        return rc ? fail(rc, "%s", err.c_str()) : ok();
+    }
+    // CUDA-core path: contiguous dO, gathered into the workspace when needed
+    if (gather) {
+        const size_t base = (workspace_for(s, dtype, algo) + 255) & ~size_t(255);
+        const size_t one = ((size_t)s.BH * N * head_dim * esize + 255) & ~size_t(255);
+        char* g = static_cast<char*>(workspace) + base;
+        rc = psa::gather_view_launch(vlo, g, s.BH, heads, N, head_dim, esize, (cudaStream_t)stream, &err);
+        if (!rc) rc = psa::gather_view_launch(vhi, g + one, s.BH, heads, N, head_dim, esize, (cudaStream_t)stream, &err);
+        if (rc) return fail(rc, "%s", err.c_str());
+        a.do_lo = g;
+        a.do_hi = g + one;
+    }
+    a.views = false;
+    rc = PSA_DISPATCH(dtype, head_dim, launch_bwd_simt, a);
+    return rc ? rc : ok();
+}
+
 }  // namespace
 
 int psa::set_last_error(int code, const std::string& msg) {
@@ -266,6 +376,49 @@ int psa_attn_bwd(const void* packed, const void* o_lo, const void* o_hi, const f
                  int head_dim, float scale, int dtype, void* stream) {
     return psa_attn_bwd_algo(packed, o_lo, o_hi, lse, do_lo, do_hi, d_packed, workspace, workspace_bytes, B, heads,
                              N, head_dim, scale, dtype, PSA_ALGO_AUTO, stream);
+}
+
+int psa_attn_bwd_ex(const void* packed, long long qkv_row_stride, const void* o_lo, const void* o_hi,
+                    long long o_row_stride, const float* lse, const psa_attn_view* do_lo,
+                    const psa_attn_view* do_hi, void* d_packed, void* workspace, size_t workspace_bytes, int B,
+                    int heads, int N, int head_dim, float scale, int dtype, int algo, void* stream) {
+    return bwd_ex(packed, qkv_row_stride, o_lo, o_hi, o_row_stride, lse, do_lo, do_hi, d_packed, workspace,
+                  workspace_bytes, B, heads, N, head_dim, scale, dtype, algo, stream);
+}
+
+size_t psa_attn_bwd_ex_workspace_bytes(const psa_attn_view* do_lo, const psa_attn_view* do_hi, int B, int heads,
+                                       int N, int head_dim, int dtype, int algo) {
+    Shape s;
+    const std::string keep = g_last_error;
+    const int rc = check_shape(B, heads, N, head_dim, 1.0f, dtype, &s);
+    g_last_error = keep;
+    if (rc || !is_bwd_algo(algo) || !do_lo || !do_hi) return 0;
+    const bool gather = !view_contiguous(to_view(do_lo), heads, N, head_dim) ||
+                        !view_contiguous(to_view(do_hi), heads, N, head_dim);
+    return ex_workspace(s, heads, dtype, algo, gather);
+}
+
+size_t psa_merge_attn_bwd_workspace_bytes(int B, int heads, int H, int W, int head_dim, int dtype, int algo) {
+    if ((long long)H * W > 0x7fffffffll || H < 0 || W < 0) return 0;
+    Shape s;
+    const std::string keep = g_last_error;
+    const int rc = check_shape(B, heads, H * W, head_dim, 1.0f, dtype, &s);
+    g_last_error = keep;
+    if (rc || !is_bwd_algo(algo)) return 0;
+    return ex_workspace(s, heads, dtype, algo, true);
+}
+
+int psa_merge_attn_bwd(const void* packed, const void* o_lo, const void* o_hi, const float* lse,
+                       const void* d_merged, void* d_packed, void* workspace, size_t workspace_bytes, int B,
+                       int heads, int H, int W, int head_dim, float scale, int dtype, int algo, void* stream) {
+    if (H < 0 || W < 0 || (long long)H * W > 0x7fffffffll) return fail(PSA_ERR_ARG, "bad H, W (%d, %d)", H, W);
+    if (!d_merged && B > 0 && heads > 0 && H > 0 && W > 0) return fail(PSA_ERR_ARG, "d_merged is NULL");
+    const int N = H * W;
+    psa::View lo{}, hi{};
+    if (d_merged) psa::merged_views(d_merged, heads, N, head_dim, dtype == PSA_F32 ? 4 : 2, &lo, &hi);
+    const psa_attn_view vlo{lo.base, lo.sB, lo.sH, lo.sN, lo.sJ}, vhi{hi.base, hi.sB, hi.sH, hi.sN, hi.sJ};
+    return bwd_ex(packed, head_dim, o_lo, o_hi, head_dim, lse, &vlo, &vhi, d_packed, workspace, workspace_bytes, B,
+                  heads, N, head_dim, scale, dtype, algo, stream);
 }
 
 int psa_attn_profile_enable(int on) {

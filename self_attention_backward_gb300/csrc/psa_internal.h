@@ -8,6 +8,13 @@
 
 namespace psa {
 
+// A strided view of a [B, heads, N, d] tensor: element (b, h, n, j) at
+// base + b*sB + h*sH + n*sN + j*sJ (elements).
+struct View {
+    const void* base;
+    long long sB, sH, sN, sJ;
+};
+
 struct BwdArgs {
     const void* packed;
     const void* o_lo;
@@ -24,6 +31,19 @@ struct BwdArgs {
     float scale;
     int dtype;
     cudaStream_t stream;
+    // Layouts (psa_attn_bwd_ex); the defaults describe contiguous tensors.
+    int heads = 1;               // B = BH / heads, for the views' batch / head strides
+    long long ld_qkv = 0;        // row stride of packed and d_packed (0: d)
+    long long ld_o = 0;          // row stride of o_lo, o_hi (0: d)
+    bool views = false;          // true: dO_lo / dO_hi are read through vlo / vhi
+    View vlo{}, vhi{};
+    long long qkv_ld() const { return ld_qkv ? ld_qkv : d; }
+    long long o_ld() const { return ld_o ? ld_o : d; }
+    // dO_lo / dO_hi as views (a contiguous [BH, N, d] tensor when !views)
+    View do_view(int which) const {
+        if (views) return which ? vhi : vlo;
+        return View{which ? do_hi : do_lo, (long long)heads * N * d, (long long)N * d, d, 1};
+    }
 };
 
 // Kernel timing scope (psa_attn_profile_enable): records a CUDA event pair
@@ -75,6 +95,13 @@ int tc_wait_selftest(cudaStream_t stream, std::string* err);
 // Reads and clears the device-side timeout flag of the tensor-core kernels
 // (call after the stream is synchronised).  Returns 1 if a wait gave up.
 int tc_take_device_error(std::string* err);
+
+// Gathers a strided view of a [BH, N, d] tensor (elements of `esize` bytes,
+// 2 or 4) into a contiguous [BH, N, d] buffer on `stream` (merge.cu).
+int gather_view_launch(const View& v, void* dst, long long BH, int heads, int N, int d, int esize,
+                       cudaStream_t stream, std::string* err);
+// The views of dO_lo / dO_hi inside a merged [B, 2*heads*d, N] tensor (merge.cu).
+void merged_views(const void* d_merged, int heads, int N, int d, int esize, View* lo, View* hi);
 
 // Sets the calling thread's psa_attn_last_error() message ("" clears it) and
 // returns `code`; for entry points defined outside psa_attn.cu.

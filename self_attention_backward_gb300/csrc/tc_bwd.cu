@@ -187,11 +187,15 @@ __device__ __forceinline__ void softmax_vals(const uint32_t (&sr)[32], const uin
 }
 
 // ---------------------------------------------------------------- main kernel
-template <int D>
+// CM: dO_lo / dO_hi come as channel-major [d, N] blocks (4-D maps over
+// [B][heads][d][N]); else as rows (4-D maps over [B][heads][N][d]).  The
+// stage's dO tiles then hold [d][64 queries] (128-byte rows), which the dP^T
+// product reads MN-major and the dV product K-major.
+template <int D, bool CM>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_do_lo, const __grid_constant__ CUtensorMap tm_do_hi,
-                const __grid_constant__ CUtensorMap tm_dq, const float4* __restrict__ stats, float* __restrict__ dq_acc, bf16* __restrict__ d_packed, int N,
+                const __grid_constant__ CUtensorMap tm_dq, int heads, long long ldq, const float4* __restrict__ stats, float* __restrict__ dq_acc, bf16* __restrict__ d_packed, int N,
                 int nkt, float scale, float scale_log2, int nfull, int tail_f, float* __restrict__ dkv_part) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -281,8 +285,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 mbar_arrive_expect_tx(sy.bar(F_QF + s), 3 * C::QTILE + 512);
                 const int q0 = (ubase + u) * C::BS;
                 tma_load_3d(st, &tm_q, 0, q0, bh * 4 + 0, sy.bar(F_QF + s));
-                tma_load_3d(st + C::QTILE, &tm_do_lo, 0, q0, bh, sy.bar(F_QF + s));
-                tma_load_3d(st + 2 * C::QTILE, &tm_do_hi, 0, q0, bh, sy.bar(F_QF + s));
+                const int hh = bh % heads, bb = bh / heads;
+                tma_load_4d(st + C::QTILE, &tm_do_lo, CM ? q0 : 0, CM ? 0 : q0, hh, bb, sy.bar(F_QF + s));
+                tma_load_4d(st + 2 * C::QTILE, &tm_do_hi, CM ? q0 : 0, CM ? 0 : q0, hh, bb, sy.bar(F_QF + s));
                 bulk_load(sb + C::OFF_ST + s * 512, st_slice + (size_t)(ubase + u) * 32, 512, sy.bar(F_QF + s));
             }
 #pragma unroll
@@ -309,8 +314,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         const int par = warp == 1 ? 0 : 1;
         constexpr int USTEP = C::TWO_ISSUERS ? 2 : 1;
         if (lane == 0) {
-            constexpr uint32_t ID_S = idesc_bf16(128, 64, 0, 0);     // S^T, dP^T: 64 queries
-            constexpr uint32_t ID_DV = idesc_bf16(128, 2 * D, 0, 1); // dV_lo | dV_hi: B MN-major
+            constexpr uint32_t ID_S = idesc_bf16(128, 64, 0, 0);     // S^T: 64 queries
+            // dP^T: B = dO rows (K-major), or MN-major from channel-major tiles
+            constexpr uint32_t ID_DP = idesc_bf16(128, 64, 0, CM ? 1 : 0);
+            // dV_lo | dV_hi: B MN-major (rows), or K-major from channel-major tiles
+            constexpr uint32_t ID_DV = idesc_bf16(128, 2 * D, 0, CM ? 0 : 1);
             constexpr uint32_t ID_DK = idesc_bf16(128, D, 0, 1);     // dK: A K-major, B MN-major
             constexpr uint32_t SBO = 8 * C::ROWB;
             constexpr uint32_t KSTEP = (16 * C::ROWB) >> 4;          // 16 rows, in descriptor address units
@@ -321,6 +329,13 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             const uint64_t dStage0 = smem_desc(sb + C::OFF_STAGE, 16, SBO, C::SW);
             const uint64_t dStage0mn = smem_desc(sb + C::OFF_STAGE + C::QTILE, C::QTILE, SBO, C::SW);
             constexpr uint32_t STAGE_U = C::STAGE >> 4, QTILE_U = C::QTILE >> 4;
+            // channel-major dO tiles: [D features][64 queries], 128-byte rows,
+            // 128B swizzle.  dP^T reads one as B MN-major (8 feature rows per
+            // 1024-byte atom, a K-step of 16 features = 2048 bytes); dV reads the
+            // lo and hi tiles, adjacent, as one K-major B of 2D rows (a K-step of
+            // 16 queries = 32 bytes inside the row)
+            const uint64_t dDoCm = smem_desc(sb + C::OFF_STAGE + C::QTILE, 8192, 1024, 2);
+            const uint64_t dDvCm = smem_desc(sb + C::OFF_STAGE + C::QTILE, 16, 1024, 2);
 
             // S^T(u) and dP^T(u) into the two halves of TMEM buffer u % NB, each with
             // its own barrier.  Their Q/dO stage is known to be loaded: the prologue
@@ -334,22 +349,33 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 mma_commit(sy.bar(F_SFS + u % (2 * C::NB)));
             };
             auto issue_dp = [&](int u) {
-                const uint64_t dQs = dStage0 + STAGE_U * (u % C::NST);
                 const uint32_t tDP = tmem + 128u * (u % C::NB) + 64;
+                if constexpr (CM) {
+                    const uint64_t dLo = dDoCm + STAGE_U * (u % C::NST);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16_ss(tDP, dVL + 2 * kk, dQs + QTILE_U + 2 * kk, ID_S, kk);
+                    for (int kk = 0; kk < D / 16; ++kk) mma_bf16_ss(tDP, dVL + 2 * kk, dLo + 128 * kk, ID_DP, kk);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16_ss(tDP, dVH + 2 * kk, dQs + 2 * QTILE_U + 2 * kk, ID_S, 1);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_bf16_ss(tDP, dVH + 2 * kk, dLo + QTILE_U + 128 * kk, ID_DP, 1);
+                } else {
+                    const uint64_t dQs = dStage0 + STAGE_U * (u % C::NST);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_bf16_ss(tDP, dVL + 2 * kk, dQs + QTILE_U + 2 * kk, ID_DP, kk);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_bf16_ss(tDP, dVH + 2 * kk, dQs + 2 * QTILE_U + 2 * kk, ID_DP, 1);
+                }
                 mma_commit(sy.bar(F_SFD + u % (2 * C::NB)));
             };
             // dV of sub-tile u (A = P^T from the S half, 64 queries = 4 k-steps)
             auto issue_dv = [&](int u) {
-                const uint64_t dGmn = dStage0mn + STAGE_U * (u % C::NST);   // [dO_lo | dO_hi], MN-major
+                // [dO_lo | dO_hi]: MN-major rows, or K-major channel-major tiles
+                const uint64_t dG = (CM ? dDvCm : dStage0mn) + STAGE_U * (u % C::NST);
+                constexpr uint32_t DV_STEP = CM ? 2u : KSTEP;
 #pragma unroll
                 for (int kk = 0; kk < C::BS / 16; ++kk)
-                    mma_bf16_ts(tmem + C::C_DV, tmem + 128u * (u % C::NB) + 8 * kk, dGmn + KSTEP * kk, ID_DV,
+                    mma_bf16_ts(tmem + C::C_DV, tmem + 128u * (u % C::NB) + 8 * kk, dG + DV_STEP * kk, ID_DV,
                                 (u > 0 || kk > 0) ? 1u : 0u);
             };
             // dK of sub-tile u (A = dS^T from the dP half); then the stage is free
@@ -554,8 +580,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             if (ok) {
                 tc_fence_after();
                 uint32_t v[D];
-                const size_t sec = (size_t)N * D;
-                bf16* out = d_packed + (size_t)bh * 4 * sec + (size_t)(k0 + jl) * D;
+                const size_t sec = (size_t)N * ldq;
+                bf16* out = d_packed + (size_t)bh * 4 * sec + (size_t)(k0 + jl) * ldq;
 #pragma unroll
                 for (int which = 0; which < 3; ++which) {
                     const uint32_t col = which == 0 ? C::C_DK : C::C_DV + (which - 1) * D;
@@ -1044,11 +1070,47 @@ pre_stats_kernel(const bf16* __restrict__ o_lo, const bf16* __restrict__ o_hi, c
     if (row < rows_pad && part == 0 && (i & 1) == 0) stats[row >> 1] = make_float4(nl, nl1, acc, d1);
 }
 
+// The same statistics for strided layouts (psa_attn_bwd_ex): O rows `ldo`
+// elements apart, dO_lo / dO_hi read through views.  One thread per query row;
+// a channel-major dO view makes consecutive threads read consecutive positions.
+template <int D>
+__global__ void __launch_bounds__(256)
+pre_stats_view_kernel(const bf16* __restrict__ o_lo, const bf16* __restrict__ o_hi, long long ldo, View vlo,
+                      View vhi, int heads, const float* __restrict__ lse, float4* __restrict__ stats,
+                      float* __restrict__ dq_acc, long long rows_pad, int N, int npad) {
+    const long long row = (long long)blockIdx.x * 256 + threadIdx.x;
+    const long long bh = row / npad;
+    const int i = (int)(row % npad);
+    const bool valid = row < rows_pad && i < N;
+    float acc = 0.f;
+    if (valid) {
+        const long long b = bh / heads, h = bh % heads;
+        const bf16* gl = static_cast<const bf16*>(vlo.base) + b * vlo.sB + h * vlo.sH + (long long)i * vlo.sN;
+        const bf16* gh = static_cast<const bf16*>(vhi.base) + b * vhi.sB + h * vhi.sH + (long long)i * vhi.sN;
+        const bf16* ol = o_lo + ((size_t)bh * N + i) * ldo;
+        const bf16* oh = o_hi + ((size_t)bh * N + i) * ldo;
+#pragma unroll 8
+        for (int j = 0; j < D; ++j) {
+            acc = fmaf(__bfloat162float(ol[j]), __bfloat162float(gl[j * vlo.sJ]), acc);
+            acc = fmaf(__bfloat162float(oh[j]), __bfloat162float(gh[j * vhi.sJ]), acc);
+        }
+        float4* z = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * N + i) * D);
+#pragma unroll
+        for (int k = 0; k < D / 4; ++k) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float nl = valid ? -lse[(size_t)bh * N + i] * kLog2e : -INFINITY;
+    // the odd row of the pair is the next lane (npad and 256 are even)
+    const float nl1 = __shfl_down_sync(0xffffffffu, nl, 1);
+    const float d1 = __shfl_down_sync(0xffffffffu, acc, 1);
+    if (row < rows_pad && (i & 1) == 0) stats[row >> 1] = make_float4(nl, nl1, acc, d1);
+}
+
 // ---------------------------------------------------------------- dQ = scale * acc -> bf16
 template <int D>
 __global__ void __launch_bounds__(256)
-dq_finalize_kernel(const float* __restrict__ dq_acc, bf16* __restrict__ d_packed, long long rows, int N,
-                   float scale, const float* __restrict__ dkv_part, int nfull, int ntail, int tail_f, int nkt) {
+dq_finalize_kernel(const float* __restrict__ dq_acc, bf16* __restrict__ d_packed, long long ldq, long long rows,
+                   int N, float scale, const float* __restrict__ dkv_part, int nfull, int ntail, int tail_f,
+                   int nkt) {
     constexpr int PPR = D / 8;  // 8-element parts per row
     const long long idx = (long long)blockIdx.x * 256 + threadIdx.x;
     if (idx >= rows * PPR) {
@@ -1076,7 +1138,7 @@ dq_finalize_kernel(const float* __restrict__ dq_acc, bf16* __restrict__ d_packed
         u.y = pack_bf16x2(acc[2] * mul, acc[3] * mul);
         u.z = pack_bf16x2(acc[4] * mul, acc[5] * mul);
         u.w = pack_bf16x2(acc[6] * mul, acc[7] * mul);
-        *reinterpret_cast<uint4*>(d_packed + (((size_t)bh * 4 + 1 + which) * N + key) * D + part * 8) = u;
+        *reinterpret_cast<uint4*>(d_packed + (((size_t)bh * 4 + 1 + which) * N + key) * ldq + part * 8) = u;
         return;
     }
     const long long row = idx / PPR;
@@ -1089,7 +1151,7 @@ dq_finalize_kernel(const float* __restrict__ dq_acc, bf16* __restrict__ d_packed
     u.y = pack_bf16x2(a.z * scale, a.w * scale);
     u.z = pack_bf16x2(b.x * scale, b.y * scale);
     u.w = pack_bf16x2(b.z * scale, b.w * scale);
-    *reinterpret_cast<uint4*>(d_packed + ((size_t)bh * 4 * N + i) * D + part * 8) = u;
+    *reinterpret_cast<uint4*>(d_packed + ((size_t)bh * 4 * N + i) * ldq + part * 8) = u;
 }
 
 // ---------------------------------------------------------------- host side
@@ -1124,26 +1186,31 @@ size_t tail_part_bytes(long long BH, int N, int d) {
     return (size_t)pieces * 128 * 3 * (size_t)d * 4;
 }
 
-template <int D>
-int launch(const BwdArgs& a, std::string* err) {
+template <int D, bool CM>
+int launch_impl(const BwdArgs& a, std::string* err) {
     using M = Cfg<D>;
     // K/V tiles: 128 rows; Q/dO sub-tiles: 64 rows (the byte counts the
     // kernel's barriers expect)
     const long long rows = a.BH * a.N;
     const int npad = (a.N + M::BS - 1) / M::BS * M::BS;
     const long long rows_pad = a.BH * npad;
+    const long long ldq = a.qkv_ld(), ldo = a.o_ld();
     float4* stats = static_cast<float4*>(a.workspace);
     char* ws = static_cast<char*>(a.workspace) + align256((size_t)rows_pad * 8);
     float* dq_acc = reinterpret_cast<float*>(ws);
+    const View vlo = a.do_view(0), vhi = a.do_view(1);
+    const long long nb = a.BH / a.heads;
     // dq_acc in 128-query boxes of min(D, 32) columns (the reduce path uses it at D <= 32)
     CUtensorMap tm_kv, tm_q, tm_lo, tm_hi, tm_dq;
-    if (!encode_bf16_rows(&tm_kv, a.packed, D, a.N, a.BH * 4, M::BM, D, err) ||
-        !encode_bf16_rows(&tm_q, a.packed, D, a.N, a.BH * 4, M::BS, D, err) ||
-        !encode_bf16_rows(&tm_lo, a.do_lo, D, a.N, a.BH, M::BS, D, err) ||
-        !encode_bf16_rows(&tm_hi, a.do_hi, D, a.N, a.BH, M::BS, D, err) ||
+    if (!encode_bf16_rows_ld(&tm_kv, a.packed, D, ldq, a.N, a.BH * 4, M::BM, D, err) ||
+        !encode_bf16_rows_ld(&tm_q, a.packed, D, ldq, a.N, a.BH * 4, M::BS, D, err) ||
+        !(CM ? encode_bf16_4d(&tm_lo, vlo.base, a.N, D, a.heads, nb, vlo.sJ, vlo.sH, vlo.sB, M::BS, D, err)
+             : encode_bf16_4d(&tm_lo, vlo.base, D, a.N, a.heads, nb, vlo.sN, vlo.sH, vlo.sB, D, M::BS, err)) ||
+        !(CM ? encode_bf16_4d(&tm_hi, vhi.base, a.N, D, a.heads, nb, vhi.sJ, vhi.sH, vhi.sB, M::BS, D, err)
+             : encode_bf16_4d(&tm_hi, vhi.base, D, a.N, a.heads, nb, vhi.sN, vhi.sH, vhi.sB, D, M::BS, err)) ||
         !encode_f32_rows(&tm_dq, dq_acc, D, a.N, a.BH, 128, D < 32 ? D : 32, err))
         return PSA_ERR_CUDA;
-    if (!set_max_dynamic_smem((const void*)bwd_main_kernel<D>, M::SMEM, err)) return PSA_ERR_CUDA;
+    if (!set_max_dynamic_smem((const void*)bwd_main_kernel<D, CM>, M::SMEM, err)) return PSA_ERR_CUDA;
     float* dkv_part = reinterpret_cast<float*>(ws + align256((size_t)rows * D * 4));
     const int nkt = (a.N + M::BM - 1) / M::BM;
     const long long units = a.BH * nkt;
@@ -1154,7 +1221,8 @@ int launch(const BwdArgs& a, std::string* err) {
     const TailSplit ts = tail_split(units, a.N, sms);
     const long long nfull = units - ts.ntail;
     const long long grid = nfull + (long long)ts.ntail * ts.f;
-    const long long pre_grid = (rows_pad + 256 / (D / 8) - 1) / (256 / (D / 8));
+    const bool plain = !a.views && ldo == D;   // contiguous O and dO: the vectorised statistics kernel
+    const long long pre_grid = plain ? (rows_pad + 256 / (D / 8) - 1) / (256 / (D / 8)) : (rows_pad + 255) / 256;
     const long long fin_grid = (rows * (D / 8) + (long long)ts.ntail * 128 * 3 * (D / 8) + 255) / 256;
     if (grid > 0x7fffffffll || pre_grid > 0x7fffffffll || fin_grid > 0x7fffffffll) {
         *err = "grid too large";
@@ -1162,24 +1230,28 @@ int launch(const BwdArgs& a, std::string* err) {
     }
     const bf16* o_lo = static_cast<const bf16*>(a.o_lo);
     const bf16* o_hi = static_cast<const bf16*>(a.o_hi);
-    const bf16* do_lo = static_cast<const bf16*>(a.do_lo);
-    const bf16* do_hi = static_cast<const bf16*>(a.do_hi);
     bf16* dp = static_cast<bf16*>(a.d_packed);
     {
         ProfScope prof(kSlotPre, a.stream);
-        pre_stats_kernel<D><<<(unsigned)pre_grid, 256, 0, a.stream>>>(o_lo, o_hi, do_lo, do_hi, a.lse, stats, dq_acc,
-                                                                      rows_pad, a.N, npad);
+        if (plain)
+            pre_stats_kernel<D><<<(unsigned)pre_grid, 256, 0, a.stream>>>(
+                o_lo, o_hi, static_cast<const bf16*>(vlo.base), static_cast<const bf16*>(vhi.base), a.lse, stats,
+                dq_acc, rows_pad, a.N, npad);
+        else
+            pre_stats_view_kernel<D><<<(unsigned)pre_grid, 256, 0, a.stream>>>(o_lo, o_hi, ldo, vlo, vhi, a.heads,
+                                                                               a.lse, stats, dq_acc, rows_pad, a.N,
+                                                                               npad);
     }
     {
         ProfScope prof(kSlotMain, a.stream);
-        bwd_main_kernel<D><<<(unsigned)grid, M::THREADS, M::SMEM, a.stream>>>(
-            tm_kv, tm_q, tm_lo, tm_hi, tm_dq, stats, dq_acc, dp, a.N, nkt, a.scale, a.scale * kLog2e, (int)nfull,
-            ts.f, dkv_part);
+        bwd_main_kernel<D, CM><<<(unsigned)grid, M::THREADS, M::SMEM, a.stream>>>(
+            tm_kv, tm_q, tm_lo, tm_hi, tm_dq, a.heads, ldq, stats, dq_acc, dp, a.N, nkt, a.scale, a.scale * kLog2e,
+            (int)nfull, ts.f, dkv_part);
     }
     {
         ProfScope prof(kSlotDq, a.stream);
-        dq_finalize_kernel<D><<<(unsigned)fin_grid, 256, 0, a.stream>>>(dq_acc, dp, rows, a.N, a.scale, dkv_part,
-                                                                        (int)nfull, ts.ntail, ts.f, nkt);
+        dq_finalize_kernel<D><<<(unsigned)fin_grid, 256, 0, a.stream>>>(dq_acc, dp, ldq, rows, a.N, a.scale,
+                                                                        dkv_part, (int)nfull, ts.ntail, ts.f, nkt);
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -1189,8 +1261,13 @@ int launch(const BwdArgs& a, std::string* err) {
     return PSA_OK;
 }
 
-// Two-pass mode: D, then the key-outer dK/dV pass, then the query-outer dQ
-// pass (tc_dq.cu).  Every output element is summed in one fixed order.
+// dO read as rows, or as channel-major [d, N] blocks (position stride 1).
+template <int D>
+int launch(const BwdArgs& a, std::string* err) {
+    const View v = a.do_view(0);
+    return (v.sN == 1 && v.sJ != 1) ? launch_impl<D, true>(a, err) : launch_impl<D, false>(a, err);
+}
+
 template <int D>
 int launch_two_pass(const BwdArgs& a, std::string* err) {
     using M = CfgS<D>;

@@ -30,11 +30,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder(std::string* err) {
 }  // namespace
 
 static bool encode_rows(CUtensorMap* map, CUtensorMapDataType type, int esize, const void* base, int D, int N, long long Z,
-                 int rows, int cols, std::string* err) {
+                 int rows, int cols, std::string* err, long long ld = 0) {
     auto enc = encoder(err);
     if (!enc) return false;
+    if (ld == 0) ld = D;
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)Z};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * esize, (cuuint64_t)N * D * esize};
+    const cuuint64_t strides[2] = {(cuuint64_t)ld * esize, (cuuint64_t)N * ld * esize};
     const cuuint32_t box[3] = {(cuuint32_t)cols, (cuuint32_t)rows, 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     const int rowb = cols * esize;
@@ -59,6 +60,34 @@ bool encode_bf16_rows(CUtensorMap* map, const void* base, int D, int N, long lon
 bool encode_f32_rows(CUtensorMap* map, const void* base, int D, int N, long long Z, int rows, int cols,
                      std::string* err) {
     return encode_rows(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, D, N, Z, rows, cols, err);
+}
+
+bool encode_bf16_rows_ld(CUtensorMap* map, const void* base, int D, long long ld, int N, long long Z, int rows,
+                         int cols, std::string* err) {
+    return encode_rows(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, D, N, Z, rows, cols, err, ld);
+}
+
+bool encode_bf16_4d(CUtensorMap* map, const void* base, long long inner, long long outer, long long heads,
+                    long long B, long long s_outer, long long s_head, long long s_batch, int box_inner,
+                    int box_outer, std::string* err) {
+    auto enc = encoder(err);
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)outer, (cuuint64_t)heads, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)s_outer * 2, (cuuint64_t)s_head * 2, (cuuint64_t)s_batch * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer, 1u, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const int rowb = box_inner * 2;
+    const CUtensorMapSwizzle sw = rowb == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : rowb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                               : CU_TENSOR_MAP_SWIZZLE_32B;
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        *err = "cuTensorMapEncodeTiled (4-d) failed (" + std::to_string((int)r) + ")";
+        return false;
+    }
+    return true;
 }
 
 bool set_max_dynamic_smem(const void* kernel, int bytes, std::string* err) {

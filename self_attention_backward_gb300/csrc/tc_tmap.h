@@ -15,6 +15,16 @@ namespace psa {
 // out of bounds and read as zeros.  Returns false and sets *err on failure.
 bool encode_bf16_rows(CUtensorMap* map, const void* base, int D, int N, long long Z, int rows, int cols,
                       std::string* err);
+// The same with rows `ld` elements apart (ld >= D, ld * 2 a multiple of 16).
+bool encode_bf16_rows_ld(CUtensorMap* map, const void* base, int D, long long ld, int N, long long Z, int rows,
+                         int cols, std::string* err);
+// 4-D map over a bf16 tensor [B][heads][outer][inner] with element strides
+// 1, s_outer, s_head, s_batch (each but the first a multiple of 8), copied in
+// boxes of box_inner x box_outer (box_inner * 2 bytes = 32, 64 or 128, the
+// swizzle span); elements past the extents read as zeros.
+bool encode_bf16_4d(CUtensorMap* map, const void* base, long long inner, long long outer, long long heads,
+                    long long B, long long s_outer, long long s_head, long long s_batch, int box_inner,
+                    int box_outer, std::string* err);
 
 // The same over an fp32 tensor of Z slices of [N, D] rows, boxes of `rows` x
 // `cols` (cols * 4 bytes a multiple of 16, at most 128; the swizzle span is the
