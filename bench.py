@@ -388,7 +388,7 @@ def run_ours(args, w):
             del b2
         line["other_workloads"] = sec
 
-    if rank == 0:
+    if rank == 0 and not args.no_extras:
         line["e2e"] = run_e2e(w, args, device, algo)
         line["forward"] = time_forward(w, bufs, flush, args.steps)
         line["merge"] = time_merge(w, bufs, flush, args.steps, algo)
@@ -509,6 +509,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the end-to-end, forward and merge legs (profiling runs)")
     args = ap.parse_args(argv)
     from self_attention_backward_gb300.inputs import WORKLOADS
     w = WORKLOADS[args.workload]

@@ -38,7 +38,7 @@ KERNEL_METRICS = ["gpu__time_duration.sum", "dram__bytes_read.sum", "dram__bytes
                   "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active"]
 # the backward kernels of each family, by function name, in launch order
 FAMILY_KERNELS = {
-    "tc": ["pre_kernel", "bwd_main_kernel", "dq_finalize_kernel"],
+    "tc": ["pre_stats_kernel", "bwd_main_kernel", "dq_finalize_kernel"],
     "tc2": ["pre_kernel", "bwd_kv_pair_kernel", "bwd_q_pair_kernel", "bwd_dkdv_kernel", "dq_kernel"],
     "simt": ["pre_kernel", "dkdv_kernel", "dq_kernel"],
 }
@@ -170,7 +170,8 @@ def measured_hbm_gbs() -> float:
 # the library's profiling slot (bench.py's kernels_ms_per_step keys) of each kernel
 SLOT_OF = {"bwd_main_kernel": "bwd_main", "bwd_kv_pair_kernel": "bwd_main", "bwd_dkdv_kernel": "bwd_main",
            "dkdv_kernel": "bwd_main", "bwd_q_pair_kernel": "bwd_dq", "dq_kernel": "bwd_dq",
-           "dq_finalize_kernel": "bwd_dq", "pre_kernel": "bwd_pre"}
+           "dq_finalize_kernel": "bwd_dq", "pre_kernel": "bwd_pre", "pre_stats_kernel": "bwd_pre",
+           "pre_stats_view_kernel": "bwd_pre"}
 
 
 def record_traffic(items, workload: str, algo: str, path=None) -> dict:
@@ -217,7 +218,7 @@ def kernel_capture_cmd(name: str, csv_path: str, bench_cmd) -> list:
 def run(out_dir: str, algo: str, workload: str | None, record: bool = False) -> int:
     os.makedirs(out_dir, exist_ok=True)
     bench = [sys.executable, "bench.py", "--steps", "2", "--warmup", str(WARMUP_STEPS), "--no-cpu",
-             "--no-secondary", "--algo", algo]
+             "--no-secondary", "--no-extras", "--algo", algo]
     if workload:
         bench += ["--workload", workload]
     # the same command must exit 0 without ncu before ncu runs it
