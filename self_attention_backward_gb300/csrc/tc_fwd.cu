@@ -63,24 +63,36 @@ struct FwdCfg {
     static constexpr int TILE = 128 * ROWB;        // [128, D] bf16 tile (Q)
     static constexpr int KT = BK * ROWB;           // [64, D] bf16 tile (K, V_lo, V_hi)
     static constexpr uint32_t SW = D == 64 ? 2u : D == 32 ? 4u : 6u;
-    static constexpr int NK = 2;                   // K stages
+    // S buffers: three at d <= 32 (3 x 64 columns next to O's 2d fit the CTA's
+    // 256), two at d = 64.  S(j + NSB) is issued after P(j) V_j, so the loop
+    // softmax -> P V -> next S spans NSB tiles: a deeper ring hides more of it.
+    static constexpr int NSB = D == 64 ? 2 : 3;
+    // K stages: as many as S buffers.  The softmax of tile j waits for
+    // K_{j+NSB} in stage (j+NSB) % NK; with NK = NSB that stage last held K_j,
+    // whose copy completed before S(j) ran, so the parity test never meets a
+    // stage two copies behind (with NK = 2 < NSB it could, and pass early).
+    static constexpr int NK = NSB;
     static constexpr int NV = 2;                   // [V_lo | V_hi] stages
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = TILE;             // K stage s at +s*KT
     static constexpr int OFF_V = OFF_K + NK * KT;  // V stage s: V_lo, V_hi at +s*2*KT
     static constexpr int OFF_BAR = OFF_V + NV * 2 * KT;
-    static constexpr int OFF_MISC = OFF_BAR + 128;
+    static constexpr int OFF_MISC = OFF_BAR + 256;
     static constexpr int USED = OFF_MISC + 64;
     static constexpr int SMEM = USED + 1024;       // two CTAs per SM
-    static constexpr uint32_t C_O = 128;           // S buffers at 0 and 64; O_lo | O_hi at 128
+    static constexpr uint32_t C_O = 64 * NSB;      // S buffers at 0, 64 (, 128); O_lo | O_hi at C_O
     static constexpr uint32_t TMEM_COLS = 256;
     static_assert(C_O + 2 * D <= TMEM_COLS, "TMEM budget");
     static_assert(2 * (SMEM + 1024) <= 233472, "two CTAs per SM");
 };
 
-// barriers: Q loaded, O final, S ready[2], P written[2] (softmax done), K full/empty[2],
-// V full/empty[2], O updated (after each P V)
-enum { F_Q = 0, F_ACC = 1, F_SF = 2, F_PF = 4, F_KF = 6, F_KE = 8, F_VF = 10, F_VE = 12, F_OD = 14 };
+// barriers: Q loaded, O final, S ready[NSB], P written[NSB] (softmax done), K
+// full/empty[NK], V full/empty[2], O updated after P(j) V_j at OD + (j & 1): a
+// rescale at tile j waits for P(j-1) V_{j-1} on a barrier whose previous phase,
+// P(j-3) V_{j-3}, finished before S(j) (issued after it) did, so the parity
+// test cannot pass a phase early even with three S buffers (a single barrier
+// could: P(j-2) V_{j-2} may still run when the softmax of j starts)
+enum { F_Q = 0, F_ACC = 1, F_SF = 2, F_PF = 5, F_KF = 8, F_KE = 11, F_VF = 14, F_VE = 16, F_OD = 18 };
 
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 2)
@@ -102,11 +114,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CU
         mbar_init(sy.bar(F_Q), 1);
         mbar_init(sy.bar(F_ACC), 1);
         mbar_init(sy.bar(F_OD), 1);
-        for (int s = 0; s < 2; ++s) {
+        mbar_init(sy.bar(F_OD + 1), 1);
+        for (int s = 0; s < C::NSB; ++s) {
             mbar_init(sy.bar(F_SF + s), 1);
             mbar_init(sy.bar(F_PF + s), 128);
+        }
+        for (int s = 0; s < C::NK; ++s) {
             mbar_init(sy.bar(F_KF + s), 1);
             mbar_init(sy.bar(F_KE + s), 1);
+        }
+        for (int s = 0; s < C::NV; ++s) {
             mbar_init(sy.bar(F_VF + s), 1);
             mbar_init(sy.bar(F_VE + s), 1);
         }
@@ -126,22 +143,36 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CU
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // lane 0 loads Q and the K tiles, lane 1 the [V_lo | V_hi] tiles: the two
+        // streams run ahead independently (the softmax of tile j waits for
+        // K_{j+NSB} before releasing P(j), whose P V frees a V stage)
         if (lane == 0) {
-            int lastk[C::NK], lastv[C::NV];
+            int lastk[C::NK];
 #pragma unroll
             for (int x = 0; x < C::NK; ++x) lastk[x] = -1;
-#pragma unroll
-            for (int x = 0; x < C::NV; ++x) lastv[x] = -1;
             mbar_arrive_expect_tx(sy.bar(F_Q), C::TILE);
             tma_load_3d(sb + C::OFF_Q, &tm_pk, 0, q0, bh * 4 + 0, sy.bar(F_Q));
             for (int j = 0; j < nk; ++j) {
-                const int sk = j % C::NK, sv = j % C::NV;
+                const int sk = j % C::NK;
                 if (!wait_bounded(sy, sy.bar(F_KE + sk), ((j / C::NK) & 1) ^ 1, 0, j)) break;
                 mbar_arrive_expect_tx(sy.bar(F_KF + sk), C::KT);
                 tma_load_3d(sb + C::OFF_K + sk * C::KT, &tm_kv, 0, j * C::BK, bh * 4 + 1, sy.bar(F_KF + sk));
 #pragma unroll
                 for (int x = 0; x < C::NK; ++x)
                     if (x == sk) lastk[x] = j;
+            }
+            if (*sy.abort) {
+                wait_drain(sy.bar(F_Q), 0);
+#pragma unroll
+                for (int x = 0; x < C::NK; ++x)
+                    if (lastk[x] >= 0) wait_drain(sy.bar(F_KF + x), (lastk[x] / C::NK) & 1);
+            }
+        } else if (lane == 1) {
+            int lastv[C::NV];
+#pragma unroll
+            for (int x = 0; x < C::NV; ++x) lastv[x] = -1;
+            for (int j = 0; j < nk; ++j) {
+                const int sv = j % C::NV;
                 if (!wait_bounded(sy, sy.bar(F_VE + sv), ((j / C::NV) & 1) ^ 1, 0, j)) break;
                 const uint32_t vs = sb + C::OFF_V + sv * 2 * C::KT;
                 mbar_arrive_expect_tx(sy.bar(F_VF + sv), 2 * C::KT);
@@ -152,10 +183,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CU
                     if (x == sv) lastv[x] = j;
             }
             if (*sy.abort) {
-                wait_drain(sy.bar(F_Q), 0);
-#pragma unroll
-                for (int x = 0; x < C::NK; ++x)
-                    if (lastk[x] >= 0) wait_drain(sy.bar(F_KF + x), (lastk[x] / C::NK) & 1);
 #pragma unroll
                 for (int x = 0; x < C::NV; ++x)
                     if (lastv[x] >= 0) wait_drain(sy.bar(F_VF + x), (lastv[x] / C::NV) & 1);
@@ -173,38 +200,42 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CU
             const uint64_t dK0 = smem_desc(sb + C::OFF_K, 16, SBO, C::SW);
             const uint64_t dV0 = smem_desc(sb + C::OFF_V, C::KT, SBO, C::SW);
             constexpr uint32_t KT_U = C::KT >> 4;
-            // S(j) = Q K_j^T into buffer j & 1; K_j is known to be loaded (the
-            // prologue waits for K_0 and K_1; the softmax warps wait for K_{j+2}
-            // before releasing P(j))
+            // S(j) = Q K_j^T into buffer j % NSB; K_j is known to be loaded (the
+            // prologue waits for the first K tiles, up to NSB; later the softmax
+            // warps wait for K_{j+NSB} before releasing P(j))
             auto issue_s = [&](int j) {
                 const int sk = j % C::NK;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16_ss(tmem + 64u * (j & 1), dQ + 2 * kk, dK0 + KT_U * sk + 2 * kk, ID_S, kk);
-                mma_commit(sy.bar(F_SF + (j & 1)));
+                    mma_bf16_ss(tmem + 64u * (j % C::NSB), dQ + 2 * kk, dK0 + KT_U * sk + 2 * kk, ID_S, kk);
+                mma_commit(sy.bar(F_SF + j % C::NSB));
                 mma_commit(sy.bar(F_KE + sk));
             };
             bool ok = wait_bounded(sy, sy.bar(F_Q), 0, 1, -1);
-            for (int j = 0; j < 2 && j < nk && ok; ++j) ok = wait_bounded(sy, sy.bar(F_KF + j), 0, 1, j);
-            if (ok) {
-                tc_fence_after();
-                for (int j = 0; j < 2 && j < nk; ++j) issue_s(j);
+            // the first NSB S products; with NSB > NK, K_j of j >= NK arrives once
+            // S(j - NK) has freed its stage, which the loop below issues in order
+            for (int j = 0; j < C::NSB && j < nk && ok; ++j) {
+                ok = wait_bounded(sy, sy.bar(F_KF + j % C::NK), (j / C::NK) & 1, 1, j);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(j);
+                }
             }
             for (int j = 0; j < nk && ok; ++j) {
                 // P(j) written over S(j), O rescaled if a row max moved, V_j and
-                // K_{j+2} loaded (the softmax warps waited for both)
-                ok = wait_bounded(sy, sy.bar(F_PF + (j & 1)), (j >> 1) & 1, 1, j);
+                // K_{j+NSB} loaded (the softmax warps waited for both)
+                ok = wait_bounded(sy, sy.bar(F_PF + j % C::NSB), (j / C::NSB) & 1, 1, j);
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t dV = dV0 + 2 * KT_U * (j % C::NV);
 #pragma unroll
                 for (int kk = 0; kk < C::BK / 16; ++kk)
-                    mma_bf16_ts(tmem + C::C_O, tmem + 64u * (j & 1) + 8 * kk, dV + KSTEP * kk, ID_O,
+                    mma_bf16_ts(tmem + C::C_O, tmem + 64u * (j % C::NSB) + 8 * kk, dV + KSTEP * kk, ID_O,
                                 (j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(sy.bar(F_VE + j % C::NV));
-                mma_commit(sy.bar(F_OD));
-                // S(j+2) overwrites P(j): issued after P(j) V_j, the pipe keeps issue order
-                if (j + 2 < nk) issue_s(j + 2);
+                mma_commit(sy.bar(F_OD + (j & 1)));
+                // S(j+NSB) overwrites P(j): issued after P(j) V_j, the pipe keeps issue order
+                if (j + C::NSB < nk) issue_s(j + C::NSB);
             }
             mma_commit(sy.bar(F_ACC));
             if (!ok) wait_drain(sy.bar(F_ACC), 0);
@@ -218,8 +249,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CU
         float m = -INFINITY, l = 0.f;              // log2-domain row max in use and row sum
         bool ok = true;
         for (int j = 0; j < nk; ++j) {
-            const uint32_t tS = trow + 64u * (j & 1);
-            ok = warp_wait(sy, sy.bar(F_SF + (j & 1)), (j >> 1) & 1, 2, j);
+            const uint32_t tS = trow + 64u * (j % C::NSB);
+            ok = warp_wait(sy, sy.bar(F_SF + j % C::NSB), (j / C::NSB) & 1, 2, j);
             if (!ok) break;
             tc_fence_after();
             const int nvalid = N - j * C::BK;      // keys of this tile that exist (>= 1)
@@ -245,7 +276,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CU
             if (j > 0 && __any_sync(0xffffffffu, move)) {
                 // O *= alpha on this warp's rows, once P(j-1) V_{j-1} has finished
                 // (every lane loads and stores: .sync.aligned)
-                ok = warp_wait(sy, sy.bar(F_OD), (j - 1) & 1, 2, j);
+                ok = warp_wait(sy, sy.bar(F_OD + ((j - 1) & 1)), ((j - 1) >> 1) & 1, 2, j);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -281,11 +312,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CU
             l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
             tmem_wait_st();
             tc_fence_before();
-            // stand-in waits for the issuer: V_j and K_{j+2} are in shared memory
+            // stand-in waits for the issuer: V_j and K_{j+NSB} are in shared memory
             ok = warp_wait(sy, sy.bar(F_VF + j % C::NV), (j / C::NV) & 1, 2, j);
-            if (ok && j + 2 < nk)
-                ok = warp_wait(sy, sy.bar(F_KF + (j + 2) % C::NK), ((j + 2) / C::NK) & 1, 2, j);
-            mbar_arrive(sy.bar(F_PF + (j & 1)));
+            if (ok && j + C::NSB < nk)
+                ok = warp_wait(sy, sy.bar(F_KF + (j + C::NSB) % C::NK), ((j + C::NSB) / C::NK) & 1, 2, j);
+            mbar_arrive(sy.bar(F_PF + j % C::NSB));
             if (!ok) break;
         }
         if (ok) ok = warp_wait(sy, sy.bar(F_ACC), 0, 2, nk);

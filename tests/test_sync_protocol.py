@@ -707,7 +707,7 @@ def test_pair_protocol_random_schedules(nsub, NB, NST, soft_waits_full):
         run_pair(nsub, NB, NST, seed * 7 + nsub, soft_waits_full)
 
 
-def run_fwd(nk, seed, p_move):
+def run_fwd(nk, seed, p_move, nsb=2):
     """One random schedule of one forward CTA over nk key tiles: the producer
     (Q once; K tile j into stage j % 2 after KE, [V_lo | V_hi] tile j into
     stage j % 2 after VE; each copy lands on its own, in any order), the MMA
@@ -715,7 +715,10 @@ def run_fwd(nk, seed, p_move):
     commits VE and OD, S(j+2)) and four softmax warps (per tile: wait SF(j);
     with probability p_move the warp's row max moves, and for j > 0 it waits
     OD(j-1) and rescales its O rows; it writes P(j), waits for V_j and K_{j+2},
-    arrives PF(j))."""
+    arrives PF(j)).  K and V copies come from two independent producer lanes.
+    nsb: the S buffers (2 at head_dim 64, 3 at head_dim <= 32):
+    S(j) goes to buffer j % nsb after P(j - nsb) V, and the softmax waits for
+    K_{j+nsb}."""
     rnd = random.Random(seed)
     bars = {}
 
@@ -724,33 +727,40 @@ def run_fwd(nk, seed, p_move):
             bars[name] = Bar(name, count)
         return bars[name]
 
+    nkst = nsb                                 # K stages, as many as S buffers
+    for x in range(nkst):
+        bar(("KF", x))
+        bar(("KE", x))
     for x in range(2):
-        for nm in ("SF", "KF", "KE", "VF", "VE"):
-            bar((nm, x))
+        bar(("VF", x))
+        bar(("VE", x))
+    for x in range(nsb):
+        bar(("SF", x))
         bar(("PF", x), 4)
-    bar("OD")
-    kst = {0: None, 1: None}
-    kuse = {0: set(), 1: set()}
+    bar(("OD", 0))
+    bar(("OD", 1))                            # O updated after P(j) V_j, alternating by tile parity
+    kst = {x: None for x in range(nkst)}
+    kuse = {x: set() for x in range(nkst)}
     vst = {0: None, 1: None}
     vuse = {0: set(), 1: set()}
-    sbuf = {0: "free", 1: "free"}
-    tq = {(b, q): None for b in range(2) for q in range(4)}
+    sbuf = {b: "free" for b in range(nsb)}
+    tq = {(b, q): None for b in range(nsb) for q in range(4)}
     o_last = {q: -1 for q in range(4)}        # last P V product applied to this warp's O rows
     o_pv = [-1]                               # last P V product executed
     fifo = []
     landing = []                              # copies in flight: (barrier, phase, effect)
 
     def mma_s(j):
-        b = j & 1
+        b = j % nsb
         assert sbuf[b] == "free", f"S({j}) overwrites buffer {b}"
-        assert kst[j % 2] == j, f"S({j}) reads K stage holding {kst[j % 2]}"
-        kuse[j % 2].add("s")
+        assert kst[j % nkst] == j, f"S({j}) reads K stage holding {kst[j % nkst]}"
+        kuse[j % nkst].add("s")
         sbuf[b] = ("S", j)
         for q in range(4):
             tq[(b, q)] = ("S", j)
 
     def mma_pv(j):
-        b = j & 1
+        b = j % nsb
         for q in range(4):
             assert tq[(b, q)] == ("P", j), f"PV({j}) reads {tq[(b, q)]}"
             assert o_last[q] == j - 1, f"PV({j}) accumulates onto O rows holding PV({o_last[q]})"
@@ -760,51 +770,54 @@ def run_fwd(nk, seed, p_move):
         o_pv[0] = j
         sbuf[b] = "free"
 
-    def producer():
+    def producer_k():
         for j in range(nk):
-            sk = j % 2
-            yield ("wait", bar(("KE", sk)), j // 2 - 1)
+            sk = j % nkst
+            yield ("wait", bar(("KE", sk)), j // nkst - 1)
             if kst[sk] is not None:
                 assert "s" in kuse[sk], f"K stage {sk} reused before S({kst[sk]}) read it"
-            landing.append((bar(("KF", sk)), j // 2, ("k", sk, j)))
-            yield ("wait", bar(("VE", sk)), j // 2 - 1)
-            if vst[sk] is not None:
-                assert "pv" in vuse[sk], f"V stage {sk} reused before PV({vst[sk]}) read it"
-            landing.append((bar(("VF", sk)), j // 2, ("v", sk, j)))
+            landing.append((bar(("KF", sk)), j // nkst, ("k", sk, j)))
+
+    def producer_v():
+        for j in range(nk):
+            sv = j % 2
+            yield ("wait", bar(("VE", sv)), j // 2 - 1)
+            if vst[sv] is not None:
+                assert "pv" in vuse[sv], f"V stage {sv} reused before PV({vst[sv]}) read it"
+            landing.append((bar(("VF", sv)), j // 2, ("v", sv, j)))
 
     def issuer():
-        for j in range(min(2, nk)):
-            yield ("wait", bar(("KF", j)), 0)
-        for j in range(min(2, nk)):
+        for j in range(min(nsb, nk)):
+            yield ("wait", bar(("KF", j % nkst)), j // nkst)
             fifo.append(("mma", mma_s, j))
-            fifo.append(("commit", bar(("SF", j & 1)), j >> 1))
-            fifo.append(("commit", bar(("KE", j % 2)), j // 2))
+            fifo.append(("commit", bar(("SF", j % nsb)), j // nsb))
+            fifo.append(("commit", bar(("KE", j % nkst)), j // nkst))
         for j in range(nk):
-            yield ("wait", bar(("PF", j & 1)), j >> 1)
+            yield ("wait", bar(("PF", j % nsb)), j // nsb)
             fifo.append(("mma", mma_pv, j))
             fifo.append(("commit", bar(("VE", j % 2)), j // 2))
-            fifo.append(("commit", bar("OD"), j))
-            if j + 2 < nk:
-                v = j + 2
+            fifo.append(("commit", bar(("OD", j & 1)), j >> 1))
+            if j + nsb < nk:
+                v = j + nsb
                 fifo.append(("mma", mma_s, v))
-                fifo.append(("commit", bar(("SF", v & 1)), v >> 1))
-                fifo.append(("commit", bar(("KE", v % 2)), v // 2))
+                fifo.append(("commit", bar(("SF", v % nsb)), v // nsb))
+                fifo.append(("commit", bar(("KE", v % nkst)), v // nkst))
 
     def softmax(q):
         for j in range(nk):
-            b = j & 1
-            yield ("wait", bar(("SF", b)), j >> 1)
+            b = j % nsb
+            yield ("wait", bar(("SF", b)), j // nsb)
             assert tq[(b, q)] == ("S", j), f"softmax({j}) reads {tq[(b, q)]}"
             if j > 0 and rnd.random() < p_move:
-                yield ("wait", bar("OD"), j - 1)
+                yield ("wait", bar(("OD", (j - 1) & 1)), (j - 1) >> 1)
                 assert o_last[q] == j - 1, f"rescale at tile {j} sees O rows at PV({o_last[q]})"
             tq[(b, q)] = ("P", j)
             yield ("wait", bar(("VF", j % 2)), j // 2)
-            if j + 2 < nk:
-                yield ("wait", bar(("KF", (j + 2) % 2)), (j + 2) // 2)
-            yield ("arrive", bar(("PF", j & 1)), j >> 1)
+            if j + nsb < nk:
+                yield ("wait", bar(("KF", (j + nsb) % nkst)), (j + nsb) // nkst)
+            yield ("arrive", bar(("PF", j % nsb)), j // nsb)
 
-    roles = [producer(), issuer()] + [softmax(q) for q in range(4)]
+    roles = [producer_k(), producer_v(), issuer()] + [softmax(q) for q in range(4)]
     pending = {}
 
     def advance(i):
@@ -868,9 +881,11 @@ def run_fwd(nk, seed, p_move):
 def test_forward_protocol_random_schedules(nk, p_move):
     """The forward with row maxima that never move after the first tile, move
     sometimes, or move on every tile (each move waits for the previous P V
-    product and rescales O); 30 random schedules each."""
+    product and rescales O), with two S buffers (head_dim 64) and three (head_dim
+    <= 32); 30 random schedules each."""
     for seed in range(30):
-        run_fwd(nk, seed * 31 + nk, p_move)
+        run_fwd(nk, seed * 31 + nk, p_move, nsb=2)
+        run_fwd(nk, seed * 37 + nk, p_move, nsb=3)
 
 
 def test_pair_protocol_relies_on_ordered_commits():
