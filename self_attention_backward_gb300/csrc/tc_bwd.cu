@@ -27,11 +27,12 @@
 // softmax-gradient warpgroups take alternate sub-tiles, so the tensor core
 // works on later sub-tiles while a warpgroup turns S/dP(u) into P and dS.  P^T
 // is written over the first 32 columns of its S^T buffer as bf16 pairs (the A
-// operand of the dV MMA); S/dP(u+NB) reuse u's buffer and are issued after
-// dV/dK(u), the pipe keeping issue order.  dS^T goes over the first 32 columns
-// of its dP^T buffer (the A operand of the dK MMA) and into a 4-block shared
-// ring (u & 3) for the dQ MMA, which needs it with queries as rows; a pair's
-// dS stays in the ring until its dQ MMA has read it.
+// operand of the dV MMA) and dS^T over the first 32 columns of its dP^T buffer
+// (the A operand of the dK MMA).  S^T(u+NB) reuses u's buffer and is issued
+// right after dV(u), the last reader of P^T(u); dP^T(u+NB) right after dK(u);
+// the pipe keeps issue order.  dS^T also goes into a 4-block shared ring
+// (u & 3) for the dQ MMA, which needs it with queries as rows; a pair's dS
+// stays in the ring until its dQ MMA has read it.
 //
 // Cost model that shaped it (measured on GB300): a tcgen05.mma with M = 128,
 // K = 16 costs about max(46, N/2) cycles, so the MMA count, not the flop
@@ -39,10 +40,12 @@
 // waits for its own MMAs in flight.  The issuing thread precomputes every
 // descriptor so that issuing an MMA is one add per operand.
 //
-// Warp roles: warp 0 TMA producer, warp 1 MMA issuer (one thread) and TMEM
-// owner, warps 2-5 / 6-9 softmax-gradient warpgroups 0 / 1 (one key row per
-// thread), warps 10-13 dQ drain (one query row per thread); for d <= 32 a
-// warp 14 whose one thread issues the dQ MMAs (480 threads, else 448).
+// Warp roles: warp 0 TMA producer (Q, dO_lo, dO_hi and the sub-tile's row
+// statistics per stage), warp 1 MMA issuer (one thread) and TMEM owner, warps
+// 2-5 / 6-9 softmax-gradient warpgroups 0 / 1 (one key row per thread), warps
+// 10-13 dQ drain (one query row per thread), warp 14 the dQ MMA issuer; for
+// d <= 32 warp 15 issues the odd sub-tiles' main MMAs and warp 1 the even ones
+// (512 threads, else 480).
 //
 // Every mbarrier wait is bounded (kTimeoutNs); on timeout the CTA sets a device
 // error word (read by psa_attn_sync_status), skips the rest of its work, waits

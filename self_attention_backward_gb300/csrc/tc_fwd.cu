@@ -16,19 +16,18 @@
 //   [O_lo | O_hi] += P [V_lo,j | V_hi,j]   (A = P from TMEM, N = 2d)
 // and at the end O / l and LSE = (m + log2 l) ln 2.  c = scale log2(e).
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 MMA issuer (one
-// thread) and TMEM owner, warps 2-5 softmax (one query row per thread, the
-// warp's TMEM lane quarter).  A CTA holds 256 TMEM columns (two 64-column S
-// buffers, then O), so two CTAs share an SM.  S(j+1) is computed while the
-// softmax works on S(j), and S(j+2) once P(j) V_j has read P(j); the other
-// CTA's softmax and MMAs fill the remaining gaps of the tensor pipe and the
-// exp2 unit.  A row max that moves by more than 2^8 makes the softmax rescale
-// O, after waiting for P(j-1) V_{j-1} to finish (rare after the first tiles).
-// K tiles rotate through two
-// shared-memory stages, [V_lo | V_hi] through two (d <= 32) or one (d = 64,
-// for two CTAs to fit an SM's shared memory); the softmax warps wait for the
-// next K and the current V before they release P, so the issuing thread waits
-// once per key tile.  All waits are bounded (tc_sync.cuh).
+// Warp roles (192 threads): warp 0 TMA producer (lane 0 Q and K, lane 1 V),
+// warp 1 MMA issuer (one thread) and TMEM owner, warps 2-5 softmax (one query
+// row per thread, the warp's TMEM lane quarter).  A CTA holds 256 TMEM columns
+// (NSB 64-column S buffers, then O), so two CTAs share an SM.  S(j+1) .. S(j+NSB-1)
+// are computed while the softmax works on S(j), and S(j+NSB) once P(j) V_j has
+// read P(j); the other CTA's softmax and MMAs fill the remaining gaps of the
+// tensor pipe and the exp2 unit.  A row max that moves by more than 2^8 makes
+// the softmax rescale O, after waiting for P(j-1) V_{j-1} to finish (rare after
+// the first tiles).  K tiles rotate through NSB shared-memory stages,
+// [V_lo | V_hi] through two; the softmax warps wait for K_{j+NSB} and the
+// current V before they release P, so the issuing thread waits once per key
+// tile.  All waits are bounded (tc_sync.cuh).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -93,6 +92,68 @@ struct FwdCfg {
 // test cannot pass a phase early even with three S buffers (a single barrier
 // could: P(j-2) V_{j-2} may still run when the softmax of j starts)
 enum { F_Q = 0, F_ACC = 1, F_SF = 2, F_PF = 5, F_KF = 8, F_KE = 11, F_VF = 14, F_VE = 16, F_OD = 18 };
+
+// x = S * c over one key tile, written back over sr, and max x over the keys
+// that exist (the first nvalid; all of them when !MASK).  Masked keys get
+// x = -inf, so that their probability below is exactly 0.  Packed f32x2
+// multiplies and three-input maxima: the softmax is issue-bound, and per-key
+// mask tests on every tile had kept the ALU pipe 62% busy.
+template <bool MASK, int BK>
+__device__ __forceinline__ float fwd_scale_max(uint32_t (&sr)[BK], float c, int nvalid) {
+    const uint64_t c2 = f2_pack(c, c);
+    float ma = -INFINITY, mb = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < BK; e += 4) {
+        float x0, x1, x2, x3;
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2), x0, x1);
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2), x2, x3);
+        if (MASK) {
+            if (e + 0 >= nvalid) x0 = -INFINITY;
+            if (e + 1 >= nvalid) x1 = -INFINITY;
+            if (e + 2 >= nvalid) x2 = -INFINITY;
+            if (e + 3 >= nvalid) x3 = -INFINITY;
+        }
+        ma = fmax3(ma, x0, x1);
+        mb = fmax3(mb, x2, x3);
+        sr[e] = __float_as_uint(x0);
+        sr[e + 1] = __float_as_uint(x1);
+        sr[e + 2] = __float_as_uint(x2);
+        sr[e + 3] = __float_as_uint(x3);
+    }
+    return fmaxf(ma, mb);
+}
+
+// P = exp2(x - m) over one key tile (x from fwd_scale_max), stored over S in
+// TMEM as bf16 pairs (all of S is in registers); returns the tile's sum of P.
+template <int BK>
+__device__ __forceinline__ float fwd_probs(const uint32_t (&sr)[BK], float m, uint32_t tS) {
+    const uint64_t m2 = f2_pack(m, m), one2 = f2_pack(1.f, 1.f);
+    uint64_t la = f2_pack(0.f, 0.f), lb = la;
+#pragma unroll
+    for (int c = 0; c < BK / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+            const int k = 32 * c + e;
+            float p0, p1, p2, p3;
+            f2_unpack(f2_sub(f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), m2), p0, p1);
+            f2_unpack(f2_sub(f2_pack(__uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3])), m2), p2, p3);
+            p0 = ex2_approx(p0);
+            p1 = ex2_approx(p1);
+            p2 = ex2_approx(p2);
+            p3 = ex2_approx(p3);
+            la = f2_fma(f2_pack(p0, p1), one2, la);
+            lb = f2_fma(f2_pack(p2, p3), one2, lb);
+            pk[e / 2] = pack_bf16x2(p0, p1);
+            pk[e / 2 + 1] = pack_bf16x2(p2, p3);
+        }
+        tmem_st_32x32b_x16(tS + 16 * c, pk);
+    }
+    float a0, a1, b0, b1;
+    f2_unpack(la, a0, a1);
+    f2_unpack(lb, b0, b1);
+    return (a0 + a1) + (b0 + b1);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 2)
@@ -259,16 +320,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CU
             for (int c = 0; c < C::BK / 32; ++c)
                 tmem_ld_32x32b_x32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
             tmem_wait_ld();
-            // scaled scores (any sign of scale) and their max, in four partial
-            // maxima to keep the dependent chains short
-            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int e = 0; e < C::BK; ++e) {
-                const float x = __uint_as_float(sr[e]) * scale_log2;
-                sr[e] = __float_as_uint(x);
-                if (e < nvalid) m4[e & 3] = fmaxf(m4[e & 3], x);
-            }
-            const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            // scaled scores and their max (masked keys -> -inf, whose exp2 is 0);
+            // only the ragged last tile pays for the key mask
+            const float mt = nvalid >= C::BK ? fwd_scale_max<false>(sr, scale_log2, nvalid)
+                                             : fwd_scale_max<true>(sr, scale_log2, nvalid);
             const bool move = mt > m + kRescaleLog2;
             const float m_new = move ? mt : m;
             const float alpha = move ? ex2_approx(m - m_new) : 1.f;   // 0 on the first tile
@@ -292,24 +347,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CU
                 tmem_wait_st();
             }
             m = m_new;
-            float l4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < C::BK / 32; ++c) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const int k = 32 * c + e;
-                    float p0 = ex2_approx(__uint_as_float(sr[k]) - m);
-                    float p1 = ex2_approx(__uint_as_float(sr[k + 1]) - m);
-                    if (k >= nvalid) p0 = 0.f;
-                    if (k + 1 >= nvalid) p1 = 0.f;
-                    l4[(e >> 1) & 3] += p0 + p1;
-                    pk[e / 2] = pack_bf16x2(p0, p1);
-                }
-                // P over the S columns (all of S is in registers)
-                tmem_st_32x32b_x16(tS + 16 * c, pk);
-            }
-            l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+            l += fwd_probs(sr, m, tS);
             tmem_wait_st();
             tc_fence_before();
             // stand-in waits for the issuer: V_j and K_{j+NSB} are in shared memory

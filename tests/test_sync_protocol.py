@@ -707,7 +707,7 @@ def test_pair_protocol_random_schedules(nsub, NB, NST, soft_waits_full):
         run_pair(nsub, NB, NST, seed * 7 + nsub, soft_waits_full)
 
 
-def run_fwd(nk, seed, p_move, nsb=2):
+def run_fwd(nk, seed, p_move, nsb=2, one_producer=False):
     """One random schedule of one forward CTA over nk key tiles: the producer
     (Q once; K tile j into stage j % 2 after KE, [V_lo | V_hi] tile j into
     stage j % 2 after VE; each copy lands on its own, in any order), the MMA
@@ -718,7 +718,8 @@ def run_fwd(nk, seed, p_move, nsb=2):
     arrives PF(j)).  K and V copies come from two independent producer lanes.
     nsb: the S buffers (2 at head_dim 64, 3 at head_dim <= 32):
     S(j) goes to buffer j % nsb after P(j - nsb) V, and the softmax waits for
-    K_{j+nsb}."""
+    K_{j+nsb}.  one_producer: K_j and V_j issued in turn by one lane (the
+    layout before K and V were split onto two lanes)."""
     rnd = random.Random(seed)
     bars = {}
 
@@ -817,7 +818,17 @@ def run_fwd(nk, seed, p_move, nsb=2):
                 yield ("wait", bar(("KF", (j + nsb) % nkst)), (j + nsb) // nkst)
             yield ("arrive", bar(("PF", j % nsb)), j // nsb)
 
-    roles = [producer_k(), producer_v(), issuer()] + [softmax(q) for q in range(4)]
+    def producer_kv():
+        # one lane: K_j, then V_j, for each j in turn
+        for j in range(nk):
+            sk, sv = j % nkst, j % 2
+            yield ("wait", bar(("KE", sk)), j // nkst - 1)
+            landing.append((bar(("KF", sk)), j // nkst, ("k", sk, j)))
+            yield ("wait", bar(("VE", sv)), j // 2 - 1)
+            landing.append((bar(("VF", sv)), j // 2, ("v", sv, j)))
+
+    producers = [producer_kv()] if one_producer else [producer_k(), producer_v()]
+    roles = producers + [issuer()] + [softmax(q) for q in range(4)]
     pending = {}
 
     def advance(i):
@@ -886,6 +897,19 @@ def test_forward_protocol_random_schedules(nk, p_move):
     for seed in range(30):
         run_fwd(nk, seed * 31 + nk, p_move, nsb=2)
         run_fwd(nk, seed * 37 + nk, p_move, nsb=3)
+
+
+@pytest.mark.parametrize("nk", [6, 9])
+def test_forward_one_producer_lane_deadlocks_with_three_buffers(nk):
+    """With K and V copies issued in turn by one lane and three S buffers, the
+    lane waits for V stage (j % 2) to be freed by P(j-2) V, which needs the
+    softmax of j-2 to see K_{j+1}, which the lane has not issued yet: every
+    schedule deadlocks.  With two S buffers the softmax of j-2 waits for K_j,
+    which the lane issued before V_j: no deadlock."""
+    for seed in range(10):
+        with pytest.raises(AssertionError, match="deadlock"):
+            run_fwd(nk, seed, 0.3, nsb=3, one_producer=True)
+        run_fwd(nk, seed, 0.3, nsb=2, one_producer=True)
 
 
 def test_pair_protocol_relies_on_ordered_commits():
