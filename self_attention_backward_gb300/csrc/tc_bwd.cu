@@ -43,7 +43,9 @@
 // Warp roles: warp 0 TMA producer (Q, dO_lo, dO_hi and the sub-tile's row
 // statistics per stage), warp 1 MMA issuer (one thread) and TMEM owner, warps
 // 2-5 / 6-9 softmax-gradient warpgroups 0 / 1 (one key row per thread), warps
-// 10-13 dQ drain (one query row per thread), warp 14 the dQ MMA issuer; for
+// 10-13 dQ drain (one query row per thread; the partials go to the fp32
+// accumulator by TMA bulk reduce) and then the dK/dV epilogue (one key row per
+// thread), warp 14 the dQ MMA issuer; for
 // d <= 32 warp 15 issues the odd sub-tiles' main MMAs and warp 1 the even ones
 // (512 threads, else 480).
 //
@@ -99,25 +101,39 @@ struct Cfg {
     static constexpr int OFF_STAGE = 3 * KTILE;    // stage s: Q, dO_lo, dO_hi at +s*STAGE
     static constexpr int STAGE = 3 * QTILE;
     static constexpr int OFF_DS = OFF_STAGE + NST * STAGE;  // dS^T ring: 4 x [128 keys][64 queries] bf16
+    // dQ drain: each 128-query partial is staged here in boxes of BOXC columns
+    // (128-byte or 64-byte rows, swizzled as the tensor map expects) and added
+    // to the fp32 accumulator by TMA bulk reduces.  Vector atomics, one row per
+    // thread, put 32 separate 16-byte requests per warp instruction into the
+    // SM's load/store path, where they held up the softmax's dS stores to
+    // shared memory by ~2 K cycles per 128-query group at head_dim 64
+    // (measured).  NDQS staging buffers of one box of min(D, 32) columns each:
+    // two, or one at head_dim 64 (what shared memory leaves room for; the drain
+    // warps also stage the dK/dV epilogue there).
+    static constexpr int BOXC = D < 32 ? D : 32;
+    static constexpr int NDQS = D == 64 ? 1 : 2;
+    static constexpr int DQS_BYTES = 128 * BOXC * 4;
+    static constexpr int OFF_DQS = OFF_DS + 4 * 16384;
     // NST x 32 float4, one per query pair c of the stage's 64 queries:
     // {-LSE_2c log2(e), -LSE_2c+1 log2(e), D_2c, D_2c+1}
-    static constexpr int OFF_ST = OFF_DS + 4 * 16384;
+    static constexpr int OFF_ST = OFF_DQS + NDQS * DQS_BYTES;
     static constexpr int OFF_BAR = OFF_ST + NST * 512;     // mbarriers (48)
     static constexpr int OFF_MISC = OFF_BAR + 384;
-    // d <= 32: the dQ drain stages each 128-query partial here (two buffers of
-    // [128][D] fp32 as boxes of at most 32 columns, 128B / 64B-swizzled rows) and
-    // adds it to the fp32 accumulator with TMA bulk reduces.  At d = 64 it adds
-    // with vector atomics: the MMA issuer bounds that kernel, and one staging
-    // buffer with three Q/dO stages (what shared memory leaves room for) was no
-    // faster (N = 400 1% faster, N = 1600 2% slower, measured).
-    static constexpr bool DQ_BULK = D <= 32;
-    static constexpr int NDQS = 2;
-    static constexpr int DQS_BYTES = 128 * D * 4;
-    static constexpr int OFF_DQS = (OFF_MISC + 64 + 1023) / 1024 * 1024;
-    static constexpr int USED = DQ_BULK ? OFF_DQS + NDQS * DQS_BYTES : OFF_MISC + 64;
-    // + 1 KB to align the base to 1024; at least 116 KB so that one CTA owns
-    // an SM (its TMEM allocation is all 512 columns)
-    static constexpr int SMEM = (USED + 1024) > 118784 ? (USED + 1024) : 118784;
+    // The dK/dV epilogue: at head_dim 64 the drain warps run it after their last
+    // group, staging in the dQ buffer (shared memory has no room for more); at
+    // head_dim <= 32 softmax warpgroup 0 runs it as soon as the last MMAs are
+    // done, with 2 KB of its own per warp (the drain's last group then runs
+    // beside it).
+    static constexpr bool EPI_DRAIN = D == 64;
+    static constexpr int OFF_EPI = OFF_MISC + 64;
+    static constexpr int USED = OFF_EPI + (EPI_DRAIN ? 0 : 4 * 2048);
+    // + 1 KB to align the base to 1024 where that fits; at head_dim 64 it does
+    // not, and the host checks once per device that the base is aligned
+    // (dyn_smem_base_aligned).  At least 116 KB so that one CTA owns an SM (its
+    // TMEM allocation is all 512 columns).
+    static constexpr bool SLACK = USED + 1024 <= 232448;
+    static constexpr int SMEM_A = SLACK ? USED + 1024 : USED;
+    static constexpr int SMEM = SMEM_A > 118784 ? SMEM_A : 118784;
     // TMEM columns (fp32): buffer b = [128b, 128b+128): S^T (64), dP^T (64)
     // (P^T is written over the first 32 columns of its S^T as bf16 pairs); then
     // dV_lo|dV_hi, dK, dQ
@@ -125,7 +141,8 @@ struct Cfg {
     static constexpr uint32_t C_DK = C_DV + 2 * D, C_DQ = C_DV + 3 * D;
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(C_DQ + D <= TMEM_COLS, "TMEM budget");
-    static_assert(USED + 1024 <= 232448, "shared memory budget");
+    static_assert(USED <= 232448, "shared memory budget");
+    static_assert(!EPI_DRAIN || NDQS * DQS_BYTES >= 4 * 2048, "the epilogue stages 2 KB per drain warp");
     static_assert(NST > NB, "the softmax's wait for the stage of u+NB would wait on its own release");
 };
 
@@ -189,6 +206,44 @@ __device__ __forceinline__ void softmax_vals(const uint32_t (&sr)[32], const uin
     }
 }
 
+// The epilogue of one warp: dK (scaled), dV_lo, dV_hi of the warp's 32 key
+// rows (TMEM lane quarter q4) as bf16 into d_packed sections 1-3, coalesced
+// through the warp's 2 KB staging buffer stg; or, for a piece of a split unit,
+// the fp32 partials into dkv_part.  Every main MMA must be complete.
+template <int D, typename C>
+__device__ __forceinline__ void dkdv_epilogue(uint32_t tmem, int q4, int lane, uint32_t stg, bf16* d_packed,
+                                              int bh, int k0, int N, long long ldq, float scale, int piece,
+                                              float* dkv_part) {
+    const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+    const int jl = q4 * 32 + lane;
+    const size_t sec = (size_t)N * ldq;
+    // row 0 of this warp's 32 key rows in section 0 of the slice
+    bf16* wrow0 = d_packed + (size_t)bh * 4 * sec + (size_t)(k0 + q4 * 32) * ldq;
+    uint32_t v[D];
+#pragma unroll
+    for (int which = 0; which < 3; ++which) {
+        const uint32_t col = which == 0 ? C::C_DK : C::C_DV + (which - 1) * D;
+        const float mul = which == 0 ? scale : 1.f;
+        tmem_ld_row<D>(trow + col, v);
+        tmem_wait_ld();
+        if (piece >= 0) {
+            // a piece's partial: [piece][key row][dK | dV_lo | dV_hi] fp32
+            float4* o = reinterpret_cast<float4*>(dkv_part + ((size_t)piece * C::BM + jl) * 3 * D + which * D);
+#pragma unroll
+            for (int e = 0; e < D; e += 4)
+                o[e / 4] = make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                                       __uint_as_float(v[e + 3]));
+        } else {
+            uint32_t w[D / 2];
+#pragma unroll
+            for (int e = 0; e < D / 2; ++e)
+                w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+            store_rows_staged<D>(stg, w, reinterpret_cast<uint16_t*>(wrow0 + (size_t)(1 + which) * sec), ldq,
+                                 N - (k0 + q4 * 32), lane);
+        }
+    }
+}
+
 // ---------------------------------------------------------------- main kernel
 // CM: dO_lo / dO_hi come as channel-major [d, N] blocks (4-D maps over
 // [B][heads][d][N]); else as rows (4-D maps over [B][heads][N][d]).  The
@@ -202,7 +257,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 int nkt, float scale, float scale_log2, int nfull, int tail_f, float* __restrict__ dkv_part) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = C::SLACK ? reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023))
+                             : smem_raw;  // the host checked the base's alignment
     const uint32_t sb = smem_u32(smem);
     Sync sy{sb + C::OFF_BAR, reinterpret_cast<volatile int*>(smem + C::OFF_MISC), &g_tc_error};
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 16);
@@ -424,7 +480,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             // all of this thread's MMAs done (also on abort, before TMEM is freed)
             const uint32_t acc_bar = sy.bar(par == 0 ? F_ACC : F_ACCB);
             mma_commit(acc_bar);
-            if (!ok) wait_drain(acc_bar, 0);
+            wait_drain(acc_bar, 0);
         }
         __syncwarp();
     } else if (warp < 10) {
@@ -573,103 +629,77 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             mbar_arrive(sy.bar(F_PF + u % kPfRingF));
             if (!ok) break;
         }
-        const int jl = q4 * 32 + lane;           // epilogue: one key row per thread
-        const bool kvalid = k0 + jl < N;
-        const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
-        // epilogue (warpgroup 0): dK, dV_lo, dV_hi rows of this thread's key
-        if (grp == 0) {
-            if (ok) ok = warp_wait(sy, sy.bar(F_ACC), 0, 2, nsub) &&
-                         (!C::TWO_ISSUERS || warp_wait(sy, sy.bar(F_ACCB), 0, 2, nsub));
-            if (ok) {
-                tc_fence_after();
-                uint32_t v[D];
-                const size_t sec = (size_t)N * ldq;
-                bf16* out = d_packed + (size_t)bh * 4 * sec + (size_t)(k0 + jl) * ldq;
-#pragma unroll
-                for (int which = 0; which < 3; ++which) {
-                    const uint32_t col = which == 0 ? C::C_DK : C::C_DV + (which - 1) * D;
-                    const float mul = which == 0 ? scale : 1.f;
-                    tmem_ld_row<D>(trow + col, v);
-                    tmem_wait_ld();
-                    if (piece >= 0) {
-                        // a piece's partial: [piece][key row][dK | dV_lo | dV_hi] fp32
-                        float4* o = reinterpret_cast<float4*>(dkv_part + ((size_t)piece * C::BM + jl) * 3 * D + which * D);
-#pragma unroll
-                        for (int e = 0; e < D; e += 4)
-                            o[e / 4] = make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                                                   __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-                    } else if (kvalid) {
-                        bf16* o = out + (size_t)(1 + which) * sec;
-#pragma unroll
-                        for (int e = 0; e < D; e += 8) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(v[e + 0]) * mul, __uint_as_float(v[e + 1]) * mul);
-                            w.y = pack_bf16x2(__uint_as_float(v[e + 2]) * mul, __uint_as_float(v[e + 3]) * mul);
-                            w.z = pack_bf16x2(__uint_as_float(v[e + 4]) * mul, __uint_as_float(v[e + 5]) * mul);
-                            w.w = pack_bf16x2(__uint_as_float(v[e + 6]) * mul, __uint_as_float(v[e + 7]) * mul);
-                            *reinterpret_cast<uint4*>(o + e) = w;
-                        }
-                    }
+        if constexpr (!C::EPI_DRAIN) {
+            if (grp == 0) {
+                if (ok) ok = warp_wait(sy, sy.bar(F_ACC), 0, 2, nsub) &&
+                             (!C::TWO_ISSUERS || warp_wait(sy, sy.bar(F_ACCB), 0, 2, nsub));
+                if (ok) {
+                    tc_fence_after();
+                    dkdv_epilogue<D, C>(tmem, q4, lane, sb + C::OFF_EPI + 2048u * (warp - 2), d_packed, bh, k0, N,
+                                        ldq, scale, piece, dkv_part);
                 }
             }
         }
     } else if (warp < 14) {
-        // ------------------------------------------------------------ dQ drain
+        // ------------------------------------------------------------ dQ drain, then the dK/dV epilogue
         const int q4 = warp & 3;
-        const int il = q4 * 32 + lane;           // query row within the 128-query group
+        const int il = q4 * 32 + lane;           // query row within the 128-query group (key row in the epilogue)
         const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
         const bool elected = warp == 10 && lane == 0;
+        // row il of a box of BOXC fp32 columns, swizzled as the tensor map expects
+        // (16-byte chunk c of a row at c xor the row bits above the 128-byte line)
+        constexpr uint32_t RB = C::BOXC * 4, M = RB == 128 ? 7u : RB == 64 ? 3u : 1u;
+        bool okd = true;
         for (int g = 0; g < ngrp; ++g) {
-            bool okw = warp_wait(sy, sy.bar(F_DQF + (g & 1)), (g >> 1) & 1, 3, g);
+            okd = warp_wait(sy, sy.bar(F_DQF + (g & 1)), (g >> 1) & 1, 3, g);
             // the four drain warps decide together (they meet at named barriers below)
-            if (C::DQ_BULK) okw = named_bar_and(2, 128, okw);
-            if (!okw) break;
+            okd = named_bar_and(2, 128, okd);
+            if (!okd) break;
             tc_fence_after();
             uint32_t v[D];
             tmem_ld_row<D>(trow + C::C_DQ, v);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(sy.bar(F_DQE + (g & 1)));
-            if constexpr (C::DQ_BULK) {
-                // staging buffer g % NDQS: the reduces that last read it (group
-                // g - NDQS) must be done reading
-                const uint32_t buf = sb + C::OFF_DQS + (g % C::NDQS) * C::DQS_BYTES;
+#pragma unroll
+            for (int h = 0; h < D / C::BOXC; ++h) {
+                // staging buffer of box b: the reduce that last read it (box b - NDQS)
+                // must be done reading
+                const int bx = g * (D / C::BOXC) + h;
+                const uint32_t buf = sb + C::OFF_DQS + (bx % C::NDQS) * C::DQS_BYTES;
                 if (elected) bulk_wait_group_read<C::NDQS - 1>();
                 named_bar_sync(1, 128);
-                // row il of each box of BOXC columns, swizzled as the tensor map
-                // expects (16-byte chunk c of a row at c xor the row bits above the
-                // 128-byte line)
-                constexpr int BOXC = D < 32 ? D : 32;
-                constexpr uint32_t RB = BOXC * 4, M = RB == 128 ? 7u : RB == 64 ? 3u : 1u;
 #pragma unroll
-                for (int c = 0; c < D / 4; ++c) {
-                    const uint32_t half = (uint32_t)c / (RB / 16), cc = (uint32_t)c % (RB / 16);
-                    const uint32_t a = (uint32_t)il * RB + 16u * cc;
-                    st_shared_v4(buf + half * 128u * RB + (a ^ (((a >> 7) & M) << 4)), v[4 * c], v[4 * c + 1],
-                                 v[4 * c + 2], v[4 * c + 3]);
+                for (int c = 0; c < C::BOXC / 4; ++c) {
+                    const uint32_t a = (uint32_t)il * RB + 16u * c;
+                    st_shared_v4(buf + (a ^ (((a >> 7) & M) << 4)), v[h * C::BOXC + 4 * c],
+                                 v[h * C::BOXC + 4 * c + 1], v[h * C::BOXC + 4 * c + 2], v[h * C::BOXC + 4 * c + 3]);
                 }
                 fence_proxy_async_smem();
                 named_bar_sync(1, 128);
                 // rows past N lie outside the tensor and are skipped
                 if (elected) {
-#pragma unroll
-                    for (int h = 0; h < D / BOXC; ++h)
-                        tma_reduce_add_3d(&tm_dq, buf + h * 128u * RB, h * BOXC, (ubase / 2 + g) * 128, bh);
+                    tma_reduce_add_3d(&tm_dq, buf, h * C::BOXC, (ubase / 2 + g) * 128, bh);
                     bulk_commit_group();
-                }
-            } else {
-                const int i = (ubase / 2 + g) * 128 + il;
-                if (i < N) {
-                    float4* dst = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * N + i) * D);
-#pragma unroll
-                    for (int e = 0; e < D; e += 4)
-                        atomicAdd(dst + e / 4, make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                                                           __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])));
                 }
             }
         }
+        if constexpr (C::EPI_DRAIN) {
+            // epilogue: dK, dV_lo, dV_hi rows of this warp's 32 keys, once every
+            // main MMA is done; the staging buffer is free once the last reduce read it
+            if (okd) okd = warp_wait(sy, sy.bar(F_ACC), 0, 2, nsub) &&
+                           (!C::TWO_ISSUERS || warp_wait(sy, sy.bar(F_ACCB), 0, 2, nsub));
+            okd = named_bar_and(2, 128, okd);
+            if (okd) {
+                if (elected) bulk_wait_group_read<0>();
+                named_bar_sync(1, 128);
+                tc_fence_after();
+                dkdv_epilogue<D, C>(tmem, q4, lane, sb + C::OFF_DQS + 2048u * (warp - 10), d_packed, bh, k0, N, ldq,
+                                    scale, piece, dkv_part);
+            }
+        }
         // every reduce has written global memory and read its staging buffer
-        if (C::DQ_BULK && elected) bulk_wait_group<0>();
+        if (elected) bulk_wait_group<0>();
     } else if (warp == 14) {
         // ------------------------------------------------------------ dQ issuer
         // dQ of the 128-query group g = sub-tiles 2g, 2g+1: A = dS (queries x keys)
@@ -1203,7 +1233,7 @@ int launch_impl(const BwdArgs& a, std::string* err) {
     float* dq_acc = reinterpret_cast<float*>(ws);
     const View vlo = a.do_view(0), vhi = a.do_view(1);
     const long long nb = a.BH / a.heads;
-    // dq_acc in 128-query boxes of min(D, 32) columns (the reduce path uses it at D <= 32)
+    // dq_acc in 128-query boxes of BOXC columns (the drain's bulk reduces)
     CUtensorMap tm_kv, tm_q, tm_lo, tm_hi, tm_dq;
     if (!encode_bf16_rows_ld(&tm_kv, a.packed, D, ldq, a.N, a.BH * 4, M::BM, D, err) ||
         !encode_bf16_rows_ld(&tm_q, a.packed, D, ldq, a.N, a.BH * 4, M::BS, D, err) ||
@@ -1211,9 +1241,17 @@ int launch_impl(const BwdArgs& a, std::string* err) {
              : encode_bf16_4d(&tm_lo, vlo.base, D, a.N, a.heads, nb, vlo.sN, vlo.sH, vlo.sB, D, M::BS, err)) ||
         !(CM ? encode_bf16_4d(&tm_hi, vhi.base, a.N, D, a.heads, nb, vhi.sJ, vhi.sH, vhi.sB, M::BS, D, err)
              : encode_bf16_4d(&tm_hi, vhi.base, D, a.N, a.heads, nb, vhi.sN, vhi.sH, vhi.sB, D, M::BS, err)) ||
-        !encode_f32_rows(&tm_dq, dq_acc, D, a.N, a.BH, 128, D < 32 ? D : 32, err))
+        !encode_f32_rows(&tm_dq, dq_acc, D, a.N, a.BH, 128, M::BOXC, err))
         return PSA_ERR_CUDA;
     if (!set_max_dynamic_smem((const void*)bwd_main_kernel<D, CM>, M::SMEM, err)) return PSA_ERR_CUDA;
+    if constexpr (!M::SLACK) {
+        const int al = dyn_smem_base_aligned(err);
+        if (al < 0) return PSA_ERR_CUDA;
+        if (al == 0) {
+            *err = "the fused kernel at this head_dim needs a 1024-byte aligned dynamic shared memory base";
+            return PSA_ERR_UNSUPPORTED;
+        }
+    }
     float* dkv_part = reinterpret_cast<float*>(ws + align256((size_t)rows * D * 4));
     const int nkt = (a.N + M::BM - 1) / M::BM;
     const long long units = a.BH * nkt;

@@ -77,7 +77,8 @@ struct FwdCfg {
     static constexpr int OFF_V = OFF_K + NK * KT;  // V stage s: V_lo, V_hi at +s*2*KT
     static constexpr int OFF_BAR = OFF_V + NV * 2 * KT;
     static constexpr int OFF_MISC = OFF_BAR + 256;
-    static constexpr int USED = OFF_MISC + 64;
+    static constexpr int OFF_EPI = OFF_MISC + 64;  // 2 KB per softmax warp: coalesced O stores
+    static constexpr int USED = OFF_EPI + 4 * 2048;
     static constexpr int SMEM = USED + 1024;       // two CTAs per SM
     static constexpr uint32_t C_O = 64 * NSB;      // S buffers at 0, 64 (, 128); O_lo | O_hi at C_O
     static constexpr uint32_t TMEM_COLS = 256;
@@ -367,23 +368,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap tm_pk, const __grid_constant__ CU
             const size_t row = (size_t)bh * N + (valid ? i : 0);
             if (valid) lse[row] = (m + __log2f(l)) * kLn2;
             const float inv_l = 1.f / l;
+            // the warp's 32 query rows, coalesced through its staging buffer
+            const int r0 = q0 + q4 * 32;
             uint32_t v[D];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 tmem_ld_row<D>(trow + C::C_O + h * D, v);
                 tmem_wait_ld();
-                if (valid) {
-                    bf16* o = (h == 0 ? o_lo : o_hi) + row * D;
+                uint32_t w[D / 2];
 #pragma unroll
-                    for (int e = 0; e < D; e += 8) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(v[e + 0]) * inv_l, __uint_as_float(v[e + 1]) * inv_l);
-                        w.y = pack_bf16x2(__uint_as_float(v[e + 2]) * inv_l, __uint_as_float(v[e + 3]) * inv_l);
-                        w.z = pack_bf16x2(__uint_as_float(v[e + 4]) * inv_l, __uint_as_float(v[e + 5]) * inv_l);
-                        w.w = pack_bf16x2(__uint_as_float(v[e + 6]) * inv_l, __uint_as_float(v[e + 7]) * inv_l);
-                        *reinterpret_cast<uint4*>(o + e) = w;
-                    }
-                }
+                for (int e = 0; e < D / 2; ++e)
+                    w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * inv_l, __uint_as_float(v[2 * e + 1]) * inv_l);
+                store_rows_staged<D>(sb + C::OFF_EPI + 2048u * (warp - 2), w,
+                                     reinterpret_cast<uint16_t*>((h == 0 ? o_lo : o_hi) + ((size_t)bh * N + r0) * D), D,
+                                     N - r0, lane);
             }
         }
     }

@@ -208,6 +208,45 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+    return v;
+}
+
+// Stores a warp's 32 consecutive rows of D bf16 values (row r of the warp held
+// by lane r as D/2 bf16 pairs w) to row0 + r*ld, rows r < nvalid only, with
+// coalesced 16-byte stores: the rows go through a 2 KB per-warp staging buffer
+// at stg (16-byte chunks XOR-swizzled within each 128-byte line, so that both
+// the row-wise writes and the linear reads are free of bank conflicts), then
+// out in linear order, 512 contiguous bytes per warp store where rows are
+// contiguous.  Writing a row per lane straight to global memory makes every
+// warp store touch 32 lines.
+template <int D>
+__device__ __forceinline__ void store_rows_staged(uint32_t stg, const uint32_t (&w)[D / 2], uint16_t* row0, long long ld,
+                                                  int nvalid, int lane) {
+    constexpr int CH = D / 8;                      // 16-byte chunks per row
+    constexpr int R = 1024 / D < 32 ? 1024 / D : 32;  // rows per 2 KB round
+    auto swz = [](uint32_t idx) { return (idx & ~7u) | ((idx & 7u) ^ ((idx >> 3) & 7u)); };
+#pragma unroll
+    for (int rr = 0; rr < 32 / R; ++rr) {
+        if (lane / R == rr) {
+            const uint32_t r = (uint32_t)(lane - rr * R);
+#pragma unroll
+            for (int c = 0; c < CH; ++c)
+                st_shared_v4(stg + 16u * swz(r * CH + c), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < R * CH / 32; ++k) {
+            const uint32_t idx = (uint32_t)lane + 32u * k;
+            const int r = rr * R + (int)(idx / CH), c = (int)(idx % CH);
+            const uint4 v = ld_shared_v4(stg + 16u * swz(idx));
+            if (r < nvalid) *reinterpret_cast<uint4*>(row0 + (long long)r * ld + 8 * c) = v;
+        }
+        __syncwarp();
+    }
+}
 
 }  // namespace tc
 }  // namespace psa

@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <map>
 #include <mutex>
 #include <set>
 #include <utility>
@@ -25,6 +26,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder(std::string* err) {
     });
     if (!fn) *err = std::string("cuTensorMapEncodeTiled unavailable: ") + cudaGetErrorString(st);
     return fn;
+}
+
+__device__ unsigned g_smem_base;
+
+// Writes the shared-window address of its dynamic shared memory.
+__global__ void smem_base_probe_kernel() {
+    extern __shared__ __align__(16) unsigned char dyn[];
+    if (threadIdx.x == 0) {
+        unsigned a;
+        asm volatile("{ .reg .u64 p; cvta.to.shared.u64 p, %1; cvt.u32.u64 %0, p; }" : "=r"(a) : "l"(dyn));
+        g_smem_base = a;
+    }
 }
 
 }  // namespace
@@ -108,6 +121,46 @@ bool set_max_dynamic_smem(const void* kernel, int bytes, std::string* err) {
     }
     done.insert({dev, kernel});
     return true;
+}
+
+}  // namespace psa
+
+namespace psa {
+
+int dyn_smem_base_aligned(std::string* err) {
+    static std::mutex mu;
+    static std::map<int, int> known;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        *err = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+        return -1;
+    }
+    std::lock_guard<std::mutex> g(mu);
+    auto it = known.find(dev);
+    if (it != known.end()) return it->second;
+    // a private stream, and this thread's capture mode relaxed for the probe, so
+    // that a first call made while the caller's stream is being captured works
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    cudaStream_t st = nullptr;
+    unsigned base = 1;
+    e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+    if (e == cudaSuccess) {
+        smem_base_probe_kernel<<<1, 32, 1024, st>>>();
+        e = cudaGetLastError();
+        if (e == cudaSuccess) e = cudaMemcpyFromSymbolAsync(&base, g_smem_base, sizeof(base), 0, cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        cudaStreamDestroy(st);
+    }
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    if (e != cudaSuccess) {
+        *err = std::string("shared memory base probe: ") + cudaGetErrorString(e);
+        return -1;
+    }
+    const int ok = (base & 1023u) == 0 ? 1 : 0;
+    known[dev] = ok;
+    return ok;
 }
 
 }  // namespace psa

@@ -38,4 +38,11 @@ bool encode_f32_rows(CUtensorMap* map, const void* base, int D, int N, long long
 // Returns false and sets *err on failure.
 bool set_max_dynamic_smem(const void* kernel, int bytes, std::string* err);
 
+// 1 if the dynamic shared memory of a kernel without static shared memory
+// starts on a 1024-byte boundary on the current device (kernels whose 128B-
+// swizzled layout fills shared memory leave no room to align it themselves),
+// 0 if not, -1 on a CUDA error (*err set).  A one-thread probe kernel, run
+// once per device on a private stream.
+int dyn_smem_base_aligned(std::string* err);
+
 }  // namespace psa
