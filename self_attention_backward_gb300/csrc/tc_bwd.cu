@@ -40,14 +40,16 @@
 // waits for its own MMAs in flight.  The issuing thread precomputes every
 // descriptor so that issuing an MMA is one add per operand.
 //
-// Warp roles: warp 0 TMA producer (Q, dO_lo, dO_hi and the sub-tile's row
-// statistics per stage), warp 1 MMA issuer (one thread) and TMEM owner, warps
-// 2-5 / 6-9 softmax-gradient warpgroups 0 / 1 (one key row per thread), warps
-// 10-13 dQ drain (one query row per thread; the partials go to the fp32
-// accumulator by TMA bulk reduce) and then the dK/dV epilogue (one key row per
-// thread), warp 14 the dQ MMA issuer; for
-// d <= 32 warp 15 issues the odd sub-tiles' main MMAs and warp 1 the even ones
-// (512 threads, else 480).
+// Persistent: one CTA per SM walks work items (units of one (batch*head,
+// 128-key tile), or pieces of one along the queries) in turn (see the kernel).
+//
+// Warp roles: warp 0 TMA producer (each item's K/V tile; the Q/dO stages: Q,
+// dO_lo, dO_hi and the sub-tile's row statistics), warp 1 MMA issuer (one thread) and TMEM owner,
+// warps 2-5 / 6-9 softmax-gradient warpgroups 0 / 1 (one key row per thread),
+// warps 10-13 dQ drain (one query row per thread; the partials go to the fp32
+// accumulator by TMA bulk reduce) and then each item's dK/dV epilogue (one key
+// row per thread), warp 14 the dQ MMA issuer; for d <= 32 warp 15 issues the
+// odd sub-tiles' main MMAs and warp 1 the even ones (512 threads, else 480).
 //
 // Every mbarrier wait is bounded (kTimeoutNs); on timeout the CTA sets a device
 // error word (read by psa_attn_sync_status), skips the rest of its work, waits
@@ -119,14 +121,7 @@ struct Cfg {
     static constexpr int OFF_ST = OFF_DQS + NDQS * DQS_BYTES;
     static constexpr int OFF_BAR = OFF_ST + NST * 512;     // mbarriers (48)
     static constexpr int OFF_MISC = OFF_BAR + 384;
-    // The dK/dV epilogue: at head_dim 64 the drain warps run it after their last
-    // group, staging in the dQ buffer (shared memory has no room for more); at
-    // head_dim <= 32 softmax warpgroup 0 runs it as soon as the last MMAs are
-    // done, with 2 KB of its own per warp (the drain's last group then runs
-    // beside it).
-    static constexpr bool EPI_DRAIN = D == 64;
-    static constexpr int OFF_EPI = OFF_MISC + 64;
-    static constexpr int USED = OFF_EPI + (EPI_DRAIN ? 0 : 4 * 2048);
+    static constexpr int USED = OFF_MISC + 64;
     // + 1 KB to align the base to 1024 where that fits; at head_dim 64 it does
     // not, and the host checks once per device that the base is aligned
     // (dyn_smem_base_aligned).  At least 116 KB so that one CTA owns an SM (its
@@ -142,7 +137,7 @@ struct Cfg {
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(C_DQ + D <= TMEM_COLS, "TMEM budget");
     static_assert(USED <= 232448, "shared memory budget");
-    static_assert(!EPI_DRAIN || NDQS * DQS_BYTES >= 4 * 2048, "the epilogue stages 2 KB per drain warp");
+    static_assert(NDQS * DQS_BYTES >= 4 * 2048, "the epilogue stages 2 KB per drain warp");
     static_assert(NST > NB, "the softmax's wait for the stage of u+NB would wait on its own release");
 };
 
@@ -178,10 +173,10 @@ static_assert(B_DQE + 2 <= 32, "barrier area holds 32 barriers");
 // (u - 2NB) before this one.  DQF, DQE, DQA as above.
 enum {
     F_KV = 0, F_SFS = 1, F_SFD = 7, F_PF = 13, F_ACC = 21, F_ACCB = 22, F_DQA = 23, F_QF = 24, F_QE = 30, F_DQF = 36,
-    F_DQE = 38
+    F_DQE = 38, F_KVE = 40, F_EPI = 41
 };
 constexpr int kPfRingF = 8;
-static_assert(F_DQE + 2 <= 48, "barrier area holds 48 barriers");
+static_assert(F_EPI + 1 <= 48, "barrier area holds 48 barriers");
 
 // P and dS of one 32-query chunk of this thread's key row, packed to bf16
 // pairs: P = exp2(S * scale*log2e - L), dS = P (dP - D).
@@ -209,42 +204,92 @@ __device__ __forceinline__ void softmax_vals(const uint32_t (&sr)[32], const uin
 // The epilogue of one warp: dK (scaled), dV_lo, dV_hi of the warp's 32 key
 // rows (TMEM lane quarter q4) as bf16 into d_packed sections 1-3, coalesced
 // through the warp's 2 KB staging buffer stg; or, for a piece of a split unit,
-// the fp32 partials into dkv_part.  Every main MMA must be complete.
+// the fp32 partials into dkv_part.  Every main MMA of the item must be
+// complete; each thread arrives on epi_bar once it has read its accumulators.
 template <int D, typename C>
-__device__ __forceinline__ void dkdv_epilogue(uint32_t tmem, int q4, int lane, uint32_t stg, bf16* d_packed,
-                                              int bh, int k0, int N, long long ldq, float scale, int piece,
-                                              float* dkv_part) {
+__device__ __forceinline__ void dkdv_epilogue(uint32_t tmem, int q4, int lane, uint32_t stg, uint32_t epi_bar,
+                                              bf16* d_packed, int bh, int k0, int N, long long ldq, float scale,
+                                              int piece, float* dkv_part) {
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
     const int jl = q4 * 32 + lane;
     const size_t sec = (size_t)N * ldq;
     // row 0 of this warp's 32 key rows in section 0 of the slice
     bf16* wrow0 = d_packed + (size_t)bh * 4 * sec + (size_t)(k0 + q4 * 32) * ldq;
-    uint32_t v[D];
+    // 32 columns (16 at head_dim 16) at a time
+    constexpr int W = D < 32 ? D : 32;
 #pragma unroll
     for (int which = 0; which < 3; ++which) {
         const uint32_t col = which == 0 ? C::C_DK : C::C_DV + (which - 1) * D;
         const float mul = which == 0 ? scale : 1.f;
-        tmem_ld_row<D>(trow + col, v);
-        tmem_wait_ld();
-        if (piece >= 0) {
-            // a piece's partial: [piece][key row][dK | dV_lo | dV_hi] fp32
-            float4* o = reinterpret_cast<float4*>(dkv_part + ((size_t)piece * C::BM + jl) * 3 * D + which * D);
 #pragma unroll
-            for (int e = 0; e < D; e += 4)
-                o[e / 4] = make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
-                                       __uint_as_float(v[e + 3]));
-        } else {
-            uint32_t w[D / 2];
+        for (int h = 0; h < D / W; ++h) {
+            uint32_t v[W];
+            tmem_ld_row<W>(trow + col + W * h, v);
+            tmem_wait_ld();
+            if (which == 2 && h == D / W - 1) {
+                // every accumulator column this thread reads is in registers
+                tc_fence_before();
+                mbar_arrive(epi_bar);
+            }
+            if (piece >= 0) {
+                // a piece's partial: [piece][key row][dK | dV_lo | dV_hi] fp32
+                float4* o = reinterpret_cast<float4*>(dkv_part + ((size_t)piece * C::BM + jl) * 3 * D + which * D +
+                                                      W * h);
 #pragma unroll
-            for (int e = 0; e < D / 2; ++e)
-                w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-            store_rows_staged<D>(stg, w, reinterpret_cast<uint16_t*>(wrow0 + (size_t)(1 + which) * sec), ldq,
-                                 N - (k0 + q4 * 32), lane);
+                for (int e = 0; e < W; e += 4)
+                    o[e / 4] = make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                                           __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+            } else {
+                uint32_t w[W / 2];
+#pragma unroll
+                for (int e = 0; e < W / 2; ++e)
+                    w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+                store_rows_staged<W>(stg, w, reinterpret_cast<uint16_t*>(wrow0 + (size_t)(1 + which) * sec) + W * h,
+                                     ldq, N - (k0 + q4 * 32), lane);
+            }
         }
     }
 }
 
+// A work item of the fused kernel: a (batch*head, 128-key tile) unit, or, for
+// the units of the last, partial wave, one of tail_f pieces of a unit along
+// the query axis (whole 128-query groups); a piece writes its dK/dV as fp32
+// partials, summed by the finalize kernel.  nsub 64-query sub-tiles starting
+// at sub-tile ubase of the slice.
+struct Item {
+    int bh, k0, ubase, nsub, piece;
+};
+__device__ __forceinline__ Item decode_item(int x, int nfull, int tail_f, int nsub_all, int nkt) {
+    Item t;
+    int unit = x;
+    t.ubase = 0;
+    t.nsub = nsub_all;
+    t.piece = -1;
+    if (unit >= nfull) {
+        t.piece = unit - nfull;
+        unit = nfull + t.piece / tail_f;
+        const int p = t.piece % tail_f, ng = (nsub_all + 1) / 2;
+        const int gb = p * ng / tail_f, ge = (p + 1) * ng / tail_f;
+        t.ubase = 2 * gb;
+        t.nsub = min(2 * ge, nsub_all) - t.ubase;
+    }
+    t.bh = unit / nkt;
+    t.k0 = (unit % nkt) * 128;
+    return t;
+}
+
 // ---------------------------------------------------------------- main kernel
+// Persistent: CTA b walks the work items b, b + gridDim.x, ... in turn.  Every
+// ring of the CTA (Q/dO stages, S/dP buffers, their barriers, PF, the dS ring,
+// the dQ barriers) runs on sub-tile and 128-query-group numbers U and G counted
+// across its items, so the producer fetches the next item's stages while the
+// current item ends, and the next item's K/V tile, S/dP products and softmax
+// overlap the current item's last dQ products, drain and epilogue.  Per item:
+// KV (its K/V tile landed) and KVE (the dQ issuer's commit after the item's
+// last dQ product: no MMA reads that tile any more); ACC / ACCB (each main
+// issuer's commit after its last dV/dK of the item); EPI (the drain warps have
+// read the item's dK/dV accumulators, which the next item's first dV/dK
+// overwrite).
 // CM: dO_lo / dO_hi come as channel-major [d, N] blocks (4-D maps over
 // [B][heads][d][N]); else as rows (4-D maps over [B][heads][N][d]).  The
 // stage's dO tiles then hold [d][64 queries] (128-byte rows), which the dP^T
@@ -253,8 +298,9 @@ template <int D, bool CM>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
 bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_do_lo, const __grid_constant__ CUtensorMap tm_do_hi,
-                const __grid_constant__ CUtensorMap tm_dq, int heads, long long ldq, const float4* __restrict__ stats, float* __restrict__ dq_acc, bf16* __restrict__ d_packed, int N,
-                int nkt, float scale, float scale_log2, int nfull, int tail_f, float* __restrict__ dkv_part) {
+                const __grid_constant__ CUtensorMap tm_dq, int heads, long long ldq, const float4* __restrict__ stats,
+                bf16* __restrict__ d_packed, int N, int nkt, float scale, float scale_log2, int nfull, int tail_f,
+                int nitems, float* __restrict__ dkv_part) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = C::SLACK ? reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023))
@@ -264,27 +310,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 16);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Work unit = (batch*head, key tile).  The units of the last, partial wave
-    // (blocks >= nfull) are each split into tail_f query ranges of whole
-    // 128-query groups; such a piece writes fp32 dK/dV partials to dkv_part,
-    // summed by the finalize kernel.  Sub-tile indices below are local to the
-    // CTA's range, which starts at sub-tile ubase.
     const int nsub_all = (N + C::BS - 1) / C::BS;
-    int unit = (int)blockIdx.x, ubase = 0, nsub = nsub_all, piece = -1;
-    if (unit >= nfull) {
-        piece = unit - nfull;
-        unit = nfull + piece / tail_f;
-        const int p = piece % tail_f, ng = (nsub_all + 1) / 2;
-        const int gb = p * ng / tail_f, ge = (p + 1) * ng / tail_f;
-        ubase = 2 * gb;
-        nsub = min(2 * ge, nsub_all) - ubase;
-    }
-    const int bh = unit / nkt, kt = unit % nkt;
-    const int k0 = kt * C::BM;
-    const int ngrp = (nsub + 1) / 2;              // 128-query groups (dQ granularity)
+    // sub-tiles over all of this CTA's items
+    int UT = 0;
+    for (int x = blockIdx.x; x < nitems; x += gridDim.x) UT += decode_item(x, nfull, tail_f, nsub_all, nkt).nsub;
 
     if (threadIdx.x == 0) {
         mbar_init(sy.bar(F_KV), 1);
+        mbar_init(sy.bar(F_KVE), 1);
+        mbar_init(sy.bar(F_EPI), 128);
         for (int b = 0; b < 2 * C::NB; ++b) {
             mbar_init(sy.bar(F_SFS + b), 1);
             mbar_init(sy.bar(F_SFD + b), 1);
@@ -308,8 +342,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         tma_prefetch_desc(&tm_do_lo);
         tma_prefetch_desc(&tm_do_hi);
     }
-    // the dS ring starts zeroed: a last, half-filled 128-query group reads a
-    // block no sub-tile wrote (rows of queries >= N, discarded, but finite)
+    // the dS ring starts zeroed: a half-filled 128-query group (an item's last)
+    // reads a block its second sub-tile did not write (rows of queries past the
+    // item, discarded, but finite)
     for (int x = threadIdx.x; x < 4 * 16384 / 16; x += C::THREADS)
         st_shared_v4(sb + C::OFF_DS + 16 * x, 0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
@@ -324,54 +359,72 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
+        // Per item: its K/V tile, once no MMA reads the previous one (KVE), then
+        // its Q/dO stages in turn (Q, dO_lo, dO_hi and the sub-tile's statistics:
+        // 32 float4 per 64-query sub-tile, padded rows -inf and 0, written by the
+        // preprocess kernel), each as soon as the stage is free (QE).  The whole
+        // warp waits, lane 0 issues: a single polling lane fed the pipeline
+        // measurably later.  An item's stages are not fetched before the previous
+        // item has finished with its K/V tile; nothing of that item waits for them
+        // (the softmax fetches its next sub-tile's statistics early only within
+        // an item).
         int last_issued[C::NST];
 #pragma unroll
         for (int s = 0; s < C::NST; ++s) last_issued[s] = -1;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(sy.bar(F_KV), 3 * C::KTILE);
-            tma_load_3d(sb + C::OFF_K, &tm_kv, 0, k0, bh * 4 + 1, sy.bar(F_KV));
-            tma_load_3d(sb + C::OFF_VL, &tm_kv, 0, k0, bh * 4 + 2, sy.bar(F_KV));
-            tma_load_3d(sb + C::OFF_VH, &tm_kv, 0, k0, bh * 4 + 3, sy.bar(F_KV));
-        }
-        // the slice's statistics, 32 float4 per 64-query sub-tile (padded rows
-        // hold -inf and 0), written by the preprocess kernel
-        const float4* st_slice = stats + (size_t)bh * nsub_all * 32;
-        int s = 0, ph = 0;
-        for (int u = 0; u < nsub; ++u) {
-            if (!warp_wait(sy, sy.bar(F_QE + s), ph ^ 1, 0, u)) break;
+        int U = 0, it = 0;
+        bool ok = true;
+        for (int x = blockIdx.x; x < nitems && ok; x += gridDim.x, ++it) {
+            const Item t = decode_item(x, nfull, tail_f, nsub_all, nkt);
+            if (it > 0 && !warp_wait(sy, sy.bar(F_KVE), (it - 1) & 1, 0, -1)) break;
             if (lane == 0) {
-                const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE;
-                mbar_arrive_expect_tx(sy.bar(F_QF + s), 3 * C::QTILE + 512);
-                const int q0 = (ubase + u) * C::BS;
-                tma_load_3d(st, &tm_q, 0, q0, bh * 4 + 0, sy.bar(F_QF + s));
-                const int hh = bh % heads, bb = bh / heads;
-                tma_load_4d(st + C::QTILE, &tm_do_lo, CM ? q0 : 0, CM ? 0 : q0, hh, bb, sy.bar(F_QF + s));
-                tma_load_4d(st + 2 * C::QTILE, &tm_do_hi, CM ? q0 : 0, CM ? 0 : q0, hh, bb, sy.bar(F_QF + s));
-                bulk_load(sb + C::OFF_ST + s * 512, st_slice + (size_t)(ubase + u) * 32, 512, sy.bar(F_QF + s));
+                mbar_arrive_expect_tx(sy.bar(F_KV), 3 * C::KTILE);
+                tma_load_3d(sb + C::OFF_K, &tm_kv, 0, t.k0, t.bh * 4 + 1, sy.bar(F_KV));
+                tma_load_3d(sb + C::OFF_VL, &tm_kv, 0, t.k0, t.bh * 4 + 2, sy.bar(F_KV));
+                tma_load_3d(sb + C::OFF_VH, &tm_kv, 0, t.k0, t.bh * 4 + 3, sy.bar(F_KV));
             }
+            const float4* st_slice = stats + (size_t)t.bh * nsub_all * 32;
+            const int hh = t.bh % heads, bb = t.bh / heads;
+            for (int u = 0; u < t.nsub; ++u, ++U) {
+                const int s = U % C::NST;
+                if (!warp_wait(sy, sy.bar(F_QE + s), ((U / C::NST) & 1) ^ 1, 0, U)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE;
+                    mbar_arrive_expect_tx(sy.bar(F_QF + s), 3 * C::QTILE + 512);
+                    const int q0 = (t.ubase + u) * C::BS;
+                    tma_load_3d(st, &tm_q, 0, q0, t.bh * 4 + 0, sy.bar(F_QF + s));
+                    tma_load_4d(st + C::QTILE, &tm_do_lo, CM ? q0 : 0, CM ? 0 : q0, hh, bb, sy.bar(F_QF + s));
+                    tma_load_4d(st + 2 * C::QTILE, &tm_do_hi, CM ? q0 : 0, CM ? 0 : q0, hh, bb, sy.bar(F_QF + s));
+                    bulk_load(sb + C::OFF_ST + s * 512, st_slice + (size_t)(t.ubase + u) * 32, 512, sy.bar(F_QF + s));
+                }
 #pragma unroll
-            for (int x = 0; x < C::NST; ++x)
-                if (x == s) last_issued[x] = u;
-            if (++s == C::NST) { s = 0; ph ^= 1; }
+                for (int y = 0; y < C::NST; ++y)
+                    if (y == s) last_issued[y] = U;
+            }
         }
         __syncwarp();
         if (*sy.abort && lane == 0) {
             // let this CTA's own copies land before its shared memory is released
-            wait_drain(sy.bar(F_KV), 0);
+            if (it > 0) wait_drain(sy.bar(F_KV), (it - 1) & 1);
 #pragma unroll
-            for (int x = 0; x < C::NST; ++x)
-                if (last_issued[x] >= 0) wait_drain(sy.bar(F_QF + x), (last_issued[x] / C::NST) & 1);
+            for (int y = 0; y < C::NST; ++y)
+                if (last_issued[y] >= 0) wait_drain(sy.bar(F_QF + y), (last_issued[y] / C::NST) & 1);
         }
     } else if (warp == 1 || warp == 15) {
         // ------------------------------------------------------------ main MMA issuers
-        // warp 1 takes the even sub-tiles, warp 15 the odd ones.  Each issues, per
-        // sub-tile u of its parity, dV/dK(u) once PF(u) shows P/dS(u) ready, then
-        // S/dP(u + NB) into the buffer dV/dK(u) just read: one thread's MMAs run in
-        // issue order, so the buffer is reused only after its last reader.  While
-        // one thread waits for its next PF (such a wait first lets its own MMAs in
-        // flight finish), the other's keep the tensor core fed.
+        // With two issuers warp 1 takes the even sub-tiles U, warp 15 the odd ones
+        // (numbered across items).  Each issues, per sub-tile U of its parity,
+        // dV/dK(U) once PF(U) shows P/dS(U) ready, then S/dP(U + NB) into the
+        // buffer dV/dK(U) just read when U + NB is in the same item: one thread's
+        // MMAs run in issue order, so the buffer is reused only after its last
+        // reader.  Warp 1 issues each item's first NB S/dP products (the item
+        // prologue), after the other issuer's last dV/dK of the previous item
+        // (whose buffers they reuse; its QE commit), the item's K/V and stages.
+        // While one thread waits for its next PF (such a wait first lets its own
+        // MMAs in flight finish), the other's keep the tensor core fed.
         const int par = warp == 1 ? 0 : 1;
-        constexpr int USTEP = C::TWO_ISSUERS ? 2 : 1;
         if (lane == 0) {
             constexpr uint32_t ID_S = idesc_bf16(128, 64, 0, 0);     // S^T: 64 queries
             // dP^T: B = dO rows (K-major), or MN-major from channel-major tiles
@@ -396,10 +449,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             const uint64_t dDoCm = smem_desc(sb + C::OFF_STAGE + C::QTILE, 8192, 1024, 2);
             const uint64_t dDvCm = smem_desc(sb + C::OFF_STAGE + C::QTILE, 16, 1024, 2);
 
-            // S^T(u) and dP^T(u) into the two halves of TMEM buffer u % NB, each with
-            // its own barrier.  Their Q/dO stage is known to be loaded: the prologue
-            // waits for it, later the softmax warpgroup that arrives PF(u-NB) has
-            // waited for it first.
+            // S^T(U) and dP^T(U) into the two halves of TMEM buffer U % NB, each with
+            // its own barrier.  Their Q/dO stage is known to be loaded: the item
+            // prologue waits for it, later the softmax warpgroup that arrives
+            // PF(U-NB) has waited for it first.
             auto issue_s = [&](int u) {
                 const uint64_t dQs = dStage0 + STAGE_U * (u % C::NST);
                 const uint32_t tS = tmem + 128u * (u % C::NB);
@@ -427,64 +480,92 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 }
                 mma_commit(sy.bar(F_SFD + u % (2 * C::NB)));
             };
-            // dV of sub-tile u (A = P^T from the S half, 64 queries = 4 k-steps)
-            auto issue_dv = [&](int u) {
+            // dV of sub-tile u (A = P^T from the S half, 64 queries = 4 k-steps);
+            // the item's first sub-tile (ul == 0) overwrites the accumulators
+            auto issue_dv = [&](int u, int ul) {
                 // [dO_lo | dO_hi]: MN-major rows, or K-major channel-major tiles
                 const uint64_t dG = (CM ? dDvCm : dStage0mn) + STAGE_U * (u % C::NST);
                 constexpr uint32_t DV_STEP = CM ? 2u : KSTEP;
 #pragma unroll
                 for (int kk = 0; kk < C::BS / 16; ++kk)
                     mma_bf16_ts(tmem + C::C_DV, tmem + 128u * (u % C::NB) + 8 * kk, dG + DV_STEP * kk, ID_DV,
-                                (u > 0 || kk > 0) ? 1u : 0u);
+                                (ul > 0 || kk > 0) ? 1u : 0u);
             };
             // dK of sub-tile u (A = dS^T from the dP half); then the stage is free
-            auto issue_dk = [&](int u) {
+            auto issue_dk = [&](int u, int ul) {
                 const uint64_t dQmn = dStage0 + STAGE_U * (u % C::NST);     // Q rows, MN-major
 #pragma unroll
                 for (int kk = 0; kk < C::BS / 16; ++kk)
                     mma_bf16_ts(tmem + C::C_DK, tmem + 128u * (u % C::NB) + 64 + 8 * kk, dQmn + KSTEP * kk, ID_DK,
-                                (u > 0 || kk > 0) ? 1u : 0u);
+                                (ul > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(sy.bar(F_QE + u % C::NST));
             };
-            bool ok = wait_bounded(sy, sy.bar(F_KV), 0, 1, -1);
-            if (par == 0) {
-                for (int u = 0; u < C::NB && u < nsub && ok; ++u)
-                    ok = wait_bounded(sy, sy.bar(F_QF + u), 0, 1, u);
-                if (ok) {
+            const uint32_t acc_bar = sy.bar(par == 0 ? F_ACC : F_ACCB);
+            bool ok = true;
+            int U0 = 0, it = 0, last_odd = -1;
+            for (int x = blockIdx.x; x < nitems; x += gridDim.x, ++it) {
+                const Item t = decode_item(x, nfull, tail_f, nsub_all, nkt);
+                if (par == 0) {
+                    // item prologue: S/dP of the first NB sub-tiles
+                    if (C::TWO_ISSUERS && last_odd >= 0)
+                        ok = wait_bounded(sy, sy.bar(F_QE + last_odd % C::NST), (last_odd / C::NST) & 1, 1, last_odd);
+                    if (ok) ok = wait_bounded(sy, sy.bar(F_KV), it & 1, 1, -1);
+                    for (int j = 0; j < C::NB && j < t.nsub && ok; ++j)
+                        ok = wait_bounded(sy, sy.bar(F_QF + (U0 + j) % C::NST), ((U0 + j) / C::NST) & 1, 1, U0 + j);
+                    if (!ok) break;
                     tc_fence_after();
-                    for (int u = 0; u < C::NB && u < nsub; ++u) {
-                        issue_s(u);
-                        issue_dp(u);
+                    for (int j = 0; j < C::NB && j < t.nsub; ++j) {
+                        issue_s(U0 + j);
+                        issue_dp(U0 + j);
                     }
                 }
-            } else if (nsub > 1 && ok && C::TWO_ISSUERS) {
-                // dV/dK(0), whose first MMAs overwrite the accumulators, must be done
-                // before this thread adds to them: its commit is QE(0)'s first phase
-                ok = wait_bounded(sy, sy.bar(F_QE + 0), 0, 1, 0);
-            }
-            // PF(u) also certifies that the Q/dO stage of u+NB is loaded (the
-            // softmax warpgroup waited for it).  The tensor core runs one thread's
-            // MMAs in issue order: S^T(u+NB) follows dV(u), the last reader of the
-            // S half, and dP^T(u+NB) follows dK(u), the last reader of the dP half;
-            // the softmax of u+NB starts on S^T while dK(u) and dP^T(u+NB) run.
-            for (int u = par; u < nsub && ok; u += USTEP) {
-                ok = wait_bounded(sy, sy.bar(F_PF + u % kPfRingF), (u / kPfRingF) & 1, 1, u);
+                // PF(U) also certifies that the stage of U+NB is loaded (the softmax
+                // warpgroup waited for it).  S^T(U+NB) follows dV(U), the last reader
+                // of the S half, and dP^T(U+NB) follows dK(U), the last reader of the
+                // dP half; the softmax of U+NB starts on S^T while dK(U) and
+                // dP^T(U+NB) run.  Before its first dV/dK of an item a thread waits
+                // for the previous item's epilogue (EPI) and, if it does not own the
+                // item's first sub-tile, for that sub-tile's dV/dK (QE), which zero
+                // the accumulators.
+                bool first = true;
+                for (int ul = 0; ul < t.nsub; ++ul) {
+                    const int U = U0 + ul;
+                    if (C::TWO_ISSUERS && (U & 1) != par) continue;
+                    ok = wait_bounded(sy, sy.bar(F_PF + U % kPfRingF), (U / kPfRingF) & 1, 1, U);
+                    if (ok && first) {
+                        if (it > 0) ok = wait_bounded(sy, sy.bar(F_EPI), (it - 1) & 1, 1, U);
+                        if (ok && ul != 0) ok = wait_bounded(sy, sy.bar(F_QE + U0 % C::NST), (U0 / C::NST) & 1, 1, U);
+                        first = false;
+                    }
+                    if (!ok) break;
+                    tc_fence_after();
+                    const bool more = ul + C::NB < t.nsub;
+                    issue_dv(U, ul);
+                    if (more) issue_s(U + C::NB);
+                    issue_dk(U, ul);
+                    if (more) issue_dp(U + C::NB);
+                }
+                // a thread without a sub-tile in this item: the ACC phases stay in
+                // step with the epilogue's waits
+                if (ok && first && it > 0) ok = wait_bounded(sy, sy.bar(F_EPI), (it - 1) & 1, 1, -1);
                 if (!ok) break;
-                tc_fence_after();
-                const int v = u + C::NB;
-                issue_dv(u);
-                if (v < nsub) issue_s(v);
-                issue_dk(u);
-                if (v < nsub) issue_dp(v);
+                mma_commit(acc_bar);
+                const int last = U0 + t.nsub - 1;
+                last_odd = (last & 1) ? last : (last - 1 >= U0 ? last - 1 : -1);
+                U0 += t.nsub;
             }
-            // all of this thread's MMAs done (also on abort, before TMEM is freed)
-            const uint32_t acc_bar = sy.bar(par == 0 ? F_ACC : F_ACCB);
-            mma_commit(acc_bar);
-            wait_drain(acc_bar, 0);
+            // all of this thread's MMAs done before TMEM is freed (also on abort)
+            if (ok) {
+                if (it > 0) wait_drain(acc_bar, (it - 1) & 1);
+            } else {
+                mma_commit(acc_bar);
+                wait_drain(acc_bar, it & 1);
+            }
         }
         __syncwarp();
     } else if (warp < 10) {
         // ------------------------------------------------------------ softmax-gradient warpgroups
+        // Warpgroup grp takes the sub-tiles U of parity grp (numbered across items).
         // TMEM fragments of the 16x256b shape: in each 16-lane half hb of the
         // warp's lane quarter, thread t holds key rows 16 hb + t/4 and 16 hb + 8 + t/4
         // and, of the sub-tile's 64 queries, the pairs 8k + 2(t%4), +1 (k < 8).  So
@@ -493,7 +574,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         const int grp = (warp - 2) >> 2;         // 0: even sub-tiles, 1: odd
         const int q4 = warp & 3;                 // TMEM lane quarter of this warp
         const int tq = lane & 3, tr = lane >> 2;
-        const bool full = k0 + C::BM <= N;       // uniform: no padded keys in this tile
         const uint64_t cs2 = f2_pack(scale_log2, scale_log2);
         // this thread's 8 query pairs of a stage: {-LSE log2(e) x2, D x2} (the
         // producer writes a stage's statistics before its QF arrive, and the stage
@@ -505,29 +585,48 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             for (int k = 0; k < 8; ++k) stat[k] = St[4 * k];
         };
         bool ok = true;
-        if (grp < nsub) {
+        if (grp < UT) {
             ok = warp_wait(sy, sy.bar(F_QF + grp % C::NST), (grp / C::NST) & 1, 2, grp);
             if (ok) load_stats(grp);
         }
-        for (int u = grp; u < nsub && ok; u += 2) {
-            const int buf = u % C::NB;
-            // One round trip for S^T(u) and the dQ product that last read dS block
-            // u & 3: it held sub-tile u-4, of 128-query group h, whose product must
-            // have read it before this sub-tile writes it.  The parity test on
-            // DQF + (h & 1) is exact: group h-2 was waited for at sub-tile u-4 by
-            // this warpgroup, and group h+2 needs PF(u).  (The product is almost
+        // the item holding sub-tile U: t, its first sub-tile U0 and group G0
+        int xi = blockIdx.x, U0 = 0, G0 = 0;
+        Item t = decode_item(xi, nfull, tail_f, nsub_all, nkt);
+        for (int U = grp; U < UT && ok; U += 2) {
+            while (U >= U0 + t.nsub) {
+                U0 += t.nsub;
+                G0 += (t.nsub + 1) / 2;
+                xi += gridDim.x;
+                t = decode_item(xi, nfull, tail_f, nsub_all, nkt);
+            }
+            const int ul = U - U0, G = G0 + (ul >> 1);
+            const int k0 = t.k0;
+            const bool full = k0 + C::BM <= N;   // uniform: no padded keys in this tile
+            if (ul < 2 && U != grp) {
+                // this warpgroup's first sub-tile of a later item: its statistics
+                // were not fetched ahead (the stage may load only after the
+                // previous item's last sub-tiles)
+                ok = warp_wait(sy, sy.bar(F_QF + U % C::NST), (U / C::NST) & 1, 2, U);
+                if (!ok) break;
+                load_stats(U);
+            }
+            const int buf = U % C::NB;
+            // One round trip for S^T(U) and the dQ product that last read the
+            // sub-tile's dS ring block 2 (G & 1) + (ul & 1): dQ(G-2).  The parity
+            // test on DQF + (G & 1) is exact: dQ(G-4) was waited for by this
+            // warpgroup earlier, and dQ(G) needs PF(U).  (The product is almost
             // always complete by now.)
-            const uint32_t bsf = sy.bar(F_SFS + u % (2 * C::NB)), psf = (u / (2 * C::NB)) & 1;
+            const uint32_t bsf = sy.bar(F_SFS + U % (2 * C::NB)), psf = (U / (2 * C::NB)) & 1;
             uint32_t bdq = bsf, pdq = psf;
-            if (u >= 4) {
-                const int h = (u - 4) >> 1;
+            if (G >= 2) {
+                const int h = G - 2;
                 bdq = sy.bar(F_DQF + (h & 1));
                 pdq = (h >> 1) & 1;
             }
-            ok = warp_wait_all(sy, bsf, psf, bdq, pdq, bsf, psf, bsf, psf, 2, u);
+            ok = warp_wait_all(sy, bsf, psf, bdq, pdq, bsf, psf, bsf, psf, 2, U);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t ds_blk = sb + C::OFF_DS + 16384 * (u & 3);
+            const uint32_t ds_blk = sb + C::OFF_DS + 16384 * (2 * (G & 1) + (ul & 1));
             // phase 1: P = exp2(S scale log2(e) - LSE log2(e)) as bf16 pairs, over
             // the S^T columns already read (the dP^T products may still run)
             uint32_t pk[2][2][8];
@@ -562,9 +661,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 }
             }
             // phase 2: dS = P (dP - D), with P as rounded for the dV product
-            ok = warp_wait(sy, sy.bar(F_SFD + u % (2 * C::NB)), (u / (2 * C::NB)) & 1, 2, u);
+            ok = warp_wait(sy, sy.bar(F_SFD + U % (2 * C::NB)), (U / (2 * C::NB)) & 1, 2, U);
             if (!ok) {
-                mbar_arrive(sy.bar(F_PF + u % kPfRingF));
+                mbar_arrive(sy.bar(F_PF + U % kPfRingF));
                 break;
             }
             tc_fence_after();
@@ -611,124 +710,135 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             tmem_wait_st();
             tc_fence_before();
             fence_proxy_async_smem();
-            // One round trip for: (a) a stand-in wait for the MMA issuer of u (see
-            // its loop): the stage of u+NB is loaded; (b) the stage of u+2, this
-            // warpgroup's next sub-tile, whose statistics it loads now.
+            // One round trip for: (a) a stand-in wait for the MMA issuer of U (see
+            // its loop): the stage of U+NB is loaded, when U+NB is in this item;
+            // (b) the stage of U+2, this warpgroup's next sub-tile, whose statistics
+            // it loads now, when U+2 is in this item.
             {
-                const bool v0 = u + C::NB < nsub, v1 = C::NB != 2 && u + 2 < nsub;
-                uint32_t b0 = sy.bar(F_QF + (u + C::NB) % C::NST), p0 = ((u + C::NB) / C::NST) & 1;
-                uint32_t b1 = sy.bar(F_QF + (u + 2) % C::NST), p1 = ((u + 2) / C::NST) & 1;
+                const bool v0 = ul + C::NB < t.nsub, v1 = ul + 2 < t.nsub;
+                uint32_t b0 = sy.bar(F_QF + (U + C::NB) % C::NST), p0 = ((U + C::NB) / C::NST) & 1;
+                uint32_t b1 = sy.bar(F_QF + (U + 2) % C::NST), p1 = ((U + 2) / C::NST) & 1;
                 if (v0 || v1) {
                     // a phase that is not needed is replaced by one that is
                     if (!v0) { b0 = b1; p0 = p1; }
                     if (!v1) { b1 = b0; p1 = p0; }
-                    ok = warp_wait_all(sy, b0, p0, b1, p1, b0, p0, b0, p0, 2, u);
+                    ok = warp_wait_all(sy, b0, p0, b1, p1, b0, p0, b0, p0, 2, U);
                 }
             }
-            if (ok && u + 2 < nsub) load_stats(u + 2);
-            mbar_arrive(sy.bar(F_PF + u % kPfRingF));
+            if (ok && ul + 2 < t.nsub) load_stats(U + 2);
+            mbar_arrive(sy.bar(F_PF + U % kPfRingF));
             if (!ok) break;
         }
-        if constexpr (!C::EPI_DRAIN) {
-            if (grp == 0) {
-                if (ok) ok = warp_wait(sy, sy.bar(F_ACC), 0, 2, nsub) &&
-                             (!C::TWO_ISSUERS || warp_wait(sy, sy.bar(F_ACCB), 0, 2, nsub));
-                if (ok) {
-                    tc_fence_after();
-                    dkdv_epilogue<D, C>(tmem, q4, lane, sb + C::OFF_EPI + 2048u * (warp - 2), d_packed, bh, k0, N,
-                                        ldq, scale, piece, dkv_part);
-                }
-            }
-        }
     } else if (warp < 14) {
-        // ------------------------------------------------------------ dQ drain, then the dK/dV epilogue
+        // ------------------------------------------------------------ dQ drain, then each item's dK/dV epilogue
         const int q4 = warp & 3;
-        const int il = q4 * 32 + lane;           // query row within the 128-query group (key row in the epilogue)
+        const int il = q4 * 32 + lane;           // query row within the 128-query group
         const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
         const bool elected = warp == 10 && lane == 0;
         // row il of a box of BOXC fp32 columns, swizzled as the tensor map expects
         // (16-byte chunk c of a row at c xor the row bits above the 128-byte line)
         constexpr uint32_t RB = C::BOXC * 4, M = RB == 128 ? 7u : RB == 64 ? 3u : 1u;
         bool okd = true;
-        for (int g = 0; g < ngrp; ++g) {
-            okd = warp_wait(sy, sy.bar(F_DQF + (g & 1)), (g >> 1) & 1, 3, g);
-            // the four drain warps decide together (they meet at named barriers below)
+        int G0 = 0, it = 0;
+        for (int x = blockIdx.x; x < nitems && okd; x += gridDim.x, ++it) {
+            const Item t = decode_item(x, nfull, tail_f, nsub_all, nkt);
+            const int ngrp = (t.nsub + 1) / 2;
+            for (int gl = 0; gl < ngrp; ++gl) {
+                const int G = G0 + gl;
+                okd = warp_wait(sy, sy.bar(F_DQF + (G & 1)), (G >> 1) & 1, 3, G);
+                // the four drain warps decide together (they meet at named barriers below)
+                okd = named_bar_and(2, 128, okd);
+                if (!okd) break;
+                tc_fence_after();
+#pragma unroll
+                for (int h = 0; h < D / C::BOXC; ++h) {
+                    uint32_t v[C::BOXC];
+                    tmem_ld_row<C::BOXC>(trow + C::C_DQ + C::BOXC * h, v);
+                    tmem_wait_ld();
+                    if (h == D / C::BOXC - 1) {
+                        // the group's accumulator is read
+                        tc_fence_before();
+                        mbar_arrive(sy.bar(F_DQE + (G & 1)));
+                    }
+                    // staging buffer of box b: the reduce that last read it (box b - NDQS)
+                    // must be done reading
+                    const int bx = G * (D / C::BOXC) + h;
+                    const uint32_t buf = sb + C::OFF_DQS + (bx % C::NDQS) * C::DQS_BYTES;
+                    if (elected) bulk_wait_group_read<C::NDQS - 1>();
+                    named_bar_sync(1, 128);
+#pragma unroll
+                    for (int c = 0; c < C::BOXC / 4; ++c) {
+                        const uint32_t a = (uint32_t)il * RB + 16u * c;
+                        st_shared_v4(buf + (a ^ (((a >> 7) & M) << 4)), v[4 * c], v[4 * c + 1], v[4 * c + 2],
+                                     v[4 * c + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    named_bar_sync(1, 128);
+                    // rows past N lie outside the tensor and are skipped
+                    if (elected) {
+                        tma_reduce_add_3d(&tm_dq, buf, h * C::BOXC, (t.ubase / 2 + gl) * 128, t.bh);
+                        bulk_commit_group();
+                    }
+                }
+            }
+            if (!okd) break;
+            // epilogue: dK, dV_lo, dV_hi rows of this warp's 32 keys, once every main
+            // MMA of the item is done; the staging buffers are free once the last
+            // reduce read them.  EPI: the accumulators are read.
+            okd = warp_wait(sy, sy.bar(F_ACC), it & 1, 3, -1) &&
+                  (!C::TWO_ISSUERS || warp_wait(sy, sy.bar(F_ACCB), it & 1, 3, -1));
             okd = named_bar_and(2, 128, okd);
             if (!okd) break;
+            if (elected) bulk_wait_group_read<0>();
+            named_bar_sync(1, 128);
             tc_fence_after();
-            uint32_t v[D];
-            tmem_ld_row<D>(trow + C::C_DQ, v);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(sy.bar(F_DQE + (g & 1)));
-#pragma unroll
-            for (int h = 0; h < D / C::BOXC; ++h) {
-                // staging buffer of box b: the reduce that last read it (box b - NDQS)
-                // must be done reading
-                const int bx = g * (D / C::BOXC) + h;
-                const uint32_t buf = sb + C::OFF_DQS + (bx % C::NDQS) * C::DQS_BYTES;
-                if (elected) bulk_wait_group_read<C::NDQS - 1>();
-                named_bar_sync(1, 128);
-#pragma unroll
-                for (int c = 0; c < C::BOXC / 4; ++c) {
-                    const uint32_t a = (uint32_t)il * RB + 16u * c;
-                    st_shared_v4(buf + (a ^ (((a >> 7) & M) << 4)), v[h * C::BOXC + 4 * c],
-                                 v[h * C::BOXC + 4 * c + 1], v[h * C::BOXC + 4 * c + 2], v[h * C::BOXC + 4 * c + 3]);
-                }
-                fence_proxy_async_smem();
-                named_bar_sync(1, 128);
-                // rows past N lie outside the tensor and are skipped
-                if (elected) {
-                    tma_reduce_add_3d(&tm_dq, buf, h * C::BOXC, (ubase / 2 + g) * 128, bh);
-                    bulk_commit_group();
-                }
-            }
-        }
-        if constexpr (C::EPI_DRAIN) {
-            // epilogue: dK, dV_lo, dV_hi rows of this warp's 32 keys, once every
-            // main MMA is done; the staging buffer is free once the last reduce read it
-            if (okd) okd = warp_wait(sy, sy.bar(F_ACC), 0, 2, nsub) &&
-                           (!C::TWO_ISSUERS || warp_wait(sy, sy.bar(F_ACCB), 0, 2, nsub));
-            okd = named_bar_and(2, 128, okd);
-            if (okd) {
-                if (elected) bulk_wait_group_read<0>();
-                named_bar_sync(1, 128);
-                tc_fence_after();
-                dkdv_epilogue<D, C>(tmem, q4, lane, sb + C::OFF_DQS + 2048u * (warp - 10), d_packed, bh, k0, N, ldq,
-                                    scale, piece, dkv_part);
-            }
+            dkdv_epilogue<D, C>(tmem, q4, lane, sb + C::OFF_DQS + 2048u * (warp - 10), sy.bar(F_EPI), d_packed,
+                                t.bh, t.k0, N, ldq, scale, t.piece, dkv_part);
+            G0 += ngrp;
         }
         // every reduce has written global memory and read its staging buffer
         if (elected) bulk_wait_group<0>();
     } else if (warp == 14) {
         // ------------------------------------------------------------ dQ issuer
-        // dQ of the 128-query group g = sub-tiles 2g, 2g+1: A = dS (queries x keys)
-        // read MN-major from the pair's two dS^T blocks (16 KB apart), B = K_j rows
-        // (MN-major).  It waits for both sub-tiles' softmax (PF) and for the drain
-        // to have read group g-1 (DQE).  PF(u+4) cannot complete before this
-        // thread has seen PF(u): the softmax of u+4 first waits for this group's
-        // DQF, so the PF ring never runs a phase ahead of it.
+        // dQ of the 128-query group G = an item's sub-tiles 2g, 2g+1: A = dS
+        // (queries x keys) read MN-major from the group's two dS^T blocks 2 (G & 1)
+        // and 2 (G & 1) + 1 (16 KB apart), B = K rows (MN-major).  It waits for the
+        // group's softmax (PF) and for the drain to have read group G-1 (DQE).  A
+        // PF phase cannot run a full ring ahead of this thread: the softmax of a
+        // sub-tile of group G+2 first waits for DQF(G).  After an item's last group
+        // it commits KVE: no MMA reads the item's K/V tile any more (the item's S/dP
+        // products completed before its softmax, which this thread waited for).
         if (lane == 0) {
             constexpr uint32_t ID_DQ = idesc_bf16(128, D, 1, 1);
             constexpr uint32_t KSTEP = (16 * C::ROWB) >> 4;
             constexpr uint32_t BLK_U = 16384 >> 4;
             const uint64_t dK = smem_desc(sb + C::OFF_K, 16, 8 * C::ROWB, C::SW);
             const uint64_t dDS0mn = smem_desc(sb + C::OFF_DS, 16384, 1024, 2);
-            bool ok = wait_bounded(sy, sy.bar(F_KV), 0, 5, -1);
-            for (int g = 0; g < ngrp && ok; ++g) {
-                const int u0 = 2 * g, u1 = 2 * g + 1;
-                ok = wait_bounded(sy, sy.bar(F_PF + u0 % kPfRingF), (u0 / kPfRingF) & 1, 5, u0);
-                if (ok && u1 < nsub) ok = wait_bounded(sy, sy.bar(F_PF + u1 % kPfRingF), (u1 / kPfRingF) & 1, 5, u1);
-                // the drain of group g-1 (this thread waited for g-2's before
-                // issuing dQ(g-1); group g+1's drain needs dQ(g+1))
-                if (ok && g > 0) ok = wait_bounded(sy, sy.bar(F_DQE + ((g - 1) & 1)), ((g - 1) >> 1) & 1, 5, g);
-                if (!ok) break;
-                tc_fence_after();
-                const uint64_t dA = dDS0mn + BLK_U * (u0 & 3);
+            bool ok = true;
+            int U0 = 0, G0 = 0;
+            for (int x = blockIdx.x; x < nitems && ok; x += gridDim.x) {
+                const Item t = decode_item(x, nfull, tail_f, nsub_all, nkt);
+                const int ngrp = (t.nsub + 1) / 2;
+                for (int gl = 0; gl < ngrp; ++gl) {
+                    const int G = G0 + gl, u0 = U0 + 2 * gl, u1 = u0 + 1;
+                    ok = wait_bounded(sy, sy.bar(F_PF + u0 % kPfRingF), (u0 / kPfRingF) & 1, 5, u0);
+                    if (ok && 2 * gl + 1 < t.nsub)
+                        ok = wait_bounded(sy, sy.bar(F_PF + u1 % kPfRingF), (u1 / kPfRingF) & 1, 5, u1);
+                    // the drain of group G-1 (this thread waited for G-2's before
+                    // issuing dQ(G-1); group G+1's drain needs dQ(G+1))
+                    if (ok && G > 0) ok = wait_bounded(sy, sy.bar(F_DQE + ((G - 1) & 1)), ((G - 1) >> 1) & 1, 5, G);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t dA = dDS0mn + BLK_U * (2 * (G & 1));
 #pragma unroll
-                for (int kk = 0; kk < C::BM / 16; ++kk)
-                    mma_bf16_ss(tmem + C::C_DQ, dA + 128 * kk, dK + KSTEP * kk, ID_DQ, kk);
-                mma_commit(sy.bar(F_DQF + (g & 1)));
+                    for (int kk = 0; kk < C::BM / 16; ++kk)
+                        mma_bf16_ss(tmem + C::C_DQ, dA + 128 * kk, dK + KSTEP * kk, ID_DQ, kk);
+                    mma_commit(sy.bar(F_DQF + (G & 1)));
+                }
+                if (!ok) break;
+                mma_commit(sy.bar(F_KVE));
+                U0 += t.nsub;
+                G0 += ngrp;
             }
             // this thread's MMAs are done before TMEM is freed (also on abort)
             mma_commit(sy.bar(F_DQA));
@@ -1261,11 +1371,14 @@ int launch_impl(const BwdArgs& a, std::string* err) {
         sms = 0;
     const TailSplit ts = tail_split(units, a.N, sms);
     const long long nfull = units - ts.ntail;
-    const long long grid = nfull + (long long)ts.ntail * ts.f;
+    const long long nitems = nfull + (long long)ts.ntail * ts.f;
+    // persistent: one CTA per SM (shared memory and TMEM hold one), each
+    // walking items b, b + grid, ...
+    const long long grid = sms > 0 && nitems > sms ? sms : nitems;
     const bool plain = !a.views && ldo == D;   // contiguous O and dO: the vectorised statistics kernel
     const long long pre_grid = plain ? (rows_pad + 256 / (D / 8) - 1) / (256 / (D / 8)) : (rows_pad + 255) / 256;
     const long long fin_grid = (rows * (D / 8) + (long long)ts.ntail * 128 * 3 * (D / 8) + 255) / 256;
-    if (grid > 0x7fffffffll || pre_grid > 0x7fffffffll || fin_grid > 0x7fffffffll) {
+    if (nitems > 0x7fffffffll || pre_grid > 0x7fffffffll || fin_grid > 0x7fffffffll) {
         *err = "grid too large";
         return PSA_ERR_UNSUPPORTED;
     }
@@ -1286,8 +1399,8 @@ int launch_impl(const BwdArgs& a, std::string* err) {
     {
         ProfScope prof(kSlotMain, a.stream);
         bwd_main_kernel<D, CM><<<(unsigned)grid, M::THREADS, M::SMEM, a.stream>>>(
-            tm_kv, tm_q, tm_lo, tm_hi, tm_dq, a.heads, ldq, stats, dq_acc, dp, a.N, nkt, a.scale, a.scale * kLog2e,
-            (int)nfull, ts.f, dkv_part);
+            tm_kv, tm_q, tm_lo, tm_hi, tm_dq, a.heads, ldq, stats, dp, a.N, nkt, a.scale, a.scale * kLog2e,
+            (int)nfull, ts.f, (int)nitems, dkv_part);
     }
     {
         ProfScope prof(kSlotDq, a.stream);

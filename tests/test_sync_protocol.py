@@ -473,6 +473,289 @@ def run_fused(nsub, NB, NST, seed, two_issuers, pf_ring=8, sf_ring=None, slow_ro
     schedule(roles, fifo, rnd, slow_role)
 
 
+def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None, plant=None):
+    """One random schedule of one persistent CTA of the fused backward kernel
+    walking several work items (units or pieces) in turn; items lists their
+    sub-tile counts.  Sub-tiles U and 128-query groups G are numbered across
+    the CTA's items, and every ring (Q/dO stages, S/dP buffers, S^T / dP^T
+    barriers, PF, dS ring blocks 2 (G & 1) + s, dQ barriers) runs on those
+    numbers; each item has its own K/V tile and dV/dK accumulators.
+
+    Roles as in run_fused, plus: the producer, per item the K/V tile after
+    KVE(i-1) (which the dQ issuer commits after the item's last dQ product),
+    then the item's Q/dO stages; main issuers of global parity (the one of
+    parity 0 issues each item's first min(NB, nsub) S/dP products, after the
+    other issuer's last dV/dK of the previous item (that sub-tile's QE commit),
+    the item's K/V (KV) and stages; before an item's first dV/dK each issuer waits for the previous
+    item's epilogue (EPI), and the issuer that does not own the item's first
+    sub-tile also for dV/dK of that sub-tile; each commits ACC per item); the
+    drain warps run each item's epilogue (ACC waits, accumulator reads, EPI
+    arrive).  plant: "no_epi_wait" drops the issuers' EPI wait; "no_kve_wait"
+    lets the K/V producer skip KVE; "accb_prologue" makes the prologue wait
+    for the other issuer's ACCB instead of its last QE."""
+    rnd = random.Random(seed)
+    nsf = 2 * NB
+    UT = sum(items)
+    item_of, ul_of = [], []
+    for it, n in enumerate(items):
+        item_of += [it] * n
+        ul_of += list(range(n))
+    bars = {}
+
+    def bar(name, count=1):
+        if name not in bars:
+            bars[name] = Bar(name, count)
+        return bars[name]
+
+    for b in range(nsf):
+        bar(("SFs", b))
+        bar(("SFd", b))
+    for x in range(pf_ring):
+        bar(("PF", x), 4)
+    for st in range(NST):
+        bar(("QF", st))
+        bar(("QE", st))
+    for x in range(2):
+        bar(("DQE", x), 4)
+        bar(("DQF", x))
+    bar("KV")
+    bar("KVE")
+    bar("ACC")
+    bar("ACCB")
+    bar("EPI", 4)
+
+    sreg = {(b, q): ("free", None) for b in range(NB) for q in range(4)}
+    dreg = {(b, q): ("free", None) for b in range(NB) for q in range(4)}
+    stage = {st: None for st in range(NST)}
+    readers = {st: set() for st in range(NST)}
+    stage_soft = {st: 0 for st in range(NST)}
+    ds = {(blk, q): ("zero", None, True) for blk in range(4) for q in range(4)}
+    acc = {q: ("idle", -1) for q in range(4)}
+    kv = [None]
+    kv_reads = {it: 0 for it in range(len(items))}       # S, dP and dQ products of the item executed
+    accum = {"item": None, "dv": 0, "dk": 0}
+    epi_read = {it: 0 for it in range(len(items))}       # drain warps done reading the item's accumulators
+    fifo = {"main": [], "main1": [], "dq": []}
+
+    def check_stage(u, what):
+        st = u % NST
+        assert stage[st] == u, f"{what}({u}) reads stage {st} holding {stage[st]}"
+        readers[st].add(what)
+
+    def check_kv(u, what):
+        assert kv[0] == item_of[u], f"{what}({u}) of item {item_of[u]} reads K/V of item {kv[0]}"
+
+    def mma_s(u):
+        b = u % NB
+        for q in range(4):
+            assert sreg[(b, q)][0] == "free", f"S({u}) overwrites {sreg[(b, q)]}"
+            sreg[(b, q)] = ("S", u)
+        check_stage(u, "s")
+        check_kv(u, "S")
+        kv_reads[item_of[u]] += 1
+
+    def mma_dp(u):
+        b = u % NB
+        for q in range(4):
+            assert dreg[(b, q)][0] == "free", f"dP({u}) overwrites {dreg[(b, q)]}"
+            dreg[(b, q)] = ("dP", u)
+        check_stage(u, "dp")
+        check_kv(u, "dP")
+        kv_reads[item_of[u]] += 1
+
+    def acc_use(u, what):
+        it, ul = item_of[u], ul_of[u]
+        if ul == 0 and what == "dv":
+            assert it == 0 or epi_read[it - 1] == 4, \
+                f"dV({u}) zeroes the accumulators before the epilogue of item {it - 1} read them"
+            accum.update(item=it, dv=0, dk=0)
+        else:
+            assert accum["item"] == it and accum["dv"] >= 1, f"{what}({u}) adds to accumulators not zeroed for item {it}"
+        accum[what] += 1
+
+    def mma_dv(u):
+        b = u % NB
+        acc_use(u, "dv")
+        for q in range(4):
+            assert sreg[(b, q)] == ("P", u), f"dV({u}) reads {sreg[(b, q)]}"
+            sreg[(b, q)] = ("free", None)
+        check_stage(u, "dv")
+
+    def mma_dk(u):
+        b = u % NB
+        acc_use(u, "dk")
+        for q in range(4):
+            assert dreg[(b, q)] == ("dS", u), f"dK({u}) reads {dreg[(b, q)]}"
+            dreg[(b, q)] = ("free", None)
+        check_stage(u, "dk")
+
+    def mma_dq(arg):
+        g, us = arg
+        for s_, u in enumerate(us):
+            blk = 2 * (g & 1) + s_
+            for q in range(4):
+                kind, uu, _ = ds[(blk, q)]
+                assert (kind, uu) == ("dS", u), f"dQ({g}) reads dS block {blk} holding {(kind, uu)}"
+                ds[(blk, q)] = ("dS", u, True)
+            check_kv(u, "dQ")
+        kv_reads[item_of[us[0]]] += 1
+        for q in range(4):
+            assert acc[q] in (("idle", -1), ("read", g - 1)), f"dQ({g}) overwrites accumulator {acc[q]}"
+            acc[q] = ("dq", g)
+
+    def producer():
+        u = 0
+        for it, n in enumerate(items):
+            if it > 0:
+                if plant != "no_kve_wait":
+                    yield ("wait", bar("KVE"), it - 1)
+                prev = items[it - 1]
+                assert kv_reads[it - 1] == 2 * prev + (prev + 1) // 2, \
+                    f"K/V of item {it} loaded while item {it - 1} still reads its tile"
+            kv[0] = it
+            yield ("arrive", bar("KV"), it)
+            for _ in range(n):
+                st = u % NST
+                yield ("wait", bar(("QE", st)), u // NST - 1)
+                if stage[st] is not None:
+                    assert readers[st] >= {"s", "dp", "dv", "dk"} and stage_soft[st] == 4, \
+                        f"stage {st} reused early: {readers[st]}, {stage_soft[st]} softmax warps done"
+                stage[st] = u
+                readers[st] = set()
+                stage_soft[st] = 0
+                yield ("arrive", bar(("QF", st)), u // NST)
+                u += 1
+
+    def issue_sdp(me, v):
+        fifo[me].append(("mma", mma_s, v))
+        fifo[me].append(("commit", bar(("SFs", v % nsf)), v // nsf))
+        fifo[me].append(("mma", mma_dp, v))
+        fifo[me].append(("commit", bar(("SFd", v % nsf)), v // nsf))
+
+    def main_issuer(par):
+        me = "main" if par == 0 else "main1"
+        u0 = 0
+        for it, n in enumerate(items):
+            if par == 0:
+                if it > 0 and two_issuers and plant == "accb_prologue":
+                    yield ("wait", bar("ACCB"), it - 1)
+                elif it > 0 and two_issuers:
+                    # the other issuer's last dV/dK of the previous item (its QE
+                    # commit; an ACCB wait could find that barrier two phases on
+                    # when the other issuer has no sub-tile in an item)
+                    odd = [u for u in range(u0 - items[it - 1], u0) if u % 2 == 1]
+                    if odd:
+                        yield ("wait", bar(("QE", odd[-1] % NST)), odd[-1] // NST)
+                yield ("wait", bar("KV"), it)
+                for j in range(min(NB, n)):
+                    yield ("wait", bar(("QF", (u0 + j) % NST)), (u0 + j) // NST)
+                for j in range(min(NB, n)):
+                    issue_sdp(me, u0 + j)
+            first = True
+            for ul in range(n):
+                u = u0 + ul
+                if two_issuers and u % 2 != par:
+                    continue
+                yield ("wait", bar(("PF", u % pf_ring)), u // pf_ring)
+                if first:
+                    if it > 0 and plant != "no_epi_wait":
+                        yield ("wait", bar("EPI"), it - 1)
+                    if ul != 0:
+                        yield ("wait", bar(("QE", u0 % NST)), u0 // NST)
+                    first = False
+                v = u + NB
+                fifo[me].append(("mma", mma_dv, u))
+                if ul + NB < n:
+                    fifo[me].append(("mma", mma_s, v))
+                    fifo[me].append(("commit", bar(("SFs", v % nsf)), v // nsf))
+                fifo[me].append(("mma", mma_dk, u))
+                fifo[me].append(("commit", bar(("QE", u % NST)), u // NST))
+                if ul + NB < n:
+                    fifo[me].append(("mma", mma_dp, v))
+                    fifo[me].append(("commit", bar(("SFd", v % nsf)), v // nsf))
+            if first and it > 0 and plant != "no_epi_wait":
+                yield ("wait", bar("EPI"), it - 1)
+            fifo[me].append(("commit", bar("ACC" if par == 0 else "ACCB"), it))
+            u0 += n
+
+    def softmax(grp, q):
+        if grp < UT:
+            yield ("wait", bar(("QF", grp % NST)), grp // NST)
+            assert stage[grp % NST] == grp
+        u0 = g0 = 0
+        for it, n in enumerate(items):
+            for ul in range(n):
+                u = u0 + ul
+                if u % 2 != grp:
+                    continue
+                g, s_ = g0 + ul // 2, ul & 1
+                b, st, blk = u % NB, u % NST, 2 * (g & 1) + s_
+                if ul < 2 and u != grp:
+                    # the first sub-tile of a later item: statistics not fetched ahead
+                    yield ("wait", bar(("QF", st)), u // NST)
+                    assert stage[st] == u
+                yield ("wait", bar(("SFs", u % nsf)), u // nsf)
+                if g >= 2:
+                    yield ("wait", bar(("DQF", (g - 2) & 1)), (g - 2) >> 1)
+                assert sreg[(b, q)] == ("S", u), f"softmax({u}) reads S region {sreg[(b, q)]}"
+                sreg[(b, q)] = ("P", u)
+                yield ("wait", bar(("SFd", u % nsf)), u // nsf)
+                assert dreg[(b, q)] == ("dP", u), f"softmax({u}) reads dP region {dreg[(b, q)]}"
+                dreg[(b, q)] = ("dS", u)
+                kind, uu, read = ds[(blk, q)]
+                assert read, f"softmax({u}) overwrites dS of sub-tile {uu} before its dQ product read it"
+                ds[(blk, q)] = ("dS", u, False)
+                stage_soft[st] += 1
+                if ul + NB < n:
+                    v = u + NB
+                    yield ("wait", bar(("QF", v % NST)), v // NST)
+                if ul + 2 < n:
+                    yield ("wait", bar(("QF", (u + 2) % NST)), (u + 2) // NST)
+                    assert stage[(u + 2) % NST] == u + 2
+                yield ("arrive", bar(("PF", u % pf_ring)), u // pf_ring)
+            u0 += n
+            g0 += (n + 1) // 2
+
+    def dq_issuer():
+        u0 = g0 = 0
+        for it, n in enumerate(items):
+            for gl in range((n + 1) // 2):
+                g = g0 + gl
+                us = [u for u in (u0 + 2 * gl, u0 + 2 * gl + 1) if u < u0 + n]
+                for u in us:
+                    yield ("wait", bar(("PF", u % pf_ring)), u // pf_ring)
+                if g > 0:
+                    yield ("wait", bar(("DQE", (g - 1) & 1)), (g - 1) >> 1)
+                fifo["dq"].append(("mma", mma_dq, (g, us)))
+                fifo["dq"].append(("commit", bar(("DQF", g & 1)), g >> 1))
+            fifo["dq"].append(("commit", bar("KVE"), it))
+            u0 += n
+            g0 += (n + 1) // 2
+
+    def drain(q):
+        g0 = 0
+        for it, n in enumerate(items):
+            for gl in range((n + 1) // 2):
+                g = g0 + gl
+                yield ("wait", bar(("DQF", g & 1)), g >> 1)
+                assert acc[q] == ("dq", g), f"drain({g}) reads {acc[q]}"
+                acc[q] = ("read", g)
+                yield ("arrive", bar(("DQE", g & 1)), g >> 1)
+            yield ("wait", bar("ACC"), it)
+            if two_issuers:
+                yield ("wait", bar("ACCB"), it)
+            assert accum == {"item": it, "dv": n, "dk": n}, f"epilogue of item {it} reads {accum}"
+            epi_read[it] += 1
+            yield ("arrive", bar("EPI"), it)
+            g0 += (n + 1) // 2
+
+    roles = [producer()]
+    roles += [main_issuer(0), main_issuer(1)] if two_issuers else [main_issuer(0)]
+    roles += [softmax(g, q) for g in range(2) for q in range(4)]
+    roles += [drain(q) for q in range(4)] + [dq_issuer()]
+    schedule(roles, fifo, rnd, slow_role)
+
+
 def schedule(roles, fifo, rnd, slow_role=None):
     """Runs coroutine roles and MMA FIFOs under a random schedule (see run)."""
     pending = {i: None for i in range(len(roles))}
@@ -1136,3 +1419,63 @@ def test_fused_protocol_with_one_slow_role(NB, NST, two):
             run_fused(17, NB, NST, seed * 31 + len(str(slow)), two, slow_role=slow)
 
 
+
+
+PERSISTENT_ITEMS = [[7, 7, 7], [7, 7, 7, 7, 7, 7, 7], [4, 4, 4, 3, 1], [1, 1, 1, 1], [2, 3, 2, 5], [25, 25],
+                    [3, 6, 9], [1, 2, 1, 2, 6], [5, 1, 4]]
+
+
+@pytest.mark.parametrize("items", PERSISTENT_ITEMS, ids=lambda x: "-".join(map(str, x)))
+@pytest.mark.parametrize("NB,NST,two", FUSED)
+def test_persistent_protocol_random_schedules(items, NB, NST, two):
+    """The persistent fused kernel over several work items per CTA (whole units
+    of 7 or 25 sub-tiles as at N = 400 and N = 1600, split pieces, single
+    sub-tiles, mixed parities), both head_dim variants, 25 random schedules
+    each."""
+    for seed in range(25):
+        run_persistent(items, NB, NST, seed * 7919 + sum(items), two)
+
+
+@pytest.mark.parametrize("NB,NST,two", FUSED)
+def test_persistent_protocol_with_one_slow_role(NB, NST, two):
+    """Each role of the persistent CTA in turn running slowly, over items of odd
+    and even lengths."""
+    nroles = 1 + (2 if two else 1) + 8 + 4 + 1
+    slows = list(range(nroles)) + ["main", "dq"] + (["main1"] if two else [])
+    for slow in slows:
+        for seed in range(8):
+            run_persistent([3, 7, 2, 5], NB, NST, seed * 131 + len(str(slow)), two, slow_role=slow)
+            run_persistent([1, 2, 1, 4], NB, NST, seed * 137 + len(str(slow)), two, slow_role=slow)
+
+
+def test_persistent_model_catches_missing_item_waits():
+    """The persistent model is not vacuous: without the issuers' wait for the
+    previous item's epilogue, some schedule zeroes the accumulators before the
+    epilogue read them; without the K/V producer's wait for KVE, some schedule
+    loads the next item's K/V while the current item still reads its tile."""
+    # roles: the producer, 2 issuers, 8 softmax warps, then the drain warps
+    for plant, msg, slow in (("no_epi_wait", "before the epilogue", 11), ("no_kve_wait", "still reads its tile", None)):
+        failures = 0
+        for seed in range(300):
+            try:
+                run_persistent([3, 4, 3], 3, 6, seed, True, plant=plant, slow_role=slow)
+            except AssertionError as e:
+                assert msg in str(e), (plant, str(e))
+                failures += 1
+        assert failures > 0, plant
+
+
+def test_persistent_prologue_must_not_wait_on_accb():
+    """Why the prologue waits for the other issuer's last QE commit and not its
+    ACCB commit: an issuer with no sub-tile in an item commits that item's ACCB
+    after the previous epilogue alone, so ACCB can complete two phases before
+    the prologue issuer looks at it.  The model finds this with the ACCB form
+    (written out here as a variant of the issuer) on items of one sub-tile."""
+    failures = 0
+    for seed in range(300):
+        try:
+            run_persistent([2, 1, 1, 1, 2, 1], 3, 6, seed, True, plant="accb_prologue", slow_role="main")
+        except AssertionError as e:
+            assert "completed before a waiter" in str(e), str(e)
+            failures += 1
+    assert failures > 0
