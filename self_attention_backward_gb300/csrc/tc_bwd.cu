@@ -49,7 +49,7 @@
 // warps 10-13 dQ drain (one query row per thread; the partials go to the fp32
 // accumulator by TMA bulk reduce) and then each item's dK/dV epilogue (one key
 // row per thread), warp 14 the dQ MMA issuer; for d <= 32 warp 15 issues the
-// odd sub-tiles' main MMAs and warp 1 the even ones (512 threads, else 480).
+// odd sub-tiles' main MMAs and warp 1 the even ones (512 threads).
 //
 // Every mbarrier wait is bounded (kTimeoutNs); on timeout the CTA sets a device
 // error word (read by psa_attn_sync_status), skips the rest of its work, waits
@@ -92,9 +92,10 @@ struct Cfg {
     static constexpr int NST = D == 64 ? 4 : 6;    // Q/dO stages
     // warps: 0 producer, 1 the main MMA issuer (with TWO_ISSUERS: of the even
     // sub-tiles, and warp 15 of the odd ones), 2-9 softmax, 10-13 dQ drain, 14
-    // the dQ MMA issuer.  Two main issuers gave 1% at head_dim 32 (N = 6400) and
-    // cost 5% at head_dim 64 (N = 1600), measured.
-    static constexpr bool TWO_ISSUERS = D != 64;
+    // the dQ MMA issuer.  Two main issuers: 1% at head_dim 32 (N = 6400); at
+    // head_dim 64 they cost 5% while the drain added dQ with vector atomics and
+    // gain 6% (N = 1600 0.210 -> 0.196 ms) since it uses bulk reduces, measured.
+    static constexpr bool TWO_ISSUERS = true;
     static constexpr int THREADS = TWO_ISSUERS ? 512 : 480;
     static constexpr uint32_t SW = D == 64 ? 2u : D == 32 ? 4u : 6u;  // swizzle code of [*, D] tiles
     static constexpr int OFF_K = 0;
@@ -205,7 +206,9 @@ __device__ __forceinline__ void softmax_vals(const uint32_t (&sr)[32], const uin
 // rows (TMEM lane quarter q4) as bf16 into d_packed sections 1-3, coalesced
 // through the warp's 2 KB staging buffer stg; or, for a piece of a split unit,
 // the fp32 partials into dkv_part.  Every main MMA of the item must be
-// complete; each thread arrives on epi_bar once it has read its accumulators.
+// complete.  Each chunk of the accumulators is zeroed once read (the next
+// item's products accumulate onto it), and each thread arrives on epi_bar once
+// its rows are read and zeroed.
 template <int D, typename C>
 __device__ __forceinline__ void dkdv_epilogue(uint32_t tmem, int q4, int lane, uint32_t stg, uint32_t epi_bar,
                                               bf16* d_packed, int bh, int k0, int N, long long ldq, float scale,
@@ -226,8 +229,12 @@ __device__ __forceinline__ void dkdv_epilogue(uint32_t tmem, int q4, int lane, u
             uint32_t v[W];
             tmem_ld_row<W>(trow + col + W * h, v);
             tmem_wait_ld();
+            const uint32_t zero[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int z = 0; z < W / 16; ++z) tmem_st_32x32b_x16(trow + col + W * h + 16 * z, zero);
             if (which == 2 && h == D / W - 1) {
-                // every accumulator column this thread reads is in registers
+                // every accumulator column of this thread's row is read and zeroed
+                tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(epi_bar);
             }
@@ -480,35 +487,39 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 }
                 mma_commit(sy.bar(F_SFD + u % (2 * C::NB)));
             };
-            // dV of sub-tile u (A = P^T from the S half, 64 queries = 4 k-steps);
-            // the item's first sub-tile (ul == 0) overwrites the accumulators
-            auto issue_dv = [&](int u, int ul) {
+            // dV of sub-tile u (A = P^T from the S half, 64 queries = 4 k-steps),
+            // added to the accumulators (which the drain warps zero for each item)
+            auto issue_dv = [&](int u) {
                 // [dO_lo | dO_hi]: MN-major rows, or K-major channel-major tiles
                 const uint64_t dG = (CM ? dDvCm : dStage0mn) + STAGE_U * (u % C::NST);
                 constexpr uint32_t DV_STEP = CM ? 2u : KSTEP;
 #pragma unroll
                 for (int kk = 0; kk < C::BS / 16; ++kk)
-                    mma_bf16_ts(tmem + C::C_DV, tmem + 128u * (u % C::NB) + 8 * kk, dG + DV_STEP * kk, ID_DV,
-                                (ul > 0 || kk > 0) ? 1u : 0u);
+                    mma_bf16_ts(tmem + C::C_DV, tmem + 128u * (u % C::NB) + 8 * kk, dG + DV_STEP * kk, ID_DV, 1u);
             };
             // dK of sub-tile u (A = dS^T from the dP half); then the stage is free
-            auto issue_dk = [&](int u, int ul) {
+            auto issue_dk = [&](int u) {
                 const uint64_t dQmn = dStage0 + STAGE_U * (u % C::NST);     // Q rows, MN-major
 #pragma unroll
                 for (int kk = 0; kk < C::BS / 16; ++kk)
-                    mma_bf16_ts(tmem + C::C_DK, tmem + 128u * (u % C::NB) + 64 + 8 * kk, dQmn + KSTEP * kk, ID_DK,
-                                (ul > 0 || kk > 0) ? 1u : 0u);
+                    mma_bf16_ts(tmem + C::C_DK, tmem + 128u * (u % C::NB) + 64 + 8 * kk, dQmn + KSTEP * kk, ID_DK, 1u);
                 mma_commit(sy.bar(F_QE + u % C::NST));
             };
             const uint32_t acc_bar = sy.bar(par == 0 ? F_ACC : F_ACCB);
             bool ok = true;
-            int U0 = 0, it = 0, last_odd = -1;
+            // kb: items so far in which the odd issuer has a sub-tile (its ACCB
+            // phases: it commits ACCB only for those)
+            int U0 = 0, it = 0, kb = 0;
             for (int x = blockIdx.x; x < nitems; x += gridDim.x, ++it) {
                 const Item t = decode_item(x, nfull, tail_f, nsub_all, nkt);
+                const bool odd_in = !C::TWO_ISSUERS || t.nsub >= 2 || (U0 & 1);
                 if (par == 0) {
-                    // item prologue: S/dP of the first NB sub-tiles
-                    if (C::TWO_ISSUERS && last_odd >= 0)
-                        ok = wait_bounded(sy, sy.bar(F_QE + last_odd % C::NST), (last_odd / C::NST) & 1, 1, last_odd);
+                    // item prologue: S/dP of the first NB sub-tiles, into buffers whose
+                    // last readers were dV/dK of earlier items: the other issuer's are
+                    // done once its latest ACCB phase is (ACCB commits track all its
+                    // MMAs; a wait on one of its QE commits could meet a stage barrier
+                    // two phases behind with 4 stages)
+                    if (C::TWO_ISSUERS && kb > 0) ok = wait_bounded(sy, sy.bar(F_ACCB), (kb - 1) & 1, 1, -1);
                     if (ok) ok = wait_bounded(sy, sy.bar(F_KV), it & 1, 1, -1);
                     for (int j = 0; j < C::NB && j < t.nsub && ok; ++j)
                         ok = wait_bounded(sy, sy.bar(F_QF + (U0 + j) % C::NST), ((U0 + j) / C::NST) & 1, 1, U0 + j);
@@ -523,43 +534,47 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 // warpgroup waited for it).  S^T(U+NB) follows dV(U), the last reader
                 // of the S half, and dP^T(U+NB) follows dK(U), the last reader of the
                 // dP half; the softmax of U+NB starts on S^T while dK(U) and
-                // dP^T(U+NB) run.  Before its first dV/dK of an item a thread waits
-                // for the previous item's epilogue (EPI) and, if it does not own the
-                // item's first sub-tile, for that sub-tile's dV/dK (QE), which zero
-                // the accumulators.
+                // dP^T(U+NB) run.  Every dV/dK product accumulates: before its first
+                // one of an item a thread waits for EPI phase `it` (phase 0: the drain
+                // warps zeroed the accumulators at the start; phase i + 1: they read
+                // item i's and zeroed them again).
                 bool first = true;
                 for (int ul = 0; ul < t.nsub; ++ul) {
                     const int U = U0 + ul;
                     if (C::TWO_ISSUERS && (U & 1) != par) continue;
                     ok = wait_bounded(sy, sy.bar(F_PF + U % kPfRingF), (U / kPfRingF) & 1, 1, U);
                     if (ok && first) {
-                        if (it > 0) ok = wait_bounded(sy, sy.bar(F_EPI), (it - 1) & 1, 1, U);
-                        if (ok && ul != 0) ok = wait_bounded(sy, sy.bar(F_QE + U0 % C::NST), (U0 / C::NST) & 1, 1, U);
+                        ok = wait_bounded(sy, sy.bar(F_EPI), it & 1, 1, U);
                         first = false;
                     }
                     if (!ok) break;
                     tc_fence_after();
                     const bool more = ul + C::NB < t.nsub;
-                    issue_dv(U, ul);
+                    issue_dv(U);
                     if (more) issue_s(U + C::NB);
-                    issue_dk(U, ul);
+                    issue_dk(U);
                     if (more) issue_dp(U + C::NB);
                 }
-                // a thread without a sub-tile in this item: the ACC phases stay in
-                // step with the epilogue's waits
-                if (ok && first && it > 0) ok = wait_bounded(sy, sy.bar(F_EPI), (it - 1) & 1, 1, -1);
                 if (!ok) break;
-                mma_commit(acc_bar);
-                const int last = U0 + t.nsub - 1;
-                last_odd = (last & 1) ? last : (last - 1 >= U0 ? last - 1 : -1);
+                if (par == 0) {
+                    // ACC every item; without a sub-tile, after the zeroing for this
+                    // item, so that its phases keep in step with the drain's waits
+                    if (first) ok = wait_bounded(sy, sy.bar(F_EPI), it & 1, 1, -1);
+                    if (!ok) break;
+                    mma_commit(acc_bar);
+                } else if (!first) {
+                    mma_commit(acc_bar);
+                }
+                if (odd_in) ++kb;
                 U0 += t.nsub;
             }
             // all of this thread's MMAs done before TMEM is freed (also on abort)
+            const int ncommit = par == 0 ? it : kb;
             if (ok) {
-                if (it > 0) wait_drain(acc_bar, (it - 1) & 1);
+                if (ncommit > 0) wait_drain(acc_bar, (ncommit - 1) & 1);
             } else {
                 mma_commit(acc_bar);
-                wait_drain(acc_bar, it & 1);
+                wait_drain(acc_bar, ncommit & 1);
             }
         }
         __syncwarp();
@@ -738,11 +753,24 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         // row il of a box of BOXC fp32 columns, swizzled as the tensor map expects
         // (16-byte chunk c of a row at c xor the row bits above the 128-byte line)
         constexpr uint32_t RB = C::BOXC * 4, M = RB == 128 ? 7u : RB == 64 ? 3u : 1u;
+        {
+            // the dK/dV accumulators start at zero (EPI phase 0); the issuers'
+            // products all accumulate
+            const uint32_t zero[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int z = 0; z < 3 * D / 16; ++z) tmem_st_32x32b_x16(trow + C::C_DV + 16 * z, zero);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(sy.bar(F_EPI));
+        }
         bool okd = true;
-        int G0 = 0, it = 0;
+        int G0 = 0, U0 = 0, it = 0, kb = 0;
         for (int x = blockIdx.x; x < nitems && okd; x += gridDim.x, ++it) {
             const Item t = decode_item(x, nfull, tail_f, nsub_all, nkt);
             const int ngrp = (t.nsub + 1) / 2;
+            // the odd issuer commits ACCB only for items it has a sub-tile in
+            const bool odd_in = !C::TWO_ISSUERS || t.nsub >= 2 || (U0 & 1);
+            if (odd_in) ++kb;
             for (int gl = 0; gl < ngrp; ++gl) {
                 const int G = G0 + gl;
                 okd = warp_wait(sy, sy.bar(F_DQF + (G & 1)), (G >> 1) & 1, 3, G);
@@ -786,7 +814,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             // MMA of the item is done; the staging buffers are free once the last
             // reduce read them.  EPI: the accumulators are read.
             okd = warp_wait(sy, sy.bar(F_ACC), it & 1, 3, -1) &&
-                  (!C::TWO_ISSUERS || warp_wait(sy, sy.bar(F_ACCB), it & 1, 3, -1));
+                  (!C::TWO_ISSUERS || !odd_in || warp_wait(sy, sy.bar(F_ACCB), (kb - 1) & 1, 3, -1));
             okd = named_bar_and(2, 128, okd);
             if (!okd) break;
             if (elected) bulk_wait_group_read<0>();
@@ -795,6 +823,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             dkdv_epilogue<D, C>(tmem, q4, lane, sb + C::OFF_DQS + 2048u * (warp - 10), sy.bar(F_EPI), d_packed,
                                 t.bh, t.k0, N, ldq, scale, t.piece, dkv_part);
             G0 += ngrp;
+            U0 += t.nsub;
         }
         // every reduce has written global memory and read its staging buffer
         if (elected) bulk_wait_group<0>();

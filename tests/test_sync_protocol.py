@@ -533,8 +533,8 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
     acc = {q: ("idle", -1) for q in range(4)}
     kv = [None]
     kv_reads = {it: 0 for it in range(len(items))}       # S, dP and dQ products of the item executed
-    accum = {"item": None, "dv": 0, "dk": 0}
-    epi_read = {it: 0 for it in range(len(items))}       # drain warps done reading the item's accumulators
+    ready_for = {q: None for q in range(4)}              # item whose products a lane quarter's accumulators await
+    counts = {}
     fifo = {"main": [], "main1": [], "dq": []}
 
     def check_stage(u, what):
@@ -564,14 +564,13 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
         kv_reads[item_of[u]] += 1
 
     def acc_use(u, what):
-        it, ul = item_of[u], ul_of[u]
-        if ul == 0 and what == "dv":
-            assert it == 0 or epi_read[it - 1] == 4, \
-                f"dV({u}) zeroes the accumulators before the epilogue of item {it - 1} read them"
-            accum.update(item=it, dv=0, dk=0)
-        else:
-            assert accum["item"] == it and accum["dv"] >= 1, f"{what}({u}) adds to accumulators not zeroed for item {it}"
-        accum[what] += 1
+        # every dV/dK product accumulates; the drain zeroes the accumulators
+        # (each warp its lane quarter) before an item and after its epilogue
+        it = item_of[u]
+        for q in range(4):
+            assert ready_for[q] == it, \
+                f"{what}({u}) of item {it} adds to accumulators quarter {q} holds for item {ready_for[q]}"
+        counts[(it, what)] = counts.get((it, what), 0) + 1
 
     def mma_dv(u):
         b = u % NB
@@ -632,6 +631,10 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
         fifo[me].append(("mma", mma_dp, v))
         fifo[me].append(("commit", bar(("SFd", v % nsf)), v // nsf))
 
+    # ACCB phases: one per item in which the odd issuer has a sub-tile
+    odd_items = [it for it, n in enumerate(items)
+                 if any((u % 2) == 1 for u in range(sum(items[:it]), sum(items[:it]) + n))]
+
     def main_issuer(par):
         me = "main" if par == 0 else "main1"
         u0 = 0
@@ -639,13 +642,18 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
             if par == 0:
                 if it > 0 and two_issuers and plant == "accb_prologue":
                     yield ("wait", bar("ACCB"), it - 1)
-                elif it > 0 and two_issuers:
-                    # the other issuer's last dV/dK of the previous item (its QE
-                    # commit; an ACCB wait could find that barrier two phases on
-                    # when the other issuer has no sub-tile in an item)
+                elif it > 0 and two_issuers and plant == "qe_prologue":
+                    # the other issuer's last dK of the previous item (its QE commit):
+                    # with 4 stages that barrier can be two phases behind
                     odd = [u for u in range(u0 - items[it - 1], u0) if u % 2 == 1]
                     if odd:
                         yield ("wait", bar(("QE", odd[-1] % NST)), odd[-1] // NST)
+                elif it > 0 and two_issuers:
+                    # the other issuer's latest ACCB phase: all its MMAs so far
+                    # (the buffers' last readers among them) are done
+                    kb = sum(1 for x in odd_items if x < it)
+                    if kb:
+                        yield ("wait", bar("ACCB"), kb - 1)
                 yield ("wait", bar("KV"), it)
                 for j in range(min(NB, n)):
                     yield ("wait", bar(("QF", (u0 + j) % NST)), (u0 + j) // NST)
@@ -658,10 +666,10 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                     continue
                 yield ("wait", bar(("PF", u % pf_ring)), u // pf_ring)
                 if first:
-                    if it > 0 and plant != "no_epi_wait":
-                        yield ("wait", bar("EPI"), it - 1)
-                    if ul != 0:
-                        yield ("wait", bar(("QE", u0 % NST)), u0 // NST)
+                    # the accumulators are zeroed for this item (EPI phase 0: at
+                    # the start; phase i + 1: after item i's epilogue)
+                    if plant != "no_epi_wait":
+                        yield ("wait", bar("EPI"), it)
                     first = False
                 v = u + NB
                 fifo[me].append(("mma", mma_dv, u))
@@ -673,9 +681,20 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                 if ul + NB < n:
                     fifo[me].append(("mma", mma_dp, v))
                     fifo[me].append(("commit", bar(("SFd", v % nsf)), v // nsf))
-            if first and it > 0 and plant != "no_epi_wait":
-                yield ("wait", bar("EPI"), it - 1)
-            fifo[me].append(("commit", bar("ACC" if par == 0 else "ACCB"), it))
+            if par == 0:
+                # ACC every item: an issuer without a sub-tile first waits for the
+                # zeroing for this item, so its phases keep in step with the drain's
+                if first and plant != "no_epi_wait":
+                    yield ("wait", bar("EPI"), it)
+                fifo[me].append(("commit", bar("ACC"), it))
+            elif plant == "accb_prologue":
+                # (the aliasing form: an ACCB commit every item)
+                if first:
+                    yield ("wait", bar("EPI"), it)
+                fifo[me].append(("commit", bar("ACCB"), it))
+            elif not first:
+                # ACCB only for items with a sub-tile of this issuer
+                fifo[me].append(("commit", bar("ACCB"), odd_items.index(it)))
             u0 += n
 
     def softmax(grp, q):
@@ -733,6 +752,8 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
             g0 += (n + 1) // 2
 
     def drain(q):
+        ready_for[q] = 0                                  # zeroed at the start
+        yield ("arrive", bar("EPI"), 0)
         g0 = 0
         for it, n in enumerate(items):
             for gl in range((n + 1) // 2):
@@ -742,11 +763,14 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                 acc[q] = ("read", g)
                 yield ("arrive", bar(("DQE", g & 1)), g >> 1)
             yield ("wait", bar("ACC"), it)
-            if two_issuers:
+            if two_issuers and plant == "accb_prologue":
                 yield ("wait", bar("ACCB"), it)
-            assert accum == {"item": it, "dv": n, "dk": n}, f"epilogue of item {it} reads {accum}"
-            epi_read[it] += 1
-            yield ("arrive", bar("EPI"), it)
+            elif two_issuers and it in odd_items:
+                yield ("wait", bar("ACCB"), odd_items.index(it))
+            assert counts.get((it, "dv"), 0) == n and counts.get((it, "dk"), 0) == n, \
+                f"epilogue of item {it} reads {counts.get((it, 'dv'), 0)} dV, {counts.get((it, 'dk'), 0)} dK products"
+            ready_for[q] = it + 1                             # read, then zeroed for the next item
+            yield ("arrive", bar("EPI"), it + 1)
             g0 += (n + 1) // 2
 
     roles = [producer()]
@@ -1345,7 +1369,9 @@ def test_single_cta_dq_protocol_random_schedules(nsub):
         run_dq_single(nsub, seed * 17 + nsub)
 
 
-FUSED = [(3, 6, True), (2, 4, False)]   # (S/dP buffers, Q/dO stages, two main issuers): head_dim <= 32, 64
+# (S/dP buffers, Q/dO stages, two main issuers): head_dim <= 32, head_dim 64,
+# and the single-issuer form (head_dim 64 before its second issuer)
+FUSED = [(3, 6, True), (2, 4, True), (2, 4, False)]
 
 
 @pytest.mark.parametrize("nsub", list(range(1, 14)) + [20, 33])
@@ -1454,7 +1480,7 @@ def test_persistent_model_catches_missing_item_waits():
     epilogue read them; without the K/V producer's wait for KVE, some schedule
     loads the next item's K/V while the current item still reads its tile."""
     # roles: the producer, 2 issuers, 8 softmax warps, then the drain warps
-    for plant, msg, slow in (("no_epi_wait", "before the epilogue", 11), ("no_kve_wait", "still reads its tile", None)):
+    for plant, msg, slow in (("no_epi_wait", "adds to accumulators", 11), ("no_kve_wait", "still reads its tile", None)):
         failures = 0
         for seed in range(300):
             try:
@@ -1465,17 +1491,21 @@ def test_persistent_model_catches_missing_item_waits():
         assert failures > 0, plant
 
 
-def test_persistent_prologue_must_not_wait_on_accb():
-    """Why the prologue waits for the other issuer's last QE commit and not its
-    ACCB commit: an issuer with no sub-tile in an item commits that item's ACCB
-    after the previous epilogue alone, so ACCB can complete two phases before
-    the prologue issuer looks at it.  The model finds this with the ACCB form
-    (written out here as a variant of the issuer) on items of one sub-tile."""
-    failures = 0
-    for seed in range(300):
-        try:
-            run_persistent([2, 1, 1, 1, 2, 1], 3, 6, seed, True, plant="accb_prologue", slow_role="main")
-        except AssertionError as e:
-            assert "completed before a waiter" in str(e), str(e)
-            failures += 1
-    assert failures > 0
+def test_persistent_prologue_waits_that_alias():
+    """Why the odd issuer commits ACCB only for items it has a sub-tile in, and
+    the prologue waits for its latest ACCB phase: (1) with an ACCB commit every
+    item, an issuer without a sub-tile in an item commits after the previous
+    epilogue alone, and ACCB can complete two phases before the prologue issuer
+    looks at it; (2) waiting instead for the odd issuer's last QE commit of the
+    previous item lets the prologue issuer, with 4 stages and 2 buffers (head_dim
+    64), find that stage barrier two phases behind when the odd issuer is slow."""
+    for plant, items, NB, NST, slow in (("accb_prologue", [2, 1, 1, 1, 2, 1], 3, 6, "main"),
+                                        ("qe_prologue", [4, 8, 5, 4, 2], 2, 4, 2)):
+        failures = 0
+        for seed in range(300):
+            try:
+                run_persistent(items, NB, NST, seed, True, plant=plant, slow_role=slow)
+            except AssertionError as e:
+                assert "completed before a waiter" in str(e) or "passed at" in str(e), str(e)
+                failures += 1
+        assert failures > 0, plant
