@@ -848,6 +848,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             for (int x = blockIdx.x; x < nitems && ok; x += gridDim.x) {
                 const Item t = decode_item(x, nfull, tail_f, nsub_all, nkt);
                 const int ngrp = (t.nsub + 1) / 2;
+                const int nkk = (min(C::BM, N - t.k0) + 15) / 16;
                 for (int gl = 0; gl < ngrp; ++gl) {
                     const int G = G0 + gl, u0 = U0 + 2 * gl, u1 = u0 + 1;
                     ok = wait_bounded(sy, sy.bar(F_PF + u0 % kPfRingF), (u0 / kPfRingF) & 1, 5, u0);
@@ -859,9 +860,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                     if (!ok) break;
                     tc_fence_after();
                     const uint64_t dA = dDS0mn + BLK_U * (2 * (G & 1));
+                    // K = the tile's keys: k-steps past the last key that exists add
+                    // nothing (its dS and K rows are zero), so a ragged last tile
+                    // (16 keys at N = 400) takes one MMA here instead of eight
 #pragma unroll
                     for (int kk = 0; kk < C::BM / 16; ++kk)
-                        mma_bf16_ss(tmem + C::C_DQ, dA + 128 * kk, dK + KSTEP * kk, ID_DQ, kk);
+                        if (kk < nkk) mma_bf16_ss(tmem + C::C_DQ, dA + 128 * kk, dK + KSTEP * kk, ID_DQ, kk);
                     mma_commit(sy.bar(F_DQF + (G & 1)));
                 }
                 if (!ok) break;
