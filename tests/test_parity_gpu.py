@@ -375,3 +375,21 @@ def test_head_dim_16_first_subtiles(N, algo):
             g = gpu_fwd_bwd(inp, algo)
             assert_within(compare(g, ref, "bf16"), "bf16")
             check_blocks(g["d_packed"], ref["d_packed"], "bf16")
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+@pytest.mark.parametrize("N,BH", [(50, 400), (100, 333), (200, 301)])
+def test_persistent_many_small_items(N, BH, d):
+    """More work items than SMs, each with one to four 64-query sub-tiles: every
+    persistent CTA walks several items whose first sub-tiles fall on either
+    issuer's parity (one-sub-tile items leave an issuer without work in them),
+    through the per-item K/V, accumulator-zeroing and epilogue barriers.  The
+    fused mode on the GPU, every 64-query block of dQ and every 128-key block
+    of dK/dV of sampled slices (the first, the last and ones in between)
+    against the oracle."""
+    inp = make_custom(BH=BH, N=N, d=d, dtype="bf16", seed=7000 + N + d)
+    slices = sorted({0, 1, 2, 151, 152, 153, BH // 2, BH - 2, BH - 1})
+    ref = oracle_fwd_bwd(inp, slices)
+    g = gpu_fwd_bwd(inp, B.PSA_ALGO_TC)
+    assert_within(compare(g, ref, "bf16", slices), "bf16")
+    check_blocks(g["d_packed"], ref["d_packed"], "bf16", slices)
