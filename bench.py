@@ -5,8 +5,12 @@ One step = one psa_attn_bwd call (every backward kernel: D preprocess, the
 dK/dV/dQ contractions, the dQ write-out) over one batch of synthetic inputs
 already resident in HBM, for the bf16 B=8, heads=2, N=6400 (80x80 map),
 head_dim=32 workload.  The forward (psa_attn_fwd) produces O and LSE once,
-before timing.  L2 (129 MB) is flushed by writing a 256 MB buffer before every
-timed step; each step is timed with CUDA events on the launching stream.
+before timing.  Before every timed step L2 (129 MB) is flushed by writing a
+256 MB buffer and then reading a second 256 MB buffer, so that the step starts
+with none of its data in L2 and no dirty line of the flush left to be written
+back while it runs (--l2-flush write: the write alone); each step is timed with
+CUDA events on the launching stream.  Per-kernel times come from a second pass
+of the same steps with events around each kernel.
 
 Metric: TFLOP/s counting 12*N^2*d per (batch, head) -- 4*N^2*d for the shared
 S recompute plus 2 * 4*N^2*d for the per-V-half dP/dV and dQ/dK terms.
@@ -250,7 +254,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_all / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(w),
+        "data": "synthetic", "config": workload_config(w, args.l2_flush),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -259,10 +263,29 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w):
+def workload_config(w, flush_mode="write+read"):
+    how = (f"{FLUSH_BYTES >> 20} MB write" if flush_mode == "write"
+           else f"{FLUSH_BYTES >> 20} MB write, then a {FLUSH_BYTES >> 20} MB read of a second buffer")
     return {"workload": w.name, "B": w.B, "heads": w.heads, "N": w.N, "feature_map": w.fmap,
             "head_dim": w.d, "storage": w.dtype, "scale": w.scale, "seed": w.seed,
-            "l2": f"flushed ({FLUSH_BYTES >> 20} MB write) before every timed step"}
+            "l2": f"flushed ({how}) before every timed step"}
+
+
+class L2Flush:
+    """Evicts L2 before a timed step: writes a buffer twice the size of L2 and,
+    in mode "write+read", then reads a second one of that size, which writes
+    the first buffer's dirty lines back before the step instead of during it."""
+
+    def __init__(self, device, mode="write+read"):
+        import torch
+        self.mode = mode
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=device) if mode != "write" else None
+
+    def __call__(self):
+        self.w.zero_()
+        if self.r is not None:
+            self.r.sum()
 
 
 def device_inputs(w, device):
@@ -288,7 +311,7 @@ def time_steps(w, bufs, steps, flush, device, algo):
     st = torch.cuda.current_stream()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a, b in evs:
-        flush.zero_()
+        flush()
         a.record(st)
         B.attn_bwd(packed, o_lo, o_hi, lse, do_lo, do_hi, w.scale, d_packed=d_packed, workspace=ws, algo=algo)
         b.record(st)
@@ -313,12 +336,10 @@ def run_ours(args, w):
     peaks, peaks_src = read_peaks()
 
     bufs = device_inputs(w, device)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(device, args.l2_flush)
     time_steps(w, bufs, max(args.warmup, 3), flush, device, algo)       # warm-up
     B.psa_attn_sync_status()
 
-    B.psa_attn_profile_read()
-    B.psa_attn_profile_enable(True)
     with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local) as cs:
         barrier(world)
         torch.cuda.synchronize()
@@ -327,8 +348,13 @@ def run_ours(args, w):
         torch.cuda.synchronize()
         barrier(world)
         wall = time.perf_counter() - t0
-    B.psa_attn_profile_enable(False)
-    prof = B.psa_attn_profile_read()
+        # per-kernel times: the same steps once more, with events around each
+        # kernel (the library then starts each kernel after the one before it)
+        B.psa_attn_profile_read()
+        B.psa_attn_profile_enable(True)
+        prof_step_ms = time_steps(w, bufs, args.steps, flush, device, algo)
+        B.psa_attn_profile_enable(False)
+        prof = B.psa_attn_profile_read()
     B.psa_attn_sync_status()
 
     ms_local = sum(step_ms) / len(step_ms)
@@ -356,13 +382,16 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": dict(workload_config(w), parallelism=f"replicas x{world}" if world > 1 else "single GPU",
-                       algo=used_algo),
+        "config": dict(workload_config(w, args.l2_flush),
+                       parallelism=f"replicas x{world}" if world > 1 else "single GPU", algo=used_algo),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic, "kernel": dom, "peak_source": peak_note},
         "step_roofline_frac": t_roof / (ms * 1e-3),
         "executed_tflops": value * EXECUTED[used_algo] / 12.0,
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]},
+        "kernel_timing": ("a second pass of the same steps with CUDA events around each kernel, the kernels "
+                          "started one after another; that pass's ms per step: "
+                          f"{statistics.mean(prof_step_ms):.4f}"),
         "gpu_launches": launches,
         "wall_s_timed_region": wall,
     }
@@ -417,7 +446,7 @@ def time_forward(w, bufs, flush, steps):
         B.attn_fwd(packed, w.scale)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a, b in evs:
-        flush.zero_()
+        flush()
         a.record(st)
         B.attn_fwd(packed, w.scale)
         b.record(st)
@@ -457,7 +486,7 @@ def time_merge(w, bufs, flush, steps, algo):
             fn()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for a, b in evs:
-            flush.zero_()
+            flush()
             a.record(st)
             fn()
             b.record(st)
@@ -507,6 +536,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--algo", choices=["auto", "simt", "tc", "tc2"], default="auto")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--l2-flush", choices=["write+read", "write"], default="write+read",
+                    help="L2 eviction before each timed step (see the module docstring)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-extras", action="store_true",

@@ -324,6 +324,10 @@ int psa_attn_selftest_wait_timeout(void* stream);
  * psa_attn_profile_read() synchronises those events, writes per-slot total
  * milliseconds and launch counts into the caller's arrays (length >= 4) and
  * clears the records.  Returns the number of slots, or a negative psa_status.
+ * Without timing, the tensor-core backward's main and finalize kernels start
+ * as programmatic dependents of the kernel before them (their blocks are
+ * scheduled while it finishes); with timing on they start after it, one by
+ * one, so that each pair of events measures one kernel.
  */
 int psa_attn_profile_enable(int on);
 int psa_attn_profile_read(float* total_ms, int* launches, int n_slots);

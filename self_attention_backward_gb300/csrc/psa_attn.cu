@@ -21,6 +21,8 @@ struct ProfRec { int slot; cudaEvent_t a, b; };
 std::vector<ProfRec> g_prof;
 }  // namespace
 
+bool prof_enabled() { return g_prof_on.load(std::memory_order_relaxed); }
+
 ProfScope::ProfScope(int slot, cudaStream_t st) : slot_(slot), st_(st) {
     if (!g_prof_on.load(std::memory_order_relaxed)) return;
     if (cudaEventCreate(&a_) != cudaSuccess || cudaEventCreate(&b_) != cudaSuccess) {

@@ -47,8 +47,11 @@ struct BwdArgs {
 };
 
 // Kernel timing scope (psa_attn_profile_enable): records a CUDA event pair
-// around the launches made while it is alive, when profiling is on.
+// around the launches made while it is alive, when profiling is on.  While it
+// is on, launches that would overlap the kernel before them (programmatic
+// dependent launch) are made plain, so that each event pair times one kernel.
 enum ProfSlot { kSlotFwd = 0, kSlotPre = 1, kSlotMain = 2, kSlotDq = 3, kNumSlots = 4 };
+bool prof_enabled();
 class ProfScope {
   public:
     ProfScope(int slot, cudaStream_t st);

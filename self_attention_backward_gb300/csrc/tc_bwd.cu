@@ -62,6 +62,7 @@
 #include <cstdio>
 #include <mutex>
 #include <string>
+#include <utility>
 
 #include "common.cuh"
 #include "psa_attn.h"
@@ -379,7 +380,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
 #pragma unroll
         for (int s = 0; s < C::NST; ++s) last_issued[s] = -1;
         int U = 0, it = 0;
-        bool ok = true;
+        bool ok = true, dep = false;
         for (int x = blockIdx.x; x < nitems && ok; x += gridDim.x, ++it) {
             const Item t = decode_item(x, nfull, tail_f, nsub_all, nkt);
             if (it > 0 && !warp_wait(sy, sy.bar(F_KVE), (it - 1) & 1, 0, -1)) break;
@@ -404,6 +405,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                     tma_load_3d(st, &tm_q, 0, q0, t.bh * 4 + 0, sy.bar(F_QF + s));
                     tma_load_4d(st + C::QTILE, &tm_do_lo, CM ? q0 : 0, CM ? 0 : q0, hh, bb, sy.bar(F_QF + s));
                     tma_load_4d(st + 2 * C::QTILE, &tm_do_hi, CM ? q0 : 0, CM ? 0 : q0, hh, bb, sy.bar(F_QF + s));
+                    if (!dep) {
+                        // the statistics come from the preprocess kernel, which
+                        // may still be running (programmatic dependent launch)
+                        griddep_wait();
+                        dep = true;
+                    }
                     bulk_load(sb + C::OFF_ST + s * 512, st_slice + (size_t)(t.ubase + u) * 32, 512, sy.bar(F_QF + s));
                 }
 #pragma unroll
@@ -763,6 +770,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             tc_fence_before();
             mbar_arrive(sy.bar(F_EPI));
         }
+        griddep_wait();                          // dq_acc is zeroed by the preprocess kernel
         bool okd = true;
         int G0 = 0, U0 = 0, it = 0, kb = 0;
         for (int x = blockIdx.x; x < nitems && okd; x += gridDim.x, ++it) {
@@ -1205,6 +1213,9 @@ __global__ void __launch_bounds__(256)
 pre_stats_kernel(const bf16* __restrict__ o_lo, const bf16* __restrict__ o_hi, const bf16* __restrict__ do_lo,
                  const bf16* __restrict__ do_hi, const float* __restrict__ lse, float4* __restrict__ stats,
                  float* __restrict__ dq_acc, long long rows_pad, int N, int npad) {
+    // the fused kernel may be scheduled once every block of this one has
+    // started; it waits for this grid's results before it reads them
+    griddep_launch_dependents();
     constexpr int TPR = D / 8;                // threads per row, 8 bf16 (16 B) each
     constexpr int RPB = 256 / TPR;
     const long long row = (long long)blockIdx.x * RPB + threadIdx.x / TPR;
@@ -1254,6 +1265,7 @@ __global__ void __launch_bounds__(256)
 pre_stats_view_kernel(const bf16* __restrict__ o_lo, const bf16* __restrict__ o_hi, long long ldo, View vlo,
                       View vhi, int heads, const float* __restrict__ lse, float4* __restrict__ stats,
                       float* __restrict__ dq_acc, long long rows_pad, int N, int npad) {
+    griddep_launch_dependents();
     const long long row = (long long)blockIdx.x * 256 + threadIdx.x;
     const long long bh = row / npad;
     const int i = (int)(row % npad);
@@ -1287,6 +1299,7 @@ __global__ void __launch_bounds__(256)
 dq_finalize_kernel(const float* __restrict__ dq_acc, bf16* __restrict__ d_packed, long long ldq, long long rows,
                    int N, float scale, const float* __restrict__ dkv_part, int nfull, int ntail, int tail_f,
                    int nkt) {
+    griddep_wait();             // the fused kernel's dQ sums and partials
     constexpr int PPR = D / 8;  // 8-element parts per row
     const long long idx = (long long)blockIdx.x * 256 + threadIdx.x;
     if (idx >= rows * PPR) {
@@ -1362,6 +1375,26 @@ size_t tail_part_bytes(long long BH, int N, int d) {
     return (size_t)pieces * 128 * 3 * (size_t)d * 4;
 }
 
+// Launches `kern` on `st`; with `dependent`, as a programmatic dependent of
+// the kernel before it on the stream, so that its blocks can be scheduled (and
+// run their set-up) while that kernel finishes.  The kernel orders its reads
+// of the earlier kernel's results with griddep_wait.
+template <typename... P, typename... A>
+cudaError_t launch_kernel(void (*kern)(P...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                          bool dependent, A&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<A>(args)...);
+}
+
 template <int D, bool CM>
 int launch_impl(const BwdArgs& a, std::string* err) {
     using M = Cfg<D>;
@@ -1429,18 +1462,24 @@ int launch_impl(const BwdArgs& a, std::string* err) {
                                                                                a.lse, stats, dq_acc, rows_pad, a.N,
                                                                                npad);
     }
+    // The fused kernel and the finalize kernel start as programmatic dependents
+    // of the kernel before them, except while kernels are timed one by one
+    // (events between them would stand in the way).
+    const bool dependent = !prof_enabled();
+    cudaError_t e = cudaSuccess;
     {
         ProfScope prof(kSlotMain, a.stream);
-        bwd_main_kernel<D, CM><<<(unsigned)grid, M::THREADS, M::SMEM, a.stream>>>(
-            tm_kv, tm_q, tm_lo, tm_hi, tm_dq, a.heads, ldq, stats, dp, a.N, nkt, a.scale, a.scale * kLog2e,
-            (int)nfull, ts.f, (int)nitems, dkv_part);
+        e = launch_kernel(bwd_main_kernel<D, CM>, (unsigned)grid, M::THREADS, M::SMEM, a.stream, dependent, tm_kv,
+                          tm_q, tm_lo, tm_hi, tm_dq, a.heads, ldq, (const float4*)stats, dp, a.N, nkt, a.scale,
+                          a.scale * kLog2e, (int)nfull, ts.f, (int)nitems, dkv_part);
     }
-    {
+    if (e == cudaSuccess) {
         ProfScope prof(kSlotDq, a.stream);
-        dq_finalize_kernel<D><<<(unsigned)fin_grid, 256, 0, a.stream>>>(dq_acc, dp, ldq, rows, a.N, a.scale,
-                                                                        dkv_part, (int)nfull, ts.ntail, ts.f, nkt);
+        e = launch_kernel(dq_finalize_kernel<D>, (unsigned)fin_grid, 256, 0, a.stream, dependent,
+                          (const float*)dq_acc, dp, ldq, rows, a.N, a.scale, (const float*)dkv_part, (int)nfull,
+                          ts.ntail, ts.f, nkt);
     }
-    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         *err = std::string("tensor-core backward launch: ") + cudaGetErrorString(e);
         return PSA_ERR_CUDA;

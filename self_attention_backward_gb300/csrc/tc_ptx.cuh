@@ -100,6 +100,15 @@ template <int N>
 __device__ __forceinline__ void bulk_wait_group() {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
+// Programmatic dependent launch.  griddep_wait: returns once every grid this
+// one depends on has completed and its memory writes are visible (at once
+// when the grid was launched without the programmatic attribute).
+// griddep_launch_dependents: lets the dependent grid be scheduled once every
+// CTA of this grid has executed it or exited (it orders no memory).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 // Named barrier `id` over `count` threads (whole warps).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
