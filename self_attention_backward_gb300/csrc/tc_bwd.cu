@@ -99,10 +99,16 @@ struct Cfg {
     static constexpr bool TWO_ISSUERS = true;
     static constexpr int THREADS = TWO_ISSUERS ? 512 : 480;
     static constexpr uint32_t SW = D == 64 ? 2u : D == 32 ? 4u : 6u;  // swizzle code of [*, D] tiles
+    // K, V_lo, V_hi of an item at OFF_K / OFF_VL / OFF_VH of K/V buffer
+    // it % KVBUF.  Two buffers where shared memory has room for them (head_dim
+    // <= 32): the next item's tiles then load while the current item runs,
+    // instead of after its last dQ product.
+    static constexpr int KVBUF = D == 64 ? 1 : 2;
+    static constexpr int KVSET = 3 * KTILE;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_VL = KTILE;
     static constexpr int OFF_VH = 2 * KTILE;
-    static constexpr int OFF_STAGE = 3 * KTILE;    // stage s: Q, dO_lo, dO_hi at +s*STAGE
+    static constexpr int OFF_STAGE = KVBUF * KVSET;  // stage s: Q, dO_lo, dO_hi at +s*STAGE
     static constexpr int STAGE = 3 * QTILE;
     static constexpr int OFF_DS = OFF_STAGE + NST * STAGE;  // dS^T ring: 4 x [128 keys][64 queries] bf16
     // dQ drain: each 128-query partial is staged here in boxes of BOXC columns
@@ -173,12 +179,17 @@ static_assert(B_DQE + 2 <= 32, "barrier area holds 32 barriers");
 // commits; with the ring each barrier has one committing thread (the issuer of
 // u - NB) and one waiting warpgroup (u's), which saw its previous phase
 // (u - 2NB) before this one.  DQF, DQE, DQA as above.
+// KV / KVE: K/V buffer b loaded, and no MMA reads it any more (F_KV and F_KVE
+// for buffer 0, F_KV1 and F_KVE1 for buffer 1); buffer it % KVBUF holds item
+// it, phase it / KVBUF.
 enum {
     F_KV = 0, F_SFS = 1, F_SFD = 7, F_PF = 13, F_ACC = 21, F_ACCB = 22, F_DQA = 23, F_QF = 24, F_QE = 30, F_DQF = 36,
-    F_DQE = 38, F_KVE = 40, F_EPI = 41
+    F_DQE = 38, F_KVE = 40, F_EPI = 41, F_KV1 = 42, F_KVE1 = 43
 };
 constexpr int kPfRingF = 8;
-static_assert(F_EPI + 1 <= 48, "barrier area holds 48 barriers");
+static_assert(F_KVE1 + 1 <= 48, "barrier area holds 48 barriers");
+__device__ __forceinline__ int kv_full(int b) { return b ? F_KV1 : F_KV; }
+__device__ __forceinline__ int kv_empty(int b) { return b ? F_KVE1 : F_KVE; }
 
 // P and dS of one 32-query chunk of this thread's key row, packed to bf16
 // pairs: P = exp2(S * scale*log2e - L), dS = P (dP - D).
@@ -324,8 +335,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
     for (int x = blockIdx.x; x < nitems; x += gridDim.x) UT += decode_item(x, nfull, tail_f, nsub_all, nkt).nsub;
 
     if (threadIdx.x == 0) {
-        mbar_init(sy.bar(F_KV), 1);
-        mbar_init(sy.bar(F_KVE), 1);
+        for (int b = 0; b < C::KVBUF; ++b) {
+            mbar_init(sy.bar(kv_full(b)), 1);
+            mbar_init(sy.bar(kv_empty(b)), 1);
+        }
         mbar_init(sy.bar(F_EPI), 128);
         for (int b = 0; b < 2 * C::NB; ++b) {
             mbar_init(sy.bar(F_SFS + b), 1);
@@ -367,15 +380,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // Per item: its K/V tile, once no MMA reads the previous one (KVE), then
-        // its Q/dO stages in turn (Q, dO_lo, dO_hi and the sub-tile's statistics:
-        // 32 float4 per 64-query sub-tile, padded rows -inf and 0, written by the
-        // preprocess kernel), each as soon as the stage is free (QE).  The whole
-        // warp waits, lane 0 issues: a single polling lane fed the pipeline
-        // measurably later.  An item's stages are not fetched before the previous
-        // item has finished with its K/V tile; nothing of that item waits for them
-        // (the softmax fetches its next sub-tile's statistics early only within
-        // an item).
+        // Per item: its K/V tile, once no MMA reads the buffer's previous one
+        // (KVE of item it - KVBUF), then its Q/dO stages in turn (Q, dO_lo, dO_hi
+        // and the sub-tile's statistics: 32 float4 per 64-query sub-tile, padded
+        // rows -inf and 0, written by the preprocess kernel), each as soon as the
+        // stage is free (QE).  The whole warp waits, lane 0 issues: a single
+        // polling lane fed the pipeline measurably later.  With one K/V buffer an
+        // item's stages are not fetched before the previous item has finished
+        // with its K/V tile; nothing of that item waits for them (the softmax
+        // fetches its next sub-tile's statistics early only within an item).
         int last_issued[C::NST];
 #pragma unroll
         for (int s = 0; s < C::NST; ++s) last_issued[s] = -1;
@@ -383,12 +396,14 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         bool ok = true, dep = false;
         for (int x = blockIdx.x; x < nitems && ok; x += gridDim.x, ++it) {
             const Item t = decode_item(x, nfull, tail_f, nsub_all, nkt);
-            if (it > 0 && !warp_wait(sy, sy.bar(F_KVE), (it - 1) & 1, 0, -1)) break;
+            const int kvb = it % C::KVBUF;
+            if (it >= C::KVBUF && !warp_wait(sy, sy.bar(kv_empty(kvb)), (it / C::KVBUF - 1) & 1, 0, -1)) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(sy.bar(F_KV), 3 * C::KTILE);
-                tma_load_3d(sb + C::OFF_K, &tm_kv, 0, t.k0, t.bh * 4 + 1, sy.bar(F_KV));
-                tma_load_3d(sb + C::OFF_VL, &tm_kv, 0, t.k0, t.bh * 4 + 2, sy.bar(F_KV));
-                tma_load_3d(sb + C::OFF_VH, &tm_kv, 0, t.k0, t.bh * 4 + 3, sy.bar(F_KV));
+                const uint32_t kvs = sb + kvb * C::KVSET, full = sy.bar(kv_full(kvb));
+                mbar_arrive_expect_tx(full, 3 * C::KTILE);
+                tma_load_3d(kvs + C::OFF_K, &tm_kv, 0, t.k0, t.bh * 4 + 1, full);
+                tma_load_3d(kvs + C::OFF_VL, &tm_kv, 0, t.k0, t.bh * 4 + 2, full);
+                tma_load_3d(kvs + C::OFF_VH, &tm_kv, 0, t.k0, t.bh * 4 + 3, full);
             }
             const float4* st_slice = stats + (size_t)t.bh * nsub_all * 32;
             const int hh = t.bh % heads, bb = t.bh / heads;
@@ -421,7 +436,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         __syncwarp();
         if (*sy.abort && lane == 0) {
             // let this CTA's own copies land before its shared memory is released
-            if (it > 0) wait_drain(sy.bar(F_KV), (it - 1) & 1);
+            // (items 0 .. it-1 were loaded; the latest of each buffer)
+            for (int j = it - 1; j >= 0 && j >= it - C::KVBUF; --j)
+                wait_drain(sy.bar(kv_full(j % C::KVBUF)), (j / C::KVBUF) & 1);
 #pragma unroll
             for (int y = 0; y < C::NST; ++y)
                 if (last_issued[y] >= 0) wait_drain(sy.bar(F_QF + y), (last_issued[y] / C::NST) & 1);
@@ -449,9 +466,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             constexpr uint32_t SBO = 8 * C::ROWB;
             constexpr uint32_t KSTEP = (16 * C::ROWB) >> 4;          // 16 rows, in descriptor address units
             // every descriptor is built once; an MMA adds its k-step offset to the address field
+            // (of K/V buffer 0; kvo, in descriptor address units, selects the item's)
             const uint64_t dK = smem_desc(sb + C::OFF_K, 16, SBO, C::SW);
             const uint64_t dVL = smem_desc(sb + C::OFF_VL, 16, SBO, C::SW);
             const uint64_t dVH = smem_desc(sb + C::OFF_VH, 16, SBO, C::SW);
+            uint32_t kvo = 0;
             const uint64_t dStage0 = smem_desc(sb + C::OFF_STAGE, 16, SBO, C::SW);
             const uint64_t dStage0mn = smem_desc(sb + C::OFF_STAGE + C::QTILE, C::QTILE, SBO, C::SW);
             constexpr uint32_t STAGE_U = C::STAGE >> 4, QTILE_U = C::QTILE >> 4;
@@ -471,7 +490,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 const uint64_t dQs = dStage0 + STAGE_U * (u % C::NST);
                 const uint32_t tS = tmem + 128u * (u % C::NB);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) mma_bf16_ss(tS, dK + 2 * kk, dQs + 2 * kk, ID_S, kk);
+                for (int kk = 0; kk < D / 16; ++kk) mma_bf16_ss(tS, dK + kvo + 2 * kk, dQs + 2 * kk, ID_S, kk);
                 mma_commit(sy.bar(F_SFS + u % (2 * C::NB)));
             };
             auto issue_dp = [&](int u) {
@@ -479,18 +498,19 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 if constexpr (CM) {
                     const uint64_t dLo = dDoCm + STAGE_U * (u % C::NST);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) mma_bf16_ss(tDP, dVL + 2 * kk, dLo + 128 * kk, ID_DP, kk);
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_bf16_ss(tDP, dVL + kvo + 2 * kk, dLo + 128 * kk, ID_DP, kk);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_bf16_ss(tDP, dVH + 2 * kk, dLo + QTILE_U + 128 * kk, ID_DP, 1);
+                        mma_bf16_ss(tDP, dVH + kvo + 2 * kk, dLo + QTILE_U + 128 * kk, ID_DP, 1);
                 } else {
                     const uint64_t dQs = dStage0 + STAGE_U * (u % C::NST);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_bf16_ss(tDP, dVL + 2 * kk, dQs + QTILE_U + 2 * kk, ID_DP, kk);
+                        mma_bf16_ss(tDP, dVL + kvo + 2 * kk, dQs + QTILE_U + 2 * kk, ID_DP, kk);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_bf16_ss(tDP, dVH + 2 * kk, dQs + 2 * QTILE_U + 2 * kk, ID_DP, 1);
+                        mma_bf16_ss(tDP, dVH + kvo + 2 * kk, dQs + 2 * QTILE_U + 2 * kk, ID_DP, 1);
                 }
                 mma_commit(sy.bar(F_SFD + u % (2 * C::NB)));
             };
@@ -520,6 +540,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             for (int x = blockIdx.x; x < nitems; x += gridDim.x, ++it) {
                 const Item t = decode_item(x, nfull, tail_f, nsub_all, nkt);
                 const bool odd_in = !C::TWO_ISSUERS || t.nsub >= 2 || (U0 & 1);
+                kvo = (uint32_t)((it % C::KVBUF) * (C::KVSET >> 4));
                 if (par == 0) {
                     // item prologue: S/dP of the first NB sub-tiles, into buffers whose
                     // last readers were dV/dK of earlier items: the other issuer's are
@@ -527,7 +548,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                     // MMAs; a wait on one of its QE commits could meet a stage barrier
                     // two phases behind with 4 stages)
                     if (C::TWO_ISSUERS && kb > 0) ok = wait_bounded(sy, sy.bar(F_ACCB), (kb - 1) & 1, 1, -1);
-                    if (ok) ok = wait_bounded(sy, sy.bar(F_KV), it & 1, 1, -1);
+                    if (ok) ok = wait_bounded(sy, sy.bar(kv_full(it % C::KVBUF)), (it / C::KVBUF) & 1, 1, -1);
                     for (int j = 0; j < C::NB && j < t.nsub && ok; ++j)
                         ok = wait_bounded(sy, sy.bar(F_QF + (U0 + j) % C::NST), ((U0 + j) / C::NST) & 1, 1, U0 + j);
                     if (!ok) break;
@@ -843,19 +864,21 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         // group's softmax (PF) and for the drain to have read group G-1 (DQE).  A
         // PF phase cannot run a full ring ahead of this thread: the softmax of a
         // sub-tile of group G+2 first waits for DQF(G).  After an item's last group
-        // it commits KVE: no MMA reads the item's K/V tile any more (the item's S/dP
-        // products completed before its softmax, which this thread waited for).
+        // it commits the KVE of the item's K/V buffer: no MMA reads the item's K/V
+        // tile any more (the item's S/dP products completed before its softmax,
+        // which this thread waited for).
         if (lane == 0) {
             constexpr uint32_t ID_DQ = idesc_bf16(128, D, 1, 1);
             constexpr uint32_t KSTEP = (16 * C::ROWB) >> 4;
             constexpr uint32_t BLK_U = 16384 >> 4;
-            const uint64_t dK = smem_desc(sb + C::OFF_K, 16, 8 * C::ROWB, C::SW);
+            const uint64_t dK0 = smem_desc(sb + C::OFF_K, 16, 8 * C::ROWB, C::SW);
             const uint64_t dDS0mn = smem_desc(sb + C::OFF_DS, 16384, 1024, 2);
             bool ok = true;
             int U0 = 0, G0 = 0;
-            for (int x = blockIdx.x; x < nitems && ok; x += gridDim.x) {
+            for (int x = blockIdx.x, it = 0; x < nitems && ok; x += gridDim.x, ++it) {
                 const Item t = decode_item(x, nfull, tail_f, nsub_all, nkt);
                 const int ngrp = (t.nsub + 1) / 2;
+                const uint64_t dK = dK0 + (uint32_t)((it % C::KVBUF) * (C::KVSET >> 4));
                 const int nkk = (min(C::BM, N - t.k0) + 15) / 16;
                 for (int gl = 0; gl < ngrp; ++gl) {
                     const int G = G0 + gl, u0 = U0 + 2 * gl, u1 = u0 + 1;
@@ -877,7 +900,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                     mma_commit(sy.bar(F_DQF + (G & 1)));
                 }
                 if (!ok) break;
-                mma_commit(sy.bar(F_KVE));
+                mma_commit(sy.bar(kv_empty(it % C::KVBUF)));
                 U0 += t.nsub;
                 G0 += ngrp;
             }

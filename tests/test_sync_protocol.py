@@ -473,7 +473,7 @@ def run_fused(nsub, NB, NST, seed, two_issuers, pf_ring=8, sf_ring=None, slow_ro
     schedule(roles, fifo, rnd, slow_role)
 
 
-def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None, plant=None):
+def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None, plant=None, kvbuf=1):
     """One random schedule of one persistent CTA of the fused backward kernel
     walking several work items (units or pieces) in turn; items lists their
     sub-tile counts.  Sub-tiles U and 128-query groups G are numbered across
@@ -481,9 +481,10 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
     barriers, PF, dS ring blocks 2 (G & 1) + s, dQ barriers) runs on those
     numbers; each item has its own K/V tile and dV/dK accumulators.
 
-    Roles as in run_fused, plus: the producer, per item the K/V tile after
-    KVE(i-1) (which the dQ issuer commits after the item's last dQ product),
-    then the item's Q/dO stages; main issuers of global parity (the one of
+    Roles as in run_fused, plus: the producer, per item the K/V tile into
+    buffer i % kvbuf after KVE of item i - kvbuf (which the dQ issuer commits,
+    on that buffer's barrier, after the item's last dQ product), then the
+    item's Q/dO stages; main issuers of global parity (the one of
     parity 0 issues each item's first min(NB, nsub) S/dP products, after the
     other issuer's last dV/dK of the previous item (that sub-tile's QE commit),
     the item's K/V (KV) and stages; before an item's first dV/dK each issuer waits for the previous
@@ -518,8 +519,9 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
     for x in range(2):
         bar(("DQE", x), 4)
         bar(("DQF", x))
-    bar("KV")
-    bar("KVE")
+    for b in range(kvbuf):
+        bar(("KV", b))
+        bar(("KVE", b))
     bar("ACC")
     bar("ACCB")
     bar("EPI", 4)
@@ -531,7 +533,7 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
     stage_soft = {st: 0 for st in range(NST)}
     ds = {(blk, q): ("zero", None, True) for blk in range(4) for q in range(4)}
     acc = {q: ("idle", -1) for q in range(4)}
-    kv = [None]
+    kv = [None] * kvbuf
     kv_reads = {it: 0 for it in range(len(items))}       # S, dP and dQ products of the item executed
     ready_for = {q: None for q in range(4)}              # item whose products a lane quarter's accumulators await
     counts = {}
@@ -543,7 +545,8 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
         readers[st].add(what)
 
     def check_kv(u, what):
-        assert kv[0] == item_of[u], f"{what}({u}) of item {item_of[u]} reads K/V of item {kv[0]}"
+        it = item_of[u]
+        assert kv[it % kvbuf] == it, f"{what}({u}) of item {it} reads K/V of item {kv[it % kvbuf]}"
 
     def mma_s(u):
         b = u % NB
@@ -605,14 +608,15 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
     def producer():
         u = 0
         for it, n in enumerate(items):
-            if it > 0:
+            b = it % kvbuf
+            if it >= kvbuf:
                 if plant != "no_kve_wait":
-                    yield ("wait", bar("KVE"), it - 1)
-                prev = items[it - 1]
-                assert kv_reads[it - 1] == 2 * prev + (prev + 1) // 2, \
-                    f"K/V of item {it} loaded while item {it - 1} still reads its tile"
-            kv[0] = it
-            yield ("arrive", bar("KV"), it)
+                    yield ("wait", bar(("KVE", b)), it // kvbuf - 1)
+                prev = items[it - kvbuf]
+                assert kv_reads[it - kvbuf] == 2 * prev + (prev + 1) // 2, \
+                    f"K/V of item {it} loaded while item {it - kvbuf} still reads its tile"
+            kv[b] = it
+            yield ("arrive", bar(("KV", b)), it // kvbuf)
             for _ in range(n):
                 st = u % NST
                 yield ("wait", bar(("QE", st)), u // NST - 1)
@@ -654,7 +658,7 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                     kb = sum(1 for x in odd_items if x < it)
                     if kb:
                         yield ("wait", bar("ACCB"), kb - 1)
-                yield ("wait", bar("KV"), it)
+                yield ("wait", bar(("KV", it % kvbuf)), it // kvbuf)
                 for j in range(min(NB, n)):
                     yield ("wait", bar(("QF", (u0 + j) % NST)), (u0 + j) // NST)
                 for j in range(min(NB, n)):
@@ -747,7 +751,7 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                     yield ("wait", bar(("DQE", (g - 1) & 1)), (g - 1) >> 1)
                 fifo["dq"].append(("mma", mma_dq, (g, us)))
                 fifo["dq"].append(("commit", bar(("DQF", g & 1)), g >> 1))
-            fifo["dq"].append(("commit", bar("KVE"), it))
+            fifo["dq"].append(("commit", bar(("KVE", it % kvbuf)), it // kvbuf))
             u0 += n
             g0 += (n + 1) // 2
 
@@ -1451,40 +1455,49 @@ PERSISTENT_ITEMS = [[7, 7, 7], [7, 7, 7, 7, 7, 7, 7], [4, 4, 4, 3, 1], [1, 1, 1,
                     [3, 6, 9], [1, 2, 1, 2, 6], [5, 1, 4]]
 
 
+# (NB, NST, two issuers, K/V buffers): head_dim <= 32 (two K/V tiles, the next
+# item's loaded while the current one runs), head_dim 64 (one), and variants
+PERSIST = [(3, 6, True, 2), (2, 4, True, 1), (3, 6, True, 1), (2, 4, False, 1), (2, 4, True, 2)]
+
+
 @pytest.mark.parametrize("items", PERSISTENT_ITEMS, ids=lambda x: "-".join(map(str, x)))
-@pytest.mark.parametrize("NB,NST,two", FUSED)
-def test_persistent_protocol_random_schedules(items, NB, NST, two):
+@pytest.mark.parametrize("NB,NST,two,kvbuf", PERSIST)
+def test_persistent_protocol_random_schedules(items, NB, NST, two, kvbuf):
     """The persistent fused kernel over several work items per CTA (whole units
     of 7 or 25 sub-tiles as at N = 400 and N = 1600, split pieces, single
     sub-tiles, mixed parities), both head_dim variants, 25 random schedules
     each."""
     for seed in range(25):
-        run_persistent(items, NB, NST, seed * 7919 + sum(items), two)
+        run_persistent(items, NB, NST, seed * 7919 + sum(items), two, kvbuf=kvbuf)
 
 
-@pytest.mark.parametrize("NB,NST,two", FUSED)
-def test_persistent_protocol_with_one_slow_role(NB, NST, two):
+@pytest.mark.parametrize("NB,NST,two,kvbuf", PERSIST)
+def test_persistent_protocol_with_one_slow_role(NB, NST, two, kvbuf):
     """Each role of the persistent CTA in turn running slowly, over items of odd
     and even lengths."""
     nroles = 1 + (2 if two else 1) + 8 + 4 + 1
     slows = list(range(nroles)) + ["main", "dq"] + (["main1"] if two else [])
     for slow in slows:
         for seed in range(8):
-            run_persistent([3, 7, 2, 5], NB, NST, seed * 131 + len(str(slow)), two, slow_role=slow)
-            run_persistent([1, 2, 1, 4], NB, NST, seed * 137 + len(str(slow)), two, slow_role=slow)
+            run_persistent([3, 7, 2, 5], NB, NST, seed * 131 + len(str(slow)), two, slow_role=slow, kvbuf=kvbuf)
+            run_persistent([1, 2, 1, 4], NB, NST, seed * 137 + len(str(slow)), two, slow_role=slow, kvbuf=kvbuf)
 
 
 def test_persistent_model_catches_missing_item_waits():
     """The persistent model is not vacuous: without the issuers' wait for the
     previous item's epilogue, some schedule zeroes the accumulators before the
     epilogue read them; without the K/V producer's wait for KVE, some schedule
-    loads the next item's K/V while the current item still reads its tile."""
+    loads the next item's K/V while the current item still reads its tile (with
+    two K/V buffers: the item after next, while a slow dQ issuer still reads
+    the tile of the item two before)."""
     # roles: the producer, 2 issuers, 8 softmax warps, then the drain warps
-    for plant, msg, slow in (("no_epi_wait", "adds to accumulators", 11), ("no_kve_wait", "still reads its tile", None)):
+    for plant, msg, slow, kvbuf in (("no_epi_wait", "adds to accumulators", 11, 1),
+                                    ("no_kve_wait", "still reads its tile", None, 1),
+                                    ("no_kve_wait", "still reads its tile", "dq", 2)):
         failures = 0
         for seed in range(300):
             try:
-                run_persistent([3, 4, 3], 3, 6, seed, True, plant=plant, slow_role=slow)
+                run_persistent([3, 4, 3, 2], 3, 6, seed, True, plant=plant, slow_role=slow, kvbuf=kvbuf)
             except AssertionError as e:
                 assert msg in str(e), (plant, str(e))
                 failures += 1
