@@ -104,6 +104,13 @@ struct Cfg {
     // <= 32): the next item's tiles then load while the current item runs,
     // instead of after its last dQ product.
     static constexpr int KVBUF = D == 64 ? 1 : 2;
+    // Where the dK product reads dS^T: from the sub-tile's dS ring block in
+    // shared memory (which the dQ product reads too), sparing the softmax a
+    // TMEM store per element, or from the dP^T half of its TMEM buffer.
+    // Measured: the ring at head_dim <= 32 (N = 6400: bwd_main 0.3714 ->
+    // 0.3678 ms), TMEM at head_dim 64 (the ring there: N = 1600 0.1905 ->
+    // 0.193 ms per step).
+    static constexpr bool DK_SMEM = D <= 32;
     static constexpr int KVSET = 3 * KTILE;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_VL = KTILE;
@@ -182,12 +189,14 @@ static_assert(B_DQE + 2 <= 32, "barrier area holds 32 barriers");
 // KV / KVE: K/V buffer b loaded, and no MMA reads it any more (F_KV and F_KVE
 // for buffer 0, F_KV1 and F_KVE1 for buffer 1); buffer it % KVBUF holds item
 // it, phase it / KVBUF.
+// DSE + b: the dK product of the latest sub-tile that wrote dS ring block b
+// has read it (one commit per use of the block, by the sub-tile's issuer).
 enum {
     F_KV = 0, F_SFS = 1, F_SFD = 7, F_PF = 13, F_ACC = 21, F_ACCB = 22, F_DQA = 23, F_QF = 24, F_QE = 30, F_DQF = 36,
-    F_DQE = 38, F_KVE = 40, F_EPI = 41, F_KV1 = 42, F_KVE1 = 43
+    F_DQE = 38, F_KVE = 40, F_EPI = 41, F_KV1 = 42, F_KVE1 = 43, F_DSE = 44
 };
 constexpr int kPfRingF = 8;
-static_assert(F_KVE1 + 1 <= 48, "barrier area holds 48 barriers");
+static_assert(F_DSE + 4 <= 48, "barrier area holds 48 barriers");
 __device__ __forceinline__ int kv_full(int b) { return b ? F_KV1 : F_KV; }
 __device__ __forceinline__ int kv_empty(int b) { return b ? F_KVE1 : F_KVE; }
 
@@ -352,6 +361,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         mbar_init(sy.bar(F_ACC), 1);
         mbar_init(sy.bar(F_ACCB), 1);
         mbar_init(sy.bar(F_DQA), 1);
+        for (int b = 0; b < 4; ++b) mbar_init(sy.bar(F_DSE + b), 1);
         for (int s = 0; s < C::NST; ++s) {
             mbar_init(sy.bar(F_QF + s), 1);
             mbar_init(sy.bar(F_QE + s), 1);
@@ -524,19 +534,32 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 for (int kk = 0; kk < C::BS / 16; ++kk)
                     mma_bf16_ts(tmem + C::C_DV, tmem + 128u * (u % C::NB) + 8 * kk, dG + DV_STEP * kk, ID_DV, 1u);
             };
-            // dK of sub-tile u (A = dS^T from the dP half); then the stage is free
-            auto issue_dk = [&](int u) {
+            // dK of sub-tile u, B = Q.  A = dS^T: with DK_SMEM from its dS ring
+            // block blk ([128 keys][64 queries] bf16, 128-byte rows, 128B swizzle:
+            // K-major, a k-step of 16 queries = 32 bytes), else from the dP half of
+            // its TMEM buffer.  Then the stage (and the block) are free.
+            const uint64_t dDSk = smem_desc(sb + C::OFF_DS, 16, 1024, 2);
+            auto issue_dk = [&](int u, int blk) {
                 const uint64_t dQmn = dStage0 + STAGE_U * (u % C::NST);     // Q rows, MN-major
+                if constexpr (C::DK_SMEM) {
+                    const uint64_t dA = dDSk + (16384u >> 4) * blk;
 #pragma unroll
-                for (int kk = 0; kk < C::BS / 16; ++kk)
-                    mma_bf16_ts(tmem + C::C_DK, tmem + 128u * (u % C::NB) + 64 + 8 * kk, dQmn + KSTEP * kk, ID_DK, 1u);
+                    for (int kk = 0; kk < C::BS / 16; ++kk)
+                        mma_bf16_ss(tmem + C::C_DK, dA + 2 * kk, dQmn + KSTEP * kk, ID_DK, 1u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < C::BS / 16; ++kk)
+                        mma_bf16_ts(tmem + C::C_DK, tmem + 128u * (u % C::NB) + 64 + 8 * kk, dQmn + KSTEP * kk,
+                                    ID_DK, 1u);
+                }
                 mma_commit(sy.bar(F_QE + u % C::NST));
+                if constexpr (C::DK_SMEM) mma_commit(sy.bar(F_DSE + blk));
             };
             const uint32_t acc_bar = sy.bar(par == 0 ? F_ACC : F_ACCB);
             bool ok = true;
             // kb: items so far in which the odd issuer has a sub-tile (its ACCB
-            // phases: it commits ACCB only for those)
-            int U0 = 0, it = 0, kb = 0;
+            // phases: it commits ACCB only for those); G0: the item's first group
+            int U0 = 0, G0 = 0, it = 0, kb = 0;
             for (int x = blockIdx.x; x < nitems; x += gridDim.x, ++it) {
                 const Item t = decode_item(x, nfull, tail_f, nsub_all, nkt);
                 const bool odd_in = !C::TWO_ISSUERS || t.nsub >= 2 || (U0 & 1);
@@ -561,7 +584,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 // PF(U) also certifies that the stage of U+NB is loaded (the softmax
                 // warpgroup waited for it).  S^T(U+NB) follows dV(U), the last reader
                 // of the S half, and dP^T(U+NB) follows dK(U), the last reader of the
-                // dP half; the softmax of U+NB starts on S^T while dK(U) and
+                // dP half when dK takes dS^T from there (dK first measured faster with
+                // the ring too); the softmax of U+NB starts on S^T while dK(U) and
                 // dP^T(U+NB) run.  Every dV/dK product accumulates: before its first
                 // one of an item a thread waits for EPI phase `it` (phase 0: the drain
                 // warps zeroed the accumulators at the start; phase i + 1: they read
@@ -580,7 +604,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                     const bool more = ul + C::NB < t.nsub;
                     issue_dv(U);
                     if (more) issue_s(U + C::NB);
-                    issue_dk(U);
+                    issue_dk(U, 2 * ((G0 + (ul >> 1)) & 1) + (ul & 1));
                     if (more) issue_dp(U + C::NB);
                 }
                 if (!ok) break;
@@ -595,6 +619,7 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 }
                 if (odd_in) ++kb;
                 U0 += t.nsub;
+                G0 += (t.nsub + 1) / 2;
             }
             // all of this thread's MMAs done before TMEM is freed (also on abort)
             const int ncommit = par == 0 ? it : kb;
@@ -632,11 +657,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             ok = warp_wait(sy, sy.bar(F_QF + grp % C::NST), (grp / C::NST) & 1, 2, grp);
             if (ok) load_stats(grp);
         }
-        // the item holding sub-tile U: t, its first sub-tile U0 and group G0
-        int xi = blockIdx.x, U0 = 0, G0 = 0;
+        // the item holding sub-tile U: t, its first sub-tile U0 and group G0;
+        // single0 / single1: groups of parity 0 / 1 with one sub-tile (an odd
+        // item's last) in earlier items, which wrote ring block 2p but not 2p + 1
+        int xi = blockIdx.x, U0 = 0, G0 = 0, single0 = 0, single1 = 0;
         Item t = decode_item(xi, nfull, tail_f, nsub_all, nkt);
         for (int U = grp; U < UT && ok; U += 2) {
             while (U >= U0 + t.nsub) {
+                if (t.nsub & 1) {
+                    if ((G0 + t.nsub / 2) & 1) ++single1;
+                    else ++single0;
+                }
                 U0 += t.nsub;
                 G0 += (t.nsub + 1) / 2;
                 xi += gridDim.x;
@@ -659,14 +690,26 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             // test on DQF + (G & 1) is exact: dQ(G-4) was waited for by this
             // warpgroup earlier, and dQ(G) needs PF(U).  (The product is almost
             // always complete by now.)
+            // With DK_SMEM also the dK product of the block's previous sub-tile:
+            // this sub-tile is use k of block 2 (G & 1) + s, k = G / 2 for s = 0
+            // and G / 2 less the earlier one-sub-tile groups of G's parity for
+            // s = 1; it waits for DSE phase k - 1 (phase k needs this sub-tile's
+            // PF).
             const uint32_t bsf = sy.bar(F_SFS + U % (2 * C::NB)), psf = (U / (2 * C::NB)) & 1;
-            uint32_t bdq = bsf, pdq = psf;
+            uint32_t bdq = bsf, pdq = psf, bds = bsf, pds = psf;
             if (G >= 2) {
                 const int h = G - 2;
                 bdq = sy.bar(F_DQF + (h & 1));
                 pdq = (h >> 1) & 1;
             }
-            ok = warp_wait_all(sy, bsf, psf, bdq, pdq, bsf, psf, bsf, psf, 2, U);
+            {
+                const int s = ul & 1, k = (G >> 1) - (s ? ((G & 1) ? single1 : single0) : 0);
+                if (C::DK_SMEM && k > 0) {
+                    bds = sy.bar(F_DSE + 2 * (G & 1) + s);
+                    pds = (k - 1) & 1;
+                }
+            }
+            ok = warp_wait_all(sy, bsf, psf, bdq, pdq, bds, pds, bsf, psf, 2, U);
             if (!ok) break;
             tc_fence_after();
             const uint32_t ds_blk = sb + C::OFF_DS + 16384 * (2 * (G & 1) + (ul & 1));
@@ -736,11 +779,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                             dk[2 * kk + e] = pack_bf16x2(d0, d1);
                         }
                     }
-                    // dS over the dP^T columns already read
-                    tmem_st_16x128b_x4(tDP + 16 * c, dk);
-                    // dS also to the 128B-swizzled ring block (row = key, 16-byte
-                    // chunk = query / 8 xor row % 8) for the dQ product: one 4-byte
-                    // word per (row, pair), bank-conflict free across the warp
+                    // dS over the dP^T columns already read, for the dK product
+                    if constexpr (!C::DK_SMEM) tmem_st_16x128b_x4(tDP + 16 * c, dk);
+                    // dS to the 128B-swizzled ring block (row = key, 16-byte chunk =
+                    // query / 8 xor row % 8) for the dQ product (and dK with
+                    // DK_SMEM): one 4-byte word per (row, pair), bank-conflict free
+                    // across the warp
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
 #pragma unroll

@@ -473,7 +473,8 @@ def run_fused(nsub, NB, NST, seed, two_issuers, pf_ring=8, sf_ring=None, slow_ro
     schedule(roles, fifo, rnd, slow_role)
 
 
-def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None, plant=None, kvbuf=1):
+def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None, plant=None, kvbuf=1,
+                   ds_smem=False, dk_first=False):
     """One random schedule of one persistent CTA of the fused backward kernel
     walking several work items (units or pieces) in turn; items lists their
     sub-tile counts.  Sub-tiles U and 128-query groups G are numbered across
@@ -491,9 +492,17 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
     item's epilogue (EPI), and the issuer that does not own the item's first
     sub-tile also for dV/dK of that sub-tile; each commits ACC per item); the
     drain warps run each item's epilogue (ACC waits, accumulator reads, EPI
-    arrive).  plant: "no_epi_wait" drops the issuers' EPI wait; "no_kve_wait"
-    lets the K/V producer skip KVE; "accb_prologue" makes the prologue wait
-    for the other issuer's ACCB instead of its last QE."""
+    arrive).  ds_smem: dK(u) reads dS(u) from its shared-memory ring block
+    (as the dQ product does), so the softmax leaves the dP region free once it
+    has read dP(u); the issuer issues dV(u), S/dP(u+NB), then dK(u) and commits
+    QE and DSE of the block (dk_first: dV(u), S(u+NB), dK(u) and its commits,
+    dP(u+NB)), and the softmax waits for the DSE of the block's
+    previous sub-tile before writing it (else the older form: dS(u) also in
+    the dP region, read there by dK(u), which precedes dP(u+NB)).  plant:
+    "no_epi_wait" drops the issuers' EPI wait; "no_kve_wait" lets the K/V
+    producer skip KVE; "no_dse_wait" drops the softmax's DSE wait;
+    "accb_prologue" makes the prologue wait for the other issuer's ACCB
+    instead of its last QE."""
     rnd = random.Random(seed)
     nsf = 2 * NB
     UT = sum(items)
@@ -525,13 +534,26 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
     bar("ACC")
     bar("ACCB")
     bar("EPI", 4)
+    for b in range(4):
+        bar(("DSE", b))
+    # dS ring block of each sub-tile (2 (G & 1) + its place in the group) and
+    # which use of that block it is
+    blk_of, use_of, uses, g0 = [], [], [0] * 4, 0
+    for n in items:
+        for ul in range(n):
+            b = 2 * ((g0 + ul // 2) & 1) + (ul & 1)
+            blk_of.append(b)
+            use_of.append(uses[b])
+            uses[b] += 1
+        g0 += (n + 1) // 2
+    ds_readers = {"dq", "dk"} if ds_smem else {"dq"}
 
     sreg = {(b, q): ("free", None) for b in range(NB) for q in range(4)}
     dreg = {(b, q): ("free", None) for b in range(NB) for q in range(4)}
     stage = {st: None for st in range(NST)}
     readers = {st: set() for st in range(NST)}
     stage_soft = {st: 0 for st in range(NST)}
-    ds = {(blk, q): ("zero", None, True) for blk in range(4) for q in range(4)}
+    ds = {(blk, q): ("zero", None, {"dq", "dk"}) for blk in range(4) for q in range(4)}
     acc = {q: ("idle", -1) for q in range(4)}
     kv = [None] * kvbuf
     kv_reads = {it: 0 for it in range(len(items))}       # S, dP and dQ products of the item executed
@@ -587,8 +609,13 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
         b = u % NB
         acc_use(u, "dk")
         for q in range(4):
-            assert dreg[(b, q)] == ("dS", u), f"dK({u}) reads {dreg[(b, q)]}"
-            dreg[(b, q)] = ("free", None)
+            if ds_smem:
+                kind, uu, rd = ds[(blk_of[u], q)]
+                assert (kind, uu) == ("dS", u), f"dK({u}) reads dS block {blk_of[u]} holding {(kind, uu)}"
+                ds[(blk_of[u], q)] = (kind, uu, rd | {"dk"})
+            else:
+                assert dreg[(b, q)] == ("dS", u), f"dK({u}) reads {dreg[(b, q)]}"
+                dreg[(b, q)] = ("free", None)
         check_stage(u, "dk")
 
     def mma_dq(arg):
@@ -596,9 +623,9 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
         for s_, u in enumerate(us):
             blk = 2 * (g & 1) + s_
             for q in range(4):
-                kind, uu, _ = ds[(blk, q)]
+                kind, uu, rd = ds[(blk, q)]
                 assert (kind, uu) == ("dS", u), f"dQ({g}) reads dS block {blk} holding {(kind, uu)}"
-                ds[(blk, q)] = ("dS", u, True)
+                ds[(blk, q)] = ("dS", u, rd | {"dq"})
             check_kv(u, "dQ")
         kv_reads[item_of[us[0]]] += 1
         for q in range(4):
@@ -680,6 +707,17 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                 if ul + NB < n:
                     fifo[me].append(("mma", mma_s, v))
                     fifo[me].append(("commit", bar(("SFs", v % nsf)), v // nsf))
+                if ds_smem:
+                    if ul + NB < n and not dk_first:
+                        fifo[me].append(("mma", mma_dp, v))
+                        fifo[me].append(("commit", bar(("SFd", v % nsf)), v // nsf))
+                    fifo[me].append(("mma", mma_dk, u))
+                    fifo[me].append(("commit", bar(("QE", u % NST)), u // NST))
+                    fifo[me].append(("commit", bar(("DSE", blk_of[u])), use_of[u]))
+                    if ul + NB < n and dk_first:
+                        fifo[me].append(("mma", mma_dp, v))
+                        fifo[me].append(("commit", bar(("SFd", v % nsf)), v // nsf))
+                    continue
                 fifo[me].append(("mma", mma_dk, u))
                 fifo[me].append(("commit", bar(("QE", u % NST)), u // NST))
                 if ul + NB < n:
@@ -720,14 +758,18 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                 yield ("wait", bar(("SFs", u % nsf)), u // nsf)
                 if g >= 2:
                     yield ("wait", bar(("DQF", (g - 2) & 1)), (g - 2) >> 1)
+                if ds_smem and use_of[u] > 0 and plant != "no_dse_wait":
+                    # dK of the block's previous sub-tile is done with it
+                    yield ("wait", bar(("DSE", blk)), use_of[u] - 1)
                 assert sreg[(b, q)] == ("S", u), f"softmax({u}) reads S region {sreg[(b, q)]}"
                 sreg[(b, q)] = ("P", u)
                 yield ("wait", bar(("SFd", u % nsf)), u // nsf)
                 assert dreg[(b, q)] == ("dP", u), f"softmax({u}) reads dP region {dreg[(b, q)]}"
-                dreg[(b, q)] = ("dS", u)
-                kind, uu, read = ds[(blk, q)]
-                assert read, f"softmax({u}) overwrites dS of sub-tile {uu} before its dQ product read it"
-                ds[(blk, q)] = ("dS", u, False)
+                dreg[(b, q)] = ("free", None) if ds_smem else ("dS", u)
+                kind, uu, rd = ds[(blk, q)]
+                assert rd >= ds_readers, \
+                    f"softmax({u}) overwrites dS of sub-tile {uu} before its {sorted(ds_readers - rd)} product read it"
+                ds[(blk, q)] = ("dS", u, set())
                 stage_soft[st] += 1
                 if ul + NB < n:
                     v = u + NB
@@ -1455,32 +1497,37 @@ PERSISTENT_ITEMS = [[7, 7, 7], [7, 7, 7, 7, 7, 7, 7], [4, 4, 4, 3, 1], [1, 1, 1,
                     [3, 6, 9], [1, 2, 1, 2, 6], [5, 1, 4]]
 
 
-# (NB, NST, two issuers, K/V buffers): head_dim <= 32 (two K/V tiles, the next
-# item's loaded while the current one runs), head_dim 64 (one), and variants
-PERSIST = [(3, 6, True, 2), (2, 4, True, 1), (3, 6, True, 1), (2, 4, False, 1), (2, 4, True, 2)]
+# (NB, NST, two issuers, K/V buffers, dK reads dS from the shared ring, dK
+# before dP(u+NB)): head_dim <= 32 (two K/V tiles, the next item's loaded
+# while the current one runs; dS from the ring), head_dim 64 (one K/V tile, dS
+# from TMEM), and variants
+PERSIST = [(3, 6, True, 2, True, True), (2, 4, True, 1, False, False), (3, 6, True, 1, False, False),
+           (2, 4, False, 1, False, False), (2, 4, True, 2, True, False), (2, 4, True, 1, True, True)]
 
 
 @pytest.mark.parametrize("items", PERSISTENT_ITEMS, ids=lambda x: "-".join(map(str, x)))
-@pytest.mark.parametrize("NB,NST,two,kvbuf", PERSIST)
-def test_persistent_protocol_random_schedules(items, NB, NST, two, kvbuf):
+@pytest.mark.parametrize("NB,NST,two,kvbuf,ds_smem,dk_first", PERSIST)
+def test_persistent_protocol_random_schedules(items, NB, NST, two, kvbuf, ds_smem, dk_first):
     """The persistent fused kernel over several work items per CTA (whole units
     of 7 or 25 sub-tiles as at N = 400 and N = 1600, split pieces, single
     sub-tiles, mixed parities), both head_dim variants, 25 random schedules
     each."""
     for seed in range(25):
-        run_persistent(items, NB, NST, seed * 7919 + sum(items), two, kvbuf=kvbuf)
+        run_persistent(items, NB, NST, seed * 7919 + sum(items), two, kvbuf=kvbuf, ds_smem=ds_smem,
+                       dk_first=dk_first)
 
 
-@pytest.mark.parametrize("NB,NST,two,kvbuf", PERSIST)
-def test_persistent_protocol_with_one_slow_role(NB, NST, two, kvbuf):
+@pytest.mark.parametrize("NB,NST,two,kvbuf,ds_smem,dk_first", PERSIST)
+def test_persistent_protocol_with_one_slow_role(NB, NST, two, kvbuf, ds_smem, dk_first):
     """Each role of the persistent CTA in turn running slowly, over items of odd
     and even lengths."""
     nroles = 1 + (2 if two else 1) + 8 + 4 + 1
     slows = list(range(nroles)) + ["main", "dq"] + (["main1"] if two else [])
+    kw = dict(kvbuf=kvbuf, ds_smem=ds_smem, dk_first=dk_first)
     for slow in slows:
         for seed in range(8):
-            run_persistent([3, 7, 2, 5], NB, NST, seed * 131 + len(str(slow)), two, slow_role=slow, kvbuf=kvbuf)
-            run_persistent([1, 2, 1, 4], NB, NST, seed * 137 + len(str(slow)), two, slow_role=slow, kvbuf=kvbuf)
+            run_persistent([3, 7, 2, 5], NB, NST, seed * 131 + len(str(slow)), two, slow_role=slow, **kw)
+            run_persistent([1, 2, 1, 4], NB, NST, seed * 137 + len(str(slow)), two, slow_role=slow, **kw)
 
 
 def test_persistent_model_catches_missing_item_waits():
@@ -1489,15 +1536,19 @@ def test_persistent_model_catches_missing_item_waits():
     epilogue read them; without the K/V producer's wait for KVE, some schedule
     loads the next item's K/V while the current item still reads its tile (with
     two K/V buffers: the item after next, while a slow dQ issuer still reads
-    the tile of the item two before)."""
+    the tile of the item two before); without the softmax's DSE wait, some
+    schedule writes a dS ring block before the dK product of its previous
+    sub-tile has read it."""
     # roles: the producer, 2 issuers, 8 softmax warps, then the drain warps
-    for plant, msg, slow, kvbuf in (("no_epi_wait", "adds to accumulators", 11, 1),
-                                    ("no_kve_wait", "still reads its tile", None, 1),
-                                    ("no_kve_wait", "still reads its tile", "dq", 2)):
+    for plant, msg, slow, kvbuf, items in (("no_epi_wait", "adds to accumulators", 11, 1, [3, 4, 3, 2]),
+                                           ("no_kve_wait", "still reads its tile", None, 1, [3, 4, 3, 2]),
+                                           ("no_kve_wait", "still reads its tile", "dq", 2, [3, 4, 3, 2]),
+                                           ("no_dse_wait", "['dk'] product read it", "main1", 2, [3, 4, 3, 2, 5])):
         failures = 0
         for seed in range(300):
             try:
-                run_persistent([3, 4, 3, 2], 3, 6, seed, True, plant=plant, slow_role=slow, kvbuf=kvbuf)
+                run_persistent(items, 3, 6, seed, True, plant=plant, slow_role=slow, kvbuf=kvbuf,
+                               ds_smem=plant == "no_dse_wait", dk_first=plant == "no_dse_wait")
             except AssertionError as e:
                 assert msg in str(e), (plant, str(e))
                 failures += 1
