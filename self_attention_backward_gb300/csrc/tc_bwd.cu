@@ -1361,18 +1361,20 @@ pre_stats_view_kernel(const bf16* __restrict__ o_lo, const bf16* __restrict__ o_
 }
 
 // ---------------------------------------------------------------- dQ = scale * acc -> bf16
-template <int D>
+// Blocks [0, nmain) convert dQ: R passes of 256 16-byte output parts each, all
+// loads of a thread issued first.  Blocks from nmain on write the dK, dV_lo,
+// dV_hi rows of the split units, one part per thread.
+template <int D, int R>
 __global__ void __launch_bounds__(256)
 dq_finalize_kernel(const float* __restrict__ dq_acc, bf16* __restrict__ d_packed, long long ldq, long long rows,
                    int N, float scale, const float* __restrict__ dkv_part, int nfull, int ntail, int tail_f,
-                   int nkt) {
+                   int nkt, int nmain) {
     griddep_wait();             // the fused kernel's dQ sums and partials
     constexpr int PPR = D / 8;  // 8-element parts per row
-    const long long idx = (long long)blockIdx.x * 256 + threadIdx.x;
-    if (idx >= rows * PPR) {
+    if ((int)blockIdx.x >= nmain) {
         // dK, dV_lo, dV_hi of the split units: the sum of their pieces'
         // partials, in piece order
-        const long long t = idx - rows * PPR;
+        const long long t = (long long)(blockIdx.x - nmain) * 256 + threadIdx.x;
         if (t >= (long long)ntail * 128 * 3 * PPR) return;
         const int part = (int)(t % PPR);
         const int which = (int)(t / PPR % 3);
@@ -1397,18 +1399,33 @@ dq_finalize_kernel(const float* __restrict__ dq_acc, bf16* __restrict__ d_packed
         *reinterpret_cast<uint4*>(d_packed + (((size_t)bh * 4 + 1 + which) * N + key) * ldq + part * 8) = u;
         return;
     }
-    const long long row = idx / PPR;
-    const int part = (int)(idx % PPR);
-    const long long bh = row / N, i = row % N;
-    const float4* src = reinterpret_cast<const float4*>(dq_acc + (size_t)row * D + part * 8);
-    const float4 a = src[0], b = src[1];
-    uint4 u;
-    u.x = pack_bf16x2(a.x * scale, a.y * scale);
-    u.y = pack_bf16x2(a.z * scale, a.w * scale);
-    u.z = pack_bf16x2(b.x * scale, b.y * scale);
-    u.w = pack_bf16x2(b.z * scale, b.w * scale);
-    *reinterpret_cast<uint4*>(d_packed + ((size_t)bh * 4 * N + i) * ldq + part * 8) = u;
+    const long long total = rows * PPR;
+    float4 a[R], b[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const long long idx = ((long long)blockIdx.x * R + r) * 256 + threadIdx.x;
+        if (idx < total) {
+            const float4* src = reinterpret_cast<const float4*>(dq_acc + (size_t)idx * 8);
+            a[r] = src[0];
+            b[r] = src[1];
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const long long idx = ((long long)blockIdx.x * R + r) * 256 + threadIdx.x;
+        if (idx >= total) continue;
+        const long long row = idx / PPR;
+        const int part = (int)(idx % PPR);
+        const long long bh = row / N, i = row % N;
+        uint4 u;
+        u.x = pack_bf16x2(a[r].x * scale, a[r].y * scale);
+        u.y = pack_bf16x2(a[r].z * scale, a[r].w * scale);
+        u.z = pack_bf16x2(b[r].x * scale, b[r].y * scale);
+        u.w = pack_bf16x2(b[r].z * scale, b[r].w * scale);
+        *reinterpret_cast<uint4*>(d_packed + ((size_t)bh * 4 * N + i) * ldq + part * 8) = u;
+    }
 }
+constexpr int kFinParts = 4;  // parts per thread of dq_finalize_kernel
 
 // ---------------------------------------------------------------- host side
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -1510,7 +1527,8 @@ int launch_impl(const BwdArgs& a, std::string* err) {
     const long long grid = sms > 0 && nitems > sms ? sms : nitems;
     const bool plain = !a.views && ldo == D;   // contiguous O and dO: the vectorised statistics kernel
     const long long pre_grid = plain ? (rows_pad + 256 / (D / 8) - 1) / (256 / (D / 8)) : (rows_pad + 255) / 256;
-    const long long fin_grid = (rows * (D / 8) + (long long)ts.ntail * 128 * 3 * (D / 8) + 255) / 256;
+    const long long fin_main = (rows * (D / 8) + 256 * kFinParts - 1) / (256 * kFinParts);
+    const long long fin_grid = fin_main + ((long long)ts.ntail * 128 * 3 * (D / 8) + 255) / 256;
     if (nitems > 0x7fffffffll || pre_grid > 0x7fffffffll || fin_grid > 0x7fffffffll) {
         *err = "grid too large";
         return PSA_ERR_UNSUPPORTED;
@@ -1542,9 +1560,9 @@ int launch_impl(const BwdArgs& a, std::string* err) {
     }
     if (e == cudaSuccess) {
         ProfScope prof(kSlotDq, a.stream);
-        e = launch_kernel(dq_finalize_kernel<D>, (unsigned)fin_grid, 256, 0, a.stream, dependent,
+        e = launch_kernel(dq_finalize_kernel<D, kFinParts>, (unsigned)fin_grid, 256, 0, a.stream, dependent,
                           (const float*)dq_acc, dp, ldq, rows, a.N, a.scale, (const float*)dkv_part, (int)nfull,
-                          ts.ntail, ts.f, nkt);
+                          ts.ntail, ts.f, nkt, (int)fin_main);
     }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
