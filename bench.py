@@ -280,7 +280,8 @@ class L2Flush:
         import torch
         self.mode = mode
         self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
-        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=device) if mode != "write" else None
+        # fp32, whose sum is one reduction kernel (an int32 sum first casts to int64)
+        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=device) if mode != "write" else None
 
     def __call__(self):
         self.w.zero_()
