@@ -393,3 +393,27 @@ def test_persistent_many_small_items(N, BH, d):
     g = gpu_fwd_bwd(inp, B.PSA_ALGO_TC)
     assert_within(compare(g, ref, "bf16", slices), "bf16")
     check_blocks(g["d_packed"], ref["d_packed"], "bf16", slices)
+
+
+@pytest.mark.parametrize("d", [32, 64])
+def test_timed_launches_match_oracle(d):
+    """With kernel timing on, the tensor-core backward launches its kernels
+    one after another (no programmatic dependent launch), with events around
+    each; the results stay those of the oracle, and the timing records one
+    launch of each backward kernel per call."""
+    inp = make_custom(BH=20, N=1000, d=d, dtype="bf16", seed=900 + d)
+    slices = [0, 19]
+    ref = oracle_fwd_bwd(inp, slices)
+    B.psa_attn_profile_read()
+    B.psa_attn_profile_enable(True)
+    try:
+        gpu = gpu_fwd_bwd(inp, B.PSA_ALGO_TC)
+    finally:
+        B.psa_attn_profile_enable(False)
+    prof = B.psa_attn_profile_read()
+    errs = compare(gpu, ref, "bf16", slices)
+    assert_within(errs, "bf16")
+    check_blocks(gpu["d_packed"], ref["d_packed"], "bf16", slices)
+    for slot in ("bwd_pre", "bwd_main", "bwd_dq"):
+        ms, n = prof[slot]
+        assert n >= 1 and ms > 0.0, (slot, prof)
