@@ -769,14 +769,13 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                         const uint64_t dd = f2_pack(st.z, st.w);
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
-                            const uint32_t pp = pk[hb][c][2 * kk + e];
                             const uint64_t t = f2_sub(f2_pack(__uint_as_float(pr[4 * kk + 2 * e]),
                                                               __uint_as_float(pr[4 * kk + 2 * e + 1])),
                                                       dd);
-                            float d0, d1;
-                            f2_unpack(f2_mul(f2_pack(__uint_as_float(pp << 16), __uint_as_float(pp & 0xffff0000u)), t),
-                                      d0, d1);
-                            dk[2 * kk + e] = pack_bf16x2(d0, d1);
+                            float t0, t1;
+                            f2_unpack(t, t0, t1);
+                            // dP - D rounded to bf16, times the bf16 P pair
+                            dk[2 * kk + e] = bf16x2_mul(pk[hb][c][2 * kk + e], pack_bf16x2(t0, t1));
                         }
                     }
                     // dS over the dP^T columns already read, for the dK product
