@@ -737,9 +737,15 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                                                       cs2, nl);
                             float x0, x1;
                             f2_unpack(x, x0, x1);
-                            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                            if (!(e ? kv1 : kv0)) p0 = p1 = 0.f;
-                            pk[hb][c][2 * kk + e] = pack_bf16x2(p0, p1);
+                            pk[hb][c][2 * kk + e] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+                        }
+                    }
+                    if (!full) {
+                        // keys past the slice's end (its last tile only): P = 0
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            if (!kv0) pk[hb][c][2 * kk] = 0u;
+                            if (!kv1) pk[hb][c][2 * kk + 1] = 0u;
                         }
                     }
                     // packed pair 4k + t%4 over the S^T columns
