@@ -761,7 +761,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             tc_fence_after();
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
-                const int r0 = q4 * 32 + 16 * hb + tr;
                 const uint32_t tDP = tmem + ((uint32_t)(q4 * 32 + 16 * hb) << 16) + 128u * buf + 64;
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -788,15 +787,18 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                     if constexpr (!C::DK_SMEM) tmem_st_16x128b_x4(tDP + 16 * c, dk);
                     // dS to the 128B-swizzled ring block (row = key, 16-byte chunk =
                     // query / 8 xor row % 8) for the dQ product (and dK with
-                    // DK_SMEM): one 4-byte word per (row, pair), bank-conflict free
-                    // across the warp
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e)
-                            st_shared_b32(ds_blk + (uint32_t)(r0 + 8 * e) * 128u +
-                                              ((uint32_t)((4 * c + kk) ^ tr) << 4) + 4u * tq,
-                                          dk[2 * kk + e]);
+                    // DK_SMEM).  The fragment is the MMA layout of 8x8 tiles (tile
+                    // kk: key rows 16 hb + 8 e + 0..7, queries 8 (4 c + kk) + 0..7), so
+                    // one stmatrix per e stores four tiles; lane l addresses row
+                    // l % 8 of tile l / 8 (the XOR spreads a tile's rows over the
+                    // banks)
+                    {
+                        const int tm = lane >> 3, rr = lane & 7;
+                        const uint32_t row = ds_blk + (uint32_t)(q4 * 32 + 16 * hb + rr) * 128u +
+                                             ((uint32_t)((4 * c + tm) ^ rr) << 4);
+                        stmatrix_x4(row, dk[0], dk[2], dk[4], dk[6]);
+                        stmatrix_x4(row + 8 * 128, dk[1], dk[3], dk[5], dk[7]);
+                    }
                 }
             }
             tmem_wait_st();

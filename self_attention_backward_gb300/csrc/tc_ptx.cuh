@@ -225,6 +225,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// Four 8x8 tiles of 16-bit elements to shared memory from the MMA fragment
+// layout (in register i, thread t holds row t/4, columns 2 (t%4) and +1 of
+// tile i, the lower column in the low half); lane l gives the address of row
+// l%8 of tile l/8 (16 bytes each).  The warp executes it together.
+__device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+
 // element-wise bf16 pair product, rounded to nearest
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
     uint32_t r;
