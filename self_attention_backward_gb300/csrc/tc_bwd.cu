@@ -189,14 +189,12 @@ static_assert(B_DQE + 2 <= 32, "barrier area holds 32 barriers");
 // KV / KVE: K/V buffer b loaded, and no MMA reads it any more (F_KV and F_KVE
 // for buffer 0, F_KV1 and F_KVE1 for buffer 1); buffer it % KVBUF holds item
 // it, phase it / KVBUF.
-// DSE + b: the dK product of the latest sub-tile that wrote dS ring block b
-// has read it (one commit per use of the block, by the sub-tile's issuer).
 enum {
     F_KV = 0, F_SFS = 1, F_SFD = 7, F_PF = 13, F_ACC = 21, F_ACCB = 22, F_DQA = 23, F_QF = 24, F_QE = 30, F_DQF = 36,
-    F_DQE = 38, F_KVE = 40, F_EPI = 41, F_KV1 = 42, F_KVE1 = 43, F_DSE = 44
+    F_DQE = 38, F_KVE = 40, F_EPI = 41, F_KV1 = 42, F_KVE1 = 43
 };
 constexpr int kPfRingF = 8;
-static_assert(F_DSE + 4 <= 48, "barrier area holds 48 barriers");
+static_assert(F_KVE1 + 1 <= 48, "barrier area holds 48 barriers");
 __device__ __forceinline__ int kv_full(int b) { return b ? F_KV1 : F_KV; }
 __device__ __forceinline__ int kv_empty(int b) { return b ? F_KVE1 : F_KVE; }
 
@@ -361,7 +359,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         mbar_init(sy.bar(F_ACC), 1);
         mbar_init(sy.bar(F_ACCB), 1);
         mbar_init(sy.bar(F_DQA), 1);
-        for (int b = 0; b < 4; ++b) mbar_init(sy.bar(F_DSE + b), 1);
         for (int s = 0; s < C::NST; ++s) {
             mbar_init(sy.bar(F_QF + s), 1);
             mbar_init(sy.bar(F_QE + s), 1);
@@ -553,7 +550,6 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                                     ID_DK, 1u);
                 }
                 mma_commit(sy.bar(F_QE + u % C::NST));
-                if constexpr (C::DK_SMEM) mma_commit(sy.bar(F_DSE + blk));
             };
             const uint32_t acc_bar = sy.bar(par == 0 ? F_ACC : F_ACCB);
             bool ok = true;
@@ -657,17 +653,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             ok = warp_wait(sy, sy.bar(F_QF + grp % C::NST), (grp / C::NST) & 1, 2, grp);
             if (ok) load_stats(grp);
         }
-        // the item holding sub-tile U: t, its first sub-tile U0 and group G0;
-        // single0 / single1: groups of parity 0 / 1 with one sub-tile (an odd
-        // item's last) in earlier items, which wrote ring block 2p but not 2p + 1
-        int xi = blockIdx.x, U0 = 0, G0 = 0, single0 = 0, single1 = 0;
+        // the item holding sub-tile U: t, its first sub-tile U0 and group G0
+        int xi = blockIdx.x, U0 = 0, G0 = 0;
         Item t = decode_item(xi, nfull, tail_f, nsub_all, nkt);
         for (int U = grp; U < UT && ok; U += 2) {
             while (U >= U0 + t.nsub) {
-                if (t.nsub & 1) {
-                    if ((G0 + t.nsub / 2) & 1) ++single1;
-                    else ++single0;
-                }
                 U0 += t.nsub;
                 G0 += (t.nsub + 1) / 2;
                 xi += gridDim.x;
@@ -690,26 +680,29 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             // test on DQF + (G & 1) is exact: dQ(G-4) was waited for by this
             // warpgroup earlier, and dQ(G) needs PF(U).  (The product is almost
             // always complete by now.)
-            // With DK_SMEM also the dK product of the block's previous sub-tile:
-            // this sub-tile is use k of block 2 (G & 1) + s, k = G / 2 for s = 0
-            // and G / 2 less the earlier one-sub-tile groups of G's parity for
-            // s = 1; it waits for DSE phase k - 1 (phase k needs this sub-tile's
-            // PF).
             const uint32_t bsf = sy.bar(F_SFS + U % (2 * C::NB)), psf = (U / (2 * C::NB)) & 1;
-            uint32_t bdq = bsf, pdq = psf, bds = bsf, pds = psf;
+            uint32_t bdq = bsf, pdq = psf;
             if (G >= 2) {
                 const int h = G - 2;
                 bdq = sy.bar(F_DQF + (h & 1));
                 pdq = (h >> 1) & 1;
             }
-            {
-                const int s = ul & 1, k = (G >> 1) - (s ? ((G & 1) ? single1 : single0) : 0);
-                if (C::DK_SMEM && k > 0) {
-                    bds = sy.bar(F_DSE + 2 * (G & 1) + s);
-                    pds = (k - 1) & 1;
-                }
+            // With DK_SMEM the dK products read the dS ring too: before this
+            // sub-tile's block is written, the dK of the block's previous
+            // sub-tile must be done.  From the item's fifth sub-tile on that is
+            // U-4 (the item's groups before its last have two sub-tiles): its
+            // QE, waited for here (its next phase needs this warpgroup's
+            // PF(U+2)).  Before that it belongs to an earlier item, whose dK
+            // products all completed before S^T(U) did: the item prologue
+            // followed the prologue thread's own dK products and waited for the
+            // other issuer's last ACCB, and every later S^T of the item follows
+            // a PF of the item.
+            uint32_t bqe = bsf, pqe = psf;
+            if (C::DK_SMEM && ul >= 4) {
+                bqe = sy.bar(F_QE + (U - 4) % C::NST);
+                pqe = ((U - 4) / C::NST) & 1;
             }
-            ok = warp_wait_all(sy, bsf, psf, bdq, pdq, bds, pds, bsf, psf, 2, U);
+            ok = warp_wait_all(sy, bsf, psf, bdq, pdq, bqe, pqe, bsf, psf, 2, U);
             if (!ok) break;
             tc_fence_after();
             const uint32_t ds_blk = sb + C::OFF_DS + 16384 * (2 * (G & 1) + (ul & 1));

@@ -474,7 +474,7 @@ def run_fused(nsub, NB, NST, seed, two_issuers, pf_ring=8, sf_ring=None, slow_ro
 
 
 def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None, plant=None, kvbuf=1,
-                   ds_smem=False, dk_first=False):
+                   ds_smem=False, dk_first=False, dse_by_qe=False):
     """One random schedule of one persistent CTA of the fused backward kernel
     walking several work items (units or pieces) in turn; items lists their
     sub-tile counts.  Sub-tiles U and 128-query groups G are numbered across
@@ -498,7 +498,14 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
     QE and DSE of the block (dk_first: dV(u), S(u+NB), dK(u) and its commits,
     dP(u+NB)), and the softmax waits for the DSE of the block's
     previous sub-tile before writing it (else the older form: dS(u) also in
-    the dP region, read there by dK(u), which precedes dP(u+NB)).  plant:
+    the dP region, read there by dK(u), which precedes dP(u+NB)).
+    dse_by_qe (with ds_smem and dk_first): no DSE barriers; with its S^T wait
+    the softmax of the item's sub-tile ul >= 4 waits for QE of sub-tile u-4,
+    the block's previous sub-tile (the item's groups before its last are
+    full).  For ul < 4 the previous sub-tile is in an earlier item, whose dK
+    products are all done before S(u) is: the prologue waits for the other
+    issuer's last ACCB and follows its own thread's dK products, and every
+    later S/dP of the item follows a PF of the item.  plant:
     "no_epi_wait" drops the issuers' EPI wait; "no_kve_wait" lets the K/V
     producer skip KVE; "no_dse_wait" drops the softmax's DSE wait;
     "accb_prologue" makes the prologue wait for the other issuer's ACCB
@@ -713,7 +720,8 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                         fifo[me].append(("commit", bar(("SFd", v % nsf)), v // nsf))
                     fifo[me].append(("mma", mma_dk, u))
                     fifo[me].append(("commit", bar(("QE", u % NST)), u // NST))
-                    fifo[me].append(("commit", bar(("DSE", blk_of[u])), use_of[u]))
+                    if not dse_by_qe:
+                        fifo[me].append(("commit", bar(("DSE", blk_of[u])), use_of[u]))
                     if ul + NB < n and dk_first:
                         fifo[me].append(("mma", mma_dp, v))
                         fifo[me].append(("commit", bar(("SFd", v % nsf)), v // nsf))
@@ -758,9 +766,11 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                 yield ("wait", bar(("SFs", u % nsf)), u // nsf)
                 if g >= 2:
                     yield ("wait", bar(("DQF", (g - 2) & 1)), (g - 2) >> 1)
-                if ds_smem and use_of[u] > 0 and plant != "no_dse_wait":
+                if ds_smem and not dse_by_qe and use_of[u] > 0 and plant != "no_dse_wait":
                     # dK of the block's previous sub-tile is done with it
                     yield ("wait", bar(("DSE", blk)), use_of[u] - 1)
+                if dse_by_qe and ul >= 4 and plant != "no_dse_wait":
+                    yield ("wait", bar(("QE", (u - 4) % NST)), (u - 4) // NST)
                 assert sreg[(b, q)] == ("S", u), f"softmax({u}) reads S region {sreg[(b, q)]}"
                 sreg[(b, q)] = ("P", u)
                 yield ("wait", bar(("SFd", u % nsf)), u // nsf)
@@ -1498,32 +1508,37 @@ PERSISTENT_ITEMS = [[7, 7, 7], [7, 7, 7, 7, 7, 7, 7], [4, 4, 4, 3, 1], [1, 1, 1,
 
 
 # (NB, NST, two issuers, K/V buffers, dK reads dS from the shared ring, dK
-# before dP(u+NB)): head_dim <= 32 (two K/V tiles, the next item's loaded
-# while the current one runs; dS from the ring), head_dim 64 (one K/V tile, dS
-# from TMEM), and variants
-PERSIST = [(3, 6, True, 2, True, True), (2, 4, True, 1, False, False), (3, 6, True, 1, False, False),
-           (2, 4, False, 1, False, False), (2, 4, True, 2, True, False), (2, 4, True, 1, True, True)]
+# before dP(u+NB), the ring guarded by QE(u-4) instead of DSE barriers):
+# head_dim <= 32 (two K/V tiles, the next item's loaded while the current one
+# runs; dS from the ring), head_dim 64 (one K/V tile, dS from TMEM), and
+# variants
+PERSIST = [(3, 6, True, 2, True, True, True), (2, 4, True, 1, False, False, False),
+           (3, 6, True, 1, False, False, False), (2, 4, False, 1, False, False, False),
+           (2, 4, True, 2, True, False, False), (2, 4, True, 1, True, True, False),
+           (3, 6, True, 2, True, True, False), (2, 4, True, 1, True, True, True)]
+PERSIST_NAMES = "NB,NST,two,kvbuf,ds_smem,dk_first,dse_by_qe"
 
 
-@pytest.mark.parametrize("items", PERSISTENT_ITEMS, ids=lambda x: "-".join(map(str, x)))
-@pytest.mark.parametrize("NB,NST,two,kvbuf,ds_smem,dk_first", PERSIST)
-def test_persistent_protocol_random_schedules(items, NB, NST, two, kvbuf, ds_smem, dk_first):
+@pytest.mark.parametrize("items", PERSISTENT_ITEMS + [[1, 1, 1, 1, 1, 1], [1, 2, 1, 1, 3, 1]],
+                         ids=lambda x: "-".join(map(str, x)))
+@pytest.mark.parametrize(PERSIST_NAMES, PERSIST)
+def test_persistent_protocol_random_schedules(items, NB, NST, two, kvbuf, ds_smem, dk_first, dse_by_qe):
     """The persistent fused kernel over several work items per CTA (whole units
     of 7 or 25 sub-tiles as at N = 400 and N = 1600, split pieces, single
-    sub-tiles, mixed parities), both head_dim variants, 25 random schedules
-    each."""
+    sub-tiles, mixed parities, runs of one-sub-tile items), both head_dim
+    variants, 25 random schedules each."""
     for seed in range(25):
         run_persistent(items, NB, NST, seed * 7919 + sum(items), two, kvbuf=kvbuf, ds_smem=ds_smem,
-                       dk_first=dk_first)
+                       dk_first=dk_first, dse_by_qe=dse_by_qe)
 
 
-@pytest.mark.parametrize("NB,NST,two,kvbuf,ds_smem,dk_first", PERSIST)
-def test_persistent_protocol_with_one_slow_role(NB, NST, two, kvbuf, ds_smem, dk_first):
+@pytest.mark.parametrize(PERSIST_NAMES, PERSIST)
+def test_persistent_protocol_with_one_slow_role(NB, NST, two, kvbuf, ds_smem, dk_first, dse_by_qe):
     """Each role of the persistent CTA in turn running slowly, over items of odd
     and even lengths."""
     nroles = 1 + (2 if two else 1) + 8 + 4 + 1
     slows = list(range(nroles)) + ["main", "dq"] + (["main1"] if two else [])
-    kw = dict(kvbuf=kvbuf, ds_smem=ds_smem, dk_first=dk_first)
+    kw = dict(kvbuf=kvbuf, ds_smem=ds_smem, dk_first=dk_first, dse_by_qe=dse_by_qe)
     for slow in slows:
         for seed in range(8):
             run_persistent([3, 7, 2, 5], NB, NST, seed * 131 + len(str(slow)), two, slow_role=slow, **kw)
@@ -1536,19 +1551,22 @@ def test_persistent_model_catches_missing_item_waits():
     epilogue read them; without the K/V producer's wait for KVE, some schedule
     loads the next item's K/V while the current item still reads its tile (with
     two K/V buffers: the item after next, while a slow dQ issuer still reads
-    the tile of the item two before); without the softmax's DSE wait, some
+    the tile of the item two before); without the softmax's DSE wait (or, in
+    the form without DSE barriers, its wait for QE of sub-tile u-4), some
     schedule writes a dS ring block before the dK product of its previous
     sub-tile has read it."""
     # roles: the producer, 2 issuers, 8 softmax warps, then the drain warps
-    for plant, msg, slow, kvbuf, items in (("no_epi_wait", "adds to accumulators", 11, 1, [3, 4, 3, 2]),
-                                           ("no_kve_wait", "still reads its tile", None, 1, [3, 4, 3, 2]),
-                                           ("no_kve_wait", "still reads its tile", "dq", 2, [3, 4, 3, 2]),
-                                           ("no_dse_wait", "['dk'] product read it", "main1", 2, [3, 4, 3, 2, 5])):
+    for plant, msg, slow, kvbuf, items, by_qe in (
+            ("no_epi_wait", "adds to accumulators", 11, 1, [3, 4, 3, 2], False),
+            ("no_kve_wait", "still reads its tile", None, 1, [3, 4, 3, 2], False),
+            ("no_kve_wait", "still reads its tile", "dq", 2, [3, 4, 3, 2], False),
+            ("no_dse_wait", "['dk'] product read it", "main1", 2, [3, 4, 3, 2, 5], False),
+            ("no_dse_wait", "['dk'] product read it", "main1", 2, [3, 4, 3, 2, 5], True)):
         failures = 0
         for seed in range(300):
             try:
                 run_persistent(items, 3, 6, seed, True, plant=plant, slow_role=slow, kvbuf=kvbuf,
-                               ds_smem=plant == "no_dse_wait", dk_first=plant == "no_dse_wait")
+                               ds_smem=plant == "no_dse_wait", dk_first=plant == "no_dse_wait", dse_by_qe=by_qe)
             except AssertionError as e:
                 assert msg in str(e), (plant, str(e))
                 failures += 1
