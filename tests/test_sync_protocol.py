@@ -474,7 +474,7 @@ def run_fused(nsub, NB, NST, seed, two_issuers, pf_ring=8, sf_ring=None, slow_ro
 
 
 def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None, plant=None, kvbuf=1,
-                   ds_smem=False, dk_first=False, dse_by_qe=False):
+                   ds_smem=False, dk_first=False, dse_by_qe=False, p_ready=False):
     """One random schedule of one persistent CTA of the fused backward kernel
     walking several work items (units or pieces) in turn; items lists their
     sub-tile counts.  Sub-tiles U and 128-query groups G are numbered across
@@ -505,7 +505,10 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
     full).  For ul < 4 the previous sub-tile is in an earlier item, whose dK
     products are all done before S(u) is: the prologue waits for the other
     issuer's last ACCB and follows its own thread's dK products, and every
-    later S/dP of the item follows a PF of the item.  plant:
+    later S/dP of the item follows a PF of the item.
+    p_ready: the softmax also arrives PR(u), a ring like PF, once P(u) is
+    written and the stage of u+NB is loaded; the issuer waits PR(u) for dV(u)
+    and S(u+NB), then PF(u) for dK(u) and dP(u+NB).  plant:
     "no_epi_wait" drops the issuers' EPI wait; "no_kve_wait" lets the K/V
     producer skip KVE; "no_dse_wait" drops the softmax's DSE wait;
     "accb_prologue" makes the prologue wait for the other issuer's ACCB
@@ -529,6 +532,7 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
         bar(("SFd", b))
     for x in range(pf_ring):
         bar(("PF", x), 4)
+        bar(("PR", x), 4)
     for st in range(NST):
         bar(("QF", st))
         bar(("QE", st))
@@ -702,7 +706,7 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                 u = u0 + ul
                 if two_issuers and u % 2 != par:
                     continue
-                yield ("wait", bar(("PF", u % pf_ring)), u // pf_ring)
+                yield ("wait", bar(("PR" if p_ready else "PF", u % pf_ring)), u // pf_ring)
                 if first:
                     # the accumulators are zeroed for this item (EPI phase 0: at
                     # the start; phase i + 1: after item i's epilogue)
@@ -714,6 +718,8 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                 if ul + NB < n:
                     fifo[me].append(("mma", mma_s, v))
                     fifo[me].append(("commit", bar(("SFs", v % nsf)), v // nsf))
+                if p_ready and plant != "no_pf_after_pr":
+                    yield ("wait", bar(("PF", u % pf_ring)), u // pf_ring)
                 if ds_smem:
                     if ul + NB < n and not dk_first:
                         fifo[me].append(("mma", mma_dp, v))
@@ -773,6 +779,13 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                     yield ("wait", bar(("QE", (u - 4) % NST)), (u - 4) // NST)
                 assert sreg[(b, q)] == ("S", u), f"softmax({u}) reads S region {sreg[(b, q)]}"
                 sreg[(b, q)] = ("P", u)
+                if p_ready:
+                    # PR(u) certifies, as PF(u) does otherwise, that the stage of
+                    # u+NB is loaded (S(u+NB) follows it)
+                    if ul + NB < n and plant != "pr_without_stage":
+                        v = u + NB
+                        yield ("wait", bar(("QF", v % NST)), v // NST)
+                    yield ("arrive", bar(("PR", u % pf_ring)), u // pf_ring)
                 yield ("wait", bar(("SFd", u % nsf)), u // nsf)
                 assert dreg[(b, q)] == ("dP", u), f"softmax({u}) reads dP region {dreg[(b, q)]}"
                 dreg[(b, q)] = ("free", None) if ds_smem else ("dS", u)
@@ -781,7 +794,7 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                     f"softmax({u}) overwrites dS of sub-tile {uu} before its {sorted(ds_readers - rd)} product read it"
                 ds[(blk, q)] = ("dS", u, set())
                 stage_soft[st] += 1
-                if ul + NB < n:
+                if ul + NB < n and not p_ready:
                     v = u + NB
                     yield ("wait", bar(("QF", v % NST)), v // NST)
                 if ul + 2 < n:
