@@ -111,6 +111,13 @@ struct Cfg {
     // 0.3678 ms), TMEM at head_dim 64 (the ring there: N = 1600 0.1905 ->
     // 0.193 ms per step).
     static constexpr bool DK_SMEM = D <= 32;
+    // A P-ready barrier (PR) per sub-tile: the issuer starts dV(u) and
+    // S^T(u+NB) once the softmax has written P(u), before its second phase,
+    // and dK(u), dP^T(u+NB) after it (PF).  Measured: at head_dim 64 N = 1600
+    // 0.1780 -> 0.1662 ms, N = 400 0.0908 -> 0.0893 ms; at head_dim 32 the
+    // issuer's second wait per sub-tile cost more than it gained (N = 6400
+    // bwd_main 0.3425 -> 0.3674 ms).
+    static constexpr bool P_READY = D == 64;
     static constexpr int KVSET = 3 * KTILE;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_VL = KTILE;
@@ -134,8 +141,8 @@ struct Cfg {
     // NST x 32 float4, one per query pair c of the stage's 64 queries:
     // {-LSE_2c log2(e), -LSE_2c+1 log2(e), D_2c, D_2c+1}
     static constexpr int OFF_ST = OFF_DQS + NDQS * DQS_BYTES;
-    static constexpr int OFF_BAR = OFF_ST + NST * 512;     // mbarriers (48)
-    static constexpr int OFF_MISC = OFF_BAR + 384;
+    static constexpr int OFF_BAR = OFF_ST + NST * 512;     // mbarriers (64)
+    static constexpr int OFF_MISC = OFF_BAR + 512;
     static constexpr int USED = OFF_MISC + 64;
     // + 1 KB to align the base to 1024 where that fits; at head_dim 64 it does
     // not, and the host checks once per device that the base is aligned
@@ -191,10 +198,10 @@ static_assert(B_DQE + 2 <= 32, "barrier area holds 32 barriers");
 // it, phase it / KVBUF.
 enum {
     F_KV = 0, F_SFS = 1, F_SFD = 7, F_PF = 13, F_ACC = 21, F_ACCB = 22, F_DQA = 23, F_QF = 24, F_QE = 30, F_DQF = 36,
-    F_DQE = 38, F_KVE = 40, F_EPI = 41, F_KV1 = 42, F_KVE1 = 43
+    F_DQE = 38, F_KVE = 40, F_EPI = 41, F_KV1 = 42, F_KVE1 = 43, F_PR = 44
 };
 constexpr int kPfRingF = 8;
-static_assert(F_KVE1 + 1 <= 48, "barrier area holds 48 barriers");
+static_assert(F_PR + kPfRingF <= 64, "barrier area holds 64 barriers");
 __device__ __forceinline__ int kv_full(int b) { return b ? F_KV1 : F_KV; }
 __device__ __forceinline__ int kv_empty(int b) { return b ? F_KVE1 : F_KVE; }
 
@@ -351,7 +358,10 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             mbar_init(sy.bar(F_SFS + b), 1);
             mbar_init(sy.bar(F_SFD + b), 1);
         }
-        for (int x = 0; x < kPfRingF; ++x) mbar_init(sy.bar(F_PF + x), 128);
+        for (int x = 0; x < kPfRingF; ++x) {
+            mbar_init(sy.bar(F_PF + x), 128);
+            mbar_init(sy.bar(F_PR + x), 128);
+        }
         mbar_init(sy.bar(F_DQF), 1);
         mbar_init(sy.bar(F_DQF + 1), 1);
         mbar_init(sy.bar(F_DQE), 128);
@@ -590,7 +600,9 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                 for (int ul = 0; ul < t.nsub; ++ul) {
                     const int U = U0 + ul;
                     if (C::TWO_ISSUERS && (U & 1) != par) continue;
-                    ok = wait_bounded(sy, sy.bar(F_PF + U % kPfRingF), (U / kPfRingF) & 1, 1, U);
+                    // PF(U), or with P_READY first PR(U): P(U) is in TMEM and the
+                    // stage of U+NB is loaded
+                    ok = wait_bounded(sy, sy.bar((C::P_READY ? F_PR : F_PF) + U % kPfRingF), (U / kPfRingF) & 1, 1, U);
                     if (ok && first) {
                         ok = wait_bounded(sy, sy.bar(F_EPI), it & 1, 1, U);
                         first = false;
@@ -600,6 +612,12 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                     const bool more = ul + C::NB < t.nsub;
                     issue_dv(U);
                     if (more) issue_s(U + C::NB);
+                    if constexpr (C::P_READY) {
+                        // PF(U): dS(U) is written and dP^T(U) read
+                        ok = wait_bounded(sy, sy.bar(F_PF + U % kPfRingF), (U / kPfRingF) & 1, 1, U);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
                     issue_dk(U, 2 * ((G0 + (ul >> 1)) & 1) + (ul & 1));
                     if (more) issue_dp(U + C::NB);
                 }
@@ -745,6 +763,20 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                     tmem_st_16x128b_x4(tS + 16 * c, pk[hb][c]);
                 }
             }
+            if constexpr (C::P_READY) {
+                // P(U) is in TMEM: the issuer of U may start dV(U) and S^T(U+NB)
+                // (PR), once the stage of U+NB is loaded (waited for here in its
+                // stead)
+                if (ul + C::NB < t.nsub)
+                    ok = warp_wait(sy, sy.bar(F_QF + (U + C::NB) % C::NST), ((U + C::NB) / C::NST) & 1, 2, U);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(sy.bar(F_PR + U % kPfRingF));
+                if (!ok) {
+                    mbar_arrive(sy.bar(F_PF + U % kPfRingF));
+                    break;
+                }
+            }
             // phase 2: dS = P (dP - D), with P as rounded for the dV product
             ok = warp_wait(sy, sy.bar(F_SFD + U % (2 * C::NB)), (U / (2 * C::NB)) & 1, 2, U);
             if (!ok) {
@@ -797,11 +829,17 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
             tmem_wait_st();
             tc_fence_before();
             fence_proxy_async_smem();
-            // One round trip for: (a) a stand-in wait for the MMA issuer of U (see
-            // its loop): the stage of U+NB is loaded, when U+NB is in this item;
-            // (b) the stage of U+2, this warpgroup's next sub-tile, whose statistics
-            // it loads now, when U+2 is in this item.
-            {
+            if constexpr (C::P_READY) {
+                // the stage of U+2, this warpgroup's next sub-tile, whose
+                // statistics it loads now, when U+2 is in this item (the stage of
+                // U+NB was waited for before PR)
+                if (ul + 2 < t.nsub)
+                    ok = warp_wait(sy, sy.bar(F_QF + (U + 2) % C::NST), ((U + 2) / C::NST) & 1, 2, U);
+            } else {
+                // One round trip for: (a) a stand-in wait for the MMA issuer of U
+                // (see its loop): the stage of U+NB is loaded, when U+NB is in this
+                // item; (b) the stage of U+2, this warpgroup's next sub-tile, whose
+                // statistics it loads now, when U+2 is in this item.
                 const bool v0 = ul + C::NB < t.nsub, v1 = ul + 2 < t.nsub;
                 uint32_t b0 = sy.bar(F_QF + (U + C::NB) % C::NST), p0 = ((U + C::NB) / C::NST) & 1;
                 uint32_t b1 = sy.bar(F_QF + (U + 2) % C::NST), p1 = ((U + 2) / C::NST) & 1;

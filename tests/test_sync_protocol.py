@@ -1521,37 +1521,38 @@ PERSISTENT_ITEMS = [[7, 7, 7], [7, 7, 7, 7, 7, 7, 7], [4, 4, 4, 3, 1], [1, 1, 1,
 
 
 # (NB, NST, two issuers, K/V buffers, dK reads dS from the shared ring, dK
-# before dP(u+NB), the ring guarded by QE(u-4) instead of DSE barriers):
-# head_dim <= 32 (two K/V tiles, the next item's loaded while the current one
-# runs; dS from the ring), head_dim 64 (one K/V tile, dS from TMEM), and
-# variants
-PERSIST = [(3, 6, True, 2, True, True, True), (2, 4, True, 1, False, False, False),
-           (3, 6, True, 1, False, False, False), (2, 4, False, 1, False, False, False),
-           (2, 4, True, 2, True, False, False), (2, 4, True, 1, True, True, False),
-           (3, 6, True, 2, True, True, False), (2, 4, True, 1, True, True, True)]
-PERSIST_NAMES = "NB,NST,two,kvbuf,ds_smem,dk_first,dse_by_qe"
+# before dP(u+NB), the ring guarded by QE(u-4) instead of DSE barriers, a
+# P-ready barrier): head_dim <= 32 (two K/V tiles, the next item's loaded
+# while the current one runs; dS from the ring), head_dim 64 (one K/V tile,
+# dS from TMEM, P-ready), and variants
+PERSIST = [(3, 6, True, 2, True, True, True, False), (2, 4, True, 1, False, False, False, True),
+           (2, 4, True, 1, False, False, False, False), (3, 6, True, 1, False, False, False, False),
+           (2, 4, False, 1, False, False, False, False), (2, 4, True, 2, True, False, False, False),
+           (2, 4, True, 1, True, True, False, False), (3, 6, True, 2, True, True, False, False),
+           (2, 4, True, 1, True, True, True, False), (3, 6, True, 2, True, True, True, True)]
+PERSIST_NAMES = "NB,NST,two,kvbuf,ds_smem,dk_first,dse_by_qe,p_ready"
 
 
 @pytest.mark.parametrize("items", PERSISTENT_ITEMS + [[1, 1, 1, 1, 1, 1], [1, 2, 1, 1, 3, 1]],
                          ids=lambda x: "-".join(map(str, x)))
 @pytest.mark.parametrize(PERSIST_NAMES, PERSIST)
-def test_persistent_protocol_random_schedules(items, NB, NST, two, kvbuf, ds_smem, dk_first, dse_by_qe):
+def test_persistent_protocol_random_schedules(items, NB, NST, two, kvbuf, ds_smem, dk_first, dse_by_qe, p_ready):
     """The persistent fused kernel over several work items per CTA (whole units
     of 7 or 25 sub-tiles as at N = 400 and N = 1600, split pieces, single
     sub-tiles, mixed parities, runs of one-sub-tile items), both head_dim
     variants, 25 random schedules each."""
     for seed in range(25):
         run_persistent(items, NB, NST, seed * 7919 + sum(items), two, kvbuf=kvbuf, ds_smem=ds_smem,
-                       dk_first=dk_first, dse_by_qe=dse_by_qe)
+                       dk_first=dk_first, dse_by_qe=dse_by_qe, p_ready=p_ready)
 
 
 @pytest.mark.parametrize(PERSIST_NAMES, PERSIST)
-def test_persistent_protocol_with_one_slow_role(NB, NST, two, kvbuf, ds_smem, dk_first, dse_by_qe):
+def test_persistent_protocol_with_one_slow_role(NB, NST, two, kvbuf, ds_smem, dk_first, dse_by_qe, p_ready):
     """Each role of the persistent CTA in turn running slowly, over items of odd
     and even lengths."""
     nroles = 1 + (2 if two else 1) + 8 + 4 + 1
     slows = list(range(nroles)) + ["main", "dq"] + (["main1"] if two else [])
-    kw = dict(kvbuf=kvbuf, ds_smem=ds_smem, dk_first=dk_first, dse_by_qe=dse_by_qe)
+    kw = dict(kvbuf=kvbuf, ds_smem=ds_smem, dk_first=dk_first, dse_by_qe=dse_by_qe, p_ready=p_ready)
     for slow in slows:
         for seed in range(8):
             run_persistent([3, 7, 2, 5], NB, NST, seed * 131 + len(str(slow)), two, slow_role=slow, **kw)
@@ -1604,3 +1605,20 @@ def test_persistent_prologue_waits_that_alias():
                 assert "completed before a waiter" in str(e) or "passed at" in str(e), str(e)
                 failures += 1
         assert failures > 0, plant
+
+
+def test_p_ready_model_catches_missing_waits():
+    """The P-ready form (head_dim 64) is not vacuous: an issuer that issues
+    dK(u) and dP(u+NB) without waiting for PF(u), or a softmax that arrives
+    PR(u) before the stage of u+NB is loaded, fails in some schedule."""
+    for plant, msgs in (("no_pf_after_pr", ("reads dS", "reads ('dP'")), ("pr_without_stage", ("reads stage",))):
+        failures = 0
+        for slow in (None, 2, 6, "main"):
+            for seed in range(60):
+                try:
+                    run_persistent([5, 7, 4], 2, 4, seed, True, slow_role=slow, plant=plant, p_ready=True)
+                except AssertionError as e:
+                    assert any(m in str(e) for m in msgs), (plant, str(e))
+                    failures += 1
+        assert failures > 0, plant
+
