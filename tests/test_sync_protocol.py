@@ -474,7 +474,7 @@ def run_fused(nsub, NB, NST, seed, two_issuers, pf_ring=8, sf_ring=None, slow_ro
 
 
 def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None, plant=None, kvbuf=1,
-                   ds_smem=False, dk_first=False, dse_by_qe=False, p_ready=False):
+                   ds_smem=False, dk_first=False, dse_by_qe=False, p_ready=False, lag=False):
     """One random schedule of one persistent CTA of the fused backward kernel
     walking several work items (units or pieces) in turn; items lists their
     sub-tile counts.  Sub-tiles U and 128-query groups G are numbered across
@@ -508,7 +508,10 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
     later S/dP of the item follows a PF of the item.
     p_ready: the softmax also arrives PR(u), a ring like PF, once P(u) is
     written and the stage of u+NB is loaded; the issuer waits PR(u) for dV(u)
-    and S(u+NB), then PF(u) for dK(u) and dP(u+NB).  plant:
+    and S(u+NB), then PF(u) for dK(u) and dP(u+NB).  lag (with p_ready): the
+    issuer waits only PR(u), then issues dV(u), S(u+NB) and the dK / dP of its
+    previous sub-tile of the item (u-2: its PF came from the same warpgroup
+    before PR(u)); after the item's last it waits PF for the pending one.  plant:
     "no_epi_wait" drops the issuers' EPI wait; "no_kve_wait" lets the K/V
     producer skip KVE; "no_dse_wait" drops the softmax's DSE wait;
     "accb_prologue" makes the prologue wait for the other issuer's ACCB
@@ -677,6 +680,19 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
     odd_items = [it for it, n in enumerate(items)
                  if any((u % 2) == 1 for u in range(sum(items[:it]), sum(items[:it]) + n))]
 
+    def issue_dkdp(me, pend):
+        # dK(u) and, within the item, dP(u+NB), with their commits (the lag form
+        # of the ring-dS, dK-first order)
+        u, ul, n = pend
+        v = u + NB
+        fifo[me].append(("mma", mma_dk, u))
+        fifo[me].append(("commit", bar(("QE", u % NST)), u // NST))
+        if ds_smem and not dse_by_qe:
+            fifo[me].append(("commit", bar(("DSE", blk_of[u])), use_of[u]))
+        if ul + NB < n:
+            fifo[me].append(("mma", mma_dp, v))
+            fifo[me].append(("commit", bar(("SFd", v % nsf)), v // nsf))
+
     def main_issuer(par):
         me = "main" if par == 0 else "main1"
         u0 = 0
@@ -702,6 +718,7 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                 for j in range(min(NB, n)):
                     issue_sdp(me, u0 + j)
             first = True
+            pending = None
             for ul in range(n):
                 u = u0 + ul
                 if two_issuers and u % 2 != par:
@@ -718,6 +735,11 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                 if ul + NB < n:
                     fifo[me].append(("mma", mma_s, v))
                     fifo[me].append(("commit", bar(("SFs", v % nsf)), v // nsf))
+                if p_ready and lag:
+                    if pending is not None:
+                        issue_dkdp(me, pending)
+                    pending = (u, ul, n)
+                    continue
                 if p_ready and plant != "no_pf_after_pr":
                     yield ("wait", bar(("PF", u % pf_ring)), u // pf_ring)
                 if ds_smem:
@@ -737,6 +759,12 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                 if ul + NB < n:
                     fifo[me].append(("mma", mma_dp, v))
                     fifo[me].append(("commit", bar(("SFd", v % nsf)), v // nsf))
+            if pending is not None:
+                pu = pending[0]
+                if plant != "lag_no_final_pf":
+                    yield ("wait", bar(("PF", pu % pf_ring)), pu // pf_ring)
+                issue_dkdp(me, pending)
+                pending = None
             if par == 0:
                 # ACC every item: an issuer without a sub-tile first waits for the
                 # zeroing for this item, so its phases keep in step with the drain's
