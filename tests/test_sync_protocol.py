@@ -1650,3 +1650,23 @@ def test_p_ready_model_catches_missing_waits():
                     failures += 1
         assert failures > 0, plant
 
+
+
+def test_lagged_issue_form():
+    """The lagged issue form (one issuer wait per sub-tile: dK / dP of the
+    previous sub-tile issued after the next PR) is sound with 6 stages and 3
+    S/dP buffers (head_dim <= 32) and deadlocks with 4 stages and 2 buffers
+    (head_dim 64): the stage that S(u+NB) needs is freed only by a dK that
+    waits for that S's softmax."""
+    kw = dict(kvbuf=2, ds_smem=True, dk_first=True, dse_by_qe=True, p_ready=True, lag=True)
+    for items in ([9, 5, 6], [3, 7, 2, 5], [1, 2, 1, 4]):
+        for seed in range(20):
+            run_persistent(items, 3, 6, seed, True, **kw)
+    deadlocks = 0
+    for seed in range(20):
+        try:
+            run_persistent([7, 7], 2, 4, seed, True, kvbuf=1, p_ready=True, lag=True)
+        except AssertionError as e:
+            assert "deadlock" in str(e), str(e)
+            deadlocks += 1
+    assert deadlocks > 0
