@@ -8,9 +8,9 @@
 // summed (the page's atomic_add into the shared dQ/dK sections is not needed
 // for that).
 //
-// Decomposition: one CTA per (batch*head, 128-key tile j).  The CTA keeps K_j,
-// V_lo,j, V_hi,j in shared memory and its dV_lo|dV_hi and dK accumulators in
-// TMEM, and sweeps over every query of its slice ("Struct PsaFa2Backward",
+// Decomposition: one work unit per (batch*head, 128-key tile j).  Its CTA keeps
+// K_j, V_lo,j, V_hi,j in shared memory and its dV_lo|dV_hi and dK accumulators
+// in TMEM, and sweeps over every query of its slice ("Struct PsaFa2Backward",
 // description: key-row gradients come from such a sweep) in 64-query
 // sub-tiles u:
 //   S^T  = K_j Q_u^T                 (M = 128 keys, N = 64 queries, K = d)
@@ -27,12 +27,14 @@
 // softmax-gradient warpgroups take alternate sub-tiles, so the tensor core
 // works on later sub-tiles while a warpgroup turns S/dP(u) into P and dS.  P^T
 // is written over the first 32 columns of its S^T buffer as bf16 pairs (the A
-// operand of the dV MMA) and dS^T over the first 32 columns of its dP^T buffer
-// (the A operand of the dK MMA).  S^T(u+NB) reuses u's buffer and is issued
-// right after dV(u), the last reader of P^T(u); dP^T(u+NB) right after dK(u);
-// the pipe keeps issue order.  dS^T also goes into a 4-block shared ring
-// (u & 3) for the dQ MMA, which needs it with queries as rows; a pair's dS
-// stays in the ring until its dQ MMA has read it.
+// operand of the dV MMA).  dS^T goes into a 4-block shared ring (block
+// 2 (g & 1) + the sub-tile's place in its pair) for the dQ MMA, which needs it
+// with queries as rows, and which the dK MMA reads too for d <= 32; for d = 64
+// dS^T also goes over the first 32 columns of its dP^T buffer as dK's A
+// operand.  S^T(u+NB) reuses u's buffer and is issued right after dV(u), the
+// last reader of P^T(u); dP^T(u+NB) right after dK(u); the pipe keeps issue
+// order.  A block of the ring is rewritten only after its dQ (and dK) MMA has
+// read it.
 //
 // Cost model that shaped it (measured on GB300): a tcgen05.mma with M = 128,
 // K = 16 costs about max(46, N/2) cycles, so the MMA count, not the flop
@@ -41,15 +43,19 @@
 // descriptor so that issuing an MMA is one add per operand.
 //
 // Persistent: one CTA per SM walks work items (units of one (batch*head,
-// 128-key tile), or pieces of one along the queries) in turn (see the kernel).
+// 128-key tile), or pieces of one along the queries) in turn (see the kernel);
+// for d <= 32 the next item's K/V tile loads into a second buffer while the
+// current item runs.  The kernel is a programmatic dependent of the
+// statistics kernel before it (it reads the statistics and the zeroed dQ
+// accumulator only after griddepcontrol.wait).
 //
 // Warp roles: warp 0 TMA producer (each item's K/V tile; the Q/dO stages: Q,
 // dO_lo, dO_hi and the sub-tile's row statistics), warp 1 MMA issuer (one thread) and TMEM owner,
 // warps 2-5 / 6-9 softmax-gradient warpgroups 0 / 1 (one key row per thread),
 // warps 10-13 dQ drain (one query row per thread; the partials go to the fp32
 // accumulator by TMA bulk reduce) and then each item's dK/dV epilogue (one key
-// row per thread), warp 14 the dQ MMA issuer; for d <= 32 warp 15 issues the
-// odd sub-tiles' main MMAs and warp 1 the even ones (512 threads).
+// row per thread), warp 14 the dQ MMA issuer; warp 15 issues the odd
+// sub-tiles' main MMAs and warp 1 the even ones (512 threads).
 //
 // Every mbarrier wait is bounded (kTimeoutNs); on timeout the CTA sets a device
 // error word (read by psa_attn_sync_status), skips the rest of its work, waits
@@ -464,10 +470,11 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
         // ------------------------------------------------------------ main MMA issuers
         // With two issuers warp 1 takes the even sub-tiles U, warp 15 the odd ones
         // (numbered across items).  Each issues, per sub-tile U of its parity,
-        // dV/dK(U) once PF(U) shows P/dS(U) ready, then S/dP(U + NB) into the
-        // buffer dV/dK(U) just read when U + NB is in the same item: one thread's
-        // MMAs run in issue order, so the buffer is reused only after its last
-        // reader.  Warp 1 issues each item's first NB S/dP products (the item
+        // dV/dK(U) once PF(U) shows P/dS(U) ready (with P_READY: dV(U) and
+        // S^T(U + NB) once PR(U) shows P(U) ready, dK(U) and dP^T(U + NB) after
+        // PF(U)), and S/dP(U + NB) into the buffer dV/dK(U) just read when U + NB
+        // is in the same item: one thread's MMAs run in issue order, so the buffer
+        // is reused only after its last reader.  Warp 1 issues each item's first NB S/dP products (the item
         // prologue), after the other issuer's last dV/dK of the previous item
         // (whose buffers they reuse; its QE commit), the item's K/V and stages.
         // While one thread waits for its next PF (such a wait first lets its own
@@ -587,8 +594,8 @@ bwd_main_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant
                         issue_dp(U0 + j);
                     }
                 }
-                // PF(U) also certifies that the stage of U+NB is loaded (the softmax
-                // warpgroup waited for it).  S^T(U+NB) follows dV(U), the last reader
+                // PF(U) (with P_READY: PR(U)) also certifies that the stage of U+NB is
+                // loaded (the softmax warpgroup waited for it).  S^T(U+NB) follows dV(U), the last reader
                 // of the S half, and dP^T(U+NB) follows dK(U), the last reader of the
                 // dP half when dK takes dS^T from there (dK first measured faster with
                 // the ring too); the softmax of U+NB starts on S^T while dK(U) and
