@@ -474,7 +474,7 @@ def run_fused(nsub, NB, NST, seed, two_issuers, pf_ring=8, sf_ring=None, slow_ro
 
 
 def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None, plant=None, kvbuf=1,
-                   ds_smem=False, dk_first=False, dse_by_qe=False, p_ready=False, lag=False):
+                   ds_smem=False, dk_first=False, dse_by_qe=False, p_ready=False, lag=False, by_kind=False):
     """One random schedule of one persistent CTA of the fused backward kernel
     walking several work items (units or pieces) in turn; items lists their
     sub-tile counts.  Sub-tiles U and 128-query groups G are numbered across
@@ -511,7 +511,13 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
     and S(u+NB), then PF(u) for dK(u) and dP(u+NB).  lag (with p_ready): the
     issuer waits only PR(u), then issues dV(u), S(u+NB) and the dK / dP of its
     previous sub-tile of the item (u-2: its PF came from the same warpgroup
-    before PR(u)); after the item's last it waits PF for the pending one.  plant:
+    before PR(u)); after the item's last it waits PF for the pending one.
+    by_kind (with p_ready): the two issuers split the work by MMA kind, not
+    by sub-tile parity: issuer A ("main") takes every sub-tile's dV(u) and
+    S(u+NB) after PR(u), issuer B ("main1") its dK(u) and dP(u+NB) after
+    PF(u), each also the item prologue's S (A) or dP (B) products; a stage is
+    free once both have committed QE (a barrier of two arrivals), and each
+    commits ACC (A) or ACCB (B) every item.  plant:
     "no_epi_wait" drops the issuers' EPI wait; "no_kve_wait" lets the K/V
     producer skip KVE; "no_dse_wait" drops the softmax's DSE wait;
     "accb_prologue" makes the prologue wait for the other issuer's ACCB
@@ -538,7 +544,7 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
         bar(("PR", x), 4)
     for st in range(NST):
         bar(("QF", st))
-        bar(("QE", st))
+        bar(("QE", st), 2 if by_kind else 1)
     for x in range(2):
         bar(("DQE", x), 4)
         bar(("DQF", x))
@@ -692,6 +698,48 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
         if ul + NB < n:
             fifo[me].append(("mma", mma_dp, v))
             fifo[me].append(("commit", bar(("SFd", v % nsf)), v // nsf))
+
+    def kind_issuer(kind):
+        # by_kind: A (kind 0) dV and S, B (kind 1) dK and dP
+        me = "main" if kind == 0 else "main1"
+        u0 = 0
+        for it, n in enumerate(items):
+            yield ("wait", bar(("KV", it % kvbuf)), it // kvbuf)
+            for j in range(min(NB, n)):
+                yield ("wait", bar(("QF", (u0 + j) % NST)), (u0 + j) // NST)
+            for j in range(min(NB, n)):
+                v = u0 + j
+                if kind == 0:
+                    fifo[me].append(("mma", mma_s, v))
+                    fifo[me].append(("commit", bar(("SFs", v % nsf)), v // nsf))
+                else:
+                    fifo[me].append(("mma", mma_dp, v))
+                    fifo[me].append(("commit", bar(("SFd", v % nsf)), v // nsf))
+            first = True
+            for ul in range(n):
+                u = u0 + ul
+                yield ("wait", bar(("PR" if kind == 0 else "PF", u % pf_ring)), u // pf_ring)
+                if first:
+                    if plant != "no_epi_wait":
+                        yield ("wait", bar("EPI"), it)
+                    first = False
+                v = u + NB
+                if kind == 0:
+                    fifo[me].append(("mma", mma_dv, u))
+                    fifo[me].append(("commit", bar(("QE", u % NST)), u // NST))
+                    if ul + NB < n:
+                        fifo[me].append(("mma", mma_s, v))
+                        fifo[me].append(("commit", bar(("SFs", v % nsf)), v // nsf))
+                else:
+                    fifo[me].append(("mma", mma_dk, u))
+                    fifo[me].append(("commit", bar(("QE", u % NST)), u // NST))
+                    if ul + NB < n:
+                        fifo[me].append(("mma", mma_dp, v))
+                        fifo[me].append(("commit", bar(("SFd", v % nsf)), v // nsf))
+            if first and plant != "no_epi_wait":
+                yield ("wait", bar("EPI"), it)
+            fifo[me].append(("commit", bar("ACC" if kind == 0 else "ACCB"), it))
+            u0 += n
 
     def main_issuer(par):
         me = "main" if par == 0 else "main1"
@@ -860,7 +908,9 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
                 acc[q] = ("read", g)
                 yield ("arrive", bar(("DQE", g & 1)), g >> 1)
             yield ("wait", bar("ACC"), it)
-            if two_issuers and plant == "accb_prologue":
+            if by_kind:
+                yield ("wait", bar("ACCB"), it)
+            elif two_issuers and plant == "accb_prologue":
                 yield ("wait", bar("ACCB"), it)
             elif two_issuers and it in odd_items:
                 yield ("wait", bar("ACCB"), odd_items.index(it))
@@ -871,7 +921,10 @@ def run_persistent(items, NB, NST, seed, two_issuers, pf_ring=8, slow_role=None,
             g0 += (n + 1) // 2
 
     roles = [producer()]
-    roles += [main_issuer(0), main_issuer(1)] if two_issuers else [main_issuer(0)]
+    if by_kind:
+        roles += [kind_issuer(0), kind_issuer(1)]
+    else:
+        roles += [main_issuer(0), main_issuer(1)] if two_issuers else [main_issuer(0)]
     roles += [softmax(g, q) for g in range(2) for q in range(4)]
     roles += [drain(q) for q in range(4)] + [dq_issuer()]
     schedule(roles, fifo, rnd, slow_role)
@@ -1670,3 +1723,25 @@ def test_lagged_issue_form():
             assert "deadlock" in str(e), str(e)
             deadlocks += 1
     assert deadlocks > 0
+
+
+def test_issuers_by_kind_form():
+    """The issuers split by MMA kind (one takes dV and S after PR, the other dK
+    and dP after PF; a stage freed by both) is sound at both head_dim
+    variants under random and slow-role schedules, and still needs its EPI
+    and stage waits."""
+    for NB, NST, kw in ((3, 6, dict(kvbuf=2, ds_smem=True, dk_first=True, dse_by_qe=True)), (2, 4, dict(kvbuf=1))):
+        for items in ([9, 5, 6], [3, 7, 2, 5], [1, 2, 1, 4], [1, 1, 1]):
+            for seed in range(10):
+                run_persistent(items, NB, NST, seed, True, p_ready=True, by_kind=True, **kw)
+                run_persistent(items, NB, NST, seed, True, p_ready=True, by_kind=True, slow_role="main1", **kw)
+        for plant in ("no_epi_wait", "pr_without_stage"):
+            failures = 0
+            for slow in (None, 2, 11, "main"):
+                for seed in range(30):
+                    try:
+                        run_persistent([5, 7, 4, 3], NB, NST, seed, True, slow_role=slow, plant=plant, p_ready=True,
+                                       by_kind=True, **kw)
+                    except AssertionError:
+                        failures += 1
+            assert failures > 0, (NB, plant)
