@@ -58,11 +58,13 @@ typedef enum {
 /* Backward kernel choice.  AUTO picks the tensor-core (tcgen05) path where it
  * exists for the (dtype, head_dim) and the CUDA-core (SIMT) path elsewhere.
  *   PSA_ALGO_TC        one key-outer pass; dQ partial sums are added to an
- *                      fp32 accumulator by bulk reduce operations, in an order
- *                      that can differ from run to run, and so can the
- *                      rounding of dQ.  (The units of its last, partial wave
- *                      are split along the queries; their dK/dV partials are
- *                      summed in a fixed order.)
+ *                      fp32 accumulator by bulk reduce operations, and the
+ *                      dK/dV products of neighbouring query sub-tiles come
+ *                      from two issuing threads, in orders that can differ
+ *                      from run to run, and so can the rounding of dQ, dK and
+ *                      dV.  (The units of its last, partial wave are split
+ *                      along the queries; their dK/dV partials are summed in
+ *                      a fixed order.)
  *   PSA_ALGO_TC_2PASS  a key-outer dK/dV pass and a query-outer dQ pass
  *                      (the split of "Struct PsaFa2Backward", description:
  *                      query gradients from a sweep over keys, key gradients
